@@ -1,0 +1,317 @@
+/*
+ * dwdp_oracle.c: plain, slow, fp64 CPU oracle of one DWDP MoE layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg are the only code that loads this library.  It
+ * shares no code, header, table or helper with the CUDA path, and nothing in
+ * the CUDA path loads it.
+ *
+ * Sources ("DWDP" = "DWDP: Distributed Weight Data Parallelism for
+ * High-Performance LLM Inference on NVL72", read through its summary pages):
+ *   - DWDP §2 (Methodology Overview): each rank keeps some experts resident and
+ *     fetches the others from peers; where an expert's weights live changes
+ *     nothing in what the layer computes.  Placement may be redundant.
+ *   - DWDP §4.2 (Eliminating Split-Weight Merge Overhead): the grouped GEMM
+ *     reads local and prefetched weights from separate buffers; again the
+ *     result is the ordinary grouped GEMM's.
+ * The pages do not print the router or the expert FFN.  This oracle takes the
+ * plain reading of the workload they describe (a DeepSeek-R1-shaped MoE
+ * block): softmax over all E experts, the k largest probabilities, weights
+ * renormalised over the chosen k; each expert a SwiGLU FFN
+ * (gate/up projection, SiLU(gate)*up, down projection); one optional shared
+ * expert added with weight 1.
+ *
+ * Storage convention (shared with the inputs, not with any kernel): bf16 values
+ * are passed as their 16-bit patterns.  x is [T][H].  The router weight is
+ * stored [E][H] (row e holds column e of the math-layout H x E matrix).  One
+ * expert's w13 is [2I][H]: rows 0..I-1 are W_gate transposed, rows I..2I-1 are
+ * W_up transposed.  Its w2 is [H][I]: W_down transposed.  So, in math layout,
+ * W_gate[h][i] = w13[i][h], W_up[h][i] = w13[I+i][h], W_down[i][h] = w2[h][i].
+ *
+ * Rounding points ("mirrored" mode, mirrored != 0): the activation a, each
+ * expert's output y and the layer output are rounded to bf16 with
+ * round-to-nearest-even; every other quantity stays in fp64.  With
+ * mirrored == 0 ("strict" mode) nothing is rounded.
+ *
+ * ORACLE_MUTANT (compile-time, default 0) plants one known mistake; the test
+ * suite builds each mutant and checks that its pins catch it.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---------------------------------------------------------------- bf16 -- */
+
+/* The bf16 value whose bit pattern is b (bf16 is the top half of an IEEE
+ * binary32). */
+double oracle_bf16_to_double(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Round v to the nearest bf16 value, ties to even, straight from fp64 (no
+ * detour through binary32, so no double rounding).  bf16 has an 8-bit
+ * significand and binary32's exponent range; below 2^-126 the quantum stays
+ * 2^-133 (subnormals).  Returns the bit pattern. */
+uint16_t oracle_round_bf16(double v) {
+    if (isnan(v)) return (uint16_t)0x7FC0;
+    if (v == 0.0) return signbit(v) ? (uint16_t)0x8000 : (uint16_t)0x0000;
+    double a = fabs(v);
+    int e = ilogb(a);            /* 2^e <= a < 2^(e+1) */
+    if (e < -126) e = -126;      /* subnormal range: fixed quantum */
+    double q = ldexp(a, 7 - e);  /* significand scaled so the quantum is 1 */
+#if ORACLE_MUTANT == 11
+    double r = floor(q);         /* planted mistake: truncation */
+#else
+    double r = nearbyint(q);     /* default rounding mode: ties to even */
+#endif
+    double rounded = ldexp(r, e - 7);
+    float f = (float)rounded;    /* exact: rounded has <= 8 significant bits */
+    if (rounded > 3.3895313892515355e38) f = INFINITY;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t bits = (uint16_t)(u >> 16);
+    if (signbit(v)) bits |= 0x8000;
+    return bits;
+}
+
+static double rb(double v) { return oracle_bf16_to_double(oracle_round_bf16(v)); }
+
+/* ------------------------------------------------------------ routing -- */
+
+/* Router logits z[t][e] = sum_h x[t][h] * Wr[h][e] (+ bias[e]), fp64.
+ * bias may be NULL. */
+void oracle_router_logits(const uint16_t* x, int64_t T, int64_t H,
+                          const uint16_t* wr, int64_t E, const float* bias,
+                          double* z) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t e = 0; e < E; ++e) {
+            double s = 0.0;
+            for (int64_t h = 0; h < H; ++h)
+                s += oracle_bf16_to_double(x[t * H + h]) * oracle_bf16_to_double(wr[e * H + h]);
+            if (bias) {
+#if ORACLE_MUTANT == 10
+                s -= (double)bias[e];  /* planted mistake: bias sign */
+#else
+                s += (double)bias[e];
+#endif
+            }
+            z[t * E + e] = s;
+        }
+    }
+}
+
+/* Top-k selection and renormalised weights for each token.
+ *
+ * The choice of experts is an integer decision taken on floating point: it is
+ * made on the logits rounded to binary32 (the precision a GPU router computes
+ * its logits in) when decide_fp32 != 0, else on the fp64 logits.  Softmax is
+ * monotone, so the k largest probabilities are the k largest logits.  Equal
+ * values go to the lower expert id.  The chosen set is listed in ascending
+ * expert id (slot j of token t is ids[t*k + j]).
+ *
+ * The weights are computed in fp64 from the fp64 logits: p = softmax(z) over
+ * all E experts, then w_j = p_{e_j} / sum over the chosen set of p. */
+void oracle_topk(const double* z, int64_t T, int64_t E, int64_t k, int decide_fp32,
+                 int32_t* ids, double* w) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const double* zt = z + t * E;
+        char* taken = (char*)calloc((size_t)E, 1);
+        for (int64_t j = 0; j < k; ++j) {
+            int64_t best = -1;
+            double bv = 0.0;
+            for (int64_t e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                double v = decide_fp32 ? (double)(float)zt[e] : zt[e];
+#if ORACLE_MUTANT == 4
+                if (best < 0 || v >= bv) { best = e; bv = v; }  /* planted: ties to higher id */
+#else
+                if (best < 0 || v > bv) { best = e; bv = v; }
+#endif
+            }
+            if (best < 0) break;  /* k > E: rejected by the caller */
+            taken[best] = 1;
+        }
+        /* list the chosen set in ascending id */
+        int64_t j = 0;
+#if ORACLE_MUTANT == 12
+        for (int64_t e = E - 1; e >= 0; --e)  /* planted: descending id */
+#else
+        for (int64_t e = 0; e < E; ++e)
+#endif
+            if (taken[e]) ids[t * k + (j++)] = (int32_t)e;
+        free(taken);
+
+        double zmax = zt[0];
+        for (int64_t e = 1; e < E; ++e) if (zt[e] > zmax) zmax = zt[e];
+        double denom = 0.0;
+        for (int64_t e = 0; e < E; ++e) denom += exp(zt[e] - zmax);
+        double psel = 0.0;
+        for (int64_t jj = 0; jj < k; ++jj) psel += exp(zt[ids[t * k + jj]] - zmax) / denom;
+        for (int64_t jj = 0; jj < k; ++jj) {
+            double p = exp(zt[ids[t * k + jj]] - zmax) / denom;
+#if ORACLE_MUTANT == 6
+            w[t * k + jj] = p;  /* planted: no renormalisation */
+#else
+            w[t * k + jj] = p / psel;
+#endif
+        }
+    }
+}
+
+/* Group the T*k (token, slot) pairs by expert.
+ *   counts[e]   = number of pairs routed to e
+ *   offsets     = exclusive scan of counts (E+1 entries; offsets[E] = T*k)
+ *   perm[r]     = flat index f = t*k + j of the pair at grouped row r
+ *   inv[f]      = grouped row of pair f
+ * Within an expert's rows, pairs keep ascending flat index (a stable counting
+ * sort).  This ordering is this build's convention: the pages do not fix one. */
+void oracle_group(const int32_t* ids, int64_t T, int64_t E, int64_t k,
+                  int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv) {
+    int64_t n = T * k;
+    for (int64_t e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t f = 0; f < n; ++f) counts[ids[f]] += 1;
+    offsets[0] = 0;
+#if ORACLE_MUTANT == 8
+    for (int64_t e = 0; e < E; ++e) offsets[e] = (e ? offsets[e - 1] : 0) + counts[e];  /* planted: inclusive */
+    offsets[E] = (int32_t)n;
+#else
+    for (int64_t e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+#endif
+    int32_t* fill = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+#if ORACLE_MUTANT == 7
+    for (int64_t f = n - 1; f >= 0; --f) {  /* planted: reversed order in a group */
+#else
+    for (int64_t f = 0; f < n; ++f) {
+#endif
+        int32_t e = ids[f];
+        int32_t r = offsets[e] + fill[e];
+        fill[e] += 1;
+        if (r < 0 || r >= n) { inv[f] = -1; continue; }  /* only a broken scan gets here */
+        perm[r] = (int32_t)f;
+        inv[f] = r;
+    }
+    free(fill);
+}
+
+/* ---------------------------------------------------------------- FFN -- */
+
+/* One expert on one token: g = x W_gate, u = x W_up, a = SiLU(g) * u,
+ * y = a W_down, with SiLU(g) = g / (1 + exp(-g)).  fp64 sums; in mirrored
+ * mode a and y are rounded to bf16.  a_tmp holds I doubles. */
+static void expert_ffn(const uint16_t* xrow, int64_t H, int64_t I,
+                       const uint16_t* w13, const uint16_t* w2, int mirrored,
+                       double* a_tmp, double* y) {
+    for (int64_t i = 0; i < I; ++i) {
+        const uint16_t* wg = w13 + i * H;
+        const uint16_t* wu = w13 + (I + i) * H;
+        double g = 0.0, u = 0.0;
+        for (int64_t h = 0; h < H; ++h) {
+            double xv = oracle_bf16_to_double(xrow[h]);
+            g += xv * oracle_bf16_to_double(wg[h]);
+            u += xv * oracle_bf16_to_double(wu[h]);
+        }
+#if ORACLE_MUTANT == 1
+        double a = g / (1.0 + exp(-g));            /* planted: up projection dropped */
+#elif ORACLE_MUTANT == 2
+        double a = g / (1.0 + exp(g)) * u;         /* planted: sign inside SiLU */
+#elif ORACLE_MUTANT == 3
+        double a = u / (1.0 + exp(-u)) * g;        /* planted: gate and up swapped */
+#else
+        double a = g / (1.0 + exp(-g)) * u;
+#endif
+        a_tmp[i] = mirrored ? rb(a) : a;
+    }
+    for (int64_t h = 0; h < H; ++h) {
+        const uint16_t* wd = w2 + h * I;
+        double s = 0.0;
+        for (int64_t i = 0; i < I; ++i) s += a_tmp[i] * oracle_bf16_to_double(wd[i]);
+        y[h] = mirrored ? rb(s) : s;
+    }
+}
+
+/* Public single-expert entry (used by the pins). */
+void oracle_expert_ffn(const uint16_t* xrow, int64_t H, int64_t I,
+                       const uint16_t* w13, const uint16_t* w2, int mirrored, double* y) {
+    double* a = (double*)malloc((size_t)I * sizeof(double));
+    expert_ffn(xrow, H, I, w13, w2, mirrored, a, y);
+    free(a);
+}
+
+/* The MoE output for n_sel tokens (rows tok[0..n_sel-1] of x), given their
+ * routing (ids/w, k slots per token, indexed by token) and per-expert weight
+ * pointers:
+ *     out[s][:] = sum_j w[t][j] * y_{ids[t][j]}(x_t) + y_shared(x_t)
+ * summed in fp64 in slot order, then the shared expert; rounded to bf16 in
+ * mirrored mode.  expert_w13[e] / expert_w2[e] point at expert e's weights
+ * wherever they live (the placement map resolved by the caller);
+ * shared_w13 may be NULL (no shared expert). */
+void oracle_moe_tokens(const uint16_t* x, int64_t H, int64_t I, int64_t k,
+                       const int64_t* tok, int64_t n_sel,
+                       const int32_t* ids, const double* w,
+                       const uint16_t* const* expert_w13, const uint16_t* const* expert_w2,
+                       const uint16_t* shared_w13, const uint16_t* shared_w2,
+                       int mirrored, double* out) {
+#pragma omp parallel
+    {
+        double* a = (double*)malloc((size_t)I * sizeof(double));
+        double* y = (double*)malloc((size_t)H * sizeof(double));
+        double* acc = (double*)malloc((size_t)H * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t s = 0; s < n_sel; ++s) {
+            int64_t t = tok[s];
+            const uint16_t* xr = x + t * H;
+            for (int64_t h = 0; h < H; ++h) acc[h] = 0.0;
+            for (int64_t j = 0; j < k; ++j) {
+                int32_t e = ids[t * k + j];
+#if ORACLE_MUTANT == 9
+                double wj = w[t * k + (j + 1) % k];  /* planted: wrong slot weight */
+#else
+                double wj = w[t * k + j];
+#endif
+                expert_ffn(xr, H, I, expert_w13[e], expert_w2[e], mirrored, a, y);
+                for (int64_t h = 0; h < H; ++h) acc[h] += wj * y[h];
+            }
+#if ORACLE_MUTANT != 5
+            if (shared_w13) {
+                expert_ffn(xr, H, I, shared_w13, shared_w2, mirrored, a, y);
+                for (int64_t h = 0; h < H; ++h) acc[h] += y[h];
+            }
+#endif
+            for (int64_t h = 0; h < H; ++h) out[s * H + h] = mirrored ? rb(acc[h]) : acc[h];
+        }
+        free(a);
+        free(y);
+        free(acc);
+    }
+}
+
+/* Threads the OpenMP runtime will use (1 without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

@@ -1,0 +1,334 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each ``pin_*`` takes an ``oracle.Oracle`` and raises AssertionError when the
+oracle disagrees with what the mathematics fixes: brute force on tiny inputs,
+closed forms, invariants, special cases that reduce to a textbook or library
+routine.  ``test_oracle_pins.py`` runs them against the oracle;
+``test_oracle_mutants.py`` runs them against builds of the oracle with one
+planted mistake each and checks that some pin fails.
+
+Independent routines used here: numpy / torch fp64 matmuls, torch's own bf16
+conversion, scipy's softmax, ``math.fsum`` and ``itertools.combinations``.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import scipy.special
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ---------------------------------------------------------------- helpers --
+def _bits_from_f32(a: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of fp32 values, by torch's conversion (RNE)."""
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _decode(bits: np.ndarray) -> np.ndarray:
+    """fp64 values of bf16 bit patterns, by torch's conversion."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    return t.to(torch.float64).numpy()
+
+
+def _rand_bits(rng, shape, std):
+    return _bits_from_f32(rng.standard_normal(shape).astype(np.float32) * np.float32(std))
+
+
+def _silu(v):
+    return v / (1.0 + np.exp(-v))
+
+
+def _dense_moe(x, wr, bias, k, w13s, w2s, sw13, sw2, orc_ids, orc_w):
+    """Dense brute force: out[t] = sum_e G[t, e] FFN_e(x_t) (+ shared), where
+    G is the dense T x E gate matrix (zero outside the chosen set), and FFN_e
+    is evaluated for EVERY expert on EVERY token with numpy fp64 matmuls."""
+    X = _decode(x)
+    T = X.shape[0]
+    E = len(w13s)
+    G = np.zeros((T, E))
+    for t in range(T):
+        for j in range(k):
+            G[t, orc_ids[t, j]] += orc_w[t, j]
+    out = np.zeros_like(X)
+    for e in range(E):
+        W13 = _decode(w13s[e])
+        I = W13.shape[0] // 2
+        Wg, Wu = W13[:I].T, W13[I:].T          # [H, I]
+        Wd = _decode(w2s[e]).T                 # [I, H]
+        Y = (_silu(X @ Wg) * (X @ Wu)) @ Wd
+        out += G[:, e:e + 1] * Y
+    if sw13 is not None:
+        W13 = _decode(sw13)
+        I = W13.shape[0] // 2
+        out += (_silu(X @ W13[:I].T) * (X @ W13[I:].T)) @ _decode(sw2).T
+    return out
+
+
+def _random_layer(rng, T, H, I, E, k, S, wstd=0.1):
+    x = _rand_bits(rng, (T, H), 1.0)
+    wr = _rand_bits(rng, (E, H), 0.3)
+    w13s = [_rand_bits(rng, (2 * I, H), wstd) for _ in range(E)]
+    w2s = [_rand_bits(rng, (H, I), wstd) for _ in range(E)]
+    sw13 = _rand_bits(rng, (2 * I, H), wstd) if S else None
+    sw2 = _rand_bits(rng, (H, I), wstd) if S else None
+    return x, wr, w13s, w2s, sw13, sw2
+
+
+# ------------------------------------------------------------------- bf16 --
+def pin_bf16(o):
+    rng = np.random.default_rng(1)
+    f = (rng.standard_normal(4000) * np.exp(rng.uniform(-30, 30, 4000))).astype(np.float32)
+    ref = _bits_from_f32(f)
+    got = np.array([o.round_bf16(float(v)) for v in f], dtype=np.uint16)
+    assert np.array_equal(got, ref), "round_bf16 disagrees with torch on binary32 inputs"
+    dec = np.array([o.bf16_to_double(int(b)) for b in ref])
+    assert np.array_equal(dec, _decode(ref)), "bf16 decode disagrees with torch"
+    # ties to even, and no double rounding through binary32
+    assert o.round_bf16(1.0 + 2.0 ** -8) == 0x3F80            # tie -> even (1.0)
+    assert o.round_bf16(1.0 + 3 * 2.0 ** -8) == 0x3F82        # tie -> even (1 + 2^-6)
+    assert o.round_bf16(1.0 + 2.0 ** -8 + 2.0 ** -40) == 0x3F81  # just above the tie
+    assert o.round_bf16(-(1.0 + 2.0 ** -8 + 2.0 ** -40)) == 0xBF81
+    assert o.round_bf16(2.0 ** -133) == 0x0001                # smallest subnormal
+    assert o.round_bf16(1e39) == 0x7F80                       # overflow -> inf
+
+
+# ---------------------------------------------------------------- routing --
+def pin_router_logits(o):
+    rng = np.random.default_rng(2)
+    T, H, E = 40, 96, 7
+    x = _rand_bits(rng, (T, H), 1.0)
+    wr = _rand_bits(rng, (E, H), 0.1)
+    bias = rng.standard_normal(E).astype(np.float32)
+    z = o.router_logits(x, wr, bias)
+    ref = _decode(x) @ _decode(wr).T + bias.astype(np.float64)[None, :]
+    assert np.allclose(z, ref, rtol=0, atol=1e-12), "router logits != x @ Wr + b"
+    z0 = o.router_logits(x, wr, None)
+    assert np.allclose(z0, _decode(x) @ _decode(wr).T, rtol=0, atol=1e-12)
+
+
+def _bruteforce_topk(zrow32, k):
+    """All k-subsets; the winner maximises the (correctly rounded) sum of p,
+    ties to the lexicographically smallest id tuple."""
+    p = np.exp(zrow32 - zrow32.max())
+    best, best_key = None, None
+    for sub in itertools.combinations(range(len(zrow32)), k):
+        s = math.fsum(p[list(sub)])
+        key = (-s, sub)
+        if best_key is None or key < best_key:
+            best, best_key = sub, key
+    return list(best)
+
+
+def pin_topk_bruteforce(o):
+    rng = np.random.default_rng(3)
+    for (T, E, k) in [(64, 8, 2), (30, 6, 3), (20, 5, 1), (12, 7, 4)]:
+        z = rng.standard_normal((T, E))
+        z[: T // 3] = np.round(z[: T // 3] * 2) / 2      # many exact ties
+        ids, w = o.topk(z, k, decide_fp32=True)
+        z32 = z.astype(np.float32).astype(np.float64)
+        for t in range(T):
+            assert list(ids[t]) == _bruteforce_topk(z32[t], k), f"top-{k} wrong at token {t}"
+
+
+def pin_weights(o):
+    rng = np.random.default_rng(4)
+    T, E, k = 50, 16, 4
+    z = rng.standard_normal((T, E)) * 3
+    ids, w = o.topk(z, k)
+    assert np.allclose(w.sum(1), 1.0, rtol=0, atol=1e-12), "weights do not sum to 1"
+    for t in range(T):
+        ref = scipy.special.softmax(z[t, ids[t]])        # renormalised over the chosen set
+        assert np.allclose(w[t], ref, rtol=1e-12, atol=0)
+        full = scipy.special.softmax(z[t])
+        assert np.allclose(w[t], full[ids[t]] / full[ids[t]].sum(), rtol=1e-12, atol=0)
+
+
+def pin_special_cases(o):
+    rng = np.random.default_rng(5)
+    z = rng.standard_normal((9, 6))
+    ids, w = o.topk(z, 6)                                # k = E: full softmax
+    assert (ids == np.arange(6)[None, :]).all()
+    assert np.allclose(w, scipy.special.softmax(z, axis=1), rtol=1e-12, atol=0)
+    ids, w = o.topk(rng.standard_normal((5, 1)), 1)      # E = 1
+    assert (ids == 0).all() and np.array_equal(w, np.ones((5, 1)))
+    ids, w = o.topk(np.full((4, 8), 0.25), 3)            # equal logits
+    assert (ids == np.arange(3)[None, :]).all()
+    assert np.allclose(w, 1.0 / 3.0, rtol=0, atol=1e-15)
+    z = np.array([[0.0, 5.0, 1.0, 5.0, -1.0]])           # hand example
+    ids, w = o.topk(z, 2)
+    assert list(ids[0]) == [1, 3] and np.allclose(w[0], [0.5, 0.5], atol=1e-15)
+    ids, w = o.topk(z, 3)
+    e5, e1 = math.exp(5.0), math.exp(1.0)
+    assert list(ids[0]) == [1, 2, 3]
+    assert np.allclose(w[0], [e5 / (2 * e5 + e1), e1 / (2 * e5 + e1), e5 / (2 * e5 + e1)],
+                       rtol=1e-14, atol=0)
+
+
+def pin_group(o):
+    rng = np.random.default_rng(6)
+    for (T, E, k) in [(64, 8, 2), (33, 5, 5), (1, 4, 1), (100, 13, 3)]:
+        z = rng.standard_normal((T, E))
+        ids, _ = o.topk(z, k)
+        counts, offsets, perm, inv = o.group(ids, E)
+        flat = ids.reshape(-1)
+        assert np.array_equal(counts, np.bincount(flat, minlength=E))
+        assert offsets[0] == 0 and np.array_equal(offsets[1:], np.cumsum(counts))
+        assert counts.sum() == T * k
+        assert np.array_equal(perm[inv], np.arange(T * k)), "perm o inv != id"
+        assert np.array_equal(inv[perm], np.arange(T * k)), "inv o perm != id"
+        for e in range(E):
+            rows = perm[offsets[e]:offsets[e + 1]]
+            assert (flat[rows] == e).all(), "row in the wrong expert group"
+            assert (np.diff(rows) > 0).all(), "group not in ascending flat index"
+        # permute -> unpermute round trip on x
+        x = rng.standard_normal((T, 3))
+        xp = x[perm // k]
+        back = xp[inv].reshape(T, k, 3)
+        assert np.array_equal(back, np.repeat(x[:, None, :], k, axis=1))
+
+
+# -------------------------------------------------------------------- FFN --
+def pin_ffn_dense(o):
+    rng = np.random.default_rng(7)
+    for (T, H, I, E, k, S) in [(24, 32, 16, 6, 3, 1), (16, 48, 8, 4, 1, 0), (10, 16, 16, 3, 3, 1)]:
+        x, wr, w13s, w2s, sw13, sw2 = _random_layer(rng, T, H, I, E, k, S)
+        r = o.route(x, wr, None, k)
+        out = o.moe_tokens(x, np.arange(T), r["ids"], r["w"], w13s, w2s, sw13, sw2, mirrored=False)
+        ref = _dense_moe(x, wr, None, k, w13s, w2s, sw13, sw2, r["ids"], r["w"])
+        scale = np.sqrt((ref ** 2).mean())
+        assert np.max(np.abs(out - ref)) <= 1e-12 * max(1.0, scale), "MoE != dense brute force"
+
+
+def pin_swiglu_textbook(o):
+    """E = k = 1, no shared expert: the layer is one SwiGLU MLP."""
+    rng = np.random.default_rng(8)
+    T, H, I = 12, 40, 24
+    x, wr, w13s, w2s, _, _ = _random_layer(rng, T, H, I, 1, 1, 0)
+    r = o.route(x, wr, None, 1)
+    out = o.moe_tokens(x, np.arange(T), r["ids"], r["w"], w13s, w2s, mirrored=False)
+    X = torch.from_numpy(_decode(x))
+    W13 = torch.from_numpy(_decode(w13s[0]))
+    Wd = torch.from_numpy(_decode(w2s[0]))
+    lin_g = torch.nn.functional.linear(X, W13[:I])       # x W_gate
+    lin_u = torch.nn.functional.linear(X, W13[I:])       # x W_up
+    ref = torch.nn.functional.linear(torch.nn.functional.silu(lin_g) * lin_u, Wd).numpy()
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12), "not the textbook SwiGLU MLP"
+
+
+def pin_linearity_and_zero(o):
+    rng = np.random.default_rng(9)
+    T, H, I, E, k = 8, 32, 16, 4, 2
+    x, wr, w13s, w2s, sw13, sw2 = _random_layer(rng, T, H, I, E, k, 1)
+    r = o.route(x, wr, None, k)
+    tok = np.arange(T)
+    for mirrored in (False, True):
+        base = o.moe_tokens(x, tok, r["ids"], r["w"], w13s, w2s, sw13, sw2, mirrored=mirrored)
+        dbl = lambda b: _bits_from_f32(_decode(b).astype(np.float32) * 2)  # exact in bf16
+        out2 = o.moe_tokens(x, tok, r["ids"], r["w"], w13s, [dbl(b) for b in w2s], sw13, dbl(sw2),
+                            mirrored=mirrored)
+        assert np.array_equal(out2, 2 * base), "not linear in W_down"
+    zeros13 = [np.zeros_like(b) for b in w13s]
+    out0 = o.moe_tokens(x, tok, r["ids"], r["w"], zeros13, w2s, np.zeros_like(sw13), sw2)
+    assert not out0.any(), "zero weights must give zero output"
+
+
+def pin_mirrored(o):
+    """Mirrored outputs are bf16 values and sit within bf16 rounding of the
+    strict ones; each expert's mirrored output equals the strict computation
+    with a and y rounded (checked through a one-expert layer)."""
+    rng = np.random.default_rng(10)
+    T, H, I, E, k = 16, 64, 32, 5, 2
+    x, wr, w13s, w2s, sw13, sw2 = _random_layer(rng, T, H, I, E, k, 1)
+    r = o.route(x, wr, None, k)
+    tok = np.arange(T)
+    m = o.moe_tokens(x, tok, r["ids"], r["w"], w13s, w2s, sw13, sw2, mirrored=True)
+    s = o.moe_tokens(x, tok, r["ids"], r["w"], w13s, w2s, sw13, sw2, mirrored=False)
+    assert np.array_equal(_decode(_bits_from_f32(m.astype(np.float32))), m)
+    rms = np.sqrt((s ** 2).mean())
+    assert np.max(np.abs(m - s)) <= 0.03 * rms
+    # one expert, by hand with torch fp64 and torch's bf16 rounding
+    X = _decode(x)
+    W13 = _decode(w13s[0])
+    Wd = _decode(w2s[0])
+    for t in range(3):
+        a = _silu(X[t] @ W13[:I].T) * (X[t] @ W13[I:].T)
+        a = torch.from_numpy(a).to(torch.bfloat16).to(torch.float64).numpy()
+        y = a @ Wd.T
+        got = o.expert_ffn(x[t], w13s[0], w2s[0], mirrored=True)
+        # y is rounded from fp64 by the oracle, from fp64 via torch here:
+        # torch may round twice (fp64 -> fp32 -> bf16), so allow one ulp
+        yb = torch.from_numpy(y).to(torch.bfloat16).to(torch.float64).numpy()
+        ulp = np.abs(yb) * 2.0 ** -7 + 1e-30
+        assert (np.abs(got - yb) <= ulp).all()
+
+
+def pin_map_invariance(o):
+    """DWDP §2: where an expert lives does not change the layer's output."""
+    import oracle as _o
+    rng = np.random.default_rng(11)
+    T, H, I, E, k = 12, 32, 16, 8, 3
+    x, wr, w13s, w2s, sw13, sw2 = _random_layer(rng, T, H, I, E, k, 1)
+    r = o.route(x, wr, None, k)
+    ref = o.moe_tokens(x, np.arange(T), r["ids"], r["w"], w13s, w2s, sw13, sw2)
+    for trial in range(4):
+        n_local = int(rng.integers(0, E + 1))
+        order = rng.permutation(E)
+        local = order[:n_local]
+        n_peers = int(rng.integers(1, 4))
+        lpool = (np.zeros((E, 2 * I, H), np.uint16), np.zeros((E, H, I), np.uint16))
+        ppools = [(np.zeros((E, 2 * I, H), np.uint16), np.zeros((E, H, I), np.uint16))
+                  for _ in range(n_peers)]
+        ls = np.full(E, -1, np.int32)
+        pid = np.full(E, -1, np.int32)
+        ps = np.full(E, -1, np.int32)
+        slots = rng.permutation(E)
+        for i, e in enumerate(local):
+            ls[e] = slots[i]
+            lpool[0][slots[i]] = w13s[e]
+            lpool[1][slots[i]] = w2s[e]
+        for e in range(E):
+            if ls[e] < 0 or rng.random() < 0.3:      # remote, or redundant copy
+                p = int(rng.integers(0, n_peers))
+                pid[e], ps[e] = p, int(rng.integers(0, E))
+                while ppools[p][0][ps[e]].any():
+                    ps[e] = (ps[e] + 1) % E
+                ppools[p][0][ps[e]] = w13s[e]
+                ppools[p][1][ps[e]] = w2s[e]
+        r13, r2 = _o.resolve_experts(E, lpool, ppools, ls, pid, ps)
+        got = o.moe_tokens(x, np.arange(T), r["ids"], r["w"], r13, r2, sw13, sw2)
+        assert np.array_equal(got, ref), "output depends on placement"
+
+
+def pin_closed_form_golden(o):
+    """The hand-worked layer in golden/tiny_closed_form.json: every expected
+    value is a closed form in sigma(v) = 1/(1+exp(-v))."""
+    with open(os.path.join(GOLDEN, "tiny_closed_form.json")) as f:
+        g = json.load(f)
+    bits = lambda a: _bits_from_f32(np.array(a, dtype=np.float32))
+    x = bits(g["x"])
+    wr = bits(g["router_w"])
+    w13s = [bits(a) for a in g["w13"]]
+    w2s = [bits(a) for a in g["w2"]]
+    k = g["k"]
+    r = o.route(x, wr, None, k)
+    assert r["ids"].tolist() == g["expected_ids"]
+    env = {"sigma": lambda v: 1.0 / (1.0 + math.exp(-v)), "exp": math.exp}
+    ew = np.array([[eval(s, {}, env) for s in row] for row in g["expected_w"]])
+    assert np.allclose(r["w"], ew, rtol=1e-14, atol=0)
+    out = o.moe_tokens(x, np.arange(x.shape[0]), r["ids"], r["w"], w13s, w2s, mirrored=False)
+    eo = np.array([[eval(s, {}, env) for s in row] for row in g["expected_out"]])
+    assert np.allclose(out, eo, rtol=1e-14, atol=1e-300)
+    assert r["counts"].tolist() == g["expected_counts"]
+    assert r["perm"].tolist() == g["expected_perm"]
+
+
+ALL_PINS = [pin_bf16, pin_router_logits, pin_topk_bruteforce, pin_weights, pin_special_cases,
+            pin_group, pin_ffn_dense, pin_swiglu_textbook, pin_linearity_and_zero, pin_mirrored,
+            pin_map_invariance, pin_closed_form_golden]
