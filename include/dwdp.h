@@ -1,0 +1,246 @@
+/*
+ * dwdp.h: C ABI of libdwdp.so, the single-rank hot path of DWDP
+ * (Distributed Weight Data Parallelism) on one GB300 (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *   [DWDP] "DWDP: Distributed Weight Data Parallelism for High-Performance LLM
+ *          Inference on NVL72" (arXiv 2604.01621), as summarised on its
+ *          summary pages;
+ *   [news] the thecoregrid.dev news summary of the same paper.
+ *
+ * One rank runs one MoE block per layer.  Some experts of each layer are
+ * resident ("local"); the others live on peers and are pulled into one of two
+ * staging buffers by asynchronous copies while the previous layer computes
+ * ([DWDP] §2 Methodology Overview).  The grouped GEMM reads each expert from
+ * whichever buffer holds it through a per-expert table, with no merge copy
+ * ([DWDP] §4.2).  Copies are cut into fixed-size slices issued round-robin
+ * over the sources ([DWDP] §4.3.2; [news]).  On one GPU the peers are emulated
+ * by separate device-memory pools.
+ *
+ * Conventions for every call:
+ *   - bf16 tensors are raw 16-bit IEEE bfloat16; every matrix is row-major
+ *     with no padding between rows.
+ *   - "device" pointers point into the current CUDA device's global memory
+ *     and must be 16-byte aligned; the caller owns every buffer it passes and
+ *     keeps it alive until the work enqueued on it has finished.
+ *   - The context owns its CUDA events, tensor-map descriptors, its small
+ *     device tables and error word, and the copy plans.  Use one context from
+ *     one host thread at a time.
+ *   - Every call validates its arguments on the host first.  A negative
+ *     return means nothing was enqueued; dwdp_last_error() says why.
+ *     Asynchronous CUDA faults surface as DWDP_ERR_CUDA from a later call.
+ *   - Kernels never trap.  A bounded wait inside a kernel that runs out sets
+ *     the context's device error word and returns; dwdp_device_status()
+ *     reports it as DWDP_ERR_DEVICE_CHECK.
+ *
+ * Weight layouts:
+ *   w13 of one expert : [2I][H]  rows 0..I-1 = W_gate^T, rows I..2I-1 = W_up^T
+ *   w2  of one expert : [H][I]   = W_down^T
+ *   a pool            : w13 [n_slots][2I][H] and w2 [n_slots][H][I]
+ *   router weight     : [E][H]   row e = column e of the H x E gate matrix
+ */
+#ifndef DWDP_H_
+#define DWDP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DWDP_ABI_VERSION 1
+#define DWDP_MAX_EXPERTS 1024
+#define DWDP_MAX_TOPK 32
+#define DWDP_MAX_LAYERS 256
+#define DWDP_MAX_PEERS 64
+
+typedef struct dwdp_ctx dwdp_ctx;
+/* Same object as cudaStream_t; NULL = the legacy default stream. */
+typedef struct CUstream_st* dwdp_stream_t;
+
+typedef enum {
+    DWDP_OK = 0,
+    DWDP_ERR_INVALID_ARG = -1,  /* bad pointer, size, index or alignment */
+    DWDP_ERR_NOT_MAPPED = -2,   /* layer has no expert map, or stage holds another layer */
+    DWDP_ERR_CUDA = -3,         /* a CUDA runtime call failed */
+    DWDP_ERR_TIMEOUT = -4,      /* dwdp_wait_stage ran out of time */
+    DWDP_ERR_UNSUPPORTED = -5,  /* shape outside what the kernels handle */
+    DWDP_ERR_DEVICE_CHECK = -6  /* a kernel reported a failed check or wait */
+} dwdp_status;
+
+typedef struct {
+    int32_t hidden;       /* H: multiple of 64 */
+    int32_t inter;        /* I: expert intermediate size, multiple of 64 */
+    int32_t n_experts;    /* E: routed experts, 1..DWDP_MAX_EXPERTS */
+    int32_t top_k;        /* k: 1..min(E, DWDP_MAX_TOPK) */
+    int32_t n_shared;     /* always-on shared experts: 0 or 1 */
+    int32_t max_tokens;   /* largest T any call will pass */
+    int32_t n_layers;     /* layers that get an expert map: 1..DWDP_MAX_LAYERS */
+    int32_t stage_slots;  /* experts each staging buffer holds (0 = no staging) */
+} dwdp_config;
+
+/* One buffer of experts: w13 [n_slots][2I][H], w2 [n_slots][H][I] (device). */
+typedef struct {
+    const void* w13;
+    const void* w2;
+    int32_t n_slots;
+} dwdp_pool;
+
+/* Routing results (all device pointers, written by dwdp_route).
+ *   topk_ids [T][k]  chosen experts of each token, ascending expert id
+ *   topk_w   [T][k]  their weights: softmax renormalised over the chosen k
+ *   counts   [E]     (token, slot) pairs routed to each expert
+ *   offsets  [E+1]   exclusive scan of counts; offsets[E] = T*k
+ *   perm     [T*k]   flat index t*k+j of the pair at grouped row r; within an
+ *                    expert, rows keep ascending flat index
+ *   inv_perm [T*k]   grouped row of pair t*k+j
+ *   logits   [T][E]  fp32 router logits x.Wr (+ bias); NULL = not returned */
+typedef struct {
+    int32_t* topk_ids;
+    float* topk_w;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* perm;
+    int32_t* inv_perm;
+    float* logits;
+} dwdp_route_out;
+
+/* One slice of a prefetch copy plan.  tensor 0 = w13, 1 = w2; offsets are in
+ * bytes from the start of the peer pool's tensor and the stage buffer's
+ * tensor. */
+typedef struct {
+    int32_t peer;
+    int32_t tensor;
+    int64_t src_offset;
+    int64_t dst_offset;
+    int64_t nbytes;
+} dwdp_copy_slice;
+
+/* ABI version of the loaded library (DWDP_ABI_VERSION). */
+int32_t dwdp_version(void);
+
+/* Create a context on the current CUDA device.  stage_w13[s] / stage_w2[s]
+ * (s = 0, 1) are the caller's two staging buffers ([DWDP] §2: double
+ * buffering), each [stage_slots][2I][H] / [stage_slots][H][I] bf16; they may
+ * be NULL when cfg->stage_slots == 0.  On success *out owns the events and
+ * descriptors listed above.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* const stage_w2[2],
+                    dwdp_ctx** out);
+
+/* Destroy a context (waits for nothing; the caller synchronises first). */
+void dwdp_destroy(dwdp_ctx* ctx);
+
+/* Text of the last error on this context (or of the last failed
+ * dwdp_create / host helper when ctx is NULL).  Never NULL. */
+const char* dwdp_last_error(const dwdp_ctx* ctx);
+
+/* Device workspace, in bytes, that dwdp_route and dwdp_moe_layer need for T
+ * tokens (the larger of the two; both may share one buffer when they run in
+ * order on one stream). */
+size_t dwdp_workspace_bytes(const dwdp_ctx* ctx, int32_t T);
+
+/* Placement of layer `layer` ([DWDP] §2: experts partitioned across peers,
+ * placement need not be disjoint; a redundant expert is read from its local
+ * copy).  For each routed expert e:
+ *   local_slot[e] >= 0  -> resident in `local` at that slot;
+ *   otherwise peer_id[e] in [0, n_peers) and peer_slot[e] name its copy in
+ *   peers[peer_id[e]], and it is staged by dwdp_prefetch_layer.
+ * local_slot, peer_id, peer_slot are host arrays [E]; local and peers are host
+ * structs describing device buffers.  shared_w13 [2I][H] / shared_w2 [H][I]
+ * (device) are the layer's shared expert, required iff n_shared == 1.  The
+ * non-resident experts take stage slots 0, 1, ... in ascending id, at most
+ * stage_slots of them.  Replaces any earlier map of the layer (the caller
+ * makes sure no enqueued work still uses it).  Errors: INVALID_ARG, CUDA. */
+int32_t dwdp_set_expert_map(dwdp_ctx* ctx, int32_t layer, const dwdp_pool* local,
+                            const dwdp_pool* peers, int32_t n_peers, const int32_t* local_slot,
+                            const int32_t* peer_id, const int32_t* peer_slot,
+                            const void* shared_w13, const void* shared_w2);
+
+/* Top-k routing with a deterministic grouping of the (token, slot) pairs by
+ * expert.  x [T][H] bf16 and w_router [E][H] bf16 are device pointers;
+ * logit_bias [E] fp32 (device) or NULL is added to every logit before the
+ * choice.  The chosen experts are the k largest logits (softmax is
+ * monotone), ties to the lower id, decided on the fp32 logits; weights are
+ * exp(z_j - z_max) / sum over the chosen set.  ws (device, ws_bytes >=
+ * dwdp_workspace_bytes) is scratch.  Enqueued on `stream`.
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router,
+                   const float* logit_bias, const dwdp_route_out* out, void* ws, size_t ws_bytes,
+                   dwdp_stream_t stream);
+
+/* Pull layer `layer`'s non-resident experts from their peer pools into stage
+ * buffer `stage` ([DWDP] §2: asynchronous prefetch of layer l+1 during layer
+ * l, double-buffered; §4.3.2: fixed-size slices, round-robin over sources).
+ * Each slice is one cudaMemcpyAsync (copy engine) of at most chunk_bytes;
+ * slices from peer p go to copy_streams[p % n_copy_streams].  The copies wait
+ * until the last dwdp_moe_layer that read this stage has finished reading it,
+ * and completion is recorded as the stage's "ready" event.  Errors:
+ * INVALID_ARG, NOT_MAPPED, CUDA. */
+int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t chunk_bytes,
+                            dwdp_stream_t const* copy_streams, int32_t n_copy_streams);
+
+/* One MoE layer for T tokens on `stream` ([DWDP] §2 and §4.2):
+ *   xp  = x rows gathered into expert order (route->perm)
+ *   a   = SiLU(xp W_gate) * (xp W_up)          per expert, bf16
+ *   y   = a W_down                             per expert, bf16
+ *   out[t] = sum_j topk_w[t][j] y[inv_perm[t*k+j]] + y_shared[t]  (fp32 sum, bf16)
+ * Each expert's weights come from the local pool or from stage `stage`, per
+ * the layer's map; the stream first waits for that stage's "ready" event when
+ * the layer has non-resident experts (per-layer arrival, [DWDP] §2).  route
+ * holds dwdp_route's outputs for the same x.  out [T][H] bf16 (device).
+ * Errors: INVALID_ARG, NOT_MAPPED, UNSUPPORTED, CUDA. */
+int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* x, int32_t T,
+                       const dwdp_route_out* route, void* out, void* ws, size_t ws_bytes,
+                       dwdp_stream_t stream);
+
+/* Host-side bounded wait for stage `stage`'s last prefetch: returns OK when
+ * it has finished, TIMEOUT after timeout_ms (>= 0), CUDA on a fault. */
+int32_t dwdp_wait_stage(dwdp_ctx* ctx, int32_t stage, int32_t timeout_ms);
+
+/* Layer whose experts stage `stage` holds (or is being filled with), -1 if
+ * none.  Host-side bookkeeping only. */
+int32_t dwdp_stage_layer(const dwdp_ctx* ctx, int32_t stage);
+
+/* Read and clear the device error word (synchronises the device).  OK, or
+ * DEVICE_CHECK with the failing check described by dwdp_last_error. */
+int32_t dwdp_device_status(dwdp_ctx* ctx);
+
+/* Split-pointer grouped GEMM on its own ([DWDP] §4.2: one kernel over several
+ * weight buffers, no merge).  For each group g in [0, G):
+ *   rows r in [row_offsets[g], row_offsets[g+1]) of a [rows][K] bf16:
+ *   d[r][n] = sum_k a[r][k] * B_g[n][k],  B_g = slot buf_slot[2g+1] of
+ *   buffer bufs[buf_slot[2g]] (each buffer [n_slots][N_b][K] bf16).
+ * epilogue 0: d bf16 [rows][N], B_g has N rows.
+ * epilogue 1: d bf16 [rows][N] = SiLU(gate) * up with gate = rows 0..N-1 and
+ *             up = rows N..2N-1 of B_g (B_g has 2N rows).
+ * epilogue 2: d fp32 [rows][N], B_g has N rows.
+ * row_offsets is a DEVICE array [G+1] (non-decreasing, row_offsets[G] <=
+ * a_rows; rows outside [0, a_rows) are not stored and raise DEVICE_CHECK);
+ * buf_slot is a HOST array [2G]; bufs is a host array of n_bufs <= 3 buffers
+ * of which only .w13 (the base) and .n_slots are read.
+ * K and N multiples of 64 (epilogue 2: N any value >= 1).  Enqueued on
+ * `stream`; uses no workspace.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+int32_t dwdp_grouped_gemm(dwdp_ctx* ctx, int32_t epilogue, const void* a, int64_t a_rows, int32_t K,
+                          int32_t N, const int32_t* row_offsets, int32_t G, const dwdp_pool* bufs,
+                          int32_t n_bufs, const int32_t* buf_slot, void* d, dwdp_stream_t stream);
+
+/* Host-only (no GPU needed): the prefetch copy plan dwdp_prefetch_layer
+ * issues for a map ([DWDP] §4.3.2).  The non-resident experts (local_slot <
+ * 0) take stage slots in ascending id; each peer's work is its w13 copies then
+ * its w2 copies in ascending expert id, merged where contiguous in both
+ * source and destination, cut into slices of chunk_bytes (the last one
+ * short); slices are emitted round-robin over peers 0..n_peers-1.  Writes up
+ * to max_out slices to out (may be NULL when max_out == 0) and the full count
+ * to *n_out.  Errors: INVALID_ARG (bad map or a non-resident expert with no
+ * peer copy). */
+int32_t dwdp_plan_prefetch(int32_t n_experts, int32_t hidden, int32_t inter,
+                           const int32_t* local_slot, const int32_t* peer_id,
+                           const int32_t* peer_slot, int32_t n_peers, size_t chunk_bytes,
+                           dwdp_copy_slice* out, int64_t max_out, int64_t* n_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DWDP_H_ */

@@ -1,0 +1,638 @@
+// dwdp_abi.cu: the C ABI of libdwdp.so (declared in include/dwdp.h).
+//
+// Host side of the DWDP single-rank hot path: argument validation, the
+// per-layer expert map and its per-expert (buffer, slot) table, TMA tensor
+// maps, the double-buffer events, the round-robin prefetch copy plan, and the
+// launches of the kernels in gemm.cu and route.cu.  Citations ([DWDP] §n) are
+// to "DWDP: Distributed Weight Data Parallelism for High-Performance LLM
+// Inference on NVL72".
+#include <chrono>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "dwdp_internal.h"
+
+using namespace dwdp;
+
+namespace {
+
+thread_local std::string g_last_error = "";
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct LayerMap {
+    bool mapped = false;
+    dwdp_pool local{};
+    std::vector<dwdp_pool> peers;
+    std::vector<int32_t> local_slot, peer_id, peer_slot, stage_slot;
+    int n_remote = 0;
+    const void* shared_w13 = nullptr;
+    const void* shared_w2 = nullptr;
+    bool has_local_map = false;
+    CUtensorMap local13{}, local2{}, shared13{}, shared2{};
+    std::vector<int2> bsrc;  // [E + n_shared]
+    std::map<size_t, std::vector<dwdp_copy_slice>> plans;
+};
+
+}  // namespace
+
+struct dwdp_ctx {
+    dwdp_config cfg{};
+    int device = 0;
+    int n_sms = 0;
+    void* stage13[2] = {nullptr, nullptr};
+    void* stage2[2] = {nullptr, nullptr};
+    CUtensorMap stage_map13[2]{}, stage_map2[2]{};
+    cudaEvent_t ready[2] = {nullptr, nullptr};
+    cudaEvent_t freed[2] = {nullptr, nullptr};
+    std::vector<cudaEvent_t> join;
+    int stage_layer[2] = {-1, -1};
+    std::vector<LayerMap> layers;
+    int* d_err = nullptr;
+    std::string err;
+    std::unique_ptr<GemmArgs> args;
+};
+
+namespace {
+
+int32_t fail(dwdp_ctx* ctx, int32_t code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    if (ctx) ctx->err = buf;
+    g_last_error = buf;
+    return code;
+}
+
+int32_t cuda_fail(dwdp_ctx* ctx, cudaError_t e, const char* what) {
+    return fail(ctx, DWDP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define DWDP_CUDA(ctx, call)                                   \
+    do {                                                       \
+        cudaError_t e_ = (call);                               \
+        if (e_ != cudaSuccess) return cuda_fail(ctx, e_, #call); \
+    } while (0)
+
+// Rows x K bf16 matrix, row-major: a 2-D map with a [128 rows x 64 cols] box,
+// 128-byte swizzle (the canonical K-major layout the MMA descriptors expect).
+bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || rows == 0) return false;
+    cuuint64_t dims[2] = {K, rows};
+    cuuint64_t strides[1] = {K * 2};
+    cuuint32_t box[2] = {BK, BM};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A weight buffer [slots][rows][K] bf16: a 3-D map, box [1 x 128 x 64].
+bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t rows, uint64_t K) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || rows == 0 || slots == 0) return false;
+    cuuint64_t dims[3] = {K, rows, slots};
+    cuuint64_t strides[2] = {K * 2, rows * K * 2};
+    cuuint32_t box[3] = {BK, BN / 2, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct WsLayout {
+    size_t logits = 0;  // route: fp32 [T][E] when the caller does not keep logits
+    size_t xp = 0, a = 0, y = 0;  // moe: offsets
+    size_t route_bytes = 0, moe_bytes = 0;
+};
+
+WsLayout ws_layout(const dwdp_config& c, int64_t T) {
+    WsLayout L;
+    const int64_t H = c.hidden, I = c.inter, E = c.n_experts, k = c.top_k, S = c.n_shared;
+    L.logits = 0;
+    L.route_bytes = align_up((size_t)(T * E * 4), 256);
+    L.xp = 0;
+    L.a = align_up((size_t)(T * k * H * 2), 256);
+    L.y = L.a + align_up((size_t)(T * (k + S) * I * 2), 256);
+    L.moe_bytes = L.y + align_up((size_t)(T * (k + S) * H * 2), 256);
+    return L;
+}
+
+// The copy plan of [DWDP] §4.3.2 (see dwdp_plan_prefetch in dwdp.h for the
+// exact order).  Returns false on an invalid map.
+bool build_plan(int32_t E, int64_t H, int64_t I, const int32_t* local_slot, const int32_t* peer_id,
+                const int32_t* peer_slot, int32_t n_peers, size_t chunk,
+                std::vector<dwdp_copy_slice>& plan, std::string& why) {
+    plan.clear();
+    if (chunk == 0) {
+        why = "chunk_bytes must be positive";
+        return false;
+    }
+    std::vector<int64_t> sslot(E, -1);
+    int64_t r = 0;
+    for (int32_t e = 0; e < E; ++e)
+        if (local_slot[e] < 0) {
+            if (!peer_id || peer_id[e] < 0 || peer_id[e] >= n_peers || !peer_slot || peer_slot[e] < 0) {
+                why = "expert " + std::to_string(e) + " is neither resident nor on a valid peer slot";
+                return false;
+            }
+            sslot[e] = r++;
+        }
+    const int64_t bytes[2] = {2 * I * H * 2, H * I * 2};
+    std::vector<std::vector<dwdp_copy_slice>> per(n_peers > 0 ? n_peers : 0);
+    for (int32_t p = 0; p < n_peers; ++p) {
+        std::vector<dwdp_copy_slice> regions;
+        for (int t = 0; t < 2; ++t) {
+            for (int32_t e = 0; e < E; ++e) {
+                if (sslot[e] < 0 || peer_id[e] != p) continue;
+                const int64_t src = (int64_t)peer_slot[e] * bytes[t], dst = sslot[e] * bytes[t];
+                if (!regions.empty()) {
+                    dwdp_copy_slice& last = regions.back();
+                    if (last.tensor == t && last.src_offset + last.nbytes == src &&
+                        last.dst_offset + last.nbytes == dst) {
+                        last.nbytes += bytes[t];
+                        continue;
+                    }
+                }
+                regions.push_back(dwdp_copy_slice{p, t, src, dst, bytes[t]});
+            }
+        }
+        for (const dwdp_copy_slice& reg : regions) {
+            for (int64_t done = 0; done < reg.nbytes;) {
+                const int64_t n = std::min<int64_t>((int64_t)chunk, reg.nbytes - done);
+                per[p].push_back(dwdp_copy_slice{p, reg.tensor, reg.src_offset + done, reg.dst_offset + done, n});
+                done += n;
+            }
+        }
+    }
+    for (size_t c = 0;; ++c) {
+        bool any = false;
+        for (int32_t p = 0; p < n_peers; ++p)
+            if (c < per[p].size()) {
+                plan.push_back(per[p][c]);
+                any = true;
+            }
+        if (!any) break;
+    }
+    return true;
+}
+
+int32_t check_device_error_word(dwdp_ctx* ctx) {
+    int h = 0;
+    DWDP_CUDA(ctx, cudaDeviceSynchronize());
+    DWDP_CUDA(ctx, cudaMemcpy(&h, ctx->d_err, sizeof h, cudaMemcpyDeviceToHost));
+    if (h != 0) {
+        DWDP_CUDA(ctx, cudaMemset(ctx->d_err, 0, sizeof(int)));
+        return fail(ctx, DWDP_ERR_DEVICE_CHECK, "device check failed: error bits 0x%x", h);
+    }
+    return DWDP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dwdp_version(void) { return DWDP_ABI_VERSION; }
+
+const char* dwdp_last_error(const dwdp_ctx* ctx) {
+    return ctx ? ctx->err.c_str() : g_last_error.c_str();
+}
+
+int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* const stage_w2[2],
+                    dwdp_ctx** out) {
+    if (!cfg || !out) return fail(nullptr, DWDP_ERR_INVALID_ARG, "cfg and out must not be NULL");
+    *out = nullptr;
+    const dwdp_config& c = *cfg;
+    if (c.hidden <= 0 || c.inter <= 0 || c.n_experts <= 0 || c.top_k <= 0 || c.max_tokens < 0 ||
+        c.n_layers <= 0 || c.stage_slots < 0 || c.n_shared < 0)
+        return fail(nullptr, DWDP_ERR_INVALID_ARG, "config has a non-positive size");
+    if (c.hidden % 64 || c.inter % 64)
+        return fail(nullptr, DWDP_ERR_UNSUPPORTED, "hidden and inter must be multiples of 64");
+    if (c.n_experts > DWDP_MAX_EXPERTS || c.top_k > DWDP_MAX_TOPK || c.top_k > c.n_experts ||
+        c.n_shared > 1 || c.n_layers > DWDP_MAX_LAYERS)
+        return fail(nullptr, DWDP_ERR_UNSUPPORTED, "E <= %d, k <= min(E, %d), n_shared <= 1, layers <= %d",
+                    DWDP_MAX_EXPERTS, DWDP_MAX_TOPK, DWDP_MAX_LAYERS);
+    if ((int64_t)c.max_tokens * (c.top_k + c.n_shared) >= (int64_t)1 << 31)
+        return fail(nullptr, DWDP_ERR_UNSUPPORTED, "max_tokens * (k + n_shared) must stay below 2^31");
+    if (c.stage_slots > 0) {
+        for (int s = 0; s < 2; ++s)
+            if (!stage_w13 || !stage_w2 || !stage_w13[s] || !stage_w2[s] || !aligned16(stage_w13[s]) ||
+                !aligned16(stage_w2[s]))
+                return fail(nullptr, DWDP_ERR_INVALID_ARG, "stage buffers must be non-NULL, 16-byte aligned");
+    }
+    std::unique_ptr<dwdp_ctx> ctx(new dwdp_ctx());
+    ctx->cfg = c;
+    ctx->args.reset(new GemmArgs());
+    cudaError_t e = cudaGetDevice(&ctx->device);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDevice");
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, ctx->device);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDeviceProperties");
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(nullptr, DWDP_ERR_UNSUPPORTED, "libdwdp is built for sm_103a; device is sm_%d%d",
+                    prop.major, prop.minor);
+    ctx->n_sms = prop.multiProcessorCount;
+    if (!encode_fn()) return fail(nullptr, DWDP_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+    for (int s = 0; s < 2; ++s) {
+        e = cudaEventCreateWithFlags(&ctx->ready[s], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->freed[s], cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaEventCreate");
+    }
+    ctx->join.resize(DWDP_MAX_PEERS, nullptr);
+    for (auto& ev : ctx->join) {
+        e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+        if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaEventCreate");
+    }
+    e = cudaMalloc(&ctx->d_err, 256);
+    if (e == cudaSuccess) e = cudaMemset(ctx->d_err, 0, 256);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "error word");
+    if (c.stage_slots > 0) {
+        for (int s = 0; s < 2; ++s) {
+            ctx->stage13[s] = stage_w13[s];
+            ctx->stage2[s] = stage_w2[s];
+            if (!encode_slots(&ctx->stage_map13[s], stage_w13[s], c.stage_slots, 2ull * c.inter, c.hidden) ||
+                !encode_slots(&ctx->stage_map2[s], stage_w2[s], c.stage_slots, c.hidden, c.inter))
+                return fail(nullptr, DWDP_ERR_CUDA, "tensor map for a stage buffer");
+        }
+    }
+    ctx->layers.resize(c.n_layers);
+    ctx->err = "";
+    *out = ctx.release();
+    return DWDP_OK;
+}
+
+void dwdp_destroy(dwdp_ctx* ctx) {
+    if (!ctx) return;
+    for (int s = 0; s < 2; ++s) {
+        if (ctx->ready[s]) cudaEventDestroy(ctx->ready[s]);
+        if (ctx->freed[s]) cudaEventDestroy(ctx->freed[s]);
+    }
+    for (auto ev : ctx->join)
+        if (ev) cudaEventDestroy(ev);
+    if (ctx->d_err) cudaFree(ctx->d_err);
+    delete ctx;
+}
+
+size_t dwdp_workspace_bytes(const dwdp_ctx* ctx, int32_t T) {
+    if (!ctx || T < 0) return 0;
+    const WsLayout L = ws_layout(ctx->cfg, T);
+    return std::max(L.route_bytes, L.moe_bytes);
+}
+
+int32_t dwdp_set_expert_map(dwdp_ctx* ctx, int32_t layer, const dwdp_pool* local, const dwdp_pool* peers,
+                            int32_t n_peers, const int32_t* local_slot, const int32_t* peer_id,
+                            const int32_t* peer_slot, const void* shared_w13, const void* shared_w2) {
+    if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
+    const dwdp_config& c = ctx->cfg;
+    if (layer < 0 || layer >= c.n_layers) return fail(ctx, DWDP_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (!local_slot) return fail(ctx, DWDP_ERR_INVALID_ARG, "local_slot must not be NULL");
+    if (n_peers < 0 || n_peers > DWDP_MAX_PEERS || (n_peers > 0 && (!peers || !peer_id || !peer_slot)))
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "bad peer arguments");
+    const int E = c.n_experts;
+    bool any_local = false;
+    for (int e = 0; e < E; ++e) {
+        if (local_slot[e] >= 0) {
+            any_local = true;
+            if (!local || local_slot[e] >= local->n_slots)
+                return fail(ctx, DWDP_ERR_INVALID_ARG, "expert %d: local slot %d outside the local pool", e,
+                            local_slot[e]);
+        } else {
+            if (n_peers == 0 || peer_id[e] < 0 || peer_id[e] >= n_peers)
+                return fail(ctx, DWDP_ERR_INVALID_ARG, "expert %d has no copy (not local, no valid peer)", e);
+            if (peer_slot[e] < 0 || peer_slot[e] >= peers[peer_id[e]].n_slots)
+                return fail(ctx, DWDP_ERR_INVALID_ARG, "expert %d: peer slot %d outside peer %d's pool", e,
+                            peer_slot[e], peer_id[e]);
+            const dwdp_pool& pp = peers[peer_id[e]];
+            if (!pp.w13 || !pp.w2 || !aligned16(pp.w13) || !aligned16(pp.w2))
+                return fail(ctx, DWDP_ERR_INVALID_ARG, "peer %d pool pointers must be non-NULL, 16-byte aligned",
+                            peer_id[e]);
+        }
+    }
+    if (any_local && (!local->w13 || !local->w2 || !aligned16(local->w13) || !aligned16(local->w2)))
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "local pool pointers must be non-NULL, 16-byte aligned");
+    if (c.n_shared && (!shared_w13 || !shared_w2 || !aligned16(shared_w13) || !aligned16(shared_w2)))
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "the shared expert's weights are required");
+    LayerMap m;
+    m.local_slot.assign(local_slot, local_slot + E);
+    m.peer_id.assign(E, -1);
+    m.peer_slot.assign(E, -1);
+    if (n_peers > 0) {
+        m.peer_id.assign(peer_id, peer_id + E);
+        m.peer_slot.assign(peer_slot, peer_slot + E);
+        m.peers.assign(peers, peers + n_peers);
+    }
+    m.stage_slot.assign(E, -1);
+    for (int e = 0; e < E; ++e)
+        if (local_slot[e] < 0) m.stage_slot[e] = m.n_remote++;
+    if (m.n_remote > c.stage_slots)
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "%d non-resident experts exceed the %d stage slots", m.n_remote,
+                    c.stage_slots);
+    if (any_local) {
+        m.local = *local;
+        if (!encode_slots(&m.local13, local->w13, local->n_slots, 2ull * c.inter, c.hidden) ||
+            !encode_slots(&m.local2, local->w2, local->n_slots, c.hidden, c.inter))
+            return fail(ctx, DWDP_ERR_CUDA, "tensor map for the local pool");
+        m.has_local_map = true;
+    }
+    if (c.n_shared) {
+        m.shared_w13 = shared_w13;
+        m.shared_w2 = shared_w2;
+        if (!encode_slots(&m.shared13, shared_w13, 1, 2ull * c.inter, c.hidden) ||
+            !encode_slots(&m.shared2, shared_w2, 1, c.hidden, c.inter))
+            return fail(ctx, DWDP_ERR_CUDA, "tensor map for the shared expert");
+    }
+    m.bsrc.resize(E + c.n_shared);
+    for (int e = 0; e < E; ++e)
+        m.bsrc[e] = (local_slot[e] >= 0) ? make_int2(0, local_slot[e]) : make_int2(1, m.stage_slot[e]);
+    if (c.n_shared) m.bsrc[E] = make_int2(2, 0);
+    m.mapped = true;
+    ctx->layers[layer] = std::move(m);
+    for (int s = 0; s < 2; ++s)
+        if (ctx->stage_layer[s] == layer) ctx->stage_layer[s] = -1;  // staged bytes follow the old map
+    return DWDP_OK;
+}
+
+int32_t dwdp_plan_prefetch(int32_t n_experts, int32_t hidden, int32_t inter, const int32_t* local_slot,
+                           const int32_t* peer_id, const int32_t* peer_slot, int32_t n_peers,
+                           size_t chunk_bytes, dwdp_copy_slice* out, int64_t max_out, int64_t* n_out) {
+    if (n_experts <= 0 || hidden <= 0 || inter <= 0 || !local_slot || !n_out || n_peers < 0 ||
+        (max_out > 0 && !out))
+        return fail(nullptr, DWDP_ERR_INVALID_ARG, "bad arguments to dwdp_plan_prefetch");
+    std::vector<dwdp_copy_slice> plan;
+    std::string why;
+    if (!build_plan(n_experts, hidden, inter, local_slot, peer_id, peer_slot, n_peers, chunk_bytes, plan, why))
+        return fail(nullptr, DWDP_ERR_INVALID_ARG, "%s", why.c_str());
+    *n_out = (int64_t)plan.size();
+    for (int64_t i = 0; i < max_out && i < (int64_t)plan.size(); ++i) out[i] = plan[i];
+    return DWDP_OK;
+}
+
+int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router, const float* logit_bias,
+                   const dwdp_route_out* out, void* ws, size_t ws_bytes, dwdp_stream_t stream) {
+    if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
+    const dwdp_config& c = ctx->cfg;
+    if (T < 0 || T > c.max_tokens) return fail(ctx, DWDP_ERR_INVALID_ARG, "T=%d outside [0, max_tokens]", T);
+    if (!out || !out->topk_ids || !out->topk_w || !out->counts || !out->offsets || !out->perm || !out->inv_perm)
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "route outputs must not be NULL (except logits)");
+    if (!aligned16(out->topk_ids) || !aligned16(out->topk_w) || !aligned16(out->counts) ||
+        !aligned16(out->offsets) || !aligned16(out->perm) || !aligned16(out->inv_perm) ||
+        (out->logits && !aligned16(out->logits)) || (logit_bias && !aligned16(logit_bias)))
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "route pointers must be 16-byte aligned");
+    if (T == 0) {
+        DWDP_CUDA(ctx, cudaMemsetAsync(out->counts, 0, sizeof(int32_t) * c.n_experts, stream));
+        DWDP_CUDA(ctx, cudaMemsetAsync(out->offsets, 0, sizeof(int32_t) * (c.n_experts + 1), stream));
+        return DWDP_OK;
+    }
+    if (!x || !w_router || !aligned16(x) || !aligned16(w_router))
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "x and w_router must be non-NULL, 16-byte aligned");
+    const WsLayout L = ws_layout(c, T);
+    float* logits = out->logits;
+    if (!logits) {
+        if (!ws || ws_bytes < L.route_bytes || !aligned16(ws))
+            return fail(ctx, DWDP_ERR_INVALID_ARG, "workspace too small (%zu < %zu) or unaligned", ws_bytes,
+                        L.route_bytes);
+        logits = reinterpret_cast<float*>(static_cast<char*>(ws) + L.logits);
+    }
+    GemmArgs& a = *ctx->args;
+    if (!encode_rows(&a.tmA[0], x, T, c.hidden) ||
+        !encode_slots(&a.tmB[0], w_router, 1, c.n_experts, c.hidden))
+        return fail(ctx, DWDP_ERR_CUDA, "tensor map for the router GEMM");
+    a.tmA[1] = a.tmA[0];
+    a.tmB[1] = a.tmB[2] = a.tmB[0];
+    a.row_offsets = nullptr;
+    a.n_routed = 0;
+    a.shared_rows = T;
+    a.shared_a_row = 0;
+    a.shared_d_row = 0;
+    a.K = c.hidden;
+    a.N = c.n_experts;
+    a.ldd = c.n_experts;
+    a.d_rows = T;
+    a.D = logits;
+    a.col_bias = logit_bias;
+    a.err = ctx->d_err;
+    a.bsrc[0] = make_int2(0, 0);
+    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_F32, a, ctx->n_sms, stream));
+    DWDP_CUDA(ctx, launch_topk(logits, nullptr, T, c.n_experts, c.top_k, out->topk_ids, out->topk_w, stream));
+    DWDP_CUDA(ctx, launch_group(out->topk_ids, T * c.top_k, c.n_experts, out->counts, out->offsets, out->perm,
+                                out->inv_perm, stream));
+    return DWDP_OK;
+}
+
+int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t chunk_bytes,
+                            dwdp_stream_t const* copy_streams, int32_t n_copy_streams) {
+    if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
+    const dwdp_config& c = ctx->cfg;
+    if (layer < 0 || layer >= c.n_layers) return fail(ctx, DWDP_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (stage < 0 || stage > 1) return fail(ctx, DWDP_ERR_INVALID_ARG, "stage must be 0 or 1");
+    if (chunk_bytes == 0) return fail(ctx, DWDP_ERR_INVALID_ARG, "chunk_bytes must be positive");
+    if (!copy_streams || n_copy_streams < 1 || n_copy_streams > DWDP_MAX_PEERS)
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "need 1..%d copy streams", DWDP_MAX_PEERS);
+    LayerMap& m = ctx->layers[layer];
+    if (!m.mapped) return fail(ctx, DWDP_ERR_NOT_MAPPED, "layer %d has no expert map", layer);
+    auto it = m.plans.find(chunk_bytes);
+    if (it == m.plans.end()) {
+        std::vector<dwdp_copy_slice> plan;
+        std::string why;
+        if (!build_plan(c.n_experts, c.hidden, c.inter, m.local_slot.data(), m.peer_id.data(), m.peer_slot.data(),
+                        (int32_t)m.peers.size(), chunk_bytes, plan, why))
+            return fail(ctx, DWDP_ERR_INVALID_ARG, "%s", why.c_str());
+        it = m.plans.emplace(chunk_bytes, std::move(plan)).first;
+    }
+    // The stage may be overwritten only once the last layer that read it is done.
+    for (int i = 0; i < n_copy_streams; ++i) DWDP_CUDA(ctx, cudaStreamWaitEvent(copy_streams[i], ctx->freed[stage], 0));
+    char* dst_base[2] = {static_cast<char*>(ctx->stage13[stage]), static_cast<char*>(ctx->stage2[stage])};
+    for (const dwdp_copy_slice& s : it->second) {
+        const dwdp_pool& pp = m.peers[s.peer];
+        const char* src = static_cast<const char*>(s.tensor == 0 ? pp.w13 : pp.w2) + s.src_offset;
+        DWDP_CUDA(ctx, cudaMemcpyAsync(dst_base[s.tensor] + s.dst_offset, src, (size_t)s.nbytes,
+                                       cudaMemcpyDeviceToDevice, copy_streams[s.peer % n_copy_streams]));
+    }
+    for (int i = 1; i < n_copy_streams; ++i) {
+        DWDP_CUDA(ctx, cudaEventRecord(ctx->join[i], copy_streams[i]));
+        DWDP_CUDA(ctx, cudaStreamWaitEvent(copy_streams[0], ctx->join[i], 0));
+    }
+    DWDP_CUDA(ctx, cudaEventRecord(ctx->ready[stage], copy_streams[0]));
+    ctx->stage_layer[stage] = layer;
+    return DWDP_OK;
+}
+
+int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* x, int32_t T,
+                       const dwdp_route_out* route, void* out, void* ws, size_t ws_bytes, dwdp_stream_t stream) {
+    if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
+    const dwdp_config& c = ctx->cfg;
+    if (layer < 0 || layer >= c.n_layers) return fail(ctx, DWDP_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (T < 0 || T > c.max_tokens) return fail(ctx, DWDP_ERR_INVALID_ARG, "T=%d outside [0, max_tokens]", T);
+    LayerMap& m = ctx->layers[layer];
+    if (!m.mapped) return fail(ctx, DWDP_ERR_NOT_MAPPED, "layer %d has no expert map", layer);
+    if (m.n_remote > 0) {
+        if (stage < 0 || stage > 1) return fail(ctx, DWDP_ERR_INVALID_ARG, "stage must be 0 or 1");
+        if (ctx->stage_layer[stage] != layer)
+            return fail(ctx, DWDP_ERR_NOT_MAPPED, "stage %d holds layer %d, not layer %d", stage,
+                        ctx->stage_layer[stage], layer);
+    }
+    if (T == 0) return DWDP_OK;
+    if (!route || !route->topk_w || !route->offsets || !route->perm || !route->inv_perm)
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "route outputs must not be NULL");
+    if (!x || !out || !aligned16(x) || !aligned16(out) || !aligned16(route->offsets) ||
+        !aligned16(route->perm) || !aligned16(route->inv_perm) || !aligned16(route->topk_w))
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "x, out and route pointers must be non-NULL, 16-byte aligned");
+    const WsLayout L = ws_layout(c, T);
+    if (!ws || ws_bytes < L.moe_bytes || !aligned16(ws))
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "workspace too small (%zu < %zu) or unaligned", ws_bytes, L.moe_bytes);
+    const int64_t k = c.top_k, S = c.n_shared, H = c.hidden, I = c.inter, E = c.n_experts;
+    const int64_t rows_r = (int64_t)T * k, rows_all = (int64_t)T * (k + S);
+    char* w = static_cast<char*>(ws);
+    void* xp = w + L.xp;
+    void* act = w + L.a;
+    void* y = w + L.y;
+
+    if (m.n_remote > 0) DWDP_CUDA(ctx, cudaStreamWaitEvent(stream, ctx->ready[stage], 0));
+    DWDP_CUDA(ctx, launch_gather(x, (int)H, route->perm, (int)rows_r, (int)k, xp, stream));
+
+    GemmArgs& a = *ctx->args;
+    // B buffers: 0 = local pool, 1 = the stage, 2 = the shared expert.  Slots
+    // no group reads get a copy of a valid map.
+    auto set_b = [&](const CUtensorMap& local, const CUtensorMap& stg, const CUtensorMap& shared) {
+        const CUtensorMap* valid = m.has_local_map ? &local : (m.n_remote > 0 ? &stg : &shared);
+        a.tmB[0] = m.has_local_map ? local : *valid;
+        a.tmB[1] = m.n_remote > 0 ? stg : *valid;
+        a.tmB[2] = S ? shared : *valid;
+    };
+    // G1: a = SiLU(xp W_gate) * (xp W_up); the shared group reads x directly.
+    if (!encode_rows(&a.tmA[0], xp, rows_r, H) || !encode_rows(&a.tmA[1], x, T, H))
+        return fail(ctx, DWDP_ERR_CUDA, "tensor maps for the gate/up GEMM");
+    set_b(m.local13, ctx->stage_map13[m.n_remote > 0 ? stage : 0], m.shared13);
+    a.row_offsets = route->offsets;
+    a.n_routed = (int32_t)E;
+    a.shared_rows = (int32_t)(T * S);
+    a.shared_a_row = 0;
+    a.shared_d_row = (int32_t)rows_r;
+    a.K = (int32_t)H;
+    a.N = (int32_t)I;
+    a.ldd = I;
+    a.d_rows = rows_all;
+    a.D = act;
+    a.col_bias = nullptr;
+    a.err = ctx->d_err;
+    for (size_t g = 0; g < m.bsrc.size(); ++g) a.bsrc[g] = m.bsrc[g];
+    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_SILU, a, ctx->n_sms, stream));
+    // G2: y = a W_down.
+    if (!encode_rows(&a.tmA[0], act, rows_all, I)) return fail(ctx, DWDP_ERR_CUDA, "tensor map for the down GEMM");
+    a.tmA[1] = a.tmA[0];
+    set_b(m.local2, ctx->stage_map2[m.n_remote > 0 ? stage : 0], m.shared2);
+    a.shared_a_row = (int32_t)rows_r;
+    a.shared_d_row = (int32_t)rows_r;
+    a.K = (int32_t)I;
+    a.N = (int32_t)H;
+    a.ldd = H;
+    a.d_rows = rows_all;
+    a.D = y;
+    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_BF16, a, ctx->n_sms, stream));
+    // The stage's weights have been read: the next prefetch into it may start.
+    if (m.n_remote > 0) DWDP_CUDA(ctx, cudaEventRecord(ctx->freed[stage], stream));
+    DWDP_CUDA(ctx, launch_combine(y, (int)H, route->inv_perm, route->topk_w, T, (int)k, rows_r, S > 0, out, stream));
+    return DWDP_OK;
+}
+
+int32_t dwdp_wait_stage(dwdp_ctx* ctx, int32_t stage, int32_t timeout_ms) {
+    if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
+    if (stage < 0 || stage > 1 || timeout_ms < 0) return fail(ctx, DWDP_ERR_INVALID_ARG, "bad stage or timeout");
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        cudaError_t e = cudaEventQuery(ctx->ready[stage]);
+        if (e == cudaSuccess) return DWDP_OK;
+        if (e != cudaErrorNotReady) return cuda_fail(ctx, e, "cudaEventQuery");
+        const auto ms = std::chrono::duration_cast<std::chrono::milliseconds>(std::chrono::steady_clock::now() - t0).count();
+        if (ms >= timeout_ms) return fail(ctx, DWDP_ERR_TIMEOUT, "stage %d not ready after %d ms", stage, timeout_ms);
+        std::this_thread::sleep_for(std::chrono::microseconds(50));
+    }
+}
+
+int32_t dwdp_stage_layer(const dwdp_ctx* ctx, int32_t stage) {
+    if (!ctx || stage < 0 || stage > 1) return -1;
+    return ctx->stage_layer[stage];
+}
+
+int32_t dwdp_device_status(dwdp_ctx* ctx) {
+    if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
+    return check_device_error_word(ctx);
+}
+
+int32_t dwdp_grouped_gemm(dwdp_ctx* ctx, int32_t epilogue, const void* a_ptr, int64_t a_rows, int32_t K,
+                          int32_t N, const int32_t* row_offsets, int32_t G, const dwdp_pool* bufs, int32_t n_bufs,
+                          const int32_t* buf_slot, void* d, dwdp_stream_t stream) {
+    if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
+    if (epilogue < 0 || epilogue > 2) return fail(ctx, DWDP_ERR_INVALID_ARG, "epilogue must be 0, 1 or 2");
+    if (G < 1 || G > DWDP_MAX_EXPERTS) return fail(ctx, DWDP_ERR_INVALID_ARG, "G must be in [1, %d]", DWDP_MAX_EXPERTS);
+    if (K <= 0 || K % 64) return fail(ctx, DWDP_ERR_UNSUPPORTED, "K must be a positive multiple of 64");
+    if (N <= 0 || (epilogue != 2 && N % 64)) return fail(ctx, DWDP_ERR_UNSUPPORTED, "N must be a positive multiple of 64");
+    if (a_rows <= 0 || a_rows >= ((int64_t)1 << 31)) return fail(ctx, DWDP_ERR_INVALID_ARG, "a_rows out of range");
+    if (!a_ptr || !d || !row_offsets || !bufs || !buf_slot || n_bufs < 1 || n_bufs > 3 || !aligned16(a_ptr) ||
+        !aligned16(d) || !aligned16(row_offsets))
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "bad pointers or buffer count");
+    GemmArgs& a = *ctx->args;
+    const uint64_t brows = (epilogue == EPI_SILU) ? 2ull * N : (uint64_t)N;
+    for (int b = 0; b < n_bufs; ++b) {
+        if (!bufs[b].w13 || !aligned16(bufs[b].w13) || bufs[b].n_slots < 1)
+            return fail(ctx, DWDP_ERR_INVALID_ARG, "buffer %d: base must be non-NULL, aligned, n_slots >= 1", b);
+        if (!encode_slots(&a.tmB[b], bufs[b].w13, bufs[b].n_slots, brows, K))
+            return fail(ctx, DWDP_ERR_CUDA, "tensor map for buffer %d", b);
+    }
+    for (int b = n_bufs; b < 3; ++b) a.tmB[b] = a.tmB[0];
+    for (int g = 0; g < G; ++g) {
+        const int b = buf_slot[2 * g], s = buf_slot[2 * g + 1];
+        if (b < 0 || b >= n_bufs || s < 0 || s >= bufs[b].n_slots)
+            return fail(ctx, DWDP_ERR_INVALID_ARG, "group %d: (buffer %d, slot %d) out of range", g, b, s);
+        a.bsrc[g] = make_int2(b, s);
+    }
+    if (!encode_rows(&a.tmA[0], a_ptr, (uint64_t)a_rows, K)) return fail(ctx, DWDP_ERR_CUDA, "tensor map for A");
+    a.tmA[1] = a.tmA[0];
+    a.row_offsets = row_offsets;
+    a.n_routed = G;
+    a.shared_rows = 0;
+    a.shared_a_row = 0;
+    a.shared_d_row = 0;
+    a.K = K;
+    a.N = N;
+    a.ldd = N;
+    a.d_rows = a_rows;
+    a.D = d;
+    a.col_bias = nullptr;
+    a.err = ctx->d_err;
+    DWDP_CUDA(ctx, launch_grouped_gemm(epilogue, a, ctx->n_sms, stream));
+    return DWDP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,77 @@
+// dwdp_internal.h: declarations shared by the translation units of libdwdp.so.
+//
+// Kernels live in gemm.cu (split-pointer grouped GEMM, tcgen05 + TMA) and
+// route.cu (top-k, grouping, gather, combine); dwdp_abi.cu is the C ABI.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; the driver is reached through an entry point)
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dwdp.h"
+
+namespace dwdp {
+
+constexpr int kMaxGroups = DWDP_MAX_EXPERTS + 1;  // routed experts + one shared
+
+enum Epilogue : int { EPI_BF16 = 0, EPI_SILU = 1, EPI_F32 = 2 };
+
+// Tile shape of the grouped GEMM: one CTA computes a 128 x 256 fp32
+// accumulator in tensor memory from 64-wide K slices staged by TMA.
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;           // 16 KiB
+constexpr int kBBytes = BN * BK * 2;           // 32 KiB
+constexpr int kStageBytes = kABytes + kBBytes;  // 48 KiB
+constexpr int kGemmThreads = 192;              // producer, MMA, 4 epilogue warps
+
+// Bits of the device error word (kernels OR them in; never trap).
+enum DeviceError : int {
+    DERR_PRODUCER_WAIT = 1 << 0,
+    DERR_MMA_FULL_WAIT = 1 << 1,
+    DERR_MMA_TMEM_WAIT = 1 << 2,
+    DERR_EPI_WAIT = 1 << 3,
+    DERR_DRAIN_WAIT = 1 << 4,
+    DERR_MMA_DONE_WAIT = 1 << 5,
+    DERR_BAD_INDEX = 1 << 6,
+};
+
+// Everything one grouped-GEMM launch needs; passed by value (grid constant).
+// Group g < n_routed has rows [row_offsets[g], row_offsets[g+1]) of A0 and D;
+// group n_routed (present when shared_rows > 0) has rows
+// [shared_a_row, +shared_rows) of A1 and [shared_d_row, +shared_rows) of D.
+// Group g reads weight slot bsrc[g].y of buffer tmB[bsrc[g].x].
+struct GemmArgs {
+    CUtensorMap tmA[2];
+    CUtensorMap tmB[3];
+    const int32_t* row_offsets;
+    int32_t n_routed;
+    int32_t shared_rows;
+    int32_t shared_a_row;
+    int32_t shared_d_row;
+    int32_t K;
+    int32_t N;      // output columns (EPI_SILU: weight rows = 2N)
+    int64_t ldd;    // D row stride, elements
+    int64_t d_rows; // rows of D: stores at or beyond it are dropped and flagged
+    void* D;
+    const float* col_bias;  // EPI_F32: added per column, may be null
+    int* err;
+    int2 bsrc[kMaxGroups];
+};
+
+size_t gemm_smem_bytes(int n_groups);
+cudaError_t launch_grouped_gemm(int epi, const GemmArgs& args, int n_sms, cudaStream_t stream);
+
+// route.cu
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k,
+                        int32_t* ids, float* w, cudaStream_t s);
+cudaError_t launch_group(const int32_t* ids, int n, int E, int32_t* counts, int32_t* offsets,
+                         int32_t* perm, int32_t* inv, cudaStream_t s);
+cudaError_t launch_gather(const void* x, int H, const int32_t* perm, int n_rows, int k, void* xp,
+                          cudaStream_t s);
+cudaError_t launch_combine(const void* y, int H, const int32_t* inv, const float* w, int T, int k,
+                           int64_t shared_row0, bool has_shared, void* out, cudaStream_t s);
+
+}  // namespace dwdp

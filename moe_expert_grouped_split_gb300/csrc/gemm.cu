@@ -1,0 +1,515 @@
+// gemm.cu: split-pointer grouped GEMM for sm_103a (tcgen05 + TMEM + TMA).
+//
+// DWDP §4.2 (Eliminating Split-Weight Merge Overhead): the grouped GEMM of
+// the MoE block reads local experts and prefetched remote experts from their
+// own buffers instead of a contiguous merged copy.  Here each weight buffer is
+// one 3-D TMA tensor map [slots][rows][K]; the per-group table (buffer, slot)
+// picks the map and the slot coordinate, so no weight byte is ever moved to
+// feed the GEMM.
+//
+// Kernel organisation (one persistent CTA per SM, 192 threads):
+//   warp 0      TMA producer: A tile [128 x 64] + B tile [256 x 64] per stage,
+//               4-stage mbarrier ring in shared memory (128B swizzle).
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
+//               and issues tcgen05.mma (M=128, N=256, K=16) from one thread.
+//   warps 2..5  epilogue: tcgen05.ld the accumulator rows of their TMEM lane
+//               quarter, apply SiLU(gate)*up or plain conversion, store.
+// Tiles are enumerated group by group, n-tile by n-tile, m-tile fastest, and
+// dealt to CTAs round-robin: CTAs running side by side share weight tiles in
+// L2.  Every wait is bounded (global timer); a wait that runs out sets a bit
+// in the device error word and the CTA drains its copies and exits.
+#include <cuda_bf16.h>
+
+#include "dwdp_internal.h"
+
+namespace dwdp {
+namespace {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+
+// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t global_timer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on one phase of an mbarrier.  Returns false when the CTA is
+// aborting (another role gave up) or when this wait ran out of time, in which
+// case it raises the abort flag and records `code` in the error word.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err, int code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicOr(err, code);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag (used while draining).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, int* err, int code) {
+    const uint64_t t0 = global_timer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer() - t0 > kWaitLimitNs) {
+            atomicOr(err, code);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major operand tile written by TMA
+// with 128-byte swizzle: rows of 128 B, 8-row atoms 1024 B apart (stride
+// byte offset), start address >> 4 in bits 0-13, leading byte offset unused
+// for this layout (1), descriptor version 1 at bits 46-47, swizzle mode 2
+// (128 B) at bits 61-63.  The tile base is 1024-byte aligned.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31},"
+        " [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return g / (1.0f + __expf(-g)) * u;
+}
+
+// Store 32 bf16 values (64 bytes) at p (16-byte aligned).
+__device__ __forceinline__ void store_bf16x32(void* p, const float* v) {
+    uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        q[i] = make_uint4(pack_bf16(v[8 * i + 0], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
+                          pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+    }
+}
+
+struct SmemLayout {
+    // offsets from the 1024-aligned base
+    static constexpr int kA = 0;
+    static constexpr int kB = kStages * kABytes;
+    static constexpr int kBars = kB + kStages * kBBytes;  // full[S], empty[S], tfull[2], tempty[2], mdone
+    static constexpr int kNumBars = 2 * kStages + 5;
+    static constexpr int kMisc = kBars + 8 * kNumBars;    // tmem base, abort flag
+    static constexpr int kTileStart = kMisc + 16;         // int32[G+1]
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + SmemLayout::kBars;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+    const uint32_t mdone_bar = bar0 + 8u * (2 * kStages + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SmemLayout::kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::kMisc + 4);
+    int32_t* tile_start = reinterpret_cast<int32_t*>(smem + SmemLayout::kTileStart);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n_routed = p.n_routed;
+    const int G = n_routed + (p.shared_rows > 0 ? 1 : 0);
+    const int ntile_cols = (EPI == EPI_SILU) ? (BN / 2) : BN;  // output columns per tile
+    const int NT = (p.N + ntile_cols - 1) / ntile_cols;
+    const int KB = (p.K + BK - 1) / BK;
+
+    // ---- tile counts per group, then an inclusive scan into tile_start ----
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+        int rows = (g < n_routed) ? (p.row_offsets[g + 1] - p.row_offsets[g]) : p.shared_rows;
+        if (rows < 0) {
+            atomicOr(p.err, DERR_BAD_INDEX);
+            rows = 0;
+        }
+        tile_start[g + 1] = ((rows + BM - 1) / BM) * NT;
+    }
+    if (threadIdx.x == 0) {
+        tile_start[0] = 0;
+        *abort_flag = 0;
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);
+        }
+        mbar_init(mdone_bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         smem_u32(tmem_slot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_map(&p.tmA[0]);
+        prefetch_map(&p.tmA[1]);
+        prefetch_map(&p.tmB[0]);
+        prefetch_map(&p.tmB[1]);
+        prefetch_map(&p.tmB[2]);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < G; base += 32) {
+            const int i = base + lane;
+            int v = (i < G) ? tile_start[i + 1] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int t = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += t;
+            }
+            v += carry;
+            if (i < G) tile_start[i + 1] = v;
+            carry = __shfl_sync(0xffffffffu, v, 31);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int total = tile_start[G];
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ----
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int pend[kStages];
+#pragma unroll
+            for (int s = 0; s < kStages; ++s) pend[s] = -1;
+            int g = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                while (tile >= tile_start[g + 1]) ++g;
+                const int mt = (tile_start[g + 1] - tile_start[g]) / NT;
+                const int local = tile - tile_start[g];
+                const int n = local / mt, m = local % mt;
+                const bool routed = g < n_routed;
+                const CUtensorMap* ma = routed ? &p.tmA[0] : &p.tmA[1];
+                const int a_row = (routed ? p.row_offsets[g] : p.shared_a_row) + m * BM;
+                const int2 src = p.bsrc[g];
+                const CUtensorMap* mb = &p.tmB[src.x];
+                int b_row0, b_row1;
+                if (EPI == EPI_SILU) {
+                    b_row0 = n * (BN / 2);
+                    b_row1 = p.N + n * (BN / 2);
+                } else {
+                    b_row0 = n * BN;
+                    b_row1 = n * BN + BN / 2;
+                }
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err, DERR_PRODUCER_WAIT)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, kStageBytes);
+                    const uint32_t sa = sbase + SmemLayout::kA + stage * kABytes;
+                    const uint32_t sb = sbase + SmemLayout::kB + stage * kBBytes;
+                    tma_load_2d(sa, ma, kb * BK, a_row, fb);
+                    tma_load_3d(sb, mb, kb * BK, b_row0, src.y, fb);
+                    tma_load_3d(sb + kBBytes / 2, mb, kb * BK, b_row1, src.y, fb);
+                    pend[stage] = (int)phase;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // never leave a copy in flight into shared memory
+#pragma unroll
+                for (int s = 0; s < kStages; ++s)
+                    if (pend[s] >= 0) mbar_wait_drain(full_bar(s), (uint32_t)pend[s], p.err, DERR_DRAIN_WAIT);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer ------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.err, DERR_MMA_TMEM_WAIT)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err, DERR_MMA_FULL_WAIT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sw128_desc(sbase + SmemLayout::kA + stage * kABytes);
+                    const uint64_t bd = sw128_desc(sbase + SmemLayout::kB + stage * kBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        // advance 16 bf16 = 32 bytes along K inside the swizzle atom
+                        tc_mma(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk),
+                               (kb > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(empty_bar(stage));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(tfull_bar(acc));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // all issued MMAs complete before TMEM is released
+            tc_commit(mdone_bar);
+            mbar_wait_drain(mdone_bar, 0, p.err, DERR_MMA_DONE_WAIT);
+        }
+    } else {
+        // ------------------------------------------------ epilogue --------
+        const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad+32)
+        const int row_in_tile = quad * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int g = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            while (tile >= tile_start[g + 1]) ++g;
+            const int mt = (tile_start[g + 1] - tile_start[g]) / NT;
+            const int local = tile - tile_start[g];
+            const int n = local / mt, m = local % mt;
+            const bool routed = g < n_routed;
+            const int rows = routed ? (p.row_offsets[g + 1] - p.row_offsets[g]) : p.shared_rows;
+            const int64_t d_row0 = routed ? p.row_offsets[g] : p.shared_d_row;
+            const int r = m * BM + row_in_tile;
+            const int64_t grow = d_row0 + r;
+            bool valid = r < rows;
+            if (valid && (grow < 0 || grow >= p.d_rows)) {
+                atomicOr(p.err, DERR_BAD_INDEX);
+                valid = false;
+            }
+
+            // the decision must be warp-uniform: tcgen05.ld below is .sync.aligned
+            const bool got = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.err, DERR_EPI_WAIT);
+            if (!__all_sync(0xffffffffu, got)) break;
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
+
+            if (EPI == EPI_SILU) {
+                __nv_bfloat16* D = reinterpret_cast<__nv_bfloat16*>(p.D);
+#pragma unroll 1
+                for (int c = 0; c < BN / 2 / 32; ++c) {
+                    uint32_t gv[32], uv[32];
+                    tmem_ld32(taddr + c * 32, gv);
+                    tmem_ld32(taddr + BN / 2 + c * 32, uv);
+                    tmem_wait_ld();
+                    const int col = n * (BN / 2) + c * 32;
+                    if (valid && col < p.N) {
+                        float o[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = silu_mul(__uint_as_float(gv[j]), __uint_as_float(uv[j]));
+                        store_bf16x32(D + grow * p.ldd + col, o);
+                    }
+                }
+            } else if (EPI == EPI_BF16) {
+                __nv_bfloat16* D = reinterpret_cast<__nv_bfloat16*>(p.D);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + c * 32, v);
+                    tmem_wait_ld();
+                    const int col = n * BN + c * 32;
+                    if (valid && col < p.N) {
+                        float o[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(v[j]);
+                        store_bf16x32(D + grow * p.ldd + col, o);
+                    }
+                }
+            } else {
+                float* D = reinterpret_cast<float*>(p.D);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(taddr + c * 32, v);
+                    tmem_wait_ld();
+                    const int col0 = n * BN + c * 32;
+                    if (valid) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int col = col0 + j;
+                            if (col < p.N) {
+                                float o = __uint_as_float(v[j]);
+                                if (p.col_bias) o += p.col_bias[col];
+                                D[grow * p.ldd + col] = o;
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base) : "memory");
+    }
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes(int n_groups) {
+    return 1024 + SmemLayout::kTileStart + sizeof(int32_t) * (size_t)(n_groups + 1);
+}
+
+cudaError_t launch_grouped_gemm(int epi, const GemmArgs& args, int n_sms, cudaStream_t stream) {
+    const int G = args.n_routed + (args.shared_rows > 0 ? 1 : 0);
+    const size_t smem = gemm_smem_bytes(G);
+    const void* fn;
+    switch (epi) {
+        case EPI_SILU: fn = (const void*)grouped_gemm_kernel<EPI_SILU>; break;
+        case EPI_BF16: fn = (const void*)grouped_gemm_kernel<EPI_BF16>; break;
+        case EPI_F32: fn = (const void*)grouped_gemm_kernel<EPI_F32>; break;
+        default: return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    void* kargs[] = {const_cast<GemmArgs*>(&args)};
+    return cudaLaunchKernel(fn, dim3(n_sms), dim3(kGemmThreads), kargs, smem, stream);
+}
+
+}  // namespace dwdp

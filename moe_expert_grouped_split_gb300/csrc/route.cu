@@ -1,0 +1,250 @@
+// route.cu: routing, grouping, gather and combine kernels of the DWDP MoE
+// block (memory- and latency-bound; coalesced 16-byte accesses, warp-level
+// top-k, no atomics on any ordered output so every index is deterministic).
+//
+// The pages do not print the router; these kernels implement the reading the
+// library documents in dwdp.h: fp32 logits, the k largest (ties to the lower
+// expert id), the chosen set listed in ascending id, weights = softmax
+// renormalised over the chosen set, and (token, slot) pairs grouped by expert
+// in ascending flat index t*k+j.
+#include <cuda_bf16.h>
+
+#include "dwdp_internal.h"
+
+namespace dwdp {
+namespace {
+
+constexpr int kMaxPerLane = DWDP_MAX_EXPERTS / 32;
+
+// One warp per token.  Lane l holds logits l, l+32, ...; k rounds of a warp
+// arg-max pick the chosen set (ties to the lower id), which is then listed in
+// ascending id.  w_j = exp(z_j - z_max) / sum_i exp(z_i - z_max) over the
+// chosen set (the full softmax denominator cancels in the renormalisation).
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits,
+                                                   const float* __restrict__ bias, int T, int E,
+                                                   int k, int32_t* __restrict__ ids,
+                                                   float* __restrict__ w) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const float* z = logits + (int64_t)t * E;
+    float v[kMaxPerLane];
+    const int per = (E + 31) >> 5;
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j) {
+        const int e = lane + 32 * j;
+        v[j] = -INFINITY;
+        if (j < per && e < E) v[j] = z[e] + (bias ? bias[e] : 0.0f);
+    }
+    uint32_t taken = 0;  // bit j: v[j] already chosen
+    int my_id = -1;      // lane s < k ends up holding the s-th chosen id
+    float my_val = 0.0f;
+    for (int s = 0; s < k; ++s) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < kMaxPerLane; ++j) {
+            const int e = lane + 32 * j;
+            if (j < per && e < E && !(taken >> j & 1u)) {
+                if (v[j] > bv || (v[j] == bv && e < bi) || bi == 0x7fffffff) {
+                    bv = v[j];
+                    bi = e;
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == s) {
+            my_id = bi;
+            my_val = bv;
+        }
+    }
+    // rank of my id among the chosen ids -> ascending-id slot
+    int rank = 0;
+    for (int s = 0; s < k; ++s) {
+        const int other = __shfl_sync(0xffffffffu, my_id, s);
+        if (lane < k && other < my_id) ++rank;
+    }
+    // z_max is the first pick
+    const float zmax = __shfl_sync(0xffffffffu, my_val, 0);
+    const float ex = (lane < k) ? __expf(my_val - zmax) : 0.0f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane < k) {
+        ids[(int64_t)t * k + rank] = my_id;
+        w[(int64_t)t * k + rank] = ex / sum;
+    }
+}
+
+__device__ __forceinline__ int block_sum(int v, int* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    int s = 0;
+    for (int i = 0; i < nw; ++i) s += red[i];
+    return s;
+}
+
+// counts[e] = #{f : ids[f] == e}; one block per expert scans all pairs.
+__global__ void __launch_bounds__(1024) count_kernel(const int32_t* __restrict__ ids, int n,
+                                                     int32_t* __restrict__ counts) {
+    __shared__ int red[32];
+    const int e = blockIdx.x;
+    int c = 0;
+    const int n4 = n >> 2;
+    const int4* ids4 = reinterpret_cast<const int4*>(ids);
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+        const int4 q = ids4[i];
+        c += (q.x == e) + (q.y == e) + (q.z == e) + (q.w == e);
+    }
+    for (int i = (n4 << 2) + threadIdx.x; i < n; i += blockDim.x) c += (ids[i] == e);
+    c = block_sum(c, red);
+    if (threadIdx.x == 0) counts[e] = c;
+}
+
+// Stable placement: block e computes offsets[e] from counts, then walks the
+// pairs in flat order; pair f with ids[f] == e gets row offsets[e] + (number
+// of earlier pairs of e).  A block-wide exclusive scan of the match flags
+// keeps the walk in order.
+__global__ void __launch_bounds__(1024) place_kernel(const int32_t* __restrict__ ids, int n, int E,
+                                                     const int32_t* __restrict__ counts,
+                                                     int32_t* __restrict__ offsets,
+                                                     int32_t* __restrict__ perm,
+                                                     int32_t* __restrict__ inv) {
+    __shared__ int red[32];
+    __shared__ int wsum[32];
+    const int e = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    int part = 0;
+    for (int i = threadIdx.x; i < e; i += blockDim.x) part += counts[i];
+    const int base = block_sum(part, red);
+    if (threadIdx.x == 0) {
+        offsets[e] = base;
+        if (e == E - 1) offsets[E] = base + counts[e];
+    }
+    int running = base;
+    for (int start = 0; start < n; start += blockDim.x) {
+        const int f = start + threadIdx.x;
+        const bool hit = f < n && ids[f] == e;
+        const uint32_t ball = __ballot_sync(0xffffffffu, hit);
+        const int in_warp = __popc(ball & ((1u << lane) - 1u));
+        __syncthreads();
+        if (lane == 0) wsum[warp] = __popc(ball);
+        __syncthreads();
+        int before = 0, total = 0;
+        for (int i = 0; i < nw; ++i) {
+            const int c = wsum[i];
+            if (i < warp) before += c;
+            total += c;
+        }
+        if (hit) {
+            const int r = running + before + in_warp;
+            perm[r] = f;
+            inv[f] = r;
+        }
+        running += total;
+    }
+}
+
+// xp[r][:] = x[perm[r] / k][:]: one warp per row, 16-byte copies.
+__global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x, int row_vecs,
+                                                     const int32_t* __restrict__ perm, int n_rows,
+                                                     int k, uint4* __restrict__ xp) {
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (r >= n_rows) return;
+    const int t = perm[r] / k;
+    const uint4* src = x + (int64_t)t * row_vecs;
+    uint4* dst = xp + (int64_t)r * row_vecs;
+    for (int i = lane; i < row_vecs; i += 32) dst[i] = __ldg(src + i);
+}
+
+__device__ __forceinline__ void acc_bf16x8(float (&a)[8], uint4 q, float s) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        a[2 * i] = fmaf(s, f.x, a[2 * i]);
+        a[2 * i + 1] = fmaf(s, f.y, a[2 * i + 1]);
+    }
+}
+
+// out[t] = sum_j w[t][j] * y[inv[t*k+j]] (slot order), then + y[shared_row0 + t];
+// fp32 sums, one bf16 rounding at the end.  One warp per token.
+__global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ y, int row_vecs,
+                                                      const int32_t* __restrict__ inv,
+                                                      const float* __restrict__ w, int T, int k,
+                                                      int64_t shared_row0, int has_shared,
+                                                      uint4* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int rows[DWDP_MAX_TOPK];
+    float ws[DWDP_MAX_TOPK];
+    for (int j = 0; j < k; ++j) {
+        rows[j] = inv[(int64_t)t * k + j];
+        ws[j] = w[(int64_t)t * k + j];
+    }
+    for (int i = lane; i < row_vecs; i += 32) {
+        float a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int j = 0; j < k; ++j) acc_bf16x8(a, __ldg(y + (int64_t)rows[j] * row_vecs + i), ws[j]);
+        if (has_shared) acc_bf16x8(a, __ldg(y + (shared_row0 + t) * row_vecs + i), 1.0f);
+        uint4 o;
+        __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) oh[q] = __floats2bfloat162_rn(a[2 * q], a[2 * q + 1]);
+        out[(int64_t)t * row_vecs + i] = o;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
+                        float* w, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    const int warps = 8;
+    topk_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(logits, bias, T, E, k, ids, w);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_group(const int32_t* ids, int n, int E, int32_t* counts, int32_t* offsets,
+                         int32_t* perm, int32_t* inv, cudaStream_t s) {
+    count_kernel<<<E, 1024, 0, s>>>(ids, n, counts);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    place_kernel<<<E, 1024, 0, s>>>(ids, n, E, counts, offsets, perm, inv);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const void* x, int H, const int32_t* perm, int n_rows, int k, void* xp,
+                          cudaStream_t s) {
+    if (n_rows <= 0) return cudaSuccess;
+    const int warps = 8;
+    gather_kernel<<<(n_rows + warps - 1) / warps, 32 * warps, 0, s>>>(
+        reinterpret_cast<const uint4*>(x), H / 8, perm, n_rows, k, reinterpret_cast<uint4*>(xp));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* y, int H, const int32_t* inv, const float* w, int T, int k,
+                           int64_t shared_row0, bool has_shared, void* out, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    const int warps = 8;
+    combine_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(
+        reinterpret_cast<const uint4*>(y), H / 8, inv, w, T, k, shared_row0, has_shared ? 1 : 0,
+        reinterpret_cast<uint4*>(out));
+    return cudaGetLastError();
+}
+
+}  // namespace dwdp

@@ -90,6 +90,9 @@ class Oracle:
             _U16P, _I64, _I64, _I64, _I64P, _I64, _I32P, _F64P,
             ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p),
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, _F64P]
+        L.oracle_grouped_gemm.restype = None
+        L.oracle_grouped_gemm.argtypes = [_U16P, _I64, _I32P, _I64, ctypes.POINTER(ctypes.c_void_p), _I64,
+                                          ctypes.c_int, _F64P]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         self.lib = L
@@ -207,6 +210,20 @@ class Oracle:
                                    int(bool(mirrored)), out)
         del keep
         return out
+
+    def grouped_gemm(self, a, row_offsets, b_list, N: int, epilogue: int) -> np.ndarray:
+        """fp64 result [rows, N] of the grouped GEMM (rows outside every
+        group stay 0).  b_list[g]: group g's weights [N or 2N][K] uint16."""
+        a = _u16(a)
+        rows, K = a.shape
+        off = np.ascontiguousarray(row_offsets, dtype=np.int32)
+        G = off.size - 1
+        assert len(b_list) == G
+        keep = [_u16(b) for b in b_list]
+        ptrs = (ctypes.c_void_p * max(1, G))(*[b.ctypes.data for b in keep])
+        d = np.zeros((rows, N), dtype=np.float64)
+        self.lib.oracle_grouped_gemm(a, K, off, G, ptrs, N, int(epilogue), d)
+        return d
 
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())

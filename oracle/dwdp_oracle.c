@@ -315,3 +315,30 @@ void oracle_set_num_threads(int n) {
     (void)n;
 #endif
 }
+
+/* -------------------------------------------------------- grouped GEMM -- */
+
+/* The grouped GEMM over split weight buffers (DWDP §4.2): for each group g,
+ * rows r in [row_offsets[g], row_offsets[g+1]) of a [rows][K]:
+ *   epilogue 0 or 2: d[r][n] = sum_k a[r][k] * B_g[n][k]              (n < N)
+ *   epilogue 1:      d[r][n] = SiLU(sum_k a[r][k] B_g[n][k]) * sum_k a[r][k] B_g[N+n][k]
+ * B_g points at group g's weights ([N][K], or [2N][K] for epilogue 1)
+ * wherever they live.  fp64 sums; d is fp64 (the caller rounds or compares). */
+void oracle_grouped_gemm(const uint16_t* a, int64_t K, const int32_t* row_offsets, int64_t G,
+                         const uint16_t* const* b, int64_t N, int epilogue, double* d) {
+    for (int64_t g = 0; g < G; ++g) {
+        const uint16_t* bg = b[g];
+#pragma omp parallel for schedule(static)
+        for (int64_t r = row_offsets[g]; r < row_offsets[g + 1]; ++r) {
+            for (int64_t n = 0; n < N; ++n) {
+                double s = 0.0, s2 = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    double av = oracle_bf16_to_double(a[r * K + k]);
+                    s += av * oracle_bf16_to_double(bg[n * K + k]);
+                    if (epilogue == 1) s2 += av * oracle_bf16_to_double(bg[(N + n) * K + k]);
+                }
+                d[r * N + n] = (epilogue == 1) ? s / (1.0 + exp(-s)) * s2 : s;
+            }
+        }
+    }
+}

@@ -332,3 +332,28 @@ def pin_closed_form_golden(o):
 ALL_PINS = [pin_bf16, pin_router_logits, pin_topk_bruteforce, pin_weights, pin_special_cases,
             pin_group, pin_ffn_dense, pin_swiglu_textbook, pin_linearity_and_zero, pin_mirrored,
             pin_map_invariance, pin_closed_form_golden]
+
+
+def pin_grouped_gemm(o):
+    """The grouped GEMM against numpy fp64 matmuls, group by group, for the
+    three epilogues; empty groups and ragged sizes included."""
+    rng = np.random.default_rng(12)
+    K, N = 48, 20
+    off = np.array([0, 5, 5, 17, 18, 30], dtype=np.int32)
+    a = _rand_bits(rng, (32, K), 1.0)
+    A = _decode(a)
+    for epi in (0, 1, 2):
+        bl = [_rand_bits(rng, ((2 if epi == 1 else 1) * N, K), 0.3) for _ in range(off.size - 1)]
+        d = o.grouped_gemm(a, off, bl, N, epi)
+        ref = np.zeros((32, N))
+        for g in range(off.size - 1):
+            Bg = _decode(bl[g])
+            r0, r1 = off[g], off[g + 1]
+            if epi == 1:
+                ref[r0:r1] = _silu(A[r0:r1] @ Bg[:N].T) * (A[r0:r1] @ Bg[N:].T)
+            else:
+                ref[r0:r1] = A[r0:r1] @ Bg.T
+        assert np.allclose(d, ref, rtol=1e-12, atol=1e-12), f"grouped GEMM epilogue {epi}"
+
+
+ALL_PINS.append(pin_grouped_gemm)

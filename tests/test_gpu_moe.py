@@ -1,0 +1,97 @@
+"""The whole MoE layer through the C ABI (route -> prefetch -> gather ->
+G1 -> G2 -> combine) against the oracle's mirrored layer, plus the DWDP
+invariant that the output does not depend on where experts live (DWDP §2):
+bit-identical GPU outputs under different local/remote/redundant maps."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import GpuLayerRun, assert_close, host_layer, to_f64
+from moe_expert_grouped_split_gb300 import inputs as I
+from moe_expert_grouped_split_gb300.build import build
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_and_check(shape, placement, seed, chunk=1 << 20, n_copy_streams=1, tokens=None):
+    build()
+    lw = I.make_layer(shape, placement, seed, 0, device="cuda")
+    x = I.make_tokens(shape.T, shape.H, seed).cuda()
+    run = GpuLayerRun(shape, lw)
+    try:
+        rb, out = run.run(x, chunk_bytes=chunk, n_copy_streams=n_copy_streams)
+        o = oracle.default()
+        ref = o.route(I.bf16_bits(x), I.bf16_bits(lw.wr), None if lw.bias is None else lw.bias.cpu().numpy(),
+                      shape.k)
+        ids = rb.topk_ids.cpu().numpy()[: shape.T]
+        same = (ids == ref["ids"]).all(axis=1)
+        tok = np.arange(shape.T) if tokens is None else np.asarray(tokens)
+        tok = tok[same[tok]]
+        w13s, w2s, sw13, sw2 = host_layer(lw)
+        want = o.moe_tokens(I.bf16_bits(x), tok, ref["ids"], ref["w"], w13s, w2s, sw13, sw2, mirrored=True)
+        got = to_f64(out)[tok]
+        assert_close(got, want, what="layer output")
+        return out
+    finally:
+        run.close()
+
+
+def test_tiny_layer():
+    shape, placement = I.tiny_layer()
+    _run_and_check(shape, placement, seed=0)
+
+
+def test_shared_expert_ragged_tokens():
+    shape = I.LayerShape(T=300, H=256, I=128, E=16, k=4, S=1)
+    _run_and_check(shape, I.split_placement(16, 5, 3), seed=1)
+
+
+def test_all_local_and_all_remote():
+    shape = I.LayerShape(T=130, H=128, I=64, E=8, k=2, S=1)
+    _run_and_check(shape, I.split_placement(8, 8, 0), seed=2)
+    _run_and_check(shape, I.split_placement(8, 0, 2), seed=2)
+
+
+def test_single_token_and_k_equals_e():
+    _run_and_check(I.LayerShape(T=1, H=128, I=64, E=4, k=2, S=1), I.split_placement(4, 2, 1), seed=3)
+    _run_and_check(I.LayerShape(T=70, H=128, I=64, E=4, k=4, S=0), I.split_placement(4, 1, 2), seed=4)
+
+
+def test_wide_hidden_multi_tile():
+    # H spans several n-tiles of the down GEMM and k-blocks of the gate/up GEMM
+    shape = I.LayerShape(T=200, H=1024, I=256, E=8, k=2, S=1)
+    _run_and_check(shape, I.split_placement(8, 3, 2), seed=5, chunk=100_000, n_copy_streams=2)
+
+
+def test_output_independent_of_placement():
+    """DWDP §2: any split or redundant placement gives the same bytes."""
+    build()
+    shape = I.LayerShape(T=257, H=256, I=128, E=12, k=3, S=1)
+    x = I.make_tokens(shape.T, shape.H, 9).cuda()
+    outs = []
+    for placement in (I.split_placement(12, 12, 0), I.split_placement(12, 4, 2),
+                      I.split_placement(12, 0, 3), I.split_placement(12, 4, 2, redundant=[5, 9, 11])):
+        lw = I.make_layer(shape, placement, 9, 0, device="cuda")
+        run = GpuLayerRun(shape, lw)
+        try:
+            _, out = run.run(x, chunk_bytes=50_000)
+            outs.append(out.clone())
+        finally:
+            run.close()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+def test_empty_batch():
+    build()
+    shape = I.LayerShape(T=0, H=128, I=64, E=4, k=2, S=0)
+    lw = I.make_layer(shape, I.split_placement(4, 2, 1), 0, 0, device="cuda")
+    run = GpuLayerRun(I.LayerShape(T=8, H=128, I=64, E=4, k=2, S=0), lw)
+    try:
+        x = torch.empty((0, 128), dtype=torch.bfloat16, device="cuda")
+        rb, out = run.run(x)
+        assert out.shape[0] == 0
+        assert (rb.counts.cpu() == 0).all() and (rb.offsets.cpu() == 0).all()
+    finally:
+        run.close()
