@@ -1,0 +1,491 @@
+"""Benchmark of the DWDP single-rank hot path on synthetic DeepSeek-R1-shaped
+MoE layers.
+
+One step = one MoE layer for one batch of T tokens, the way a DWDP rank runs
+it (DWDP §2): route + gather + gate/up GEMM + down GEMM + combine on the
+compute stream, while the next layer's 192 non-resident experts are copied
+from three emulated peer pools into the other stage buffer in 16 MB slices
+issued round-robin (DWDP §4.3.2) on a copy stream.  Two distinct layers
+alternate, so every step's weights (22.6 GB read by the GEMMs) and copies
+(16.9 GB) are far larger than L2: no flush is needed between steps.
+
+Prints one JSON line.  ``value`` = tokens/s over the timed steps with inputs
+resident in HBM; ``e2e`` = the same with each step's tokens copied in from
+pinned host memory and the layer output copied back, inside the timed
+region.  ``roofline`` describes the dominant kernel (the gate/up grouped GEMM)
+timed with CUDA events recorded around it by the library on its own stream.
+``cpu_baseline`` times the CPU oracle on a bounded token sample.
+
+--impl reference runs the same metric with the CPU oracle on host cores.
+Multi-GPU: replicas only (each rank runs the same independent workload on
+its own GPU; no data-path collective); the timing is max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s & TFLOP/s at 8K tokens, prefetch overlapped; % of TC peak"
+UNIT = "tokens/s"
+
+WORKLOADS = {
+    # name: (T, description)
+    "r1_moe_layer_8k": 8192,
+    "r1_moe_layer_256": 256,
+}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="r1_moe_layer_8k", choices=sorted(WORKLOADS))
+    p.add_argument("--chunk-mb", type=float, default=16.0)
+    p.add_argument("--copy-streams", type=int, default=1)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extras", action="store_true", help="skip compute-only / copy-only / e2e legs")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------- helpers ----
+def layer_flops(T, H, I, E, k, S):
+    """Algorithmic FLOPs of one layer: router 2*T*H*E, experts T*(k+S)*6*H*I."""
+    return 2 * T * H * E + T * (k + S) * 6 * H * I
+
+
+def g1_flops(T, H, I, k, S):
+    """Gate/up grouped GEMM: 2 * (rows) * H * 2I with rows = T*(k+S)."""
+    return 4 * T * (k + S) * H * I
+
+
+class ClockSampler:
+    """nvidia-smi clocks sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.25)
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# -------------------------------------------------------- our arm ----------
+class Workload:
+    """Two R1-shaped layers (alternating) with their pools, a Runtime and the
+    per-step token batches, all resident in HBM."""
+
+    def __init__(self, T, chunk_bytes, n_copy_streams, base_seed=0):
+        import torch
+
+        from moe_expert_grouped_split_gb300 import binding as B
+        from moe_expert_grouped_split_gb300 import inputs as I
+
+        self.B, self.I, self.torch = B, I, torch
+        self.shape, self.placement = I.r1_layer(T)
+        sh = self.shape
+        self.layers = [I.make_layer(sh, self.placement, base_seed, l, device="cuda") for l in range(2)]
+        self.rt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, 2, self.placement.n_remote())
+        for l, lw in enumerate(self.layers):
+            self.rt.set_layer(l, lw)
+        self.x = [I.make_tokens(sh.T, sh.H, base_seed, step=s, device="cuda") for s in range(2)]
+        self.rb = B.RouteBuffers(sh.T, sh.E, sh.k)
+        self.out = torch.empty((sh.T, sh.H), dtype=torch.bfloat16, device="cuda")
+        self.compute = torch.cuda.Stream()
+        self.copies = [torch.cuda.Stream() for _ in range(n_copy_streams)]
+        self.chunk = int(chunk_bytes)
+
+    def step(self, i, prefetch_next=True, x=None):
+        l = i % 2
+        x = self.x[l] if x is None else x
+        with self.torch.cuda.stream(self.compute):
+            self.rt.route(x, self.layers[l].wr, None, self.rb, self.compute)
+            self.rt.moe(l, l, x, self.rb, self.out, self.compute)
+        if prefetch_next:
+            self.rt.prefetch((i + 1) % 2, (i + 1) % 2, self.chunk, self.copies)
+
+    def prologue(self):
+        self.rt.prefetch(0, 0, self.chunk, self.copies)
+
+    def sync(self):
+        self.torch.cuda.synchronize()
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from moe_expert_grouped_split_gb300 import binding as B
+
+    torch.cuda.set_device(local_rank)
+    T = WORKLOADS[args.workload]
+    wl = Workload(T, args.chunk_mb * (1 << 20), args.copy_streams)
+    sh = wl.shape
+    K, W = args.steps, args.warmup
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([v], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            return float(t.item())
+        return v
+
+    # phase events per timed step (recorded by the library on the compute stream)
+    phases = [[ev() for _ in range(7)] for _ in range(K)]
+    for ps in phases:
+        for e in ps:
+            e.record(wl.compute)
+    torch.cuda.synchronize()
+
+    # ---- overlapped steps (the metric) ----
+    wl.prologue()
+    n = 0
+    for i in range(W):
+        wl.step(n)
+        n += 1
+    wl.sync()
+    barrier()
+    start, stop = ev(), ev()
+    with ClockSampler(local_rank) as clk:
+        start.record(wl.compute)
+        for c in wl.copies:
+            c.wait_stream(wl.compute)
+        for i in range(K):
+            B.dwdp_set_phase_events(wl.rt.ctx, phases[i])
+            wl.step(n)
+            n += 1
+        B.dwdp_set_phase_events(wl.rt.ctx, None)
+        for c in wl.copies:
+            wl.compute.wait_stream(c)
+        stop.record(wl.compute)
+        stop.synchronize()
+    assert wl.rt.device_status() == 0
+    ms_total = start.elapsed_time(stop)
+    ms_total = max_over_ranks(ms_total)
+    barrier()
+    ms_step = ms_total / K
+    value = world * K * T / (ms_total / 1e3)
+    ph = [[phases[i][j].elapsed_time(phases[i][j + 1]) for j in range(6)] for i in range(K)]
+    avg = [sum(p[j] for p in ph) / K for j in range(6)]
+    names = ["route", "wait_stage", "gather", "gate_up_gemm", "down_gemm", "combine"]
+    phase_ms = {n_: round(a, 4) for n_, a in zip(names, avg)}
+
+    res = {"ms_total": ms_total, "ms_step": ms_step, "value": value, "phase_ms": phase_ms, "clocks": clk.summary()}
+
+    if not args.no_extras:
+        # ---- compute only: same steps, every expert already staged, no copies ----
+        wl.sync()
+        for l in (0, 1):
+            wl.rt.prefetch(l, l, wl.chunk, wl.copies)
+        wl.sync()
+        a, b = ev(), ev()
+        for i in range(2):
+            wl.step(i, prefetch_next=False)
+        a.record(wl.compute)
+        for i in range(K):
+            wl.step(i, prefetch_next=False)
+        b.record(wl.compute)
+        b.synchronize()
+        res["compute_only_ms_step"] = a.elapsed_time(b) / K
+        # ---- copy only ----
+        a, b = ev(), ev()
+        a.record(wl.copies[0])
+        for i in range(K):
+            wl.rt.prefetch(i % 2, i % 2, wl.chunk, wl.copies)
+        b.record(wl.copies[0])
+        b.synchronize()
+        res["copy_only_ms_step"] = a.elapsed_time(b) / K
+        # ---- e2e: tokens in from pinned host memory, output back ----
+        xh = [x.cpu().pin_memory() for x in wl.x]
+        oh = torch.empty((T, sh.H), dtype=torch.bfloat16).pin_memory()
+        xd = torch.empty_like(wl.x[0])
+        for l in (0, 1):
+            wl.rt.prefetch(l, l, wl.chunk, wl.copies)
+        wl.sync()
+        wl.prologue()
+        for i in range(2):
+            with torch.cuda.stream(wl.compute):
+                xd.copy_(xh[i % 2], non_blocking=True)
+            wl.step(i, x=xd)
+            with torch.cuda.stream(wl.compute):
+                oh.copy_(wl.out, non_blocking=True)
+        wl.sync()
+        barrier()
+        a, b = ev(), ev()
+        a.record(wl.compute)
+        for c in wl.copies:
+            c.wait_stream(wl.compute)
+        for i in range(2, 2 + K):
+            with torch.cuda.stream(wl.compute):
+                xd.copy_(xh[i % 2], non_blocking=True)
+            wl.step(i, x=xd)
+            with torch.cuda.stream(wl.compute):
+                oh.copy_(wl.out, non_blocking=True)
+        for c in wl.copies:
+            wl.compute.wait_stream(c)
+        b.record(wl.compute)
+        b.synchronize()
+        e2e_ms = max_over_ranks(a.elapsed_time(b))
+        res["e2e"] = {"value": world * K * T / (e2e_ms / 1e3), "unit": UNIT,
+                      "h2d_bytes_per_step": T * sh.H * 2, "d2h_bytes_per_step": T * sh.H * 2}
+        assert wl.rt.device_status() == 0
+    res["wl"] = wl
+    return res
+
+
+def cpu_baseline_sample(wl, target_s=15.0, max_tokens=512):
+    """The oracle as it stands on host cores, on a seeded token sample of the
+    same workload (the layer's rows are independent, so a sample's cost per
+    token is the layer's)."""
+    import numpy as np
+
+    import oracle
+    from moe_expert_grouped_split_gb300 import inputs as I
+
+    o = oracle.default()
+    sh = wl.shape
+    lw = wl.layers[0]
+    x = I.bf16_bits(wl.x[0])
+    rng = np.random.default_rng(1234)
+    order = rng.permutation(sh.T)
+    wr = I.bf16_bits(lw.wr)
+    cache = {}
+    pl = lw.placement
+
+    def weights_for(ids):
+        need = sorted(set(int(e) for e in np.unique(ids)) - set(cache))
+        for e in need:
+            if pl.local_slot[e] >= 0:
+                w13, w2 = lw.local_w13[pl.local_slot[e]], lw.local_w2[pl.local_slot[e]]
+            else:
+                w13, w2 = lw.peer_w13[pl.peer_id[e]][pl.peer_slot[e]], lw.peer_w2[pl.peer_id[e]][pl.peer_slot[e]]
+            cache[e] = (I.bf16_bits(w13), I.bf16_bits(w2))
+        w13s = [cache.get(e, (None, None))[0] for e in range(sh.E)]
+        w2s = [cache.get(e, (None, None))[1] for e in range(sh.E)]
+        return w13s, w2s
+
+    sw13, sw2 = I.bf16_bits(lw.shared_w13), I.bf16_bits(lw.shared_w2)
+
+    def run(tokens):
+        xs = np.ascontiguousarray(x[tokens])
+        r_pre = o.route(xs, wr, None, sh.k)            # routing, untimed pass to learn the experts
+        w13s, w2s = weights_for(r_pre["ids"])          # host copies of those experts (untimed)
+        t0 = time.perf_counter()
+        r = o.route(xs, wr, None, sh.k)
+        o.moe_tokens(xs, np.arange(len(tokens)), r["ids"], r["w"], w13s, w2s, sw13, sw2, mirrored=True)
+        return time.perf_counter() - t0
+
+    n = 8
+    dt = run(order[:n])
+    per_tok = dt / n
+    n2 = int(min(max_tokens, max(n, target_s / max(per_tok, 1e-9))))
+    if n2 > n:
+        dt = run(order[:n2])
+        n = n2
+    return {"value": n / dt, "unit": UNIT, "cores": o.num_threads(), "kind": "oracle",
+            "sample": f"{n} seeded tokens of the {sh.T}-token R1-shaped layer (routing + 8 routed experts + "
+                      f"shared expert per token, fp64, {dt:.1f} s)"}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return main_reference(args, rank, world)
+
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    from moe_expert_grouped_split_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+    res = run_ours(args, rank, world, local_rank)
+    wl = res.pop("wl")
+    sh = wl.shape
+    peaks, src = measured_peaks()
+    flops_layer = layer_flops(sh.T, sh.H, sh.I, sh.E, sh.k, sh.S)
+    g1 = g1_flops(sh.T, sh.H, sh.I, sh.k, sh.S)
+    g1_ms = res["phase_ms"]["gate_up_gemm"]
+    g1_tflops = g1 / (g1_ms / 1e3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    layer_tflops = flops_layer / (res["ms_step"] / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(res["value"], 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_step"], 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights; R1 MoE layer shapes)",
+        "config": {"workload": args.workload, "T": sh.T, "H": sh.H, "I": sh.I, "E": sh.E, "k": sh.k,
+                   "shared": sh.S, "local_experts": int((wl.placement.local_slot >= 0).sum()),
+                   "remote_experts": wl.placement.n_remote(), "peer_pools": wl.placement.n_peers,
+                   "chunk_mb": args.chunk_mb, "copy_streams": args.copy_streams, "layers_alternating": 2,
+                   "l2": "inputs larger than L2 (22.6 GB of expert weights + 16.9 GB of copies per step)",
+                   "parallelism": "replicas" if world > 1 else "single rank"},
+        "tflops": round(layer_tflops, 1),
+        "tc_peak_frac": round(layer_tflops / peak, 4),
+        "phase_ms": res["phase_ms"],
+        "roofline": {"kernel": "gate_up_grouped_gemm", "bound": "tensor", "achieved": round(g1_tflops, 1),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(g1_tflops / peak, 4), "traffic": None,
+                     "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside a long step)",
+                     "algorithmic_flops_per_launch": g1},
+        "clocks": res["clocks"],
+        "gpu_launches": 8 * args.steps,
+    }
+    if "e2e" in res:
+        line["e2e"] = {k_: (round(v, 1) if isinstance(v, float) else v) for k_, v in res["e2e"].items()}
+        comp, copy = res["compute_only_ms_step"], res["copy_only_ms_step"]
+        exposed = max(0.0, res["ms_step"] - comp)
+        line["prefetch"] = {"compute_only_ms": round(comp, 4), "copy_only_ms": round(copy, 4),
+                            "overlapped_ms": round(res["ms_step"], 4), "exposed_ms": round(exposed, 4),
+                            "hidden_frac": round(max(0.0, 1.0 - exposed / copy), 4) if copy > 0 else None,
+                            "model_max_ms": round(max(comp, copy), 4),
+                            "copy_gbs": round(wl.placement.n_remote() * 3 * sh.H * sh.I * 2 / (copy / 1e3) / 1e9, 1)}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main_reference(args, rank, world):
+    """The oracle as it stands, timed on host cores, same metric and unit."""
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    from moe_expert_grouped_split_gb300 import inputs as I
+
+    T = WORKLOADS[args.workload]
+    shape, placement = I.r1_layer(T)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    o = oracle.default()
+    x_all = I.bf16_bits(I.make_tokens(T, shape.H, 0, device=dev))
+    wr = I.bf16_bits(I.randn_bf16((shape.E, shape.H), 0.02, I.seed_for(0, "Wr", 0), dev))
+    rng = np.random.default_rng(99)
+    per_step = 4
+    cache = {}
+
+    def expert(e):
+        if e not in cache:
+            cache[e] = (I.bf16_bits(I.randn_bf16((2 * shape.I, shape.H), 0.02, I.seed_for(0, "W13", 0, e), dev)),
+                        I.bf16_bits(I.randn_bf16((shape.H, shape.I), 0.02, I.seed_for(0, "W2", 0, e), dev)))
+        return cache[e]
+
+    sw13 = I.bf16_bits(I.randn_bf16((2 * shape.I, shape.H), 0.02, I.seed_for(0, "W13s", 0), dev))
+    sw2 = I.bf16_bits(I.randn_bf16((shape.H, shape.I), 0.02, I.seed_for(0, "W2s", 0), dev))
+    times = []
+    ntok = 0
+    for s in range(args.warmup + args.steps):
+        tok = rng.choice(T, size=per_step, replace=False)
+        xs = np.ascontiguousarray(x_all[tok])
+        pre = o.route(xs, wr, None, shape.k)
+        for e in np.unique(pre["ids"]):
+            expert(int(e))
+        w13s = [cache[e][0] if e in cache else None for e in range(shape.E)]
+        w2s = [cache[e][1] if e in cache else None for e in range(shape.E)]
+        t0 = time.perf_counter()
+        r = o.route(xs, wr, None, shape.k)
+        o.moe_tokens(xs, np.arange(per_step), r["ids"], r["w"], w13s, w2s, sw13, sw2, mirrored=True)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+            ntok += per_step
+    total = sum(times)
+    value = ntok / total
+    tokens_per_step = T
+    ms_step = tokens_per_step / value * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, R1 MoE layer shapes)",
+        "config": {"workload": args.workload, "T": T, "H": shape.H, "I": shape.I, "E": shape.E, "k": shape.k,
+                   "shared": shape.S},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": o.num_threads(), "kind": "oracle",
+                         "sample": f"{per_step} seeded tokens per step of the {T}-token layer, {args.steps} "
+                                   f"timed steps ({total:.1f} s); ms_per_step extrapolates to {T} tokens"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -206,6 +206,17 @@ int32_t dwdp_stage_layer(const dwdp_ctx* ctx, int32_t stage);
  * DEVICE_CHECK with the failing check described by dwdp_last_error. */
 int32_t dwdp_device_status(dwdp_ctx* ctx);
 
+/* Optional phase timing.  events is a host array of DWDP_PHASE_EVENTS
+ * caller-owned cudaEvent_t (or NULL to stop).  While set, dwdp_route records
+ * events[0] at its start and events[1] at its end on its stream, and
+ * dwdp_moe_layer records events[2] after waiting for its stage, events[3]
+ * after the gather, events[4] after the gate/up GEMM, events[5] after the
+ * down GEMM and events[6] after the combine.  The context keeps the pointers
+ * until the next call; the caller keeps the events alive.  Errors:
+ * INVALID_ARG. */
+#define DWDP_PHASE_EVENTS 7
+int32_t dwdp_set_phase_events(dwdp_ctx* ctx, void* const* events, int32_t n_events);
+
 /* Split-pointer grouped GEMM on its own ([DWDP] §4.2: one kernel over several
  * weight buffers, no merge).  For each group g in [0, G):
  *   rows r in [row_offsets[g], row_offsets[g+1]) of a [rows][K] bf16:

@@ -68,6 +68,7 @@ SIGNATURES = [
     ("dwdp_wait_stage", _I32, [_VP, _I32, _I32]),
     ("dwdp_stage_layer", _I32, [_VP, _I32]),
     ("dwdp_device_status", _I32, [_VP]),
+    ("dwdp_set_phase_events", _I32, [_VP, ctypes.POINTER(_VP), _I32]),
     ("dwdp_grouped_gemm", _I32, [_VP, _I32, _VP, ctypes.c_int64, _I32, _I32, _VP, _I32, ctypes.POINTER(dwdp_pool),
                                  _I32, _I32P, _VP, _VP]),
     ("dwdp_plan_prefetch", _I32, [_I32, _I32, _I32, _I32P, _I32P, _I32P, _I32, ctypes.c_size_t,
@@ -202,6 +203,16 @@ def dwdp_device_status(ctx) -> int:
     if rc not in (0, -6):
         _check(ctx, rc)
     return rc
+
+
+def dwdp_set_phase_events(ctx, events) -> None:
+    """events: a list of DWDP_PHASE_EVENTS torch.cuda.Event (timing enabled)
+    or None."""
+    if events is None:
+        _check(ctx, lib().dwdp_set_phase_events(ctx, None, 0))
+        return
+    arr = (_VP * len(events))(*[e.cuda_event for e in events])
+    _check(ctx, lib().dwdp_set_phase_events(ctx, arr, len(events)))
 
 
 def dwdp_grouped_gemm(ctx, epilogue, a, a_rows, K, N, row_offsets, G, bufs, buf_slot, d, stream=None) -> None:

@@ -75,6 +75,8 @@ struct dwdp_ctx {
     int stage_layer[2] = {-1, -1};
     std::vector<LayerMap> layers;
     int* d_err = nullptr;
+    cudaEvent_t phase[DWDP_PHASE_EVENTS] = {};
+    bool phases_on = false;
     std::string err;
     std::unique_ptr<GemmArgs> args;
 };
@@ -206,6 +208,11 @@ bool build_plan(int32_t E, int64_t H, int64_t I, const int32_t* local_slot, cons
         if (!any) break;
     }
     return true;
+}
+
+// Records phase event i on s when phase timing is on.
+cudaError_t mark(dwdp_ctx* ctx, int i, cudaStream_t s) {
+    return ctx->phases_on ? cudaEventRecord(ctx->phase[i], s) : cudaSuccess;
 }
 
 int32_t check_device_error_word(dwdp_ctx* ctx) {
@@ -424,6 +431,7 @@ int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router
                         L.route_bytes);
         logits = reinterpret_cast<float*>(static_cast<char*>(ws) + L.logits);
     }
+    DWDP_CUDA(ctx, mark(ctx, 0, stream));
     GemmArgs& a = *ctx->args;
     if (!encode_rows(&a.tmA[0], x, T, c.hidden) ||
         !encode_slots(&a.tmB[0], w_router, 1, c.n_experts, c.hidden))
@@ -447,6 +455,7 @@ int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router
     DWDP_CUDA(ctx, launch_topk(logits, nullptr, T, c.n_experts, c.top_k, out->topk_ids, out->topk_w, stream));
     DWDP_CUDA(ctx, launch_group(out->topk_ids, T * c.top_k, c.n_experts, out->counts, out->offsets, out->perm,
                                 out->inv_perm, stream));
+    DWDP_CUDA(ctx, mark(ctx, 1, stream));
     return DWDP_OK;
 }
 
@@ -519,7 +528,9 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     void* y = w + L.y;
 
     if (m.n_remote > 0) DWDP_CUDA(ctx, cudaStreamWaitEvent(stream, ctx->ready[stage], 0));
+    DWDP_CUDA(ctx, mark(ctx, 2, stream));
     DWDP_CUDA(ctx, launch_gather(x, (int)H, route->perm, (int)rows_r, (int)k, xp, stream));
+    DWDP_CUDA(ctx, mark(ctx, 3, stream));
 
     GemmArgs& a = *ctx->args;
     // B buffers: 0 = local pool, 1 = the stage, 2 = the shared expert.  Slots
@@ -548,6 +559,7 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     a.err = ctx->d_err;
     for (size_t g = 0; g < m.bsrc.size(); ++g) a.bsrc[g] = m.bsrc[g];
     DWDP_CUDA(ctx, launch_grouped_gemm(EPI_SILU, a, ctx->n_sms, stream));
+    DWDP_CUDA(ctx, mark(ctx, 4, stream));
     // G2: y = a W_down.
     if (!encode_rows(&a.tmA[0], act, rows_all, I)) return fail(ctx, DWDP_ERR_CUDA, "tensor map for the down GEMM");
     a.tmA[1] = a.tmA[0];
@@ -560,9 +572,11 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     a.d_rows = rows_all;
     a.D = y;
     DWDP_CUDA(ctx, launch_grouped_gemm(EPI_BF16, a, ctx->n_sms, stream));
+    DWDP_CUDA(ctx, mark(ctx, 5, stream));
     // The stage's weights have been read: the next prefetch into it may start.
     if (m.n_remote > 0) DWDP_CUDA(ctx, cudaEventRecord(ctx->freed[stage], stream));
     DWDP_CUDA(ctx, launch_combine(y, (int)H, route->inv_perm, route->topk_w, T, (int)k, rows_r, S > 0, out, stream));
+    DWDP_CUDA(ctx, mark(ctx, 6, stream));
     return DWDP_OK;
 }
 
@@ -583,6 +597,21 @@ int32_t dwdp_wait_stage(dwdp_ctx* ctx, int32_t stage, int32_t timeout_ms) {
 int32_t dwdp_stage_layer(const dwdp_ctx* ctx, int32_t stage) {
     if (!ctx || stage < 0 || stage > 1) return -1;
     return ctx->stage_layer[stage];
+}
+
+int32_t dwdp_set_phase_events(dwdp_ctx* ctx, void* const* events, int32_t n_events) {
+    if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
+    if (!events) {
+        ctx->phases_on = false;
+        return DWDP_OK;
+    }
+    if (n_events != DWDP_PHASE_EVENTS) return fail(ctx, DWDP_ERR_INVALID_ARG, "need %d events", DWDP_PHASE_EVENTS);
+    for (int i = 0; i < DWDP_PHASE_EVENTS; ++i) {
+        if (!events[i]) return fail(ctx, DWDP_ERR_INVALID_ARG, "event %d is NULL", i);
+        ctx->phase[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+    ctx->phases_on = true;
+    return DWDP_OK;
 }
 
 int32_t dwdp_device_status(dwdp_ctx* ctx) {

@@ -51,7 +51,10 @@ def _route_case(T, H, E, k, seed, router_std=0.02, bias=None, zero_router=False)
         else:
             check_grouping_properties(ids, counts, offsets, perm, inv, E)
         w = rb.topk_w.cpu().numpy().astype(np.float64)
-        assert np.abs(w[same] - ref["w"][same]).max(initial=0) <= 2e-6
+        # w_j = exp(z_j) / sum_i exp(z_i) over the chosen set, so
+        # |dw_j| <= w_j * 2 max|dz| (+ fp32 rounding of the softmax itself)
+        bound = 2.0 * err * w[same] + 2e-6
+        assert (np.abs(w[same] - ref["w"][same]) <= bound).all()
         assert np.allclose(w.sum(1), 1.0, atol=2e-6)
         return ids, w
     finally:
