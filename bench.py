@@ -36,10 +36,25 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer tokens/s & TFLOP/s at 8K tokens, prefetch overlapped; % of TC peak"
 UNIT = "tokens/s"
 
+def _r1(T):
+    def make():
+        from moe_expert_grouped_split_gb300 import inputs as I
+        return I.r1_layer(T)
+    return make
+
+
+def _r1_small():
+    """R1 layer widths (H=7168, I=2048) with 16 routed experts, top-4, one
+    shared expert and 1024 tokens (256 rows per expert, as at 8K tokens with
+    256 experts and top-8): a few GB, for profiler captures."""
+    from moe_expert_grouped_split_gb300 import inputs as I
+    return I.LayerShape(T=1024, H=7168, I=2048, E=16, k=4, S=1), I.split_placement(16, 4, 3)
+
+
 WORKLOADS = {
-    # name: (T, description)
-    "r1_moe_layer_8k": 8192,
-    "r1_moe_layer_256": 256,
+    "r1_moe_layer_8k": _r1(8192),
+    "r1_moe_layer_256": _r1(256),
+    "r1_small_profile": _r1_small,
 }
 
 
@@ -130,19 +145,36 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def max_over_ranks(v: float, world: int, device="cuda") -> float:
+    """Max of a per-rank timing over all ranks (replicas: the job ends when
+    the slowest rank does)."""
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: int, steps: int, world: int, ms_max: float) -> float:
+    """Units processed by all ranks per second, timed by the slowest rank."""
+    return world * steps * units_per_rank_step / (ms_max / 1e3)
+
+
 # -------------------------------------------------------- our arm ----------
 class Workload:
     """Two R1-shaped layers (alternating) with their pools, a Runtime and the
     per-step token batches, all resident in HBM."""
 
-    def __init__(self, T, chunk_bytes, n_copy_streams, base_seed=0):
+    def __init__(self, make_shape, chunk_bytes, n_copy_streams, base_seed=0):
         import torch
 
         from moe_expert_grouped_split_gb300 import binding as B
         from moe_expert_grouped_split_gb300 import inputs as I
 
         self.B, self.I, self.torch = B, I, torch
-        self.shape, self.placement = I.r1_layer(T)
+        self.shape, self.placement = make_shape()
         sh = self.shape
         self.layers = [I.make_layer(sh, self.placement, base_seed, l, device="cuda") for l in range(2)]
         self.rt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, 2, self.placement.n_remote())
@@ -177,9 +209,9 @@ def run_ours(args, rank, world, local_rank):
     from moe_expert_grouped_split_gb300 import binding as B
 
     torch.cuda.set_device(local_rank)
-    T = WORKLOADS[args.workload]
-    wl = Workload(T, args.chunk_mb * (1 << 20), args.copy_streams)
+    wl = Workload(WORKLOADS[args.workload], args.chunk_mb * (1 << 20), args.copy_streams)
     sh = wl.shape
+    T = sh.T
     K, W = args.steps, args.warmup
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
@@ -188,13 +220,6 @@ def run_ours(args, rank, world, local_rank):
             import torch.distributed as dist
             dist.barrier()
 
-    def max_over_ranks(v):
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([v], dtype=torch.float64, device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            return float(t.item())
-        return v
 
     # phase events per timed step (recorded by the library on the compute stream)
     phases = [[ev() for _ in range(7)] for _ in range(K)]
@@ -227,10 +252,10 @@ def run_ours(args, rank, world, local_rank):
         stop.synchronize()
     assert wl.rt.device_status() == 0
     ms_total = start.elapsed_time(stop)
-    ms_total = max_over_ranks(ms_total)
+    ms_total = max_over_ranks(ms_total, world)
     barrier()
     ms_step = ms_total / K
-    value = world * K * T / (ms_total / 1e3)
+    value = whole_job_rate(T, K, world, ms_total)
     ph = [[phases[i][j].elapsed_time(phases[i][j + 1]) for j in range(6)] for i in range(K)]
     avg = [sum(p[j] for p in ph) / K for j in range(6)]
     names = ["route", "wait_stage", "gather", "gate_up_gemm", "down_gemm", "combine"]
@@ -249,10 +274,14 @@ def run_ours(args, rank, world, local_rank):
             wl.step(i, prefetch_next=False)
         a.record(wl.compute)
         for i in range(K):
+            B.dwdp_set_phase_events(wl.rt.ctx, phases[i])
             wl.step(i, prefetch_next=False)
+        B.dwdp_set_phase_events(wl.rt.ctx, None)
         b.record(wl.compute)
         b.synchronize()
         res["compute_only_ms_step"] = a.elapsed_time(b) / K
+        ph = [[phases[i][j].elapsed_time(phases[i][j + 1]) for j in range(6)] for i in range(K)]
+        res["compute_only_phase_ms"] = {n_: round(sum(p[j] for p in ph) / K, 4) for j, n_ in enumerate(names)}
         # ---- copy only ----
         a, b = ev(), ev()
         a.record(wl.copies[0])
@@ -291,8 +320,8 @@ def run_ours(args, rank, world, local_rank):
             wl.compute.wait_stream(c)
         b.record(wl.compute)
         b.synchronize()
-        e2e_ms = max_over_ranks(a.elapsed_time(b))
-        res["e2e"] = {"value": world * K * T / (e2e_ms / 1e3), "unit": UNIT,
+        e2e_ms = max_over_ranks(a.elapsed_time(b), world)
+        res["e2e"] = {"value": whole_job_rate(T, K, world, e2e_ms), "unit": UNIT,
                       "h2d_bytes_per_step": T * sh.H * 2, "d2h_bytes_per_step": T * sh.H * 2}
         assert wl.rt.device_status() == 0
     res["wl"] = wl
@@ -413,7 +442,8 @@ def main():
                             "overlapped_ms": round(res["ms_step"], 4), "exposed_ms": round(exposed, 4),
                             "hidden_frac": round(max(0.0, 1.0 - exposed / copy), 4) if copy > 0 else None,
                             "model_max_ms": round(max(comp, copy), 4),
-                            "copy_gbs": round(wl.placement.n_remote() * 3 * sh.H * sh.I * 2 / (copy / 1e3) / 1e9, 1)}
+                            "copy_gbs": round(wl.placement.n_remote() * 3 * sh.H * sh.I * 2 / (copy / 1e3) / 1e9, 1),
+                            "compute_only_phase_ms": res["compute_only_phase_ms"]}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_sample(wl)
     if rank == 0:
@@ -433,8 +463,8 @@ def main_reference(args, rank, world):
     import oracle
     from moe_expert_grouped_split_gb300 import inputs as I
 
-    T = WORKLOADS[args.workload]
-    shape, placement = I.r1_layer(T)
+    shape, placement = WORKLOADS[args.workload]()
+    T = shape.T
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     o = oracle.default()
     x_all = I.bf16_bits(I.make_tokens(T, shape.H, 0, device=dev))
