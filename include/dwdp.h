@@ -236,6 +236,31 @@ int32_t dwdp_grouped_gemm(dwdp_ctx* ctx, int32_t epilogue, const void* a, int64_
                           int32_t N, const int32_t* row_offsets, int32_t G, const dwdp_pool* bufs,
                           int32_t n_bufs, const int32_t* buf_slot, void* d, dwdp_stream_t stream);
 
+/* Routing that allocates no device memory (the paper has no counterpart: it
+ * serves callers that cannot call cudaMalloc where they route tokens, e.g. a
+ * framework whose caching allocator owns all device memory, a latency-bound
+ * serving loop that cannot afford the synchronisation cudaMalloc may imply,
+ * or a host with a memory budget fixed at start-up).
+ * Computes exactly what dwdp_route computes (same kernels, same results) for
+ * x [T][hidden], w_router [n_experts][hidden], logit_bias [n_experts] or
+ * NULL, without a context or workspace; out->logits is ignored (the logits
+ * stay in the scratch).  Its scratch is one file-scope device array of
+ * DWDP_STATIC_SCRATCH_BYTES (16 MiB) of fp32 logits plus an error word,
+ * held by every GPU that loads this library until the process exits, so
+ * T * n_experts * 4 must not exceed DWDP_STATIC_SCRATCH_BYTES (else
+ * INVALID_ARG, nothing enqueued).  The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Every call on a
+ * device shares the one array and it keeps the last call's contents (the
+ * error word is cleared on `stream` at the start of each call): calls whose
+ * work overlaps on the GPU (other streams, other threads) race on it.  Calls
+ * no cudaMalloc, cudaFree or other allocating routine.  Errors (text in
+ * dwdp_last_error(NULL)): INVALID_ARG, UNSUPPORTED, CUDA. */
+#define DWDP_STATIC_SCRATCH_BYTES (16u << 20)
+int32_t dwdp_route_static(const void* x, int32_t T, int32_t hidden, int32_t n_experts, int32_t top_k,
+                          const void* w_router, const float* logit_bias, const dwdp_route_out* out,
+                          dwdp_stream_t stream);
+
 /* Host-only (no GPU needed): the prefetch copy plan dwdp_prefetch_layer
  * issues for a map ([DWDP] §4.3.2).  The non-resident experts (local_slot <
  * 0) take stage slots in ascending id; each peer's work is its w13 copies then

@@ -71,6 +71,7 @@ SIGNATURES = [
     ("dwdp_set_phase_events", _I32, [_VP, ctypes.POINTER(_VP), _I32]),
     ("dwdp_grouped_gemm", _I32, [_VP, _I32, _VP, ctypes.c_int64, _I32, _I32, _VP, _I32, ctypes.POINTER(dwdp_pool),
                                  _I32, _I32P, _VP, _VP]),
+    ("dwdp_route_static", _I32, [_VP, _I32, _I32, _I32, _I32, _VP, _VP, ctypes.POINTER(dwdp_route_out), _VP]),
     ("dwdp_plan_prefetch", _I32, [_I32, _I32, _I32, _I32P, _I32P, _I32P, _I32, ctypes.c_size_t,
                                   ctypes.POINTER(dwdp_copy_slice), ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]),
 ]
@@ -220,6 +221,13 @@ def dwdp_grouped_gemm(ctx, epilogue, a, a_rows, K, N, row_offsets, G, bufs, buf_
     bs, bsp = _i32(buf_slot)
     _check(ctx, lib().dwdp_grouped_gemm(ctx, epilogue, _ptr(a), a_rows, K, N, _ptr(row_offsets), G, barr,
                                         len(bufs), bsp, _ptr(d), _stream(stream)))
+
+
+def dwdp_route_static(x, T, hidden, n_experts, top_k, w_router, logit_bias, out: dwdp_route_out,
+                      stream=None) -> None:
+    """Routing without a context or workspace (no device allocation)."""
+    _check(None, lib().dwdp_route_static(_ptr(x), T, hidden, n_experts, top_k, _ptr(w_router), _ptr(logit_bias),
+                                         ctypes.byref(out), _stream(stream)))
 
 
 def dwdp_plan_prefetch(n_experts, hidden, inter, local_slot, peer_id, peer_slot, n_peers, chunk_bytes):

@@ -20,7 +20,7 @@ PKG = Path(__file__).resolve().parent
 CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = PKG / "libdwdp.so"
-SOURCES = ["gemm.cu", "route.cu", "dwdp_abi.cu"]
+SOURCES = ["gemm.cu", "route.cu", "dwdp_abi.cu", "route_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]
 

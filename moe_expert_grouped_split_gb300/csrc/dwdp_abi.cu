@@ -62,6 +62,39 @@ struct LayerMap {
 
 }  // namespace
 
+namespace dwdp {
+
+// Rows x K bf16 matrix, row-major: a 2-D map with a [128 rows x 64 cols] box,
+// 128-byte swizzle (the canonical K-major layout the MMA descriptors expect).
+bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || rows == 0) return false;
+    cuuint64_t dims[2] = {K, rows};
+    cuuint64_t strides[1] = {K * 2};
+    cuuint32_t box[2] = {BK, BM};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A weight buffer [slots][rows][K] bf16: a 3-D map, box [1 x 128 x 64].
+bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t rows, uint64_t K) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || rows == 0 || slots == 0) return false;
+    cuuint64_t dims[3] = {K, rows, slots};
+    cuuint64_t strides[2] = {K * 2, rows * K * 2};
+    cuuint32_t box[3] = {BK, BN / 2, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+void set_last_error(const char* msg) { g_last_error = msg; }
+
+}  // namespace dwdp
+
 struct dwdp_ctx {
     dwdp_config cfg{};
     int device = 0;
@@ -103,33 +136,6 @@ int32_t cuda_fail(dwdp_ctx* ctx, cudaError_t e, const char* what) {
         cudaError_t e_ = (call);                               \
         if (e_ != cudaSuccess) return cuda_fail(ctx, e_, #call); \
     } while (0)
-
-// Rows x K bf16 matrix, row-major: a 2-D map with a [128 rows x 64 cols] box,
-// 128-byte swizzle (the canonical K-major layout the MMA descriptors expect).
-bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn || rows == 0) return false;
-    cuuint64_t dims[2] = {K, rows};
-    cuuint64_t strides[1] = {K * 2};
-    cuuint32_t box[2] = {BK, BM};
-    cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// A weight buffer [slots][rows][K] bf16: a 3-D map, box [1 x 128 x 64].
-bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t rows, uint64_t K) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn || rows == 0 || slots == 0) return false;
-    cuuint64_t dims[3] = {K, rows, slots};
-    cuuint64_t strides[2] = {K * 2, rows * K * 2};
-    cuuint32_t box[3] = {BK, BN / 2, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -61,6 +61,14 @@ struct GemmArgs {
     int2 bsrc[kMaxGroups];
 };
 
+// TMA tensor maps (dwdp_abi.cu): a rows x K bf16 matrix (box 128 x 64) and
+// a weight buffer [slots][rows][K] (box 1 x 128 x 64), both 128 B swizzle.
+bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K);
+bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t rows, uint64_t K);
+
+// Sets the text dwdp_last_error(NULL) returns on this thread (dwdp_abi.cu).
+void set_last_error(const char* msg);
+
 size_t gemm_smem_bytes(int n_groups);
 cudaError_t launch_grouped_gemm(int epi, const GemmArgs& args, int n_sms, cudaStream_t stream);
 
