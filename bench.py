@@ -65,7 +65,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="r1_moe_layer_8k", choices=sorted(WORKLOADS))
-    p.add_argument("--chunk-mb", type=float, default=16.0)
+    p.add_argument("--chunk-mb", type=float, default=32.0)
     p.add_argument("--copy-streams", type=int, default=1)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extras", action="store_true", help="skip compute-only / copy-only / e2e legs")
@@ -81,6 +81,36 @@ def layer_flops(T, H, I, E, k, S):
 def g1_flops(T, H, I, k, S):
     """Gate/up grouped GEMM: 2 * (rows) * H * 2I with rows = T*(k+S)."""
     return 4 * T * (k + S) * H * I
+
+
+def g1_bytes(T, H, I, E_active, k, S):
+    """Gate/up grouped GEMM, algorithmic HBM bytes: every active expert's
+    w13 once (2I*H bf16), the gathered rows and x once, a written once."""
+    return (E_active + S) * 2 * I * H * 2 + T * (k + S) * H * 2 + T * (k + S) * I * 2
+
+
+def step_bytes(T, H, I, E_active, k, S, R):
+    """Algorithmic HBM bytes of one overlapped step: weights once
+    ((E_active+S)*3*H*I bf16), xp / a / y written and read once, x read and
+    out written, and the prefetch of R experts (read + write, both on this
+    GPU's HBM under the one-GPU emulation)."""
+    return ((E_active + S) * 3 * H * I * 2 + 2 * T * k * H * 2 + 2 * T * (k + S) * I * 2
+            + 2 * T * (k + S) * H * 2 + 2 * T * H * 2 + 2 * R * 3 * H * I * 2)
+
+
+def measured_traffic(kernel_file: str):
+    """dram__bytes_read.sum + dram__bytes_write.sum per launch of the gate/up
+    GEMM from the committed ncu summary, or None when the kernel source has
+    changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gate_up_gemm_traffic_r1_moe_layer_8k.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    with open(kernel_file, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    return rec["dram_bytes_per_launch"] if rec.get("gemm_cu_sha256") == sha else None
 
 
 class ClockSampler:
@@ -412,6 +442,10 @@ def main():
     g1_ms = res["phase_ms"]["gate_up_gemm"]
     g1_tflops = g1 / (g1_ms / 1e3) / 1e12
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    hbm = peaks["hbm_gbs"]
+    e_active = int((wl.rb.counts[: sh.E] > 0).sum().item())
+    g1b = g1_bytes(sh.T, sh.H, sh.I, e_active, sh.k, sh.S)
+    sb = step_bytes(sh.T, sh.H, sh.I, e_active, sh.k, sh.S, wl.placement.n_remote())
     layer_tflops = flops_layer / (res["ms_step"] / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": round(res["value"], 1), "unit": UNIT, "n_gpus": world,
@@ -428,9 +462,15 @@ def main():
         "tc_peak_frac": round(layer_tflops / peak, 4),
         "phase_ms": res["phase_ms"],
         "roofline": {"kernel": "gate_up_grouped_gemm", "bound": "tensor", "achieved": round(g1_tflops, 1),
-                     "peak": peak, "unit": "TFLOP/s", "frac": round(g1_tflops / peak, 4), "traffic": None,
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(g1_tflops / peak, 4),
+                     "traffic": measured_traffic(os.path.join(ROOT, "moe_expert_grouped_split_gb300", "csrc",
+                                                              "gemm.cu")),
+                     "algorithmic_bytes_per_launch": g1b,
                      "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside a long step)",
                      "algorithmic_flops_per_launch": g1},
+        "step_hbm": {"bound": "hbm", "achieved": round(sb / (res["ms_step"] / 1e3) / 1e9, 1), "peak": hbm,
+                     "unit": "GB/s", "frac": round(sb / (res["ms_step"] / 1e3) / 1e9 / hbm, 4),
+                     "algorithmic_bytes_per_step": sb, "peak_source": f"{src} hbm_gbs"},
         "clocks": res["clocks"],
         "gpu_launches": 8 * args.steps,
     }

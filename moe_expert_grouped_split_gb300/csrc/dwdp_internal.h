@@ -26,6 +26,7 @@ constexpr int kABytes = BM * BK * 2;           // 16 KiB
 constexpr int kBBytes = BN * BK * 2;           // 32 KiB
 constexpr int kStageBytes = kABytes + kBBytes;  // 48 KiB
 constexpr int kGemmThreads = 192;              // producer, MMA, 4 epilogue warps
+constexpr int kClusterCtas = 2;                // CTAs per cluster (co-scheduled on one GPC)
 
 // Bits of the device error word (kernels OR them in; never trap).
 enum DeviceError : int {

@@ -20,6 +20,8 @@
 // in the device error word and the CTA drains its copies and exits.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "dwdp_internal.h"
 
 namespace dwdp {
@@ -508,8 +510,33 @@ cudaError_t launch_grouped_gemm(int epi, const GemmArgs& args, int n_sms, cudaSt
     }
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+    if (e != cudaSuccess) return e;
+    // CTAs 2c and 2c+1 form one cluster, so they run on one GPC (one die).
+    // The round-robin tile order gives them tiles 2p and 2p+1: sibling
+    // m-tiles of one (group, n-tile), which read the same weight tile at the
+    // same time and so share it in that die's L2 instead of each die
+    // fetching it from HBM.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kClusterCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(kClusterCtas);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    // persistent grid: every cluster resident at once
+    cfg.gridDim = dim3(kClusterCtas * std::min(clusters, n_sms / kClusterCtas));
     void* kargs[] = {const_cast<GemmArgs*>(&args)};
-    return cudaLaunchKernel(fn, dim3(n_sms), dim3(kGemmThreads), kargs, smem, stream);
+    return cudaLaunchKernelExC(&cfg, fn, kargs);
 }
 
 }  // namespace dwdp
