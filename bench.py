@@ -4,17 +4,24 @@ MoE layers.
 One step = one MoE layer for one batch of T tokens, the way a DWDP rank runs
 it (DWDP §2): route + gather + gate/up GEMM + down GEMM + combine on the
 compute stream, while the next layer's 192 non-resident experts are copied
-from three emulated peer pools into the other stage buffer in 16 MB slices
-issued round-robin (DWDP §4.3.2) on a copy stream.  Two distinct layers
-alternate, so every step's weights (22.6 GB read by the GEMMs) and copies
-(16.9 GB) are far larger than L2: no flush is needed between steps.
+from three emulated peer pools into the other stage buffer in fixed-size
+slices issued round-robin (DWDP §4.3.2) on a copy stream.  Two distinct
+layers alternate, so every step's weights (22.6 GB read by the GEMMs) and
+copies (16.9 GB) are far larger than L2: no flush is needed between steps.
 
 Prints one JSON line.  ``value`` = tokens/s over the timed steps with inputs
 resident in HBM; ``e2e`` = the same with each step's tokens copied in from
 pinned host memory and the layer output copied back, inside the timed
 region.  ``roofline`` describes the dominant kernel (the gate/up grouped GEMM)
-timed with CUDA events recorded around it by the library on its own stream.
-``cpu_baseline`` times the CPU oracle on a bounded token sample.
+timed with CUDA events the library records around it on its own stream;
+``step_hbm`` relates the step's algorithmic HBM bytes to the measured HBM
+peak.  ``cpu_baseline`` times the CPU oracle on a bounded token sample.
+
+Workloads (--workload): r1_moe_layer_8k (default), r1_zipf_16k (Zipf-skewed
+routing, 16 hottest experts replicated), r1_moe_layer_256 (decode-like;
+--chunk-sweep reports exposed copy time per chunk size), r1_pipeline_4layer
+(4 layers per step with attention-sized GEMM stand-ins, T per step uniform in
+[6554, 8192], 16 steps) and r1_small_profile (for profiler captures).
 
 --impl reference runs the same metric with the CPU oracle on host cores.
 Multi-GPU: replicas only (each rank runs the same independent workload on
@@ -24,10 +31,12 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import subprocess
 import sys
 import time
+from collections import namedtuple
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -36,10 +45,18 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer tokens/s & TFLOP/s at 8K tokens, prefetch overlapped; % of TC peak"
 UNIT = "tokens/s"
 
-def _r1(T):
+Spec = namedtuple("Spec", "shape placement router_std bias")
+
+
+def _r1(T, zipf=False, router_std=0.02):
     def make():
         from moe_expert_grouped_split_gb300 import inputs as I
-        return I.r1_layer(T)
+        shape, placement = I.r1_layer(T)
+        bias = None
+        if zipf:
+            bias = I.zipf_bias(shape.E, 1.2, I.seed_for(0, "zipf"))
+            placement = I.split_placement(shape.E, 64, 3, redundant=I.hottest_experts(bias, 16))
+        return Spec(shape, placement, router_std, bias)
     return make
 
 
@@ -48,17 +65,19 @@ def _r1_small():
     shared expert and 1024 tokens (256 rows per expert, as at 8K tokens with
     256 experts and top-8): a few GB, for profiler captures."""
     from moe_expert_grouped_split_gb300 import inputs as I
-    return I.LayerShape(T=1024, H=7168, I=2048, E=16, k=4, S=1), I.split_placement(16, 4, 3)
+    return Spec(I.LayerShape(T=1024, H=7168, I=2048, E=16, k=4, S=1), I.split_placement(16, 4, 3), 0.02, None)
 
 
 WORKLOADS = {
     "r1_moe_layer_8k": _r1(8192),
-    "r1_moe_layer_256": _r1(256),
+    "r1_zipf_16k": _r1(16384, zipf=True),
+    "r1_moe_layer_256": _r1(256, router_std=1.0 / math.sqrt(7168)),
+    "r1_pipeline_4layer": _r1(8192),
     "r1_small_profile": _r1_small,
 }
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=20)
@@ -67,9 +86,10 @@ def parse():
     p.add_argument("--workload", default="r1_moe_layer_8k", choices=sorted(WORKLOADS))
     p.add_argument("--chunk-mb", type=float, default=32.0)
     p.add_argument("--copy-streams", type=int, default=1)
+    p.add_argument("--chunk-sweep", default="", help="comma-separated chunk sizes in MB (exposed copy per size)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extras", action="store_true", help="skip compute-only / copy-only / e2e legs")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 # ------------------------------------------------------------- helpers ----
@@ -123,6 +143,7 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.lines = []
 
     def __enter__(self):
         try:
@@ -147,7 +168,7 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, power = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in self.lines:
             f = [x.strip() for x in l.split(",")]
@@ -156,6 +177,7 @@ class ClockSampler:
             try:
                 sm.append(float(f[1]))
                 mx = float(f[2])
+                power.append(float(f[3]))
             except ValueError:
                 continue
             for n, v in zip(names, f[5:9]):
@@ -163,7 +185,8 @@ class ClockSampler:
                     reasons.add(n)
         sm.sort()
         med = sm[len(sm) // 2] if sm else None
-        return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
 
 
 def measured_peaks():
@@ -192,73 +215,82 @@ def whole_job_rate(units_per_rank_step: int, steps: int, world: int, ms_max: flo
     return world * steps * units_per_rank_step / (ms_max / 1e3)
 
 
+PHASES = ["route", "wait_stage", "gather", "gate_up_gemm", "down_gemm", "combine"]
+
+
 # -------------------------------------------------------- our arm ----------
 class Workload:
-    """Two R1-shaped layers (alternating) with their pools, a Runtime and the
-    per-step token batches, all resident in HBM."""
+    """n_layers R1-shaped layers with their pools, a Runtime, route buffers
+    and per-layer token batches, all resident in HBM."""
 
-    def __init__(self, make_shape, chunk_bytes, n_copy_streams, base_seed=0):
+    def __init__(self, spec: Spec, chunk_bytes, n_copy_streams, n_layers=2, base_seed=0):
         import torch
 
         from moe_expert_grouped_split_gb300 import binding as B
         from moe_expert_grouped_split_gb300 import inputs as I
 
         self.B, self.I, self.torch = B, I, torch
-        self.shape, self.placement = make_shape()
+        self.spec = spec
+        self.shape, self.placement = spec.shape, spec.placement
         sh = self.shape
-        self.layers = [I.make_layer(sh, self.placement, base_seed, l, device="cuda") for l in range(2)]
-        self.rt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, 2, self.placement.n_remote())
+        self.n_layers = n_layers
+        self.layers = [I.make_layer(sh, self.placement, base_seed, l, device="cuda", router_std=spec.router_std,
+                                    bias=spec.bias) for l in range(n_layers)]
+        self.rt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, n_layers, self.placement.n_remote())
         for l, lw in enumerate(self.layers):
             self.rt.set_layer(l, lw)
-        self.x = [I.make_tokens(sh.T, sh.H, base_seed, step=s, device="cuda") for s in range(2)]
+        self.x = [I.make_tokens(sh.T, sh.H, base_seed, step=s, device="cuda") for s in range(n_layers)]
         self.rb = B.RouteBuffers(sh.T, sh.E, sh.k)
         self.out = torch.empty((sh.T, sh.H), dtype=torch.bfloat16, device="cuda")
         self.compute = torch.cuda.Stream()
         self.copies = [torch.cuda.Stream() for _ in range(n_copy_streams)]
         self.chunk = int(chunk_bytes)
+        self.issue_s = []
+
+    def layer_step(self, layer, stage, T=None, x=None):
+        T = self.shape.T if T is None else T
+        x = (self.x[layer] if x is None else x)[:T]
+        with self.torch.cuda.stream(self.compute):
+            self.rt.route(x, self.layers[layer].wr, self.layers[layer].bias, self.rb, self.compute)
+            self.rt.moe(layer, stage, x, self.rb, self.out[:T], self.compute)
+
+    def prefetch(self, layer, stage):
+        t0 = time.perf_counter()
+        self.rt.prefetch(layer, stage, self.chunk, self.copies)
+        self.issue_s.append(time.perf_counter() - t0)
 
     def step(self, i, prefetch_next=True, x=None):
-        l = i % 2
-        x = self.x[l] if x is None else x
-        with self.torch.cuda.stream(self.compute):
-            self.rt.route(x, self.layers[l].wr, None, self.rb, self.compute)
-            self.rt.moe(l, l, x, self.rb, self.out, self.compute)
+        """Step i of the two-layer alternation: layer i%2 from stage i%2, and
+        the prefetch of layer (i+1)%2 into the other stage."""
+        l = i % self.n_layers
+        self.layer_step(l, i % 2, x=x)
         if prefetch_next:
-            self.rt.prefetch((i + 1) % 2, (i + 1) % 2, self.chunk, self.copies)
+            self.prefetch((i + 1) % self.n_layers, (i + 1) % 2)
 
     def prologue(self):
-        self.rt.prefetch(0, 0, self.chunk, self.copies)
+        self.prefetch(0, 0)
 
     def sync(self):
         self.torch.cuda.synchronize()
 
 
-def run_ours(args, rank, world, local_rank):
-    import torch
-
-    from moe_expert_grouped_split_gb300 import binding as B
-
-    torch.cuda.set_device(local_rank)
-    wl = Workload(WORKLOADS[args.workload], args.chunk_mb * (1 << 20), args.copy_streams)
-    sh = wl.shape
-    T = sh.T
-    K, W = args.steps, args.warmup
-    ev = lambda: torch.cuda.Event(enable_timing=True)
-
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-
-    # phase events per timed step (recorded by the library on the compute stream)
-    phases = [[ev() for _ in range(7)] for _ in range(K)]
-    for ps in phases:
-        for e in ps:
-            e.record(wl.compute)
+def _events(torch, n):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:          # create the underlying CUDA events now
+        e.record()
     torch.cuda.synchronize()
+    return evs
 
-    # ---- overlapped steps (the metric) ----
+
+def _phase_avg(phases, K):
+    ph = [[phases[i][j].elapsed_time(phases[i][j + 1]) for j in range(6)] for i in range(K)]
+    return {n_: round(sum(p[j] for p in ph) / K, 4) for j, n_ in enumerate(PHASES)}
+
+
+def run_overlapped(wl, K, W, world, phases, clocks_index=0, barrier=lambda: None):
+    """K timed steps (after W warm-up steps) of the two-layer alternation with
+    the next layer's prefetch overlapped; max over ranks."""
+    torch, B = wl.torch, wl.B
     wl.prologue()
     n = 0
     for i in range(W):
@@ -266,13 +298,14 @@ def run_ours(args, rank, world, local_rank):
         n += 1
     wl.sync()
     barrier()
-    start, stop = ev(), ev()
-    with ClockSampler(local_rank) as clk:
+    start, stop = _events(torch, 2)
+    with ClockSampler(clocks_index) as clk:
         start.record(wl.compute)
         for c in wl.copies:
             c.wait_stream(wl.compute)
         for i in range(K):
-            B.dwdp_set_phase_events(wl.rt.ctx, phases[i])
+            if phases is not None:
+                B.dwdp_set_phase_events(wl.rt.ctx, phases[i])
             wl.step(n)
             n += 1
         B.dwdp_set_phase_events(wl.rt.ctx, None)
@@ -281,79 +314,212 @@ def run_ours(args, rank, world, local_rank):
         stop.record(wl.compute)
         stop.synchronize()
     assert wl.rt.device_status() == 0
-    ms_total = start.elapsed_time(stop)
-    ms_total = max_over_ranks(ms_total, world)
-    barrier()
-    ms_step = ms_total / K
-    value = whole_job_rate(T, K, world, ms_total)
-    ph = [[phases[i][j].elapsed_time(phases[i][j + 1]) for j in range(6)] for i in range(K)]
-    avg = [sum(p[j] for p in ph) / K for j in range(6)]
-    names = ["route", "wait_stage", "gather", "gate_up_gemm", "down_gemm", "combine"]
-    phase_ms = {n_: round(a, 4) for n_, a in zip(names, avg)}
+    ms_total = max_over_ranks(start.elapsed_time(stop), world)
+    return ms_total, clk.summary()
 
-    res = {"ms_total": ms_total, "ms_step": ms_step, "value": value, "phase_ms": phase_ms, "clocks": clk.summary()}
 
-    if not args.no_extras:
-        # ---- compute only: same steps, every expert already staged, no copies ----
-        wl.sync()
-        for l in (0, 1):
-            wl.rt.prefetch(l, l, wl.chunk, wl.copies)
-        wl.sync()
-        a, b = ev(), ev()
-        for i in range(2):
-            wl.step(i, prefetch_next=False)
-        a.record(wl.compute)
-        for i in range(K):
+def run_compute_only(wl, K, phases=None):
+    """K steps with every expert already staged and no copies (the
+    all-resident reference for the exposed-prefetch figure)."""
+    torch, B = wl.torch, wl.B
+    wl.sync()
+    for l in (0, 1):
+        wl.prefetch(l, l)
+    wl.sync()
+    for i in range(2):
+        wl.step(i, prefetch_next=False)
+    a, b = _events(torch, 2)
+    a.record(wl.compute)
+    for i in range(K):
+        if phases is not None:
             B.dwdp_set_phase_events(wl.rt.ctx, phases[i])
-            wl.step(i, prefetch_next=False)
-        B.dwdp_set_phase_events(wl.rt.ctx, None)
-        b.record(wl.compute)
-        b.synchronize()
-        res["compute_only_ms_step"] = a.elapsed_time(b) / K
-        ph = [[phases[i][j].elapsed_time(phases[i][j + 1]) for j in range(6)] for i in range(K)]
-        res["compute_only_phase_ms"] = {n_: round(sum(p[j] for p in ph) / K, 4) for j, n_ in enumerate(names)}
-        # ---- copy only ----
-        a, b = ev(), ev()
-        a.record(wl.copies[0])
-        for i in range(K):
-            wl.rt.prefetch(i % 2, i % 2, wl.chunk, wl.copies)
-        b.record(wl.copies[0])
-        b.synchronize()
-        res["copy_only_ms_step"] = a.elapsed_time(b) / K
-        # ---- e2e: tokens in from pinned host memory, output back ----
-        xh = [x.cpu().pin_memory() for x in wl.x]
-        oh = torch.empty((T, sh.H), dtype=torch.bfloat16).pin_memory()
-        xd = torch.empty_like(wl.x[0])
-        for l in (0, 1):
-            wl.rt.prefetch(l, l, wl.chunk, wl.copies)
-        wl.sync()
-        wl.prologue()
-        for i in range(2):
-            with torch.cuda.stream(wl.compute):
-                xd.copy_(xh[i % 2], non_blocking=True)
-            wl.step(i, x=xd)
-            with torch.cuda.stream(wl.compute):
-                oh.copy_(wl.out, non_blocking=True)
-        wl.sync()
-        barrier()
-        a, b = ev(), ev()
+        wl.step(i, prefetch_next=False)
+    B.dwdp_set_phase_events(wl.rt.ctx, None)
+    b.record(wl.compute)
+    b.synchronize()
+    return a.elapsed_time(b) / K
+
+
+def run_copy_only(wl, K):
+    torch = wl.torch
+    wl.sync()
+    a, b = _events(torch, 2)
+    a.record(wl.copies[0])
+    for c in wl.copies[1:]:
+        c.wait_stream(wl.copies[0])
+    for i in range(K):
+        wl.prefetch(i % 2, i % 2)
+    b.record(wl.copies[0])
+    b.synchronize()
+    return a.elapsed_time(b) / K
+
+
+def run_e2e(wl, K, world, barrier=lambda: None):
+    """The metric through the public API with host buffers: each step copies
+    its tokens in from pinned host memory and its output back."""
+    torch = wl.torch
+    sh = wl.shape
+    T = sh.T
+    xh = [x.cpu().pin_memory() for x in wl.x]
+    oh = torch.empty((T, sh.H), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(wl.x[0])
+    wl.sync()
+    wl.prologue()
+    for i in range(2):
+        with torch.cuda.stream(wl.compute):
+            xd.copy_(xh[i % 2], non_blocking=True)
+        wl.step(i, x=xd)
+        with torch.cuda.stream(wl.compute):
+            oh.copy_(wl.out, non_blocking=True)
+    wl.sync()
+    barrier()
+    a, b = _events(torch, 2)
+    a.record(wl.compute)
+    for c in wl.copies:
+        c.wait_stream(wl.compute)
+    for i in range(2, 2 + K):
+        with torch.cuda.stream(wl.compute):
+            xd.copy_(xh[i % 2], non_blocking=True)
+        wl.step(i, x=xd)
+        with torch.cuda.stream(wl.compute):
+            oh.copy_(wl.out, non_blocking=True)
+    for c in wl.copies:
+        wl.compute.wait_stream(c)
+    b.record(wl.compute)
+    b.synchronize()
+    assert wl.rt.device_status() == 0
+    e2e_ms = max_over_ranks(a.elapsed_time(b), world)
+    return {"value": round(whole_job_rate(T, K, world, e2e_ms), 1), "unit": UNIT,
+            "h2d_bytes_per_step": T * sh.H * 2, "d2h_bytes_per_step": T * sh.H * 2}
+
+
+def run_layer_bench(args, world, local_rank, barrier):
+    """The single-layer workloads (8K default, Zipf 16K, 256 tokens)."""
+    import torch
+    torch.cuda.set_device(local_rank)
+    spec = WORKLOADS[args.workload]()
+    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams)
+    sh = wl.shape
+    K, W = args.steps, args.warmup
+    phases = [_events(torch, 7) for _ in range(K)]
+    ms_total, clocks = run_overlapped(wl, K, W, world, phases, local_rank, barrier)
+    barrier()
+    res = {"ms_step": ms_total / K, "value": whole_job_rate(sh.T, K, world, ms_total),
+           "phase_ms": _phase_avg(phases, K), "clocks": clocks,
+           "issue_ms": round(1e3 * sum(wl.issue_s) / max(1, len(wl.issue_s)), 3)}
+    e_active = int((wl.rb.counts[: sh.E] > 0).sum().item())
+    res["e_active"] = e_active
+    if not args.no_extras:
+        res["compute_only_ms"] = run_compute_only(wl, K, phases)
+        res["compute_only_phase_ms"] = _phase_avg(phases, K)
+        res["copy_only_ms"] = run_copy_only(wl, K)
+        res["e2e"] = run_e2e(wl, K, world, barrier)
+    if args.chunk_sweep:
+        sweep = []
+        comp = res.get("compute_only_ms") or run_compute_only(wl, K)
+        for mb in [float(v) for v in args.chunk_sweep.split(",") if v]:
+            wl.chunk = int(mb * (1 << 20))
+            wl.issue_s = []
+            ms, _ = run_overlapped(wl, K, W, world, None, local_rank, barrier)
+            issue = 1e3 * sum(wl.issue_s) / max(1, len(wl.issue_s))
+            copy = run_copy_only(wl, K)
+            over = ms / K
+            exposed = max(0.0, over - comp)
+            sweep.append({"chunk_mb": mb, "overlapped_ms": round(over, 4), "copy_only_ms": round(copy, 4),
+                          "compute_only_ms": round(comp, 4), "exposed_ms": round(exposed, 4),
+                          "hidden_frac": round(max(0.0, 1 - exposed / copy), 4) if copy > 0 else None,
+                          "host_issue_ms_per_prefetch": round(issue, 3),
+                          "slices_per_prefetch": len(wl.B.dwdp_plan_prefetch(
+                              sh.E, sh.H, sh.I, wl.placement.local_slot, wl.placement.peer_id,
+                              wl.placement.peer_slot, wl.placement.n_peers, wl.chunk))})
+        res["chunk_sweep"] = sweep
+    res["wl"] = wl
+    return res
+
+
+def run_pipeline_bench(args, world, local_rank, barrier):
+    """Four distinct R1 layers per step with an attention-sized GEMM
+    stand-in (x . W_attn, T x 7168 x 7168, on this library's grouped GEMM)
+    after each MoE layer; layer l+1's experts are prefetched while layer l's
+    MoE block and layer l+1's stand-in run (DWDP §2).  T per step is
+    uniform in [6554, 8192] (0.8x-1.0x of 8K), 16 steps by default."""
+    import numpy as np
+    import torch
+
+    from moe_expert_grouped_split_gb300 import binding as B
+    from moe_expert_grouped_split_gb300 import inputs as I
+
+    torch.cuda.set_device(local_rank)
+    spec = WORKLOADS[args.workload]()
+    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, n_layers=4)
+    sh = wl.shape
+    steps = args.steps
+    Ts = I.step_token_counts(steps + args.warmup, 6554, 8192, 0)
+    w_attn = I.randn_bf16((1, sh.H, sh.H), 0.02, I.seed_for(0, "W_attn"), "cuda")
+    scratch = torch.empty((sh.T, sh.H), dtype=torch.bfloat16, device="cuda")
+    offs = torch.zeros((len(Ts), 4), dtype=torch.int32)
+    offs[:, 1] = torch.tensor(Ts, dtype=torch.int32)
+    offs = offs.cuda()
+
+    def attn_standin(l, s):
+        x = wl.x[l][: Ts[s]]
+        with torch.cuda.stream(wl.compute):
+            B.dwdp_grouped_gemm(wl.rt.ctx, B.EPI_BF16, x, Ts[s], sh.H, sh.H, offs[s], 1, [w_attn], [0, 0],
+                                scratch, wl.compute)
+
+    def run(s_from, s_to, with_copies, layer_of=lambda g: g % 4):
+        g = s_from * 4
+        for s in range(s_from, s_to):
+            for l in range(4):
+                lay = layer_of(g)
+                stage = g % 2 if with_copies else lay % 2
+                wl.layer_step(lay, stage, T=Ts[s])
+                if with_copies:
+                    wl.prefetch(layer_of(g + 1), (g + 1) % 2)
+                attn_standin(layer_of(g + 1), s)
+                g += 1
+
+    ev = lambda: _events(torch, 2)
+    # overlapped: prologue (layer 0 into stage 0) outside the timed steps
+    wl.prefetch(0, 0)
+    run(0, args.warmup, True)
+    wl.sync()
+    barrier()
+    a, b = ev()
+    with ClockSampler(local_rank) as clk:
         a.record(wl.compute)
         for c in wl.copies:
             c.wait_stream(wl.compute)
-        for i in range(2, 2 + K):
-            with torch.cuda.stream(wl.compute):
-                xd.copy_(xh[i % 2], non_blocking=True)
-            wl.step(i, x=xd)
-            with torch.cuda.stream(wl.compute):
-                oh.copy_(wl.out, non_blocking=True)
+        run(args.warmup, args.warmup + steps, True)
         for c in wl.copies:
             wl.compute.wait_stream(c)
         b.record(wl.compute)
         b.synchronize()
-        e2e_ms = max_over_ranks(a.elapsed_time(b), world)
-        res["e2e"] = {"value": whole_job_rate(T, K, world, e2e_ms), "unit": UNIT,
-                      "h2d_bytes_per_step": T * sh.H * 2, "d2h_bytes_per_step": T * sh.H * 2}
-        assert wl.rt.device_status() == 0
+    assert wl.rt.device_status() == 0
+    ms = max_over_ranks(a.elapsed_time(b), world)
+    tokens = 4 * sum(Ts[args.warmup:])
+    res = {"ms_step": ms / steps, "value": world * tokens / (ms / 1e3), "clocks": clk.summary()}
+    if not args.no_extras:
+        # compute only: the same sequence with layers 0 and 1 (staged once)
+        # standing in for 2 and 3 (same shapes, same routing statistics)
+        wl.sync()
+        wl.prefetch(0, 0)
+        wl.prefetch(1, 1)
+        wl.sync()
+        a, b = ev()
+        a.record(wl.compute)
+        run(args.warmup, args.warmup + steps, False, layer_of=lambda g: g % 2)
+        b.record(wl.compute)
+        b.synchronize()
+        res["compute_only_ms"] = a.elapsed_time(b) / steps
+        a, b = ev()
+        a.record(wl.copies[0])
+        for g in range(4 * steps):
+            wl.prefetch(g % 4, g % 2)
+        b.record(wl.copies[0])
+        b.synchronize()
+        res["copy_only_ms"] = a.elapsed_time(b) / steps
+    res["tokens_per_step"] = [int(t) for t in Ts[args.warmup:]]
     res["wl"] = wl
     return res
 
@@ -374,6 +540,7 @@ def cpu_baseline_sample(wl, target_s=15.0, max_tokens=512):
     rng = np.random.default_rng(1234)
     order = rng.permutation(sh.T)
     wr = I.bf16_bits(lw.wr)
+    bias = None if lw.bias is None else lw.bias.cpu().numpy()
     cache = {}
     pl = lw.placement
 
@@ -389,27 +556,28 @@ def cpu_baseline_sample(wl, target_s=15.0, max_tokens=512):
         w2s = [cache.get(e, (None, None))[1] for e in range(sh.E)]
         return w13s, w2s
 
-    sw13, sw2 = I.bf16_bits(lw.shared_w13), I.bf16_bits(lw.shared_w2)
+    sw13 = I.bf16_bits(lw.shared_w13) if lw.shared_w13 is not None else None
+    sw2 = I.bf16_bits(lw.shared_w2) if lw.shared_w2 is not None else None
 
     def run(tokens):
         xs = np.ascontiguousarray(x[tokens])
-        r_pre = o.route(xs, wr, None, sh.k)            # routing, untimed pass to learn the experts
+        r_pre = o.route(xs, wr, bias, sh.k)            # routing, untimed pass to learn the experts
         w13s, w2s = weights_for(r_pre["ids"])          # host copies of those experts (untimed)
         t0 = time.perf_counter()
-        r = o.route(xs, wr, None, sh.k)
+        r = o.route(xs, wr, bias, sh.k)
         o.moe_tokens(xs, np.arange(len(tokens)), r["ids"], r["w"], w13s, w2s, sw13, sw2, mirrored=True)
         return time.perf_counter() - t0
 
     n = 8
     dt = run(order[:n])
     per_tok = dt / n
-    n2 = int(min(max_tokens, max(n, target_s / max(per_tok, 1e-9))))
+    n2 = int(min(max_tokens, sh.T, max(n, target_s / max(per_tok, 1e-9))))
     if n2 > n:
         dt = run(order[:n2])
         n = n2
-    return {"value": n / dt, "unit": UNIT, "cores": o.num_threads(), "kind": "oracle",
-            "sample": f"{n} seeded tokens of the {sh.T}-token R1-shaped layer (routing + 8 routed experts + "
-                      f"shared expert per token, fp64, {dt:.1f} s)"}
+    return {"value": round(n / dt, 3), "unit": UNIT, "cores": o.num_threads(), "kind": "oracle",
+            "sample": f"{n} seeded tokens of the {sh.T}-token R1-shaped layer (routing + {sh.k} routed experts"
+                      f"{' + shared expert' if sh.S else ''} per token, fp64, {dt:.1f} s)"}
 
 
 def main():
@@ -429,24 +597,20 @@ def main():
     from moe_expert_grouped_split_gb300.build import build
     if rank == 0 or world == 1:
         build()
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
 
-    res = run_ours(args, rank, world, local_rank)
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    barrier()
+    pipeline = args.workload == "r1_pipeline_4layer"
+    res = (run_pipeline_bench if pipeline else run_layer_bench)(args, world, local_rank, barrier)
     wl = res.pop("wl")
     sh = wl.shape
     peaks, src = measured_peaks()
-    flops_layer = layer_flops(sh.T, sh.H, sh.I, sh.E, sh.k, sh.S)
-    g1 = g1_flops(sh.T, sh.H, sh.I, sh.k, sh.S)
-    g1_ms = res["phase_ms"]["gate_up_gemm"]
-    g1_tflops = g1 / (g1_ms / 1e3) / 1e12
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     hbm = peaks["hbm_gbs"]
-    e_active = int((wl.rb.counts[: sh.E] > 0).sum().item())
-    g1b = g1_bytes(sh.T, sh.H, sh.I, e_active, sh.k, sh.S)
-    sb = step_bytes(sh.T, sh.H, sh.I, e_active, sh.k, sh.S, wl.placement.n_remote())
-    layer_tflops = flops_layer / (res["ms_step"] / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": round(res["value"], 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_step"], 4),
@@ -455,36 +619,67 @@ def main():
         "config": {"workload": args.workload, "T": sh.T, "H": sh.H, "I": sh.I, "E": sh.E, "k": sh.k,
                    "shared": sh.S, "local_experts": int((wl.placement.local_slot >= 0).sum()),
                    "remote_experts": wl.placement.n_remote(), "peer_pools": wl.placement.n_peers,
-                   "chunk_mb": args.chunk_mb, "copy_streams": args.copy_streams, "layers_alternating": 2,
-                   "l2": "inputs larger than L2 (22.6 GB of expert weights + 16.9 GB of copies per step)",
+                   "chunk_mb": args.chunk_mb, "copy_streams": args.copy_streams,
+                   "layers": wl.n_layers,
+                   "l2": "inputs larger than L2 (22.6 GB of expert weights + 16.9 GB of copies per layer)",
                    "parallelism": "replicas" if world > 1 else "single rank"},
-        "tflops": round(layer_tflops, 1),
-        "tc_peak_frac": round(layer_tflops / peak, 4),
-        "phase_ms": res["phase_ms"],
-        "roofline": {"kernel": "gate_up_grouped_gemm", "bound": "tensor", "achieved": round(g1_tflops, 1),
-                     "peak": peak, "unit": "TFLOP/s", "frac": round(g1_tflops / peak, 4),
-                     "traffic": measured_traffic(os.path.join(ROOT, "moe_expert_grouped_split_gb300", "csrc",
-                                                              "gemm.cu")),
-                     "algorithmic_bytes_per_launch": g1b,
-                     "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside a long step)",
-                     "algorithmic_flops_per_launch": g1},
-        "step_hbm": {"bound": "hbm", "achieved": round(sb / (res["ms_step"] / 1e3) / 1e9, 1), "peak": hbm,
-                     "unit": "GB/s", "frac": round(sb / (res["ms_step"] / 1e3) / 1e9 / hbm, 4),
-                     "algorithmic_bytes_per_step": sb, "peak_source": f"{src} hbm_gbs"},
         "clocks": res["clocks"],
-        "gpu_launches": 8 * args.steps,
     }
-    if "e2e" in res:
-        line["e2e"] = {k_: (round(v, 1) if isinstance(v, float) else v) for k_, v in res["e2e"].items()}
-        comp, copy = res["compute_only_ms_step"], res["copy_only_ms_step"]
+    if pipeline:
+        flops = sum(4 * (layer_flops(T, sh.H, sh.I, sh.E, sh.k, sh.S) + 2 * T * sh.H * sh.H)
+                    for T in res["tokens_per_step"]) / len(res["tokens_per_step"])
+        line["config"]["tokens_per_step"] = res["tokens_per_step"]
+        line["config"]["attention_standin"] = "bf16 GEMM T x 7168 x 7168 after every MoE layer"
+        line["tflops"] = round(flops / (res["ms_step"] / 1e3) / 1e12, 1)
+        line["gpu_launches"] = args.steps * 4 * 9
+    else:
+        flops_layer = layer_flops(sh.T, sh.H, sh.I, sh.E, sh.k, sh.S)
+        g1 = g1_flops(sh.T, sh.H, sh.I, sh.k, sh.S)
+        g1_tflops = g1 / (res["phase_ms"]["gate_up_gemm"] / 1e3) / 1e12
+        g1b = g1_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S)
+        sb = step_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S, wl.placement.n_remote())
+        layer_tflops = flops_layer / (res["ms_step"] / 1e3) / 1e12
+        traffic = None
+        if args.workload == "r1_moe_layer_8k":
+            traffic = measured_traffic(os.path.join(ROOT, "moe_expert_grouped_split_gb300", "csrc", "gemm.cu"))
+        g1_s = res["phase_ms"]["gate_up_gemm"] / 1e3
+        if g1 / g1b >= peak * 1e12 / (hbm * 1e9):     # arithmetic intensity at or above the ridge
+            roof = {"kernel": "gate_up_grouped_gemm", "bound": "tensor", "achieved": round(g1_tflops, 1),
+                    "peak": peak, "unit": "TFLOP/s", "frac": round(g1_tflops / peak, 4),
+                    "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside a long step)"}
+        else:
+            gbs = g1b / g1_s / 1e9
+            roof = {"kernel": "gate_up_grouped_gemm", "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
+                    "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_source": f"{src} hbm_gbs"}
+        roof.update({"traffic": traffic, "algorithmic_flops_per_launch": g1, "algorithmic_bytes_per_launch": g1b,
+                     "arithmetic_intensity": round(g1 / g1b, 1)})
+        line.update({
+            "tflops": round(layer_tflops, 1),
+            "tc_peak_frac": round(layer_tflops / peak, 4),
+            "phase_ms": res["phase_ms"],
+            "roofline": roof,
+            "step_hbm": {"bound": "hbm", "achieved": round(sb / (res["ms_step"] / 1e3) / 1e9, 1), "peak": hbm,
+                         "unit": "GB/s", "frac": round(sb / (res["ms_step"] / 1e3) / 1e9 / hbm, 4),
+                         "algorithmic_bytes_per_step": sb, "peak_source": f"{src} hbm_gbs"},
+            "host_issue_ms_per_prefetch": res["issue_ms"],
+            "gpu_launches": 8 * args.steps,
+        })
+        if "chunk_sweep" in res:
+            line["chunk_sweep"] = res["chunk_sweep"]
+    if "compute_only_ms" in res:
+        comp, copy = res["compute_only_ms"], res["copy_only_ms"]
         exposed = max(0.0, res["ms_step"] - comp)
-        line["prefetch"] = {"compute_only_ms": round(comp, 4), "copy_only_ms": round(copy, 4),
-                            "overlapped_ms": round(res["ms_step"], 4), "exposed_ms": round(exposed, 4),
-                            "hidden_frac": round(max(0.0, 1.0 - exposed / copy), 4) if copy > 0 else None,
-                            "model_max_ms": round(max(comp, copy), 4),
-                            "copy_gbs": round(wl.placement.n_remote() * 3 * sh.H * sh.I * 2 / (copy / 1e3) / 1e9, 1),
-                            "compute_only_phase_ms": res["compute_only_phase_ms"]}
-    if rank == 0 and not args.no_cpu_baseline:
+        pre = {"compute_only_ms": round(comp, 4), "copy_only_ms": round(copy, 4),
+               "overlapped_ms": round(res["ms_step"], 4), "exposed_ms": round(exposed, 4),
+               "hidden_frac": round(max(0.0, 1.0 - exposed / copy), 4) if copy > 0 else None,
+               "model_max_ms": round(max(comp, copy), 4)}
+        if not pipeline:
+            pre["copy_gbs"] = round(wl.placement.n_remote() * 3 * sh.H * sh.I * 2 / (copy / 1e3) / 1e9, 1)
+            pre["compute_only_phase_ms"] = res["compute_only_phase_ms"]
+        line["prefetch"] = pre
+    if "e2e" in res:
+        line["e2e"] = res["e2e"]
+    if rank == 0 and not args.no_cpu_baseline and not pipeline:
         line["cpu_baseline"] = cpu_baseline_sample(wl)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -503,12 +698,13 @@ def main_reference(args, rank, world):
     import oracle
     from moe_expert_grouped_split_gb300 import inputs as I
 
-    shape, placement = WORKLOADS[args.workload]()
+    spec = WORKLOADS[args.workload]()
+    shape = spec.shape
     T = shape.T
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     o = oracle.default()
     x_all = I.bf16_bits(I.make_tokens(T, shape.H, 0, device=dev))
-    wr = I.bf16_bits(I.randn_bf16((shape.E, shape.H), 0.02, I.seed_for(0, "Wr", 0), dev))
+    wr = I.bf16_bits(I.randn_bf16((shape.E, shape.H), spec.router_std, I.seed_for(0, "Wr", 0), dev))
     rng = np.random.default_rng(99)
     per_step = 4
     cache = {}
@@ -519,20 +715,22 @@ def main_reference(args, rank, world):
                         I.bf16_bits(I.randn_bf16((shape.H, shape.I), 0.02, I.seed_for(0, "W2", 0, e), dev)))
         return cache[e]
 
-    sw13 = I.bf16_bits(I.randn_bf16((2 * shape.I, shape.H), 0.02, I.seed_for(0, "W13s", 0), dev))
-    sw2 = I.bf16_bits(I.randn_bf16((shape.H, shape.I), 0.02, I.seed_for(0, "W2s", 0), dev))
+    sw13 = sw2 = None
+    if shape.S:
+        sw13 = I.bf16_bits(I.randn_bf16((2 * shape.I, shape.H), 0.02, I.seed_for(0, "W13s", 0), dev))
+        sw2 = I.bf16_bits(I.randn_bf16((shape.H, shape.I), 0.02, I.seed_for(0, "W2s", 0), dev))
     times = []
     ntok = 0
     for s in range(args.warmup + args.steps):
         tok = rng.choice(T, size=per_step, replace=False)
         xs = np.ascontiguousarray(x_all[tok])
-        pre = o.route(xs, wr, None, shape.k)
+        pre = o.route(xs, wr, spec.bias, shape.k)
         for e in np.unique(pre["ids"]):
             expert(int(e))
         w13s = [cache[e][0] if e in cache else None for e in range(shape.E)]
         w2s = [cache[e][1] if e in cache else None for e in range(shape.E)]
         t0 = time.perf_counter()
-        r = o.route(xs, wr, None, shape.k)
+        r = o.route(xs, wr, spec.bias, shape.k)
         o.moe_tokens(xs, np.arange(per_step), r["ids"], r["w"], w13s, w2s, sw13, sw2, mirrored=True)
         dt = time.perf_counter() - t0
         if s >= args.warmup:
@@ -540,8 +738,7 @@ def main_reference(args, rank, world):
             ntok += per_step
     total = sum(times)
     value = ntok / total
-    tokens_per_step = T
-    ms_step = tokens_per_step / value * 1e3
+    ms_step = T / value * 1e3
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 1),

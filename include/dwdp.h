@@ -172,11 +172,15 @@ int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router
 /* Pull layer `layer`'s non-resident experts from their peer pools into stage
  * buffer `stage` ([DWDP] §2: asynchronous prefetch of layer l+1 during layer
  * l, double-buffered; §4.3.2: fixed-size slices, round-robin over sources).
- * Each slice is one cudaMemcpyAsync (copy engine) of at most chunk_bytes;
- * slices from peer p go to copy_streams[p % n_copy_streams].  The copies wait
- * until the last dwdp_moe_layer that read this stage has finished reading it,
- * and completion is recorded as the stage's "ready" event.  Errors:
- * INVALID_ARG, NOT_MAPPED, CUDA. */
+ * Each slice is one device-to-device memcpy node (copy engine, no SMs) of at
+ * most chunk_bytes in a CUDA graph that the context builds on first use for
+ * this (chunk_bytes, stage, n_copy_streams) and keeps until the layer's map
+ * is replaced; slices from peer p form chain p % n_copy_streams of the graph
+ * (chains may run on separate copy engines), each chain in plan order.  The
+ * graph is launched on copy_streams[0] (the other streams are not used)
+ * after that stream waits until the last dwdp_moe_layer that read this
+ * stage has finished reading it; completion is recorded as the stage's
+ * "ready" event.  Errors: INVALID_ARG, NOT_MAPPED, CUDA. */
 int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t chunk_bytes,
                             dwdp_stream_t const* copy_streams, int32_t n_copy_streams);
 

@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <tuple>
 #include <memory>
 #include <mutex>
 #include <string>
@@ -58,6 +59,12 @@ struct LayerMap {
     CUtensorMap local13{}, local2{}, shared13{}, shared2{};
     std::vector<int2> bsrc;  // [E + n_shared]
     std::map<size_t, std::vector<dwdp_copy_slice>> plans;
+    // copy plans as CUDA graphs of memcpy nodes, keyed by (chunk, stage, chains)
+    std::map<std::tuple<size_t, int, int>, cudaGraphExec_t> graphs;
+    void release() {
+        for (auto& kv : graphs) cudaGraphExecDestroy(kv.second);
+        graphs.clear();
+    }
 };
 
 }  // namespace
@@ -104,7 +111,6 @@ struct dwdp_ctx {
     CUtensorMap stage_map13[2]{}, stage_map2[2]{};
     cudaEvent_t ready[2] = {nullptr, nullptr};
     cudaEvent_t freed[2] = {nullptr, nullptr};
-    std::vector<cudaEvent_t> join;
     int stage_layer[2] = {-1, -1};
     std::vector<LayerMap> layers;
     int* d_err = nullptr;
@@ -282,11 +288,6 @@ int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* cons
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->freed[s], cudaEventDisableTiming);
         if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaEventCreate");
     }
-    ctx->join.resize(DWDP_MAX_PEERS, nullptr);
-    for (auto& ev : ctx->join) {
-        e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-        if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaEventCreate");
-    }
     e = cudaMalloc(&ctx->d_err, 256);
     if (e == cudaSuccess) e = cudaMemset(ctx->d_err, 0, 256);
     if (e != cudaSuccess) return cuda_fail(nullptr, e, "error word");
@@ -311,8 +312,7 @@ void dwdp_destroy(dwdp_ctx* ctx) {
         if (ctx->ready[s]) cudaEventDestroy(ctx->ready[s]);
         if (ctx->freed[s]) cudaEventDestroy(ctx->freed[s]);
     }
-    for (auto ev : ctx->join)
-        if (ev) cudaEventDestroy(ev);
+    for (LayerMap& m : ctx->layers) m.release();
     if (ctx->d_err) cudaFree(ctx->d_err);
     delete ctx;
 }
@@ -390,6 +390,7 @@ int32_t dwdp_set_expert_map(dwdp_ctx* ctx, int32_t layer, const dwdp_pool* local
         m.bsrc[e] = (local_slot[e] >= 0) ? make_int2(0, local_slot[e]) : make_int2(1, m.stage_slot[e]);
     if (c.n_shared) m.bsrc[E] = make_int2(2, 0);
     m.mapped = true;
+    ctx->layers[layer].release();
     ctx->layers[layer] = std::move(m);
     for (int s = 0; s < 2; ++s)
         if (ctx->stage_layer[s] == layer) ctx->stage_layer[s] = -1;  // staged bytes follow the old map
@@ -485,19 +486,37 @@ int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t 
             return fail(ctx, DWDP_ERR_INVALID_ARG, "%s", why.c_str());
         it = m.plans.emplace(chunk_bytes, std::move(plan)).first;
     }
+    // The plan as one CUDA graph of memcpy nodes (built once per chunk size,
+    // stage and chain count): slices of peer p form chain p % n_copy_streams,
+    // in plan order, so one launch replaces thousands of host calls and the
+    // chains may run on separate copy engines.
+    const auto key = std::make_tuple(chunk_bytes, (int)stage, (int)n_copy_streams);
+    auto git = m.graphs.find(key);
+    if (git == m.graphs.end() && !it->second.empty()) {
+        cudaGraph_t g = nullptr;
+        DWDP_CUDA(ctx, cudaGraphCreate(&g, 0));
+        std::vector<cudaGraphNode_t> tail(n_copy_streams, nullptr);
+        char* dst_base[2] = {static_cast<char*>(ctx->stage13[stage]), static_cast<char*>(ctx->stage2[stage])};
+        cudaError_t e = cudaSuccess;
+        for (const dwdp_copy_slice& sl : it->second) {
+            const dwdp_pool& pp = m.peers[sl.peer];
+            const char* src = static_cast<const char*>(sl.tensor == 0 ? pp.w13 : pp.w2) + sl.src_offset;
+            cudaGraphNode_t& t = tail[sl.peer % n_copy_streams];
+            cudaGraphNode_t node;
+            e = cudaGraphAddMemcpyNode1D(&node, g, t ? &t : nullptr, t ? 1 : 0, dst_base[sl.tensor] + sl.dst_offset,
+                                         src, (size_t)sl.nbytes, cudaMemcpyDeviceToDevice);
+            if (e != cudaSuccess) break;
+            t = node;
+        }
+        cudaGraphExec_t exec = nullptr;
+        if (e == cudaSuccess) e = cudaGraphInstantiate(&exec, g, 0);
+        cudaGraphDestroy(g);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "building the prefetch graph");
+        git = m.graphs.emplace(key, exec).first;
+    }
     // The stage may be overwritten only once the last layer that read it is done.
-    for (int i = 0; i < n_copy_streams; ++i) DWDP_CUDA(ctx, cudaStreamWaitEvent(copy_streams[i], ctx->freed[stage], 0));
-    char* dst_base[2] = {static_cast<char*>(ctx->stage13[stage]), static_cast<char*>(ctx->stage2[stage])};
-    for (const dwdp_copy_slice& s : it->second) {
-        const dwdp_pool& pp = m.peers[s.peer];
-        const char* src = static_cast<const char*>(s.tensor == 0 ? pp.w13 : pp.w2) + s.src_offset;
-        DWDP_CUDA(ctx, cudaMemcpyAsync(dst_base[s.tensor] + s.dst_offset, src, (size_t)s.nbytes,
-                                       cudaMemcpyDeviceToDevice, copy_streams[s.peer % n_copy_streams]));
-    }
-    for (int i = 1; i < n_copy_streams; ++i) {
-        DWDP_CUDA(ctx, cudaEventRecord(ctx->join[i], copy_streams[i]));
-        DWDP_CUDA(ctx, cudaStreamWaitEvent(copy_streams[0], ctx->join[i], 0));
-    }
+    DWDP_CUDA(ctx, cudaStreamWaitEvent(copy_streams[0], ctx->freed[stage], 0));
+    if (git != m.graphs.end()) DWDP_CUDA(ctx, cudaGraphLaunch(git->second, copy_streams[0]));
     DWDP_CUDA(ctx, cudaEventRecord(ctx->ready[stage], copy_streams[0]));
     ctx->stage_layer[stage] = layer;
     return DWDP_OK;
