@@ -87,6 +87,8 @@ def parse(argv=None):
     p.add_argument("--chunk-mb", type=float, default=32.0)
     p.add_argument("--copy-streams", type=int, default=1)
     p.add_argument("--chunk-sweep", default="", help="comma-separated chunk sizes in MB (exposed copy per size)")
+    p.add_argument("--merge-copy", action="store_true",
+                   help="also time the merge-copy baseline (one contiguous weight buffer per layer)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extras", action="store_true", help="skip compute-only / copy-only / e2e legs")
     return p.parse_args(argv)
@@ -433,8 +435,104 @@ def run_layer_bench(args, world, local_rank, barrier):
                               sh.E, sh.H, sh.I, wl.placement.local_slot, wl.placement.peer_id,
                               wl.placement.peer_slot, wl.placement.n_peers, wl.chunk))})
         res["chunk_sweep"] = sweep
+    if args.merge_copy:
+        res["merge_copy"] = run_merge_baseline(wl, K, W)
     res["wl"] = wl
     return res
+
+
+def run_merge_baseline(wl, K, W):
+    """The pages' baseline before split-weight management (DWDP §4.2): the
+    grouped GEMM reads ONE contiguous [E] weight buffer, so after the
+    non-resident experts arrive the resident ones are merged into it with a
+    device-to-device copy on the critical path.  Built from the public ABI
+    only, in the variant most favourable to the baseline: the prefetch lands
+    directly in the merged buffer (stage slots 0..R-1) and only the resident
+    experts are copied (slots R..E-1), then the same kernels run on a map
+    in which every expert is resident in that buffer.  Returns ms per step
+    (overlapped and with every expert already staged) and the merge bytes."""
+    torch, B = wl.torch, wl.B
+    sh, pl = wl.shape, wl.placement
+    if (pl.local_slot >= 0).sum() != pl.n_local_slots or pl.n_remote() + pl.n_local_slots != sh.E:
+        return None   # redundant placements have no single merged layout
+    mrt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, 6, sh.E)
+    stage_slot = [-1] * sh.E
+    r = 0
+    for e in range(sh.E):
+        if pl.local_slot[e] < 0:
+            stage_slot[e] = r
+            r += 1
+    R = r
+    merged_slot = [stage_slot[e] if pl.local_slot[e] < 0 else R + int(pl.local_slot[e]) for e in range(sh.E)]
+    for l, lw in enumerate(wl.layers):
+        mrt.set_layer(l, lw)                               # layers 0, 1: where the prefetch reads from
+        for s in (0, 1):                                   # layers 2+2l+s: everything resident in merged[s]
+            local = B.pool(mrt.stage_w13[s], mrt.stage_w2[s])
+            B.dwdp_set_expert_map(mrt.ctx, 2 + 2 * l + s, local, [], merged_slot, [-1] * sh.E, [-1] * sh.E,
+                                  lw.shared_w13, lw.shared_w2)
+    w13_bytes = 2 * sh.I * sh.H * 2
+    w2_bytes = sh.H * sh.I * 2
+    n_local = pl.n_local_slots
+    merge_bytes = n_local * (w13_bytes + w2_bytes)
+    ev = lambda: torch.cuda.Event()
+    arrived = [ev(), ev()]
+    freed = [ev(), ev()]
+
+    def prefetch(l, s, copies=True):
+        wl.copies[0].wait_event(freed[s])
+        if copies:
+            mrt.prefetch(l, s, wl.chunk, wl.copies)
+        arrived[s].record(wl.copies[0])
+
+    def step(i, prefetch_next=True):
+        l, s = i % 2, i % 2
+        lw = wl.layers[l]
+        x = wl.x[l]
+        with torch.cuda.stream(wl.compute):
+            wl.compute.wait_event(arrived[s])
+            # the merge: resident experts into slots R.. of the stage's buffer
+            mrt.stage_w13[s][R:R + n_local].copy_(lw.local_w13[:n_local], non_blocking=True)
+            mrt.stage_w2[s][R:R + n_local].copy_(lw.local_w2[:n_local], non_blocking=True)
+            mrt.route(x, lw.wr, lw.bias, wl.rb, wl.compute)
+            mrt.moe(2 + 2 * l + s, s, x, wl.rb, wl.out, wl.compute)
+            freed[s].record(wl.compute)
+        if prefetch_next:
+            prefetch((i + 1) % 2, (i + 1) % 2)
+
+    wl.sync()
+    prefetch(0, 0)
+    for i in range(W):
+        step(i)
+    wl.sync()
+    a, b = _events(torch, 2)
+    a.record(wl.compute)
+    for c in wl.copies:
+        c.wait_stream(wl.compute)
+    for i in range(W, W + K):
+        step(i)
+    for c in wl.copies:
+        wl.compute.wait_stream(c)
+    b.record(wl.compute)
+    b.synchronize()
+    over = a.elapsed_time(b) / K
+    # every expert already staged: merge + compute only
+    wl.sync()
+    for l in (0, 1):
+        prefetch(l, l)
+    wl.sync()
+    for i in range(2):
+        step(i, prefetch_next=False)
+    a, b = _events(torch, 2)
+    a.record(wl.compute)
+    for i in range(K):
+        step(i, prefetch_next=False)
+    b.record(wl.compute)
+    b.synchronize()
+    comp = a.elapsed_time(b) / K
+    assert mrt.device_status() == 0
+    mrt.close()
+    return {"overlapped_ms": round(over, 4), "compute_only_ms": round(comp, 4),
+            "merge_bytes_per_layer": merge_bytes, "merged_experts_copied": n_local}
 
 
 def run_pipeline_bench(args, world, local_rank, barrier):
@@ -662,6 +760,7 @@ def main():
                          "unit": "GB/s", "frac": round(sb / (res["ms_step"] / 1e3) / 1e9 / hbm, 4),
                          "algorithmic_bytes_per_step": sb, "peak_source": f"{src} hbm_gbs"},
             "host_issue_ms_per_prefetch": res["issue_ms"],
+            "merge_copy_baseline": res.get("merge_copy"),
             "gpu_launches": 8 * args.steps,
         })
         if "chunk_sweep" in res:
@@ -676,6 +775,10 @@ def main():
         if not pipeline:
             pre["copy_gbs"] = round(wl.placement.n_remote() * 3 * sh.H * sh.I * 2 / (copy / 1e3) / 1e9, 1)
             pre["compute_only_phase_ms"] = res["compute_only_phase_ms"]
+            # kernel slowdown while the copy engine runs (analogue of the pages'
+            # communication-computation interference, DWDP appendix A)
+            pre["interference"] = {n_: round(res["phase_ms"][n_] / max(res["compute_only_phase_ms"][n_], 1e-9), 3)
+                                   for n_ in PHASES if n_ != "wait_stage"}
         line["prefetch"] = pre
     if "e2e" in res:
         line["e2e"] = res["e2e"]
