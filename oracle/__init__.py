@@ -58,6 +58,7 @@ _F32P = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
 _I32P = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
 _I64P = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
 _I64 = ctypes.c_int64
+_U8P = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
 
 
 def _u16(a) -> np.ndarray:
@@ -93,6 +94,17 @@ class Oracle:
         L.oracle_grouped_gemm.restype = None
         L.oracle_grouped_gemm.argtypes = [_U16P, _I64, _I32P, _I64, ctypes.POINTER(ctypes.c_void_p), _I64,
                                           ctypes.c_int, _F64P]
+        L.oracle_e4m3_to_double.restype = ctypes.c_double
+        L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_encode.restype = ctypes.c_uint8
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+        L.oracle_quantize_row_e4m3.restype = None
+        L.oracle_quantize_row_e4m3.argtypes = [_F32P, _I64, _U8P, ctypes.POINTER(ctypes.c_float)]
+        L.oracle_moe_tokens_fp8.restype = None
+        L.oracle_moe_tokens_fp8.argtypes = [
+            _U16P, _I64, _I64, _I64, _I64P, _I64, _I32P, _F64P,
+            ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), _F32P, _F32P,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_float, ctypes.c_int, _F64P]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         self.lib = L
@@ -224,6 +236,63 @@ class Oracle:
         d = np.zeros((rows, N), dtype=np.float64)
         self.lib.oracle_grouped_gemm(a, K, off, G, ptrs, N, int(epilogue), d)
         return d
+
+    # -- FP8 (E4M3) ---------------------------------------------------------
+    def e4m3_encode(self, v: float) -> int:
+        return int(self.lib.oracle_e4m3_encode(float(v)))
+
+    def e4m3_decode(self, code: int) -> float:
+        return self.lib.oracle_e4m3_to_double(int(code))
+
+    def quantize_row_e4m3(self, row) -> tuple:
+        """(codes uint8 [n], scale) of one row of binary32 values."""
+        r = np.ascontiguousarray(row, dtype=np.float32)
+        codes = np.zeros(r.size, dtype=np.uint8)
+        s = ctypes.c_float()
+        self.lib.oracle_quantize_row_e4m3(r, r.size, codes, ctypes.byref(s))
+        return codes, float(s.value)
+
+    def moe_tokens_fp8(self, x, tokens, ids, w, expert_w13, expert_w2, w13_scale, w2_scale,
+                       shared_w13=None, shared_w2=None, shared_s13=1.0, shared_s2=1.0,
+                       mirrored: bool = True) -> np.ndarray:
+        """Layer output rows with E4M3 expert weights (uint8 codes, per-tensor
+        scales) and per-row E4M3 activations; see dwdp_oracle.c."""
+        x = _u16(x)
+        T, H = x.shape
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        w = np.ascontiguousarray(w, dtype=np.float64)
+        k = ids.shape[1]
+        tok = np.ascontiguousarray(tokens, dtype=np.int64)
+        E = len(expert_w13)
+        keep, I = [], None
+        p13 = (ctypes.c_void_p * E)()
+        p2 = (ctypes.c_void_p * E)()
+        for e in range(E):
+            if expert_w13[e] is None:
+                continue
+            a13 = np.ascontiguousarray(expert_w13[e], dtype=np.uint8)
+            a2 = np.ascontiguousarray(expert_w2[e], dtype=np.uint8)
+            I = a13.shape[0] // 2
+            assert a13.shape == (2 * I, H) and a2.shape == (H, I)
+            keep += [a13, a2]
+            p13[e], p2[e] = a13.ctypes.data, a2.ctypes.data
+        for e in (np.unique(ids[tok]) if tok.size else []):
+            if p13[int(e)] is None:
+                raise ValueError(f"expert {int(e)} is routed to but has no weights")
+        s13 = s2 = None
+        if shared_w13 is not None:
+            s13 = np.ascontiguousarray(shared_w13, dtype=np.uint8)
+            s2 = np.ascontiguousarray(shared_w2, dtype=np.uint8)
+            I = s13.shape[0] // 2
+        sc13 = np.ascontiguousarray(w13_scale, dtype=np.float32)
+        sc2 = np.ascontiguousarray(w2_scale, dtype=np.float32)
+        out = np.zeros((tok.size, H), dtype=np.float64)
+        self.lib.oracle_moe_tokens_fp8(x, H, I, k, tok, tok.size, ids, w, p13, p2, sc13, sc2,
+                                       s13.ctypes.data if s13 is not None else None,
+                                       s2.ctypes.data if s2 is not None else None,
+                                       float(shared_s13), float(shared_s2), int(bool(mirrored)), out)
+        del keep
+        return out
 
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())

@@ -342,3 +342,155 @@ void oracle_grouped_gemm(const uint16_t* a, int64_t K, const int32_t* row_offset
         }
     }
 }
+
+/* ------------------------------------------------------- FP8 (E4M3) -- */
+
+/* The FP8 path (next row of the build, not on the pages, which run NVFP4
+ * weights): expert weights are E4M3 codes with one scale per expert tensor;
+ * activations are quantized per row (per token for x, per (token, expert)
+ * row for a) to E4M3 with scale = amax / 448.
+ *
+ * E4M3 as used here: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits;
+ * no infinities; 0x7F / 0xFF are NaN; largest finite 448 = 1.75 * 2^8;
+ * smallest normal 2^-6; subnormals are multiples of 2^-9.  Encoding rounds
+ * to nearest, ties to even, and saturates to +-448 ("satfinite"). */
+double oracle_e4m3_to_double(uint8_t b) {
+    int s = b >> 7, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+uint8_t oracle_e4m3_encode(double v) {
+    if (isnan(v)) return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    double r;
+    if (a >= 448.0) {
+        r = 448.0;
+    } else if (a == 0.0) {
+        return sign;
+    } else {
+        int e = ilogb(a);
+        if (e < -6) e = -6;                       /* subnormal range: quantum 2^-9 */
+#if ORACLE_MUTANT == 13
+        r = ldexp(floor(ldexp(a, 3 - e)), e - 3); /* planted: truncation */
+#else
+        r = ldexp(nearbyint(ldexp(a, 3 - e)), e - 3);
+#endif
+        if (r > 448.0) r = 448.0;
+    }
+    if (r == 0.0) return sign;
+    int er = ilogb(r);
+    if (er < -6) return sign | (uint8_t)(r / ldexp(1.0, -9));         /* subnormal */
+    int mant = (int)((r / ldexp(1.0, er) - 1.0) * 8.0);
+    return sign | (uint8_t)((er + 7) << 3) | (uint8_t)mant;
+}
+
+/* Quantize one row of n values (each a binary32 value) to E4M3 with
+ * scale = amax / 448 computed in binary32 (1 when the row is all zero); each
+ * code is the E4M3 encoding of the binary32 quotient v / scale.  Both
+ * divisions are binary32 operations, as the kernels perform them, so the
+ * codes are integer decisions taken in the kernels' precision. */
+void oracle_quantize_row_e4m3(const float* v, int64_t n, uint8_t* codes, float* scale) {
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(v[i]);
+        if (a > amax) amax = a;
+    }
+#if ORACLE_MUTANT == 14
+    float s = amax > 0.0f ? amax / 440.0f : 1.0f;   /* planted: wrong full-scale value */
+#else
+    float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+#endif
+    for (int64_t i = 0; i < n; ++i) {
+        volatile float q = v[i] / s;                 /* one binary32 rounding */
+        codes[i] = oracle_e4m3_encode((double)q);
+    }
+    *scale = s;
+}
+
+/* One expert on one token with E4M3 weights (w13 [2I][H], w2 [H][I] codes,
+ * per-tensor scales s13, s2): x is quantized per row, g and u are fp64 sums
+ * of products of decoded codes times sx * s13, a = SiLU(g) * u (bf16 in
+ * mirrored mode), a is quantized per row, y = fp64 sum times sa * s2 (bf16
+ * in mirrored mode).  xq / sx are the token's quantized row, computed once
+ * by the caller. */
+static void expert_ffn_fp8(const uint8_t* xq, float sx, int64_t H, int64_t I, const uint8_t* w13, float s13,
+                           const uint8_t* w2, float s2, int mirrored, float* a_tmp, uint8_t* aq_tmp, double* y) {
+    for (int64_t i = 0; i < I; ++i) {
+        const uint8_t* wg = w13 + i * H;
+        const uint8_t* wu = w13 + (I + i) * H;
+        double g = 0.0, u = 0.0;
+        for (int64_t h = 0; h < H; ++h) {
+            double xv = oracle_e4m3_to_double(xq[h]);
+            g += xv * oracle_e4m3_to_double(wg[h]);
+            u += xv * oracle_e4m3_to_double(wu[h]);
+        }
+#if ORACLE_MUTANT == 15
+        g *= (double)s13;                          /* planted: activation scale dropped */
+        u *= (double)s13;
+#else
+        g *= (double)sx * (double)s13;
+        u *= (double)sx * (double)s13;
+#endif
+        double a = g / (1.0 + exp(-g)) * u;
+        a_tmp[i] = (float)(mirrored ? rb(a) : a);
+    }
+    float sa;
+    oracle_quantize_row_e4m3(a_tmp, I, aq_tmp, &sa);
+    for (int64_t h = 0; h < H; ++h) {
+        const uint8_t* wd = w2 + h * I;
+        double s = 0.0;
+        for (int64_t i = 0; i < I; ++i) s += oracle_e4m3_to_double(aq_tmp[i]) * oracle_e4m3_to_double(wd[i]);
+        s *= (double)sa * (double)s2;
+        y[h] = mirrored ? rb(s) : s;
+    }
+}
+
+/* The FP8 layer for n_sel tokens: as oracle_moe_tokens, with E4M3 expert
+ * weights and scales (w13_scale[e], w2_scale[e]; shared_* for the shared
+ * expert, whose w13 may be NULL).  In strict mode (mirrored == 0) a is
+ * quantized from its fp64 value rounded once to binary32. */
+void oracle_moe_tokens_fp8(const uint16_t* x, int64_t H, int64_t I, int64_t k, const int64_t* tok, int64_t n_sel,
+                           const int32_t* ids, const double* w, const uint8_t* const* expert_w13,
+                           const uint8_t* const* expert_w2, const float* w13_scale, const float* w2_scale,
+                           const uint8_t* shared_w13, const uint8_t* shared_w2, float shared_s13,
+                           float shared_s2, int mirrored, double* out) {
+#pragma omp parallel
+    {
+        float* xr = (float*)malloc((size_t)H * sizeof(float));
+        uint8_t* xq = (uint8_t*)malloc((size_t)H);
+        float* a = (float*)malloc((size_t)I * sizeof(float));
+        uint8_t* aq = (uint8_t*)malloc((size_t)I);
+        double* y = (double*)malloc((size_t)H * sizeof(double));
+        double* acc = (double*)malloc((size_t)H * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t s = 0; s < n_sel; ++s) {
+            int64_t t = tok[s];
+            for (int64_t h = 0; h < H; ++h) xr[h] = (float)oracle_bf16_to_double(x[t * H + h]);
+            float sx;
+            oracle_quantize_row_e4m3(xr, H, xq, &sx);
+            for (int64_t h = 0; h < H; ++h) acc[h] = 0.0;
+            for (int64_t j = 0; j < k; ++j) {
+                int32_t e = ids[t * k + j];
+                expert_ffn_fp8(xq, sx, H, I, expert_w13[e], w13_scale[e], expert_w2[e], w2_scale[e], mirrored, a, aq,
+                               y);
+                for (int64_t h = 0; h < H; ++h) acc[h] += w[t * k + j] * y[h];
+            }
+            if (shared_w13) {
+                expert_ffn_fp8(xq, sx, H, I, shared_w13, shared_s13, shared_w2, shared_s2, mirrored, a, aq, y);
+                for (int64_t h = 0; h < H; ++h) acc[h] += y[h];
+            }
+            for (int64_t h = 0; h < H; ++h) out[s * H + h] = mirrored ? rb(acc[h]) : acc[h];
+        }
+        free(xr);
+        free(xq);
+        free(a);
+        free(aq);
+        free(y);
+        free(acc);
+    }
+}

@@ -357,3 +357,113 @@ def pin_grouped_gemm(o):
 
 
 ALL_PINS.append(pin_grouped_gemm)
+
+
+# ------------------------------------------------------------ FP8 (E4M3) --
+def _e4m3_torch(v32: np.ndarray) -> np.ndarray:
+    """E4M3 codes of binary32 values by torch's conversion (RNE, no
+    saturation: only used on values within +-464)."""
+    return torch.from_numpy(np.ascontiguousarray(v32, dtype=np.float32)).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
+
+
+def _e4m3_decode_torch(codes: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn) \
+        .to(torch.float64).numpy()
+
+
+def pin_e4m3(o):
+    rng = np.random.default_rng(13)
+    v = (rng.standard_normal(6000) * np.exp(rng.uniform(-9, 6, 6000))).astype(np.float32)
+    v = v[np.abs(v) <= 464]
+    got = np.array([o.e4m3_encode(float(a)) for a in v], dtype=np.uint8)
+    assert np.array_equal(got, _e4m3_torch(v)), "E4M3 encoding disagrees with torch"
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    dec = np.array([o.e4m3_decode(int(c)) for c in codes])
+    assert np.array_equal(dec, _e4m3_decode_torch(codes)), "E4M3 decoding disagrees with torch"
+    # saturation, ties to even, subnormals (by the format's definition)
+    assert o.e4m3_encode(1000.0) == 0x7E and o.e4m3_encode(-470.0) == 0xFE
+    assert o.e4m3_encode(1.0625) == 0x38          # tie between 1 and 1.125 -> even (1)
+    assert o.e4m3_encode(1.1875) == 0x3A          # tie between 1.125 and 1.25 -> even (1.25)
+    assert o.e4m3_encode(2.0 ** -9) == 0x01 and o.e4m3_encode(2.0 ** -10) == 0x00
+
+
+def pin_quantize_rows(o):
+    rng = np.random.default_rng(14)
+    for n in (1, 7, 256, 2048):
+        row = (rng.standard_normal(n) * rng.uniform(0.01, 50)).astype(np.float32)
+        codes, scale = o.quantize_row_e4m3(row)
+        amax = np.float32(np.abs(row).max())
+        assert scale == np.float32(amax / np.float32(448.0))
+        ref = _e4m3_torch(row / np.float32(scale))
+        assert np.array_equal(codes, ref), "row codes differ from torch's encoding of v / scale"
+        i = int(np.argmax(np.abs(row)))
+        assert codes[i] & 0x7F == 0x7E, "the row's largest value must map to +-448"
+        deq = _e4m3_decode_torch(codes) * scale
+        assert np.all(np.abs(deq - row) <= np.abs(row) * 2.0 ** -4 + scale * 2.0 ** -10)
+    codes, scale = o.quantize_row_e4m3(np.zeros(5, np.float32))
+    assert scale == 1.0 and not codes.any()
+
+
+def _fp8_layer(rng, T, H, I, E, S):
+    x = _rand_bits(rng, (T, H), 1.0)
+    wr = _rand_bits(rng, (E, H), 0.3)
+    mk = lambda shape: _e4m3_torch(rng.standard_normal(shape).astype(np.float32))
+    w13s = [mk((2 * I, H)) for _ in range(E)]
+    w2s = [mk((H, I)) for _ in range(E)]
+    s13 = rng.uniform(0.02, 0.05, E).astype(np.float32)
+    s2 = rng.uniform(0.02, 0.05, E).astype(np.float32)
+    sw = (mk((2 * I, H)), mk((H, I)), np.float32(0.03), np.float32(0.04)) if S else None
+    return x, wr, w13s, w2s, s13, s2, sw
+
+
+def _dense_fp8(x, ids, w, w13s, w2s, s13, s2, sw):
+    """Dense brute force of the FP8 layer: every expert on every token, torch's
+    E4M3 conversion for every quantization, numpy fp64 matmuls, a rounded
+    once to binary32 before its quantization (strict mode)."""
+    X32 = _decode(x).astype(np.float32)
+    T, H = X32.shape
+    E = len(w13s)
+    xs = np.abs(X32).max(axis=1) / np.float32(448.0)
+    xs[xs == 0] = 1
+    XQ = _e4m3_decode_torch(_e4m3_torch(X32 / xs[:, None])) * xs.astype(np.float64)[:, None]
+    G = np.zeros((T, E))
+    for t in range(T):
+        for j in range(ids.shape[1]):
+            G[t, ids[t, j]] += w[t, j]
+
+    def ffn(W13c, W2c, sc13, sc2):
+        W13 = _e4m3_decode_torch(W13c) * np.float64(sc13)
+        W2 = _e4m3_decode_torch(W2c) * np.float64(sc2)
+        I = W13.shape[0] // 2
+        A = (_silu(XQ @ W13[:I].T) * (XQ @ W13[I:].T)).astype(np.float32)
+        sa = np.abs(A).max(axis=1) / np.float32(448.0)
+        sa[sa == 0] = 1
+        AQ = _e4m3_decode_torch(_e4m3_torch(A / sa[:, None])) * sa.astype(np.float64)[:, None]
+        return AQ @ W2.T
+
+    out = np.zeros((T, H))
+    for e in range(E):
+        out += G[:, e:e + 1] * ffn(w13s[e], w2s[e], s13[e], s2[e])
+    if sw is not None:
+        out += ffn(*sw)
+    return out
+
+
+def pin_fp8_dense(o):
+    rng = np.random.default_rng(15)
+    for (T, H, I, E, k, S) in [(20, 32, 16, 5, 2, 1), (12, 64, 32, 3, 3, 0)]:
+        x, wr, w13s, w2s, s13, s2, sw = _fp8_layer(rng, T, H, I, E, S)
+        r = o.route(x, wr, None, k)
+        kw = {} if sw is None else dict(shared_w13=sw[0], shared_w2=sw[1], shared_s13=sw[2], shared_s2=sw[3])
+        got = o.moe_tokens_fp8(x, np.arange(T), r["ids"], r["w"], w13s, w2s, s13, s2, mirrored=False, **kw)
+        ref = _dense_fp8(x, r["ids"], r["w"], w13s, w2s, s13, s2, sw)
+        scale = np.sqrt((ref ** 2).mean())
+        assert np.max(np.abs(got - ref)) <= 1e-9 * max(1.0, scale), "FP8 layer != dense brute force"
+        # mirrored mode: bf16-valued outputs close to strict
+        m = o.moe_tokens_fp8(x, np.arange(T), r["ids"], r["w"], w13s, w2s, s13, s2, mirrored=True, **kw)
+        assert np.array_equal(_decode(_bits_from_f32(m.astype(np.float32))), m)
+        assert np.max(np.abs(m - got)) <= 0.1 * scale
+
+
+ALL_PINS += [pin_e4m3, pin_quantize_rows, pin_fp8_dense]

@@ -20,6 +20,9 @@ MUTANTS = {
     10: "router bias subtracted",
     11: "bf16 rounding truncates",
     12: "chosen set listed in descending id",
+    13: "E4M3 encoding truncates",
+    14: "activation full-scale value 440 instead of 448",
+    15: "FP8 activation scale dropped from the gate/up sums",
 }
 
 
