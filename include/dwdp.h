@@ -38,6 +38,8 @@
  *   w2  of one expert : [H][I]   = W_down^T
  *   a pool            : w13 [n_slots][2I][H] and w2 [n_slots][H][I]
  *   router weight     : [E][H]   row e = column e of the H x E gate matrix
+ * Expert weights are bf16, or 1-byte E4M3 codes in an E4M3 context; the
+ * router weight and the activations passed in and out are always bf16.
  */
 #ifndef DWDP_H_
 #define DWDP_H_
@@ -49,7 +51,7 @@
 extern "C" {
 #endif
 
-#define DWDP_ABI_VERSION 1
+#define DWDP_ABI_VERSION 2
 #define DWDP_MAX_EXPERTS 1024
 #define DWDP_MAX_TOPK 32
 #define DWDP_MAX_LAYERS 256
@@ -78,7 +80,18 @@ typedef struct {
     int32_t max_tokens;   /* largest T any call will pass */
     int32_t n_layers;     /* layers that get an expert map: 1..DWDP_MAX_LAYERS */
     int32_t stage_slots;  /* experts each staging buffer holds (0 = no staging) */
+    int32_t weight_dtype; /* DWDP_DTYPE_BF16, or DWDP_DTYPE_E4M3 (see below) */
 } dwdp_config;
+
+/* Expert weight types.  DWDP_DTYPE_E4M3 (an FP8 variant of the layer; the
+ * pages run NVFP4 expert weights, DWDP §5.1): pools and stage buffers hold
+ * 1-byte E4M3 codes (w = code * scale, one scale per expert tensor, given by
+ * dwdp_set_expert_scales); the layer quantizes its activations per row to
+ * E4M3 (scale = row amax / 448, binary32, round-to-nearest-even,
+ * saturating) before each expert GEMM, and the GEMMs run on FP8 tensor
+ * cores.  Routing stays bf16. */
+#define DWDP_DTYPE_BF16 0
+#define DWDP_DTYPE_E4M3 1
 
 /* One buffer of experts: w13 [n_slots][2I][H], w2 [n_slots][H][I] (device). */
 typedef struct {
@@ -156,6 +169,15 @@ int32_t dwdp_set_expert_map(dwdp_ctx* ctx, int32_t layer, const dwdp_pool* local
                             const dwdp_pool* peers, int32_t n_peers, const int32_t* local_slot,
                             const int32_t* peer_id, const int32_t* peer_slot,
                             const void* shared_w13, const void* shared_w2);
+
+/* Per-expert-tensor weight scales of layer `layer` for DWDP_DTYPE_E4M3
+ * contexts: expert e's gate/up weights are w13 codes * w13_scale[e], its down
+ * weights w2 codes * w2_scale[e] (host arrays [E]); shared_* for the shared
+ * expert (ignored when n_shared == 0).  Required before dwdp_moe_layer on an
+ * E4M3 context; kept until replaced.  Errors: INVALID_ARG (bf16 context, bad
+ * layer, non-finite or non-positive scale). */
+int32_t dwdp_set_expert_scales(dwdp_ctx* ctx, int32_t layer, const float* w13_scale, const float* w2_scale,
+                               float shared_w13_scale, float shared_w2_scale);
 
 /* Top-k routing with a deterministic grouping of the (token, slot) pairs by
  * expert.  x [T][H] bf16 and w_router [E][H] bf16 are device pointers;
@@ -272,9 +294,10 @@ int32_t dwdp_route_static(const void* x, int32_t T, int32_t hidden, int32_t n_ex
  * source and destination, cut into slices of chunk_bytes (the last one
  * short); slices are emitted round-robin over peers 0..n_peers-1.  Writes up
  * to max_out slices to out (may be NULL when max_out == 0) and the full count
- * to *n_out.  Errors: INVALID_ARG (bad map or a non-resident expert with no
+ * to *n_out.  elem_bytes is the size of one weight element (2 for bf16, 1
+ * for E4M3).  Errors: INVALID_ARG (bad map or a non-resident expert with no
  * peer copy). */
-int32_t dwdp_plan_prefetch(int32_t n_experts, int32_t hidden, int32_t inter,
+int32_t dwdp_plan_prefetch(int32_t n_experts, int32_t hidden, int32_t inter, int32_t elem_bytes,
                            const int32_t* local_slot, const int32_t* peer_id,
                            const int32_t* peer_slot, int32_t n_peers, size_t chunk_bytes,
                            dwdp_copy_slice* out, int64_t max_out, int64_t* n_out);

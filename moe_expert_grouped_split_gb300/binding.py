@@ -18,6 +18,7 @@ DWDP_OK = 0
 STATUS = {0: "OK", -1: "INVALID_ARG", -2: "NOT_MAPPED", -3: "CUDA", -4: "TIMEOUT", -5: "UNSUPPORTED",
           -6: "DEVICE_CHECK"}
 EPI_BF16, EPI_SILU, EPI_F32 = 0, 1, 2
+DTYPE_BF16, DTYPE_E4M3 = 0, 1
 
 
 class DwdpError(RuntimeError):
@@ -29,7 +30,7 @@ class DwdpError(RuntimeError):
 class dwdp_config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
-                ("n_layers", ctypes.c_int32), ("stage_slots", ctypes.c_int32)]
+                ("n_layers", ctypes.c_int32), ("stage_slots", ctypes.c_int32), ("weight_dtype", ctypes.c_int32)]
 
 
 class dwdp_pool(ctypes.Structure):
@@ -69,10 +70,12 @@ SIGNATURES = [
     ("dwdp_stage_layer", _I32, [_VP, _I32]),
     ("dwdp_device_status", _I32, [_VP]),
     ("dwdp_set_phase_events", _I32, [_VP, ctypes.POINTER(_VP), _I32]),
+    ("dwdp_set_expert_scales", _I32, [_VP, _I32, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float),
+                                      ctypes.c_float, ctypes.c_float]),
     ("dwdp_grouped_gemm", _I32, [_VP, _I32, _VP, ctypes.c_int64, _I32, _I32, _VP, _I32, ctypes.POINTER(dwdp_pool),
                                  _I32, _I32P, _VP, _VP]),
     ("dwdp_route_static", _I32, [_VP, _I32, _I32, _I32, _I32, _VP, _VP, ctypes.POINTER(dwdp_route_out), _VP]),
-    ("dwdp_plan_prefetch", _I32, [_I32, _I32, _I32, _I32P, _I32P, _I32P, _I32, ctypes.c_size_t,
+    ("dwdp_plan_prefetch", _I32, [_I32, _I32, _I32, _I32, _I32P, _I32P, _I32P, _I32, ctypes.c_size_t,
                                   ctypes.POINTER(dwdp_copy_slice), ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]),
 ]
 
@@ -128,8 +131,8 @@ def dwdp_version() -> int:
 
 
 def dwdp_create(hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots,
-                stage_w13=(None, None), stage_w2=(None, None)) -> int:
-    cfg = dwdp_config(hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots)
+                stage_w13=(None, None), stage_w2=(None, None), weight_dtype=DTYPE_BF16) -> int:
+    cfg = dwdp_config(hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots, weight_dtype)
     s13 = (_VP * 2)(_ptr(stage_w13[0]), _ptr(stage_w13[1]))
     s2 = (_VP * 2)(_ptr(stage_w2[0]), _ptr(stage_w2[1]))
     out = _VP()
@@ -230,16 +233,25 @@ def dwdp_route_static(x, T, hidden, n_experts, top_k, w_router, logit_bias, out:
                                          ctypes.byref(out), _stream(stream)))
 
 
-def dwdp_plan_prefetch(n_experts, hidden, inter, local_slot, peer_id, peer_slot, n_peers, chunk_bytes):
+def dwdp_set_expert_scales(ctx, layer, w13_scale, w2_scale, shared_w13_scale=1.0, shared_w2_scale=1.0) -> None:
+    s13 = np.ascontiguousarray(w13_scale, dtype=np.float32)
+    s2 = np.ascontiguousarray(w2_scale, dtype=np.float32)
+    fp = ctypes.POINTER(ctypes.c_float)
+    _check(ctx, lib().dwdp_set_expert_scales(ctx, layer, s13.ctypes.data_as(fp), s2.ctypes.data_as(fp),
+                                             float(shared_w13_scale), float(shared_w2_scale)))
+
+
+def dwdp_plan_prefetch(n_experts, hidden, inter, local_slot, peer_id, peer_slot, n_peers, chunk_bytes,
+                       elem_bytes=2):
     """The copy plan as a list of (peer, tensor, src_offset, dst_offset, nbytes)."""
     ls, lsp = _i32(local_slot)
     pi, pip = _i32(peer_id)
     ps, psp = _i32(peer_slot)
     n = ctypes.c_int64()
-    _check(None, lib().dwdp_plan_prefetch(n_experts, hidden, inter, lsp, pip, psp, n_peers, chunk_bytes,
+    _check(None, lib().dwdp_plan_prefetch(n_experts, hidden, inter, elem_bytes, lsp, pip, psp, n_peers, chunk_bytes,
                                           None, 0, ctypes.byref(n)))
     arr = (dwdp_copy_slice * max(1, n.value))()
-    _check(None, lib().dwdp_plan_prefetch(n_experts, hidden, inter, lsp, pip, psp, n_peers, chunk_bytes,
+    _check(None, lib().dwdp_plan_prefetch(n_experts, hidden, inter, elem_bytes, lsp, pip, psp, n_peers, chunk_bytes,
                                           arr, n.value, ctypes.byref(n)))
     return [(s.peer, s.tensor, s.src_offset, s.dst_offset, s.nbytes) for s in arr[: n.value]]
 
@@ -268,9 +280,9 @@ class Runtime:
     allocations); methods forward to the C ABI."""
 
     def __init__(self, hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots,
-                 device="cuda"):
+                 device="cuda", weight_dtype=DTYPE_BF16):
         import torch
-        bf = torch.bfloat16
+        bf = torch.uint8 if weight_dtype == DTYPE_E4M3 else torch.bfloat16
         self.cfg = dict(hidden=hidden, inter=inter, n_experts=n_experts, top_k=top_k, n_shared=n_shared,
                         max_tokens=max_tokens, n_layers=n_layers, stage_slots=stage_slots)
         if stage_slots > 0:
@@ -280,7 +292,7 @@ class Runtime:
             self.stage_w13 = [None, None]
             self.stage_w2 = [None, None]
         self.ctx = dwdp_create(hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots,
-                               self.stage_w13, self.stage_w2)
+                               self.stage_w13, self.stage_w2, weight_dtype)
         self.ws_bytes = max(256, dwdp_workspace_bytes(self.ctx, max_tokens))
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
         self._keep = {}
@@ -292,6 +304,8 @@ class Runtime:
         peers = [pool(a, b) for a, b in zip(lw.peer_w13, lw.peer_w2)]
         dwdp_set_expert_map(self.ctx, layer, local, peers, pl.local_slot, pl.peer_id, pl.peer_slot,
                             lw.shared_w13, lw.shared_w2)
+        if getattr(lw, "w13_scale", None) is not None:
+            dwdp_set_expert_scales(self.ctx, layer, lw.w13_scale, lw.w2_scale, lw.shared_s13, lw.shared_s2)
         self._keep[layer] = lw
 
     def route(self, x, w_router, bias, rb: RouteBuffers, stream=None) -> None:

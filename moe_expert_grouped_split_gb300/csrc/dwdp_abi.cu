@@ -7,6 +7,7 @@
 // to "DWDP: Distributed Weight Data Parallelism for High-Performance LLM
 // Inference on NVL72".
 #include <chrono>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -58,6 +59,7 @@ struct LayerMap {
     bool has_local_map = false;
     CUtensorMap local13{}, local2{}, shared13{}, shared2{};
     std::vector<int2> bsrc;  // [E + n_shared]
+    std::vector<float> scale13, scale2;  // E4M3 weight scales [E + n_shared] (empty until set)
     std::map<size_t, std::vector<dwdp_copy_slice>> plans;
     // copy plans as CUDA graphs of memcpy nodes, keyed by (chunk, stage, chains)
     std::map<std::tuple<size_t, int, int>, cudaGraphExec_t> graphs;
@@ -71,29 +73,29 @@ struct LayerMap {
 
 namespace dwdp {
 
-// Rows x K bf16 matrix, row-major: a 2-D map with a [128 rows x 64 cols] box,
+// Rows x K matrix, row-major: a 2-D map with a [128 rows x 128 bytes] box,
 // 128-byte swizzle (the canonical K-major layout the MMA descriptors expect).
-bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K) {
+bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, int elem_bytes) {
     EncodeTiledFn fn = encode_fn();
     if (!fn || rows == 0) return false;
     cuuint64_t dims[2] = {K, rows};
-    cuuint64_t strides[1] = {K * 2};
-    cuuint32_t box[2] = {BK, BM};
+    cuuint64_t strides[1] = {K * elem_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)(BK_BYTES / elem_bytes), BM};
     cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+    return fn(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// A weight buffer [slots][rows][K] bf16: a 3-D map, box [1 x 128 x 64].
-bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t rows, uint64_t K) {
+// A weight buffer [slots][rows][K]: a 3-D map, box [1 x 128 rows x 128 bytes].
+bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t rows, uint64_t K, int elem_bytes) {
     EncodeTiledFn fn = encode_fn();
     if (!fn || rows == 0 || slots == 0) return false;
     cuuint64_t dims[3] = {K, rows, slots};
-    cuuint64_t strides[2] = {K * 2, rows * K * 2};
-    cuuint32_t box[3] = {BK, BN / 2, 1};
+    cuuint64_t strides[2] = {K * elem_bytes, rows * K * elem_bytes};
+    cuuint32_t box[3] = {(cuuint32_t)(BK_BYTES / elem_bytes), BN / 2, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+    return fn(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -106,6 +108,7 @@ struct dwdp_ctx {
     dwdp_config cfg{};
     int device = 0;
     int n_sms = 0;
+    int elem_bytes = 2;  // expert weight element size: 2 bf16, 1 E4M3
     void* stage13[2] = {nullptr, nullptr};
     void* stage2[2] = {nullptr, nullptr};
     CUtensorMap stage_map13[2]{}, stage_map2[2]{};
@@ -147,25 +150,42 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct WsLayout {
     size_t logits = 0;  // route: fp32 [T][E] when the caller does not keep logits
-    size_t xp = 0, a = 0, y = 0;  // moe: offsets
+    // moe offsets: gathered rows xp, activations a, expert outputs y; E4M3
+    // contexts also keep x's codes/scales (xq, sx), xp's scales (sxp) and
+    // a's codes/scales (aq, sa).
+    size_t xp = 0, a = 0, y = 0, xq = 0, sx = 0, sxp = 0, aq = 0, sa = 0;
     size_t route_bytes = 0, moe_bytes = 0;
 };
 
 WsLayout ws_layout(const dwdp_config& c, int64_t T) {
     WsLayout L;
     const int64_t H = c.hidden, I = c.inter, E = c.n_experts, k = c.top_k, S = c.n_shared;
+    const int64_t eb = (c.weight_dtype == DWDP_DTYPE_E4M3) ? 1 : 2;  // bytes of a GEMM operand element
     L.logits = 0;
     L.route_bytes = align_up((size_t)(T * E * 4), 256);
-    L.xp = 0;
-    L.a = align_up((size_t)(T * k * H * 2), 256);
-    L.y = L.a + align_up((size_t)(T * (k + S) * I * 2), 256);
-    L.moe_bytes = L.y + align_up((size_t)(T * (k + S) * H * 2), 256);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o += align_up(bytes, 256);
+        return at;
+    };
+    L.xp = take((size_t)(T * k * H * eb));
+    L.a = take((size_t)(T * (k + S) * I * 2));
+    L.y = take((size_t)(T * (k + S) * H * 2));
+    if (eb == 1) {
+        L.xq = take((size_t)(T * H));
+        L.sx = take((size_t)T * 4);
+        L.sxp = take((size_t)(T * k) * 4);
+        L.aq = take((size_t)(T * (k + S) * I));
+        L.sa = take((size_t)(T * (k + S)) * 4);
+    }
+    L.moe_bytes = o;
     return L;
 }
 
 // The copy plan of [DWDP] §4.3.2 (see dwdp_plan_prefetch in dwdp.h for the
 // exact order).  Returns false on an invalid map.
-bool build_plan(int32_t E, int64_t H, int64_t I, const int32_t* local_slot, const int32_t* peer_id,
+bool build_plan(int32_t E, int64_t H, int64_t I, int64_t elem, const int32_t* local_slot, const int32_t* peer_id,
                 const int32_t* peer_slot, int32_t n_peers, size_t chunk,
                 std::vector<dwdp_copy_slice>& plan, std::string& why) {
     plan.clear();
@@ -183,7 +203,7 @@ bool build_plan(int32_t E, int64_t H, int64_t I, const int32_t* local_slot, cons
             }
             sslot[e] = r++;
         }
-    const int64_t bytes[2] = {2 * I * H * 2, H * I * 2};
+    const int64_t bytes[2] = {2 * I * H * elem, H * I * elem};
     std::vector<std::vector<dwdp_copy_slice>> per(n_peers > 0 ? n_peers : 0);
     for (int32_t p = 0; p < n_peers; ++p) {
         std::vector<dwdp_copy_slice> regions;
@@ -254,7 +274,8 @@ int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* cons
     *out = nullptr;
     const dwdp_config& c = *cfg;
     if (c.hidden <= 0 || c.inter <= 0 || c.n_experts <= 0 || c.top_k <= 0 || c.max_tokens < 0 ||
-        c.n_layers <= 0 || c.stage_slots < 0 || c.n_shared < 0)
+        c.n_layers <= 0 || c.stage_slots < 0 || c.n_shared < 0 ||
+        (c.weight_dtype != DWDP_DTYPE_BF16 && c.weight_dtype != DWDP_DTYPE_E4M3))
         return fail(nullptr, DWDP_ERR_INVALID_ARG, "config has a non-positive size");
     if (c.hidden % 64 || c.inter % 64)
         return fail(nullptr, DWDP_ERR_UNSUPPORTED, "hidden and inter must be multiples of 64");
@@ -272,6 +293,7 @@ int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* cons
     }
     std::unique_ptr<dwdp_ctx> ctx(new dwdp_ctx());
     ctx->cfg = c;
+    ctx->elem_bytes = (c.weight_dtype == DWDP_DTYPE_E4M3) ? 1 : 2;
     ctx->args.reset(new GemmArgs());
     cudaError_t e = cudaGetDevice(&ctx->device);
     if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDevice");
@@ -295,8 +317,9 @@ int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* cons
         for (int s = 0; s < 2; ++s) {
             ctx->stage13[s] = stage_w13[s];
             ctx->stage2[s] = stage_w2[s];
-            if (!encode_slots(&ctx->stage_map13[s], stage_w13[s], c.stage_slots, 2ull * c.inter, c.hidden) ||
-                !encode_slots(&ctx->stage_map2[s], stage_w2[s], c.stage_slots, c.hidden, c.inter))
+            if (!encode_slots(&ctx->stage_map13[s], stage_w13[s], c.stage_slots, 2ull * c.inter, c.hidden,
+                              ctx->elem_bytes) ||
+                !encode_slots(&ctx->stage_map2[s], stage_w2[s], c.stage_slots, c.hidden, c.inter, ctx->elem_bytes))
                 return fail(nullptr, DWDP_ERR_CUDA, "tensor map for a stage buffer");
         }
     }
@@ -373,16 +396,16 @@ int32_t dwdp_set_expert_map(dwdp_ctx* ctx, int32_t layer, const dwdp_pool* local
                     c.stage_slots);
     if (any_local) {
         m.local = *local;
-        if (!encode_slots(&m.local13, local->w13, local->n_slots, 2ull * c.inter, c.hidden) ||
-            !encode_slots(&m.local2, local->w2, local->n_slots, c.hidden, c.inter))
+        if (!encode_slots(&m.local13, local->w13, local->n_slots, 2ull * c.inter, c.hidden, ctx->elem_bytes) ||
+            !encode_slots(&m.local2, local->w2, local->n_slots, c.hidden, c.inter, ctx->elem_bytes))
             return fail(ctx, DWDP_ERR_CUDA, "tensor map for the local pool");
         m.has_local_map = true;
     }
     if (c.n_shared) {
         m.shared_w13 = shared_w13;
         m.shared_w2 = shared_w2;
-        if (!encode_slots(&m.shared13, shared_w13, 1, 2ull * c.inter, c.hidden) ||
-            !encode_slots(&m.shared2, shared_w2, 1, c.hidden, c.inter))
+        if (!encode_slots(&m.shared13, shared_w13, 1, 2ull * c.inter, c.hidden, ctx->elem_bytes) ||
+            !encode_slots(&m.shared2, shared_w2, 1, c.hidden, c.inter, ctx->elem_bytes))
             return fail(ctx, DWDP_ERR_CUDA, "tensor map for the shared expert");
     }
     m.bsrc.resize(E + c.n_shared);
@@ -390,6 +413,8 @@ int32_t dwdp_set_expert_map(dwdp_ctx* ctx, int32_t layer, const dwdp_pool* local
         m.bsrc[e] = (local_slot[e] >= 0) ? make_int2(0, local_slot[e]) : make_int2(1, m.stage_slot[e]);
     if (c.n_shared) m.bsrc[E] = make_int2(2, 0);
     m.mapped = true;
+    m.scale13 = ctx->layers[layer].scale13;
+    m.scale2 = ctx->layers[layer].scale2;
     ctx->layers[layer].release();
     ctx->layers[layer] = std::move(m);
     for (int s = 0; s < 2; ++s)
@@ -397,15 +422,38 @@ int32_t dwdp_set_expert_map(dwdp_ctx* ctx, int32_t layer, const dwdp_pool* local
     return DWDP_OK;
 }
 
-int32_t dwdp_plan_prefetch(int32_t n_experts, int32_t hidden, int32_t inter, const int32_t* local_slot,
+int32_t dwdp_set_expert_scales(dwdp_ctx* ctx, int32_t layer, const float* w13_scale, const float* w2_scale,
+                               float shared_w13_scale, float shared_w2_scale) {
+    if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
+    const dwdp_config& c = ctx->cfg;
+    if (c.weight_dtype != DWDP_DTYPE_E4M3) return fail(ctx, DWDP_ERR_INVALID_ARG, "scales apply to E4M3 contexts only");
+    if (layer < 0 || layer >= c.n_layers) return fail(ctx, DWDP_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (!w13_scale || !w2_scale) return fail(ctx, DWDP_ERR_INVALID_ARG, "scale arrays must not be NULL");
+    std::vector<float> s13(w13_scale, w13_scale + c.n_experts), s2(w2_scale, w2_scale + c.n_experts);
+    if (c.n_shared) {
+        s13.push_back(shared_w13_scale);
+        s2.push_back(shared_w2_scale);
+    }
+    for (size_t i = 0; i < s13.size(); ++i)
+        if (!(s13[i] > 0.0f) || !(s2[i] > 0.0f) || !std::isfinite(s13[i]) || !std::isfinite(s2[i]))
+            return fail(ctx, DWDP_ERR_INVALID_ARG, "scale %zu must be positive and finite", i);
+    ctx->layers[layer].scale13 = std::move(s13);
+    ctx->layers[layer].scale2 = std::move(s2);
+    return DWDP_OK;
+}
+
+int32_t dwdp_plan_prefetch(int32_t n_experts, int32_t hidden, int32_t inter, int32_t elem_bytes,
+                           const int32_t* local_slot,
                            const int32_t* peer_id, const int32_t* peer_slot, int32_t n_peers,
                            size_t chunk_bytes, dwdp_copy_slice* out, int64_t max_out, int64_t* n_out) {
-    if (n_experts <= 0 || hidden <= 0 || inter <= 0 || !local_slot || !n_out || n_peers < 0 ||
+    if (n_experts <= 0 || hidden <= 0 || inter <= 0 || (elem_bytes != 1 && elem_bytes != 2) || !local_slot ||
+        !n_out || n_peers < 0 ||
         (max_out > 0 && !out))
         return fail(nullptr, DWDP_ERR_INVALID_ARG, "bad arguments to dwdp_plan_prefetch");
     std::vector<dwdp_copy_slice> plan;
     std::string why;
-    if (!build_plan(n_experts, hidden, inter, local_slot, peer_id, peer_slot, n_peers, chunk_bytes, plan, why))
+    if (!build_plan(n_experts, hidden, inter, elem_bytes, local_slot, peer_id, peer_slot, n_peers, chunk_bytes, plan,
+                    why))
         return fail(nullptr, DWDP_ERR_INVALID_ARG, "%s", why.c_str());
     *n_out = (int64_t)plan.size();
     for (int64_t i = 0; i < max_out && i < (int64_t)plan.size(); ++i) out[i] = plan[i];
@@ -458,7 +506,7 @@ int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router
     a.col_bias = logit_bias;
     a.err = ctx->d_err;
     a.bsrc[0] = make_int2(0, 0);
-    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_F32, a, ctx->n_sms, stream));
+    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_F32, false, a, ctx->n_sms, stream));
     DWDP_CUDA(ctx, launch_topk(logits, nullptr, T, c.n_experts, c.top_k, out->topk_ids, out->topk_w, stream));
     DWDP_CUDA(ctx, launch_group(out->topk_ids, T * c.top_k, c.n_experts, out->counts, out->offsets, out->perm,
                                 out->inv_perm, stream));
@@ -481,7 +529,8 @@ int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t 
     if (it == m.plans.end()) {
         std::vector<dwdp_copy_slice> plan;
         std::string why;
-        if (!build_plan(c.n_experts, c.hidden, c.inter, m.local_slot.data(), m.peer_id.data(), m.peer_slot.data(),
+        if (!build_plan(c.n_experts, c.hidden, c.inter, ctx->elem_bytes, m.local_slot.data(), m.peer_id.data(),
+                        m.peer_slot.data(),
                         (int32_t)m.peers.size(), chunk_bytes, plan, why))
             return fail(ctx, DWDP_ERR_INVALID_ARG, "%s", why.c_str());
         it = m.plans.emplace(chunk_bytes, std::move(plan)).first;
@@ -547,14 +596,28 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
         return fail(ctx, DWDP_ERR_INVALID_ARG, "workspace too small (%zu < %zu) or unaligned", ws_bytes, L.moe_bytes);
     const int64_t k = c.top_k, S = c.n_shared, H = c.hidden, I = c.inter, E = c.n_experts;
     const int64_t rows_r = (int64_t)T * k, rows_all = (int64_t)T * (k + S);
+    const bool f8 = ctx->elem_bytes == 1;
+    if (f8 && m.scale13.size() != m.bsrc.size())
+        return fail(ctx, DWDP_ERR_NOT_MAPPED, "layer %d has no E4M3 weight scales (dwdp_set_expert_scales)", layer);
     char* w = static_cast<char*>(ws);
     void* xp = w + L.xp;
     void* act = w + L.a;
     void* y = w + L.y;
+    void* xq = w + L.xq;
+    float* sx = reinterpret_cast<float*>(w + L.sx);
+    float* sxp = reinterpret_cast<float*>(w + L.sxp);
+    void* aq = w + L.aq;
+    float* sa = reinterpret_cast<float*>(w + L.sa);
 
     if (m.n_remote > 0) DWDP_CUDA(ctx, cudaStreamWaitEvent(stream, ctx->ready[stage], 0));
     DWDP_CUDA(ctx, mark(ctx, 2, stream));
-    DWDP_CUDA(ctx, launch_gather(x, (int)H, route->perm, (int)rows_r, (int)k, xp, stream));
+    if (f8) {
+        // x rows to E4M3 (per-token scales), then gathered into expert order
+        DWDP_CUDA(ctx, launch_quantize_rows(x, T, (int)H, xq, sx, stream));
+        DWDP_CUDA(ctx, launch_gather_fp8(xq, sx, (int)H, route->perm, (int)rows_r, (int)k, xp, sxp, stream));
+    } else {
+        DWDP_CUDA(ctx, launch_gather(x, (int)H, route->perm, (int)rows_r, (int)k, xp, stream));
+    }
     DWDP_CUDA(ctx, mark(ctx, 3, stream));
 
     GemmArgs& a = *ctx->args;
@@ -566,9 +629,13 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
         a.tmB[1] = m.n_remote > 0 ? stg : *valid;
         a.tmB[2] = S ? shared : *valid;
     };
-    // G1: a = SiLU(xp W_gate) * (xp W_up); the shared group reads x directly.
-    if (!encode_rows(&a.tmA[0], xp, rows_r, H) || !encode_rows(&a.tmA[1], x, T, H))
+    // G1: a = SiLU(xp W_gate) * (xp W_up); the shared group reads x directly
+    // (E4M3: xp / x codes, dequantized in the epilogue by row scale * weight scale).
+    if (!encode_rows(&a.tmA[0], xp, rows_r, H, ctx->elem_bytes) ||
+        !encode_rows(&a.tmA[1], f8 ? xq : x, T, H, ctx->elem_bytes))
         return fail(ctx, DWDP_ERR_CUDA, "tensor maps for the gate/up GEMM");
+    a.row_scale[0] = sxp;
+    a.row_scale[1] = sx;
     set_b(m.local13, ctx->stage_map13[m.n_remote > 0 ? stage : 0], m.shared13);
     a.row_offsets = route->offsets;
     a.n_routed = (int32_t)E;
@@ -582,12 +649,20 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     a.D = act;
     a.col_bias = nullptr;
     a.err = ctx->d_err;
-    for (size_t g = 0; g < m.bsrc.size(); ++g) a.bsrc[g] = m.bsrc[g];
-    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_SILU, a, ctx->n_sms, stream));
+    for (size_t g = 0; g < m.bsrc.size(); ++g) {
+        a.bsrc[g] = m.bsrc[g];
+        if (f8) a.gscale[g] = m.scale13[g];
+    }
+    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_SILU, f8, a, ctx->n_sms, stream));
     DWDP_CUDA(ctx, mark(ctx, 4, stream));
-    // G2: y = a W_down.
-    if (!encode_rows(&a.tmA[0], act, rows_all, I)) return fail(ctx, DWDP_ERR_CUDA, "tensor map for the down GEMM");
+    // G2: y = a W_down (E4M3: a's rows quantized first; this phase includes it).
+    if (f8) DWDP_CUDA(ctx, launch_quantize_rows(act, rows_all, (int)I, aq, sa, stream));
+    if (!encode_rows(&a.tmA[0], f8 ? aq : act, rows_all, I, ctx->elem_bytes))
+        return fail(ctx, DWDP_ERR_CUDA, "tensor map for the down GEMM");
     a.tmA[1] = a.tmA[0];
+    a.row_scale[0] = a.row_scale[1] = sa;
+    if (f8)
+        for (size_t g = 0; g < m.bsrc.size(); ++g) a.gscale[g] = m.scale2[g];
     set_b(m.local2, ctx->stage_map2[m.n_remote > 0 ? stage : 0], m.shared2);
     a.shared_a_row = (int32_t)rows_r;
     a.shared_d_row = (int32_t)rows_r;
@@ -596,7 +671,7 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     a.ldd = H;
     a.d_rows = rows_all;
     a.D = y;
-    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_BF16, a, ctx->n_sms, stream));
+    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_BF16, f8, a, ctx->n_sms, stream));
     DWDP_CUDA(ctx, mark(ctx, 5, stream));
     // The stage's weights have been read: the next prefetch into it may start.
     if (m.n_remote > 0) DWDP_CUDA(ctx, cudaEventRecord(ctx->freed[stage], stream));
@@ -685,7 +760,7 @@ int32_t dwdp_grouped_gemm(dwdp_ctx* ctx, int32_t epilogue, const void* a_ptr, in
     a.D = d;
     a.col_bias = nullptr;
     a.err = ctx->d_err;
-    DWDP_CUDA(ctx, launch_grouped_gemm(epilogue, a, ctx->n_sms, stream));
+    DWDP_CUDA(ctx, launch_grouped_gemm(epilogue, false, a, ctx->n_sms, stream));
     return DWDP_OK;
 }
 

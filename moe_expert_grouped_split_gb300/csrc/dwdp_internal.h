@@ -17,10 +17,12 @@ constexpr int kMaxGroups = DWDP_MAX_EXPERTS + 1;  // routed experts + one shared
 enum Epilogue : int { EPI_BF16 = 0, EPI_SILU = 1, EPI_F32 = 2 };
 
 // Tile shape of the grouped GEMM: one CTA computes a 128 x 256 fp32
-// accumulator in tensor memory from 64-wide K slices staged by TMA.
+// accumulator in tensor memory from K slices of 128 bytes per row staged by
+// TMA (64 bf16 or 128 E4M3 elements).
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int BK = 64;
+constexpr int BK = 64;        // bf16 elements per K slice (128 bytes)
+constexpr int BK_BYTES = 128;
 constexpr int kStages = 4;
 constexpr int kABytes = BM * BK * 2;           // 16 KiB
 constexpr int kBBytes = BN * BK * 2;           // 32 KiB
@@ -59,19 +61,27 @@ struct GemmArgs {
     void* D;
     const float* col_bias;  // EPI_F32: added per column, may be null
     int* err;
+    // E4M3 operands only: the fp32 accumulator is multiplied by the A row's
+    // scale (routed rows: row_scale[0][A row], shared rows: row_scale[1][A row])
+    // and by the group's weight scale gscale[g].
+    const float* row_scale[2];
     int2 bsrc[kMaxGroups];
+    float gscale[kMaxGroups];
 };
 
-// TMA tensor maps (dwdp_abi.cu): a rows x K bf16 matrix (box 128 x 64) and
-// a weight buffer [slots][rows][K] (box 1 x 128 x 64), both 128 B swizzle.
-bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K);
-bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t rows, uint64_t K);
+// TMA tensor maps (dwdp_abi.cu): a rows x K matrix (box 128 rows x 128 B)
+// and a weight buffer [slots][rows][K] (box 1 x 128 rows x 128 B), both
+// 128 B swizzle; elem_bytes 2 = bf16, 1 = E4M3 codes.
+bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, int elem_bytes = 2);
+bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t rows, uint64_t K,
+                  int elem_bytes = 2);
 
 // Sets the text dwdp_last_error(NULL) returns on this thread (dwdp_abi.cu).
 void set_last_error(const char* msg);
 
 size_t gemm_smem_bytes(int n_groups);
-cudaError_t launch_grouped_gemm(int epi, const GemmArgs& args, int n_sms, cudaStream_t stream);
+// fp8: both operands are E4M3 codes (K counted in elements = bytes).
+cudaError_t launch_grouped_gemm(int epi, bool fp8, const GemmArgs& args, int n_sms, cudaStream_t stream);
 
 // route.cu
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k,
@@ -80,6 +90,11 @@ cudaError_t launch_group(const int32_t* ids, int n, int E, int32_t* counts, int3
                          int32_t* perm, int32_t* inv, cudaStream_t s);
 cudaError_t launch_gather(const void* x, int H, const int32_t* perm, int n_rows, int k, void* xp,
                           cudaStream_t s);
+// E4M3 rows: codes[r][:] and scale[r] of bf16 rows (scale = amax / 448).
+cudaError_t launch_quantize_rows(const void* in, int64_t rows, int cols, void* codes, float* scale, cudaStream_t s);
+// Gathered E4M3 rows: xp[r] = xq[perm[r] / k], sxp[r] = sx[perm[r] / k].
+cudaError_t launch_gather_fp8(const void* xq, const float* sx, int H, const int32_t* perm, int n_rows, int k,
+                              void* xp, float* sxp, cudaStream_t s);
 cudaError_t launch_combine(const void* y, int H, const int32_t* inv, const float* w, int T, int k,
                            int64_t shared_row0, bool has_shared, void* out, cudaStream_t s);
 

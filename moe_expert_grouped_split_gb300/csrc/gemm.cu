@@ -29,11 +29,13 @@ namespace {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
 
-// Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// Instruction descriptors.  kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits
-// 17-22, M >> 4 at bits 24-28.
+// 17-22, M >> 4 at bits 24-28.  kind::f8f6f4: the same with A and B E4M3
+// (format 0).
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                             ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t kIdescE4M3 = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -145,14 +147,25 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// One 128 x 256 MMA step: K = 16 bf16 or K = 32 E4M3 elements (32 bytes).
+template <bool F8>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-        : "memory");
+    if constexpr (F8) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(kIdescE4M3), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+            : "memory");
+    }
 }
 
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
@@ -210,8 +223,9 @@ struct SmemLayout {
     static constexpr int kTileStart = kMisc + 16;         // int32[G+1]
 };
 
-template <int EPI>
+template <int EPI, bool F8>
 __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
+    constexpr int KE = F8 ? BK_BYTES : BK;  // K elements per 128-byte slice
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -232,7 +246,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     const int G = n_routed + (p.shared_rows > 0 ? 1 : 0);
     const int ntile_cols = (EPI == EPI_SILU) ? (BN / 2) : BN;  // output columns per tile
     const int NT = (p.N + ntile_cols - 1) / ntile_cols;
-    const int KB = (p.K + BK - 1) / BK;
+    const int KB = (p.K + KE - 1) / KE;
 
     // ---- tile counts per group, then an inclusive scan into tile_start ----
     for (int g = threadIdx.x; g < G; g += blockDim.x) {
@@ -330,9 +344,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                     mbar_arrive_expect_tx(fb, kStageBytes);
                     const uint32_t sa = sbase + SmemLayout::kA + stage * kABytes;
                     const uint32_t sb = sbase + SmemLayout::kB + stage * kBBytes;
-                    tma_load_2d(sa, ma, kb * BK, a_row, fb);
-                    tma_load_3d(sb, mb, kb * BK, b_row0, src.y, fb);
-                    tma_load_3d(sb + kBBytes / 2, mb, kb * BK, b_row1, src.y, fb);
+                    tma_load_2d(sa, ma, kb * KE, a_row, fb);
+                    tma_load_3d(sb, mb, kb * KE, b_row0, src.y, fb);
+                    tma_load_3d(sb + kBBytes / 2, mb, kb * KE, b_row1, src.y, fb);
                     pend[stage] = (int)phase;
                     if (++stage == kStages) {
                         stage = 0;
@@ -371,9 +385,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                     const uint64_t ad = sw128_desc(sbase + SmemLayout::kA + stage * kABytes);
                     const uint64_t bd = sw128_desc(sbase + SmemLayout::kB + stage * kBBytes);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        // advance 16 bf16 = 32 bytes along K inside the swizzle atom
-                        tc_mma(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk),
+                    for (int kk = 0; kk < BK_BYTES / 32; ++kk) {
+                        // advance 32 bytes (16 bf16 / 32 E4M3) along K inside the swizzle atom
+                        tc_mma<F8>(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk),
                                (kb > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc_commit(empty_bar(stage));
@@ -415,6 +429,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                 atomicOr(p.err, DERR_BAD_INDEX);
                 valid = false;
             }
+            // E4M3: dequantize with the A row's scale times the group's weight scale
+            float sc = 1.0f;
+            if (F8 && valid) {
+                const int64_t arow = (routed ? (int64_t)p.row_offsets[g] : (int64_t)p.shared_a_row) + r;
+                sc = __ldg(p.row_scale[routed ? 0 : 1] + arow) * p.gscale[g];
+            }
 
             // the decision must be warp-uniform: tcgen05.ld below is .sync.aligned
             const bool got = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.err, DERR_EPI_WAIT);
@@ -434,7 +454,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                     if (valid && col < p.N) {
                         float o[32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = silu_mul(__uint_as_float(gv[j]), __uint_as_float(uv[j]));
+                        for (int j = 0; j < 32; ++j)
+                            o[j] = silu_mul(__uint_as_float(gv[j]) * sc, __uint_as_float(uv[j]) * sc);
                         store_bf16x32(D + grow * p.ldd + col, o);
                     }
                 }
@@ -449,7 +470,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                     if (valid && col < p.N) {
                         float o[32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(v[j]);
+                        for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(v[j]) * sc;
                         store_bf16x32(D + grow * p.ldd + col, o);
                     }
                 }
@@ -498,15 +519,23 @@ size_t gemm_smem_bytes(int n_groups) {
     return 1024 + SmemLayout::kTileStart + sizeof(int32_t) * (size_t)(n_groups + 1);
 }
 
-cudaError_t launch_grouped_gemm(int epi, const GemmArgs& args, int n_sms, cudaStream_t stream) {
+cudaError_t launch_grouped_gemm(int epi, bool fp8, const GemmArgs& args, int n_sms, cudaStream_t stream) {
     const int G = args.n_routed + (args.shared_rows > 0 ? 1 : 0);
     const size_t smem = gemm_smem_bytes(G);
     const void* fn;
-    switch (epi) {
-        case EPI_SILU: fn = (const void*)grouped_gemm_kernel<EPI_SILU>; break;
-        case EPI_BF16: fn = (const void*)grouped_gemm_kernel<EPI_BF16>; break;
-        case EPI_F32: fn = (const void*)grouped_gemm_kernel<EPI_F32>; break;
-        default: return cudaErrorInvalidValue;
+    if (fp8) {
+        switch (epi) {
+            case EPI_SILU: fn = (const void*)grouped_gemm_kernel<EPI_SILU, true>; break;
+            case EPI_BF16: fn = (const void*)grouped_gemm_kernel<EPI_BF16, true>; break;
+            default: return cudaErrorInvalidValue;
+        }
+    } else {
+        switch (epi) {
+            case EPI_SILU: fn = (const void*)grouped_gemm_kernel<EPI_SILU, false>; break;
+            case EPI_BF16: fn = (const void*)grouped_gemm_kernel<EPI_BF16, false>; break;
+            case EPI_F32: fn = (const void*)grouped_gemm_kernel<EPI_F32, false>; break;
+            default: return cudaErrorInvalidValue;
+        }
     }
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

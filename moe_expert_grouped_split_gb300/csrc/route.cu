@@ -8,6 +8,7 @@
 // renormalised over the chosen set, and (token, slot) pairs grouped by expert
 // in ascending flat index t*k+j.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "dwdp_internal.h"
 
@@ -209,7 +210,80 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
     }
 }
 
+// E4M3 rows, one warp per row: amax of the row (binary32, exact for bf16
+// inputs), scale = amax / 448 (1 for an all-zero row), code = E4M3 of the
+// binary32 quotient v / scale, rounded to nearest even and saturated to
+// +-448.  cols is a multiple of 8.
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restrict__ in, int64_t rows, int cols,
+                                                            uint2* __restrict__ codes, float* __restrict__ scale) {
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    const int nv = cols / 8;
+    const uint4* src = in + r * nv;
+    float amax = 0.0f;
+    for (int i = lane; i < nv; i += 32) {
+        const uint4 q = __ldg(src + i);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(h[j]);
+            amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    if (lane == 0) scale[r] = s;
+    uint2* dst = codes + r * nv;
+    for (int i = lane; i < nv; i += 32) {
+        const uint4 q = __ldg(src + i);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+        uint32_t w[2] = {0, 0};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(h[j]);
+            const uint32_t c0 = __nv_cvt_float_to_fp8(f.x / s, __NV_SATFINITE, __NV_E4M3);
+            const uint32_t c1 = __nv_cvt_float_to_fp8(f.y / s, __NV_SATFINITE, __NV_E4M3);
+            w[j >> 1] |= (c0 | (c1 << 8)) << ((j & 1) * 16);
+        }
+        dst[i] = make_uint2(w[0], w[1]);
+    }
+}
+
+// xp[r][:] = xq[perm[r] / k][:] (E4M3 codes, H bytes per row), sxp[r] =
+// sx[perm[r] / k]: one warp per row, 16-byte copies.
+__global__ void __launch_bounds__(256) gather_fp8_kernel(const uint4* __restrict__ xq, const float* __restrict__ sx,
+                                                         int row_vecs, const int32_t* __restrict__ perm, int n_rows,
+                                                         int k, uint4* __restrict__ xp, float* __restrict__ sxp) {
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (r >= n_rows) return;
+    const int t = perm[r] / k;
+    const uint4* src = xq + (int64_t)t * row_vecs;
+    uint4* dst = xp + (int64_t)r * row_vecs;
+    for (int i = lane; i < row_vecs; i += 32) dst[i] = __ldg(src + i);
+    if (lane == 0) sxp[r] = sx[t];
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_rows(const void* in, int64_t rows, int cols, void* codes, float* scale, cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    const int warps = 8;
+    quantize_rows_kernel<<<(unsigned)((rows + warps - 1) / warps), 32 * warps, 0, s>>>(
+        reinterpret_cast<const uint4*>(in), rows, cols, reinterpret_cast<uint2*>(codes), scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_fp8(const void* xq, const float* sx, int H, const int32_t* perm, int n_rows, int k,
+                              void* xp, float* sxp, cudaStream_t s) {
+    if (n_rows <= 0) return cudaSuccess;
+    const int warps = 8;
+    gather_fp8_kernel<<<(n_rows + warps - 1) / warps, 32 * warps, 0, s>>>(
+        reinterpret_cast<const uint4*>(xq), sx, H / 16, perm, n_rows, k, reinterpret_cast<uint4*>(xp), sxp);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
                         float* w, cudaStream_t s) {

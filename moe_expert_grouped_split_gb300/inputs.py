@@ -178,6 +178,70 @@ def make_layer(shape: LayerShape, placement: Placement, base_seed: int, layer: i
     return LayerWeights(shape, placement, wr, bt, lw13, lw2, pw13, pw2, sw13, sw2)
 
 
+@dataclass
+class LayerWeightsFp8(LayerWeights):
+    """As LayerWeights, with uint8 E4M3 weight codes in the pools and one
+    scale per expert tensor (w = code * scale)."""
+    w13_scale: np.ndarray | None = None   # [E] float32
+    w2_scale: np.ndarray | None = None    # [E] float32
+    shared_s13: float = 1.0
+    shared_s2: float = 1.0
+
+
+def e4m3_codes(shape, seed: int, device="cpu", out: torch.Tensor | None = None) -> torch.Tensor:
+    """Synthetic E4M3 weight codes: N(0, 1) drawn in fp32 and converted by
+    torch's float8_e4m3fn cast, returned (or written) as uint8."""
+    g = _gen(device, seed)
+    v = torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32)
+    c = v.to(torch.float8_e4m3fn).view(torch.uint8)
+    if out is None:
+        return c
+    out.copy_(c)
+    return out
+
+
+def make_layer_fp8(shape: LayerShape, placement: Placement, base_seed: int, layer: int, device="cpu",
+                   router_std: float = 0.02, bias: np.ndarray | None = None) -> LayerWeightsFp8:
+    """One MoE layer with E4M3 expert weights: codes ~ E4M3(N(0, 1)) and a
+    per-tensor scale ~ 0.02 * U(0.8, 1.2) per expert, so w = code * scale has
+    roughly the bf16 layers' N(0, 0.02^2) spread.  Codes and scales depend only
+    on (base seed, layer, expert), not on placement."""
+    H, I, E = shape.H, shape.I, shape.E
+    u8 = torch.uint8
+    wr = randn_bf16((E, H), router_std, seed_for(base_seed, "Wr", layer), device)
+    lw13 = torch.empty((max(1, placement.n_local_slots), 2 * I, H), dtype=u8, device=device)
+    lw2 = torch.empty((max(1, placement.n_local_slots), H, I), dtype=u8, device=device)
+    pw13 = [torch.empty((placement.peer_slots, 2 * I, H), dtype=u8, device=device) for _ in range(placement.n_peers)]
+    pw2 = [torch.empty((placement.peer_slots, H, I), dtype=u8, device=device) for _ in range(placement.n_peers)]
+    for e in range(E):
+        d13, d2 = [], []
+        if placement.local_slot[e] >= 0:
+            d13.append(lw13[placement.local_slot[e]])
+            d2.append(lw2[placement.local_slot[e]])
+        if placement.peer_id[e] >= 0:
+            d13.append(pw13[placement.peer_id[e]][placement.peer_slot[e]])
+            d2.append(pw2[placement.peer_id[e]][placement.peer_slot[e]])
+        e4m3_codes((2 * I, H), seed_for(base_seed, "W13q", layer, e), device, out=d13[0])
+        e4m3_codes((H, I), seed_for(base_seed, "W2q", layer, e), device, out=d2[0])
+        for d in d13[1:]:
+            d.copy_(d13[0])
+        for d in d2[1:]:
+            d.copy_(d2[0])
+    rng = np.random.Generator(np.random.PCG64(seed_for(base_seed, "fp8_scales", layer)))
+    s13 = (0.02 * rng.uniform(0.8, 1.2, E)).astype(np.float32)
+    s2 = (0.02 * rng.uniform(0.8, 1.2, E)).astype(np.float32)
+    sw13 = sw2 = None
+    ss13 = ss2 = 1.0
+    if shape.S:
+        sw13 = e4m3_codes((2 * I, H), seed_for(base_seed, "W13qs", layer), device)
+        sw2 = e4m3_codes((H, I), seed_for(base_seed, "W2qs", layer), device)
+        ss13, ss2 = float(np.float32(0.02)), float(np.float32(0.021))
+    bt = None
+    if bias is not None:
+        bt = torch.as_tensor(np.asarray(bias, dtype=np.float32)).to(device)
+    return LayerWeightsFp8(shape, placement, wr, bt, lw13, lw2, pw13, pw2, sw13, sw2, s13, s2, ss13, ss2)
+
+
 def make_tokens(T: int, H: int, base_seed: int, step: int = 0, device="cpu") -> torch.Tensor:
     """Activations x ~ N(0, 1) as bf16 [T, H]."""
     return randn_bf16((T, H), 1.0, seed_for(base_seed, "x", step), device)

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), f"{n} not exported"
     bound = {s[0] for s in B.SIGNATURES}
     assert set(names) == bound, "binding and header disagree"
-    assert B.dwdp_version() == 1
+    assert B.dwdp_version() == 2
 
 
 def _random_map(rng, E, P, redundant=0.0):
@@ -64,8 +64,9 @@ def test_plan_matches_oracle(lib):
         I = 64 * int(rng.integers(1, 3))
         ls, pid, ps = _random_map(rng, E, P, redundant=0.2)
         chunk = int(rng.choice([1000, 4096, 65536, 10 ** 9, int(rng.integers(100, 300000))]))
-        got = B.dwdp_plan_prefetch(E, H, I, ls, pid, ps, P, chunk)
-        want = oracle.plan_prefetch(E, H, I, ls.tolist(), pid.tolist(), ps.tolist(), P, chunk)
+        eb = int(rng.choice([1, 2]))
+        got = B.dwdp_plan_prefetch(E, H, I, ls, pid, ps, P, chunk, elem_bytes=eb)
+        want = oracle.plan_prefetch(E, H, I, ls.tolist(), pid.tolist(), ps.tolist(), P, chunk, elem_bytes=eb)
         assert got == want, f"trial {trial}"
 
 
@@ -94,6 +95,8 @@ def test_host_validation_without_gpu(lib):
     # NULL config / out are rejected before any CUDA call
     out = ctypes.c_void_p()
     assert lib.dwdp_create(None, None, None, ctypes.byref(out)) == -1
+    cfg = B.dwdp_config(256, 128, 8, 2, 0, 64, 1, 0, 7)       # unknown weight type
+    assert lib.dwdp_create(ctypes.byref(cfg), None, None, ctypes.byref(out)) == -1
     cfg = B.dwdp_config(100, 128, 8, 2, 0, 64, 1, 0)          # H not a multiple of 64
     assert lib.dwdp_create(ctypes.byref(cfg), None, None, ctypes.byref(out)) == -5
     cfg = B.dwdp_config(256, 128, 8, 9, 0, 64, 1, 0)          # k > E

@@ -1,0 +1,91 @@
+"""The E4M3 (FP8) layer through the C ABI against the oracle's FP8 layer
+(mirrored mode): expert weights as E4M3 codes with one scale per expert
+tensor, activations quantized per row to E4M3 (binary32 decisions on both
+sides, so the codes of x are identical), FP8 tcgen05 GEMMs.  Also: the FP8
+output does not depend on placement (DWDP §2), and the staged E4M3 bytes
+equal their sources."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import assert_close, to_f64
+from moe_expert_grouped_split_gb300 import binding as B
+from moe_expert_grouped_split_gb300 import inputs as I
+from moe_expert_grouped_split_gb300.build import build
+
+pytestmark = pytest.mark.gpu
+
+
+def _u8(t):
+    return t.detach().contiguous().cpu().numpy().view(np.uint8)
+
+
+def _expert_codes(lw, e):
+    pl = lw.placement
+    if pl.local_slot[e] >= 0:
+        return _u8(lw.local_w13[pl.local_slot[e]]), _u8(lw.local_w2[pl.local_slot[e]])
+    return _u8(lw.peer_w13[pl.peer_id[e]][pl.peer_slot[e]]), _u8(lw.peer_w2[pl.peer_id[e]][pl.peer_slot[e]])
+
+
+def _run(shape, placement, seed, tokens=None, router_std=0.02, chunk=1 << 20):
+    build()
+    lw = I.make_layer_fp8(shape, placement, seed, 0, device="cuda", router_std=router_std)
+    x = I.make_tokens(shape.T, shape.H, seed).cuda()
+    rt = B.Runtime(shape.H, shape.I, shape.E, shape.k, shape.S, shape.T, 1, max(1, placement.n_remote()),
+                   weight_dtype=B.DTYPE_E4M3)
+    try:
+        rt.set_layer(0, lw)
+        rb = B.RouteBuffers(shape.T, shape.E, shape.k)
+        out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
+        if placement.n_remote() > 0:
+            rt.prefetch(0, 0, chunk, [torch.cuda.Stream()])
+        rt.route(x, lw.wr, None, rb)
+        rt.moe(0, 0, x, rb, out)
+        torch.cuda.synchronize()
+        assert rt.device_status() == 0
+        o = oracle.default()
+        tok = np.arange(shape.T) if tokens is None else np.asarray(tokens)
+        xs = I.bf16_bits(x)
+        ref = o.route(xs[tok], I.bf16_bits(lw.wr), None, shape.k)
+        ids = rb.topk_ids.cpu().numpy()[tok]
+        same = (ids == ref["ids"]).all(axis=1)
+        sub = np.nonzero(same)[0]
+        used = np.unique(ref["ids"][sub])
+        w13s, w2s = [None] * shape.E, [None] * shape.E
+        for e in used:
+            w13s[e], w2s[e] = _expert_codes(lw, int(e))
+        kw = {}
+        if shape.S:
+            kw = dict(shared_w13=_u8(lw.shared_w13), shared_w2=_u8(lw.shared_w2), shared_s13=lw.shared_s13,
+                      shared_s2=lw.shared_s2)
+        want = o.moe_tokens_fp8(xs[tok], sub, ref["ids"], ref["w"], w13s, w2s, lw.w13_scale, lw.w2_scale,
+                                mirrored=True, **kw)
+        got = to_f64(out)[tok[sub]]
+        assert_close(got, want, what="E4M3 layer output")
+        return out.clone(), lw
+    finally:
+        rt.close()
+
+
+def test_fp8_small_layer_with_shared_expert():
+    _run(I.LayerShape(T=200, H=256, I=128, E=8, k=2, S=1), I.split_placement(8, 4, 1), seed=0)
+
+
+def test_fp8_ragged_many_experts():
+    _run(I.LayerShape(T=333, H=512, I=256, E=16, k=4, S=0), I.split_placement(16, 5, 3), seed=1)
+
+
+def test_fp8_output_independent_of_placement():
+    shape = I.LayerShape(T=130, H=256, I=128, E=8, k=2, S=1)
+    a, _ = _run(shape, I.split_placement(8, 8, 0), seed=2)
+    b, _ = _run(shape, I.split_placement(8, 0, 2), seed=2)
+    c, _ = _run(shape, I.split_placement(8, 3, 2, redundant=[4, 6]), seed=2)
+    assert torch.equal(a, b) and torch.equal(a, c)
+
+
+def test_fp8_r1_layer_sample():
+    # full R1 shapes in the benchmark's launch configuration, 24 sampled tokens
+    shape, pl = I.r1_layer(8192)
+    rng = np.random.default_rng(3)
+    _run(shape, pl, seed=3, tokens=np.sort(rng.choice(8192, 24, replace=False)), chunk=32 << 20)
