@@ -86,6 +86,8 @@ def parse(argv=None):
     p.add_argument("--workload", default="r1_moe_layer_8k", choices=sorted(WORKLOADS))
     p.add_argument("--chunk-mb", type=float, default=32.0)
     p.add_argument("--copy-streams", type=int, default=1)
+    p.add_argument("--dtype", default="bf16", choices=["bf16", "fp8"],
+                   help="expert weight type (fp8: E4M3 weights and activations, a next-row variant)")
     p.add_argument("--chunk-sweep", default="", help="comma-separated chunk sizes in MB (exposed copy per size)")
     p.add_argument("--merge-copy", action="store_true",
                    help="also time the merge-copy baseline (one contiguous weight buffer per layer)")
@@ -105,19 +107,25 @@ def g1_flops(T, H, I, k, S):
     return 4 * T * (k + S) * H * I
 
 
-def g1_bytes(T, H, I, E_active, k, S):
+def g1_bytes(T, H, I, E_active, k, S, wb=2):
     """Gate/up grouped GEMM, algorithmic HBM bytes: every active expert's
-    w13 once (2I*H bf16), the gathered rows and x once, a written once."""
-    return (E_active + S) * 2 * I * H * 2 + T * (k + S) * H * 2 + T * (k + S) * I * 2
+    w13 once (2I*H elements of wb bytes), the gathered rows and x once (same
+    element size), a written once (bf16)."""
+    return (E_active + S) * 2 * I * H * wb + T * (k + S) * H * wb + T * (k + S) * I * 2
 
 
-def step_bytes(T, H, I, E_active, k, S, R):
+def step_bytes(T, H, I, E_active, k, S, R, wb=2):
     """Algorithmic HBM bytes of one overlapped step: weights once
-    ((E_active+S)*3*H*I bf16), xp / a / y written and read once, x read and
-    out written, and the prefetch of R experts (read + write, both on this
-    GPU's HBM under the one-GPU emulation)."""
-    return ((E_active + S) * 3 * H * I * 2 + 2 * T * k * H * 2 + 2 * T * (k + S) * I * 2
-            + 2 * T * (k + S) * H * 2 + 2 * T * H * 2 + 2 * R * 3 * H * I * 2)
+    ((E_active+S)*3*H*I elements of wb bytes), xp / a / y written and read
+    once, x read and out written, and the prefetch of R experts (read +
+    write, both on this GPU's HBM under the one-GPU emulation).  With E4M3
+    weights (wb = 1) the GEMM operands xp and a are E4M3 too, plus x's and
+    a's quantization passes (codes written and read once)."""
+    b = ((E_active + S) * 3 * H * I * wb + 2 * T * k * H * wb + 2 * T * (k + S) * I * 2
+         + 2 * T * (k + S) * H * 2 + 2 * T * H * 2 + 2 * R * 3 * H * I * wb)
+    if wb == 1:
+        b += 2 * T * H + 2 * T * (k + S) * I
+    return b
 
 
 def measured_traffic(kernel_file: str):
@@ -225,7 +233,7 @@ class Workload:
     """n_layers R1-shaped layers with their pools, a Runtime, route buffers
     and per-layer token batches, all resident in HBM."""
 
-    def __init__(self, spec: Spec, chunk_bytes, n_copy_streams, n_layers=2, base_seed=0):
+    def __init__(self, spec: Spec, chunk_bytes, n_copy_streams, n_layers=2, base_seed=0, fp8=False):
         import torch
 
         from moe_expert_grouped_split_gb300 import binding as B
@@ -233,12 +241,15 @@ class Workload:
 
         self.B, self.I, self.torch = B, I, torch
         self.spec = spec
+        self.fp8 = fp8
         self.shape, self.placement = spec.shape, spec.placement
         sh = self.shape
         self.n_layers = n_layers
-        self.layers = [I.make_layer(sh, self.placement, base_seed, l, device="cuda", router_std=spec.router_std,
-                                    bias=spec.bias) for l in range(n_layers)]
-        self.rt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, n_layers, self.placement.n_remote())
+        make = I.make_layer_fp8 if fp8 else I.make_layer
+        self.layers = [make(sh, self.placement, base_seed, l, device="cuda", router_std=spec.router_std,
+                            bias=spec.bias) for l in range(n_layers)]
+        self.rt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, n_layers, self.placement.n_remote(),
+                            weight_dtype=B.DTYPE_E4M3 if fp8 else B.DTYPE_BF16)
         for l, lw in enumerate(self.layers):
             self.rt.set_layer(l, lw)
         self.x = [I.make_tokens(sh.T, sh.H, base_seed, step=s, device="cuda") for s in range(n_layers)]
@@ -400,7 +411,7 @@ def run_layer_bench(args, world, local_rank, barrier):
     import torch
     torch.cuda.set_device(local_rank)
     spec = WORKLOADS[args.workload]()
-    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams)
+    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, fp8=args.dtype == "fp8")
     sh = wl.shape
     K, W = args.steps, args.warmup
     phases = [_events(torch, 7) for _ in range(K)]
@@ -549,7 +560,7 @@ def run_pipeline_bench(args, world, local_rank, barrier):
 
     torch.cuda.set_device(local_rank)
     spec = WORKLOADS[args.workload]()
-    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, n_layers=4)
+    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, n_layers=4, fp8=args.dtype == "fp8")
     sh = wl.shape
     steps = args.steps
     Ts = I.step_token_counts(steps + args.warmup, 6554, 8192, 0)
@@ -649,13 +660,15 @@ def cpu_baseline_sample(wl, target_s=15.0, max_tokens=512):
                 w13, w2 = lw.local_w13[pl.local_slot[e]], lw.local_w2[pl.local_slot[e]]
             else:
                 w13, w2 = lw.peer_w13[pl.peer_id[e]][pl.peer_slot[e]], lw.peer_w2[pl.peer_id[e]][pl.peer_slot[e]]
-            cache[e] = (I.bf16_bits(w13), I.bf16_bits(w2))
+            cache[e] = (conv(w13), conv(w2))
         w13s = [cache.get(e, (None, None))[0] for e in range(sh.E)]
         w2s = [cache.get(e, (None, None))[1] for e in range(sh.E)]
         return w13s, w2s
 
-    sw13 = I.bf16_bits(lw.shared_w13) if lw.shared_w13 is not None else None
-    sw2 = I.bf16_bits(lw.shared_w2) if lw.shared_w2 is not None else None
+    fp8 = getattr(wl, "fp8", False)
+    conv = (lambda t: t.detach().contiguous().cpu().numpy().view(np.uint8)) if fp8 else I.bf16_bits
+    sw13 = conv(lw.shared_w13) if lw.shared_w13 is not None else None
+    sw2 = conv(lw.shared_w2) if lw.shared_w2 is not None else None
 
     def run(tokens):
         xs = np.ascontiguousarray(x[tokens])
@@ -663,7 +676,11 @@ def cpu_baseline_sample(wl, target_s=15.0, max_tokens=512):
         w13s, w2s = weights_for(r_pre["ids"])          # host copies of those experts (untimed)
         t0 = time.perf_counter()
         r = o.route(xs, wr, bias, sh.k)
-        o.moe_tokens(xs, np.arange(len(tokens)), r["ids"], r["w"], w13s, w2s, sw13, sw2, mirrored=True)
+        if fp8:
+            o.moe_tokens_fp8(xs, np.arange(len(tokens)), r["ids"], r["w"], w13s, w2s, lw.w13_scale, lw.w2_scale,
+                             sw13, sw2, lw.shared_s13, lw.shared_s2, mirrored=True)
+        else:
+            o.moe_tokens(xs, np.arange(len(tokens)), r["ids"], r["w"], w13s, w2s, sw13, sw2, mirrored=True)
         return time.perf_counter() - t0
 
     n = 8
@@ -708,16 +725,22 @@ def main():
     sh = wl.shape
     peaks, src = measured_peaks()
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    fp8 = args.dtype == "fp8"
+    wb = 1 if fp8 else 2
+    peak_note = f"{src} bf16_tflops_sustained (kernel timed inside a long step)"
+    if fp8:   # measured bf16 peak x the nominal dense fp8 / bf16 ratio (4.5 / 2.25)
+        peak = peak * 2.0
+        peak_note = f"{src} bf16_tflops_sustained x 2 (nominal dense E4M3 / bf16 ratio), kernel inside a long step"
     hbm = peaks["hbm_gbs"]
     line = {
         "metric": METRIC, "value": round(res["value"], 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_step"], 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights; R1 MoE layer shapes)",
         "config": {"workload": args.workload, "T": sh.T, "H": sh.H, "I": sh.I, "E": sh.E, "k": sh.k,
                    "shared": sh.S, "local_experts": int((wl.placement.local_slot >= 0).sum()),
                    "remote_experts": wl.placement.n_remote(), "peer_pools": wl.placement.n_peers,
-                   "chunk_mb": args.chunk_mb, "copy_streams": args.copy_streams,
+                   "chunk_mb": args.chunk_mb, "copy_streams": args.copy_streams, "expert_weights": args.dtype,
                    "layers": wl.n_layers,
                    "l2": "inputs larger than L2 (22.6 GB of expert weights + 16.9 GB of copies per layer)",
                    "parallelism": "replicas" if world > 1 else "single rank"},
@@ -728,23 +751,24 @@ def main():
                     for T in res["tokens_per_step"]) / len(res["tokens_per_step"])
         line["config"]["tokens_per_step"] = res["tokens_per_step"]
         line["config"]["attention_standin"] = "bf16 GEMM T x 7168 x 7168 after every MoE layer"
+        line["config"]["expert_weights"] = args.dtype
         line["tflops"] = round(flops / (res["ms_step"] / 1e3) / 1e12, 1)
         line["gpu_launches"] = args.steps * 4 * 9
     else:
         flops_layer = layer_flops(sh.T, sh.H, sh.I, sh.E, sh.k, sh.S)
         g1 = g1_flops(sh.T, sh.H, sh.I, sh.k, sh.S)
         g1_tflops = g1 / (res["phase_ms"]["gate_up_gemm"] / 1e3) / 1e12
-        g1b = g1_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S)
-        sb = step_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S, wl.placement.n_remote())
+        g1b = g1_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S, wb)
+        sb = step_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S, wl.placement.n_remote(), wb)
         layer_tflops = flops_layer / (res["ms_step"] / 1e3) / 1e12
         traffic = None
-        if args.workload == "r1_moe_layer_8k":
+        if args.workload == "r1_moe_layer_8k" and not fp8:
             traffic = measured_traffic(os.path.join(ROOT, "moe_expert_grouped_split_gb300", "csrc", "gemm.cu"))
         g1_s = res["phase_ms"]["gate_up_gemm"] / 1e3
         if g1 / g1b >= peak * 1e12 / (hbm * 1e9):     # arithmetic intensity at or above the ridge
             roof = {"kernel": "gate_up_grouped_gemm", "bound": "tensor", "achieved": round(g1_tflops, 1),
                     "peak": peak, "unit": "TFLOP/s", "frac": round(g1_tflops / peak, 4),
-                    "peak_source": f"{src} bf16_tflops_sustained (kernel timed inside a long step)"}
+                    "peak_source": peak_note}
         else:
             gbs = g1b / g1_s / 1e9
             roof = {"kernel": "gate_up_grouped_gemm", "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
@@ -773,7 +797,7 @@ def main():
                "hidden_frac": round(max(0.0, 1.0 - exposed / copy), 4) if copy > 0 else None,
                "model_max_ms": round(max(comp, copy), 4)}
         if not pipeline:
-            pre["copy_gbs"] = round(wl.placement.n_remote() * 3 * sh.H * sh.I * 2 / (copy / 1e3) / 1e9, 1)
+            pre["copy_gbs"] = round(wl.placement.n_remote() * 3 * sh.H * sh.I * wb / (copy / 1e3) / 1e9, 1)
             pre["compute_only_phase_ms"] = res["compute_only_phase_ms"]
             # kernel slowdown while the copy engine runs (analogue of the pages'
             # communication-computation interference, DWDP appendix A)

@@ -77,6 +77,28 @@ def test_many_groups(rt):
     _case(rt, B.EPI_SILU, K=128, N=128, sizes=sizes, n_bufs=2, slots=8, seed=12)
 
 
+def test_device_check_reports_rows_outside_the_output(rt):
+    """Group rows live in device memory, so the host cannot check them: rows
+    at or past a_rows are not stored, the kernel sets the context's device
+    error word, and dwdp_device_status reports DEVICE_CHECK once (then
+    clears it); the context stays usable."""
+    a = torch.ones((64, 64), dtype=torch.bfloat16, device="cuda")
+    b = torch.ones((1, 64, 64), dtype=torch.bfloat16, device="cuda")
+    d = torch.zeros((200, 64), dtype=torch.bfloat16, device="cuda")
+    off = torch.tensor([0, 100], dtype=torch.int32, device="cuda")     # 100 rows, but a_rows = 64
+    B.dwdp_grouped_gemm(rt.ctx, 0, a, 64, 64, 64, off, 1, [b], [0, 0], d)
+    torch.cuda.synchronize()
+    assert rt.device_status() == -6
+    assert "error bits" in B.dwdp_last_error(rt.ctx)
+    assert (d[64:].float() == 0).all(), "rows past a_rows were written"
+    assert (d[:64].float() == 64).all()
+    assert rt.device_status() == 0                                     # cleared, context usable
+    off2 = torch.tensor([0, 64], dtype=torch.int32, device="cuda")
+    B.dwdp_grouped_gemm(rt.ctx, 0, a, 64, 64, 64, off2, 1, [b], [0, 0], d)
+    torch.cuda.synchronize()
+    assert rt.device_status() == 0
+
+
 def test_rejects_bad_arguments(rt):
     a = torch.zeros((8, 64), dtype=torch.bfloat16, device="cuda")
     b = torch.zeros((1, 64, 64), dtype=torch.bfloat16, device="cuda")
