@@ -122,6 +122,30 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// As tma_load_3d, but the box lands at the same shared-memory offset in every
+// CTA of the cluster named in cta_mask, each completing its own mbarrier at
+// the same offset.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                               uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(cta_mask)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA in the cluster arrives, then waits for all.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
 }
@@ -171,6 +195,16 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// Commit that arrives on the mbarrier at the same offset in every CTA of
+// cta_mask once this thread's MMAs have finished reading shared memory.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(cta_mask)
         : "memory");
 }
 
@@ -247,6 +281,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     const int ntile_cols = (EPI == EPI_SILU) ? (BN / 2) : BN;  // output columns per tile
     const int NT = (p.N + ntile_cols - 1) / ntile_cols;
     const int KB = (p.K + KE - 1) / KE;
+    // Paired mode: the two CTAs of a cluster hold tiles 2p and 2p+1 (every
+    // group has an even number of tiles when NT is even, so a pair never
+    // straddles two groups).  When both tiles use the same weight tile (same
+    // n-tile: sibling m-tiles) each CTA loads one half of it and multicasts it
+    // to both; either way each stage is refilled only after BOTH CTAs' MMAs
+    // have finished with it (commits are multicast), so the pair stays in step.
+    const bool paired = (EPI != EPI_F32) && (NT % 2 == 0);
+    const uint32_t crank = cluster_ctarank();
 
     // ---- tile counts per group, then an inclusive scan into tile_start ----
     for (int g = threadIdx.x; g < G; g += blockDim.x) {
@@ -262,7 +304,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         *abort_flag = 0;
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), paired ? 2 : 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
@@ -286,6 +328,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         prefetch_map(&p.tmB[2]);
     }
     __syncthreads();
+    // the peer's barriers must be initialised before anything is multicast into them
+    if (paired) cluster_sync();
     if (warp == 0) {
         int carry = 0;
         for (int base = 0; base < G; base += 32) {
@@ -335,6 +379,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                     b_row0 = n * BN;
                     b_row1 = n * BN + BN / 2;
                 }
+                // the pair shares the weight tile when the peer's tile (tile ^ 1,
+                // same group) has the same n-tile
+                const bool share = paired && (((local ^ 1) / mt) == n);
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err, DERR_PRODUCER_WAIT)) {
                         ok = false;
@@ -345,8 +392,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                     const uint32_t sa = sbase + SmemLayout::kA + stage * kABytes;
                     const uint32_t sb = sbase + SmemLayout::kB + stage * kBBytes;
                     tma_load_2d(sa, ma, kb * KE, a_row, fb);
-                    tma_load_3d(sb, mb, kb * KE, b_row0, src.y, fb);
-                    tma_load_3d(sb + kBBytes / 2, mb, kb * KE, b_row1, src.y, fb);
+                    if (share) {
+                        // my half of the weight tile, into both CTAs' stages
+                        const uint32_t off = crank ? (uint32_t)(kBBytes / 2) : 0u;
+                        tma_load_3d_mc(sb + off, mb, kb * KE, crank ? b_row1 : b_row0, src.y, fb, (uint16_t)0x3);
+                    } else {
+                        tma_load_3d(sb, mb, kb * KE, b_row0, src.y, fb);
+                        tma_load_3d(sb + kBBytes / 2, mb, kb * KE, b_row1, src.y, fb);
+                    }
                     pend[stage] = (int)phase;
                     if (++stage == kStages) {
                         stage = 0;
@@ -390,7 +443,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                         tc_mma<F8>(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk),
                                (kb > 0 || kk > 0) ? 1u : 0u);
                     }
-                    tc_commit(empty_bar(stage));
+                    // Paired CTAs always free a stage in both CTAs, shared tile or not:
+                    // if a pair could drift apart on unshared tiles, the first shared
+                    // tile's multicast could land in a stage the slower CTA still reads.
+                    if (paired)
+                        tc_commit_mc(empty_bar(stage), (uint16_t)0x3);
+                    else
+                        tc_commit(empty_bar(stage));
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -507,6 +566,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 
     tc_fence_before();
     __syncthreads();
+    // neither CTA of a pair leaves while the other may still multicast into
+    // its shared memory or arrive on its barriers
+    if (paired) cluster_sync();
     tc_fence_after();
     if (warp == 1) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem_base) : "memory");
