@@ -260,23 +260,24 @@ class Workload:
         self.chunk = int(chunk_bytes)
         self.issue_s = []
 
-    def layer_step(self, layer, stage, T=None, x=None):
+    def layer_step(self, layer, stage, T=None, x=None, out=None):
         T = self.shape.T if T is None else T
         x = (self.x[layer] if x is None else x)[:T]
+        out = (self.out if out is None else out)[:T]
         with self.torch.cuda.stream(self.compute):
             self.rt.route(x, self.layers[layer].wr, self.layers[layer].bias, self.rb, self.compute)
-            self.rt.moe(layer, stage, x, self.rb, self.out[:T], self.compute)
+            self.rt.moe(layer, stage, x, self.rb, out, self.compute)
 
     def prefetch(self, layer, stage):
         t0 = time.perf_counter()
         self.rt.prefetch(layer, stage, self.chunk, self.copies)
         self.issue_s.append(time.perf_counter() - t0)
 
-    def step(self, i, prefetch_next=True, x=None):
+    def step(self, i, prefetch_next=True, x=None, out=None):
         """Step i of the two-layer alternation: layer i%2 from stage i%2, and
         the prefetch of layer (i+1)%2 into the other stage."""
         l = i % self.n_layers
-        self.layer_step(l, i % 2, x=x)
+        self.layer_step(l, i % 2, x=x, out=out)
         if prefetch_next:
             self.prefetch((i + 1) % self.n_layers, (i + 1) % 2)
 
@@ -369,35 +370,50 @@ def run_copy_only(wl, K):
 
 def run_e2e(wl, K, world, barrier=lambda: None):
     """The metric through the public API with host buffers: each step copies
-    its tokens in from pinned host memory and its output back."""
+    its tokens in from pinned host memory and its output back to pinned host
+    memory, inside the timed region.  The copies run on their own streams,
+    double-buffered, so step i+1's tokens arrive and step i-1's output
+    leaves while step i computes."""
     torch = wl.torch
     sh = wl.shape
     T = sh.T
     xh = [x.cpu().pin_memory() for x in wl.x]
-    oh = torch.empty((T, sh.H), dtype=torch.bfloat16).pin_memory()
-    xd = torch.empty_like(wl.x[0])
+    oh = [torch.empty((T, sh.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    xd = [torch.empty_like(wl.x[0]) for _ in range(2)]
+    od = [torch.empty_like(wl.out) for _ in range(2)]
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    x_ready, x_free, o_ready, o_free = ([torch.cuda.Event() for _ in range(2)] for _ in range(4))
+
+    def step(i):
+        b = i % 2
+        h2d.wait_event(x_free[b])                 # step i-2 has finished reading xd[b]
+        with torch.cuda.stream(h2d):
+            xd[b].copy_(xh[i % 2], non_blocking=True)
+        x_ready[b].record(h2d)
+        wl.compute.wait_event(x_ready[b])
+        wl.compute.wait_event(o_free[b])          # step i-2's output has left od[b]
+        wl.step(i, x=xd[b], out=od[b])
+        x_free[b].record(wl.compute)
+        o_ready[b].record(wl.compute)
+        d2h.wait_event(o_ready[b])
+        with torch.cuda.stream(d2h):
+            oh[b].copy_(od[b], non_blocking=True)
+        o_free[b].record(d2h)
+
     wl.sync()
     wl.prologue()
     for i in range(2):
-        with torch.cuda.stream(wl.compute):
-            xd.copy_(xh[i % 2], non_blocking=True)
-        wl.step(i, x=xd)
-        with torch.cuda.stream(wl.compute):
-            oh.copy_(wl.out, non_blocking=True)
+        step(i)
     wl.sync()
     barrier()
     a, b = _events(torch, 2)
     a.record(wl.compute)
-    for c in wl.copies:
-        c.wait_stream(wl.compute)
+    for s_ in wl.copies + [h2d, d2h]:
+        s_.wait_stream(wl.compute)
     for i in range(2, 2 + K):
-        with torch.cuda.stream(wl.compute):
-            xd.copy_(xh[i % 2], non_blocking=True)
-        wl.step(i, x=xd)
-        with torch.cuda.stream(wl.compute):
-            oh.copy_(wl.out, non_blocking=True)
-    for c in wl.copies:
-        wl.compute.wait_stream(c)
+        step(i)
+    for s_ in wl.copies + [h2d, d2h]:
+        wl.compute.wait_stream(s_)
     b.record(wl.compute)
     b.synchronize()
     assert wl.rt.device_status() == 0

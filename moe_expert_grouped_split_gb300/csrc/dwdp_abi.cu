@@ -150,6 +150,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct WsLayout {
     size_t logits = 0;  // route: fp32 [T][E] when the caller does not keep logits
+    size_t group = 0;   // route: scratch of the chunked grouping
     // moe offsets: gathered rows xp, activations a, expert outputs y; E4M3
     // contexts also keep x's codes/scales (xq, sx), xp's scales (sxp) and
     // a's codes/scales (aq, sa).
@@ -162,7 +163,8 @@ WsLayout ws_layout(const dwdp_config& c, int64_t T) {
     const int64_t H = c.hidden, I = c.inter, E = c.n_experts, k = c.top_k, S = c.n_shared;
     const int64_t eb = (c.weight_dtype == DWDP_DTYPE_E4M3) ? 1 : 2;  // bytes of a GEMM operand element
     L.logits = 0;
-    L.route_bytes = align_up((size_t)(T * E * 4), 256);
+    L.group = align_up((size_t)(T * E * 4), 256);
+    L.route_bytes = L.group + align_up(group_chunked_scratch_bytes((int)(T * k), (int)E), 256);
     size_t o = 0;
     auto take = [&](size_t bytes) {
         const size_t at = o;
@@ -479,13 +481,12 @@ int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router
     if (!x || !w_router || !aligned16(x) || !aligned16(w_router))
         return fail(ctx, DWDP_ERR_INVALID_ARG, "x and w_router must be non-NULL, 16-byte aligned");
     const WsLayout L = ws_layout(c, T);
+    if (!ws || ws_bytes < L.route_bytes || !aligned16(ws))
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "workspace too small (%zu < %zu) or unaligned", ws_bytes,
+                    L.route_bytes);
     float* logits = out->logits;
-    if (!logits) {
-        if (!ws || ws_bytes < L.route_bytes || !aligned16(ws))
-            return fail(ctx, DWDP_ERR_INVALID_ARG, "workspace too small (%zu < %zu) or unaligned", ws_bytes,
-                        L.route_bytes);
-        logits = reinterpret_cast<float*>(static_cast<char*>(ws) + L.logits);
-    }
+    if (!logits) logits = reinterpret_cast<float*>(static_cast<char*>(ws) + L.logits);
+    int32_t* group_scratch = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.group);
     DWDP_CUDA(ctx, mark(ctx, 0, stream));
     GemmArgs& a = *ctx->args;
     if (!encode_rows(&a.tmA[0], x, T, c.hidden) ||
@@ -508,8 +509,8 @@ int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router
     a.bsrc[0] = make_int2(0, 0);
     DWDP_CUDA(ctx, launch_grouped_gemm(EPI_F32, false, a, ctx->n_sms, stream));
     DWDP_CUDA(ctx, launch_topk(logits, nullptr, T, c.n_experts, c.top_k, out->topk_ids, out->topk_w, stream));
-    DWDP_CUDA(ctx, launch_group(out->topk_ids, T * c.top_k, c.n_experts, out->counts, out->offsets, out->perm,
-                                out->inv_perm, stream));
+    DWDP_CUDA(ctx, launch_group_chunked(out->topk_ids, T * c.top_k, c.n_experts, out->counts, out->offsets,
+                                        out->perm, out->inv_perm, group_scratch, stream));
     DWDP_CUDA(ctx, mark(ctx, 1, stream));
     return DWDP_OK;
 }

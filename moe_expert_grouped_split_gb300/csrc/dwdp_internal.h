@@ -88,6 +88,11 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
                         int32_t* ids, float* w, cudaStream_t s);
 cudaError_t launch_group(const int32_t* ids, int n, int E, int32_t* counts, int32_t* offsets,
                          int32_t* perm, int32_t* inv, cudaStream_t s);
+// The same grouping in three passes over chunks of 1024 pairs; needs
+// group_chunked_scratch_bytes(n, E) of device scratch (E <= 1024).
+size_t group_chunked_scratch_bytes(int n, int E);
+cudaError_t launch_group_chunked(const int32_t* ids, int n, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                 int32_t* inv, int32_t* scratch, cudaStream_t s);
 cudaError_t launch_gather(const void* x, int H, const int32_t* perm, int n_rows, int k, void* xp,
                           cudaStream_t s);
 // E4M3 rows: codes[r][:] and scale[r] of bf16 rows (scale = amax / 448).

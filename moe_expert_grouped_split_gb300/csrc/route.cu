@@ -159,6 +159,83 @@ __global__ void __launch_bounds__(1024) place_kernel(const int32_t* __restrict__
     }
 }
 
+// The same grouping as count_kernel + place_kernel, in three passes over
+// chunks of kChunk consecutive pairs (one 1024-thread block per chunk):
+//   chunk_count:  hist[c][e] = pairs of chunk c routed to expert e
+//   chunk_scan:   counts, offsets, and base[c][e] = offsets[e] + pairs of
+//                 e in chunks before c
+//   chunk_place:  pair f of chunk c with expert e goes to row base[c][e] +
+//                 (pairs of e earlier in the chunk), ranked with warp
+//                 match_any inside a warp and per-warp counts across warps.
+// Every row is the stable (ascending flat index) position, as before.
+constexpr int kChunk = 1024;
+
+__global__ void __launch_bounds__(kChunk) chunk_count_kernel(const int32_t* __restrict__ ids, int n, int E,
+                                                             int32_t* __restrict__ hist) {
+    extern __shared__ int h[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
+    __syncthreads();
+    const int f = blockIdx.x * kChunk + threadIdx.x;
+    if (f < n) atomicAdd(&h[ids[f]], 1);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = h[e];
+}
+
+// One block of >= E threads: thread e walks the chunks of expert e.
+__global__ void __launch_bounds__(1024) chunk_scan_kernel(int32_t* __restrict__ hist, int n_chunks, int E,
+                                                          int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ offsets) {
+    __shared__ int scan[1024];
+    const int e = threadIdx.x;
+    int c_e = 0;
+    if (e < E)
+        for (int c = 0; c < n_chunks; ++c) {
+            const int v = hist[(int64_t)c * E + e];
+            hist[(int64_t)c * E + e] = c_e;  // pairs of e before chunk c
+            c_e += v;
+        }
+    scan[e] = (e < E) ? c_e : 0;
+    __syncthreads();
+    // inclusive scan over experts (Hillis-Steele in shared memory)
+    for (int o = 1; o < 1024; o <<= 1) {
+        const int v = (e >= o) ? scan[e - o] : 0;
+        __syncthreads();
+        scan[e] += v;
+        __syncthreads();
+    }
+    if (e < E) {
+        const int base = scan[e] - c_e;
+        counts[e] = c_e;
+        offsets[e] = base;
+        if (e == E - 1) offsets[E] = scan[e];
+        for (int c = 0; c < n_chunks; ++c) hist[(int64_t)c * E + e] += base;
+    }
+}
+
+__global__ void __launch_bounds__(kChunk) chunk_place_kernel(const int32_t* __restrict__ ids, int n, int E,
+                                                             const int32_t* __restrict__ base,
+                                                             int32_t* __restrict__ perm,
+                                                             int32_t* __restrict__ inv) {
+    extern __shared__ uint8_t wc[];  // [32 warps][E]: pairs of e in each warp (<= 32)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wc[i] = 0;
+    const int f = blockIdx.x * kChunk + threadIdx.x;
+    const bool valid = f < n;
+    const int e = valid ? ids[f] : -1;
+    __syncthreads();
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const int rank_w = __popc(peers & ((1u << lane) - 1u));
+    if (valid && lane == __ffs(peers) - 1) wc[warp * E + e] = (uint8_t)__popc(peers);
+    __syncthreads();
+    if (valid) {
+        int before = 0;
+        for (int w = 0; w < warp; ++w) before += wc[w * E + e];
+        const int r = base[(int64_t)blockIdx.x * E + e] + before + rank_w;
+        perm[r] = f;
+        inv[f] = r;
+    }
+}
+
 // xp[r][:] = x[perm[r] / k][:]: one warp per row, 16-byte copies.
 __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x, int row_vecs,
                                                      const int32_t* __restrict__ perm, int n_rows,
@@ -299,6 +376,27 @@ cudaError_t launch_group(const int32_t* ids, int n, int E, int32_t* counts, int3
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     place_kernel<<<E, 1024, 0, s>>>(ids, n, E, counts, offsets, perm, inv);
+    return cudaGetLastError();
+}
+
+size_t group_chunked_scratch_bytes(int n, int E) {
+    return sizeof(int32_t) * (size_t)((n + kChunk - 1) / kChunk) * (size_t)E;
+}
+
+cudaError_t launch_group_chunked(const int32_t* ids, int n, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                 int32_t* inv, int32_t* scratch, cudaStream_t s) {
+    const int n_chunks = (n + kChunk - 1) / kChunk;
+    if (n_chunks == 0) {
+        cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, s);
+        return e != cudaSuccess ? e : cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), s);
+    }
+    chunk_count_kernel<<<n_chunks, kChunk, sizeof(int) * E, s>>>(ids, n, E, scratch);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    chunk_scan_kernel<<<1, 1024, 0, s>>>(scratch, n_chunks, E, counts, offsets);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    chunk_place_kernel<<<n_chunks, kChunk, 32 * E, s>>>(ids, n, E, scratch, perm, inv);
     return cudaGetLastError();
 }
 
