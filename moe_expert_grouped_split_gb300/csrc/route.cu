@@ -246,7 +246,16 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x
     const int t = perm[r] / k;
     const uint4* src = x + (int64_t)t * row_vecs;
     uint4* dst = xp + (int64_t)r * row_vecs;
-    for (int i = lane; i < row_vecs; i += 32) dst[i] = __ldg(src + i);
+    int i = lane;
+    for (; i + 96 < row_vecs; i += 128) {  // four 16-byte loads in flight per lane
+        const uint4 v0 = __ldg(src + i), v1 = __ldg(src + i + 32), v2 = __ldg(src + i + 64),
+                    v3 = __ldg(src + i + 96);
+        dst[i] = v0;
+        dst[i + 32] = v1;
+        dst[i + 64] = v2;
+        dst[i + 96] = v3;
+    }
+    for (; i < row_vecs; i += 32) dst[i] = __ldg(src + i);
 }
 
 __device__ __forceinline__ void acc_bf16x8(float (&a)[8], uint4 q, float s) {
@@ -283,6 +292,43 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
         __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
         for (int q = 0; q < 4; ++q) oh[q] = __floats2bfloat162_rn(a[2 * q], a[2 * q + 1]);
+        out[(int64_t)t * row_vecs + i] = o;
+    }
+}
+
+// combine_kernel with k fixed at compile time: the token's rows and weights
+// stay in registers and all k (+1) row loads are issued before the sums,
+// which are the same fp32 operations in the same order.
+template <int KC>
+__global__ void __launch_bounds__(256) combine_kernel_k(const uint4* __restrict__ y, int row_vecs,
+                                                        const int32_t* __restrict__ inv,
+                                                        const float* __restrict__ w, int T,
+                                                        int64_t shared_row0, int has_shared,
+                                                        uint4* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int64_t rows[KC];
+    float ws[KC];
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+        rows[j] = (int64_t)inv[(int64_t)t * KC + j] * row_vecs;
+        ws[j] = w[(int64_t)t * KC + j];
+    }
+    const int64_t srow = (shared_row0 + t) * row_vecs;
+    for (int i = lane; i < row_vecs; i += 32) {
+        uint4 q[KC + 1];
+#pragma unroll
+        for (int j = 0; j < KC; ++j) q[j] = __ldg(y + rows[j] + i);
+        if (has_shared) q[KC] = __ldg(y + srow + i);
+        float a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+        for (int j = 0; j < KC; ++j) acc_bf16x8(a, q[j], ws[j]);
+        if (has_shared) acc_bf16x8(a, q[KC], 1.0f);
+        uint4 o;
+        __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) oh[c] = __floats2bfloat162_rn(a[2 * c], a[2 * c + 1]);
         out[(int64_t)t * row_vecs + i] = o;
     }
 }
@@ -413,9 +459,16 @@ cudaError_t launch_combine(const void* y, int H, const int32_t* inv, const float
                            int64_t shared_row0, bool has_shared, void* out, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     const int warps = 8;
-    combine_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(
-        reinterpret_cast<const uint4*>(y), H / 8, inv, w, T, k, shared_row0, has_shared ? 1 : 0,
-        reinterpret_cast<uint4*>(out));
+    const dim3 grid((T + warps - 1) / warps), block(32 * warps);
+    const uint4* yv = reinterpret_cast<const uint4*>(y);
+    uint4* ov = reinterpret_cast<uint4*>(out);
+    const int hs = has_shared ? 1 : 0;
+    switch (k) {
+        case 2: combine_kernel_k<2><<<grid, block, 0, s>>>(yv, H / 8, inv, w, T, shared_row0, hs, ov); break;
+        case 4: combine_kernel_k<4><<<grid, block, 0, s>>>(yv, H / 8, inv, w, T, shared_row0, hs, ov); break;
+        case 8: combine_kernel_k<8><<<grid, block, 0, s>>>(yv, H / 8, inv, w, T, shared_row0, hs, ov); break;
+        default: combine_kernel<<<grid, block, 0, s>>>(yv, H / 8, inv, w, T, k, shared_row0, hs, ov);
+    }
     return cudaGetLastError();
 }
 
