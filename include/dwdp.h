@@ -207,7 +207,7 @@ int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t 
                             dwdp_stream_t const* copy_streams, int32_t n_copy_streams);
 
 /* One MoE layer for T tokens on `stream` ([DWDP] §2 and §4.2):
- *   xp  = x rows gathered into expert order (route->perm)
+ *   xp  = x rows copied into expert order (row route->inv_perm[t*k+j] = x[t])
  *   a   = SiLU(xp W_gate) * (xp W_up)          per expert, bf16
  *   y   = a W_down                             per expert, bf16
  *   out[t] = sum_j topk_w[t][j] y[inv_perm[t*k+j]] + y_shared[t]  (fp32 sum, bf16)

@@ -615,9 +615,9 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     if (f8) {
         // x rows to E4M3 (per-token scales), then gathered into expert order
         DWDP_CUDA(ctx, launch_quantize_rows(x, T, (int)H, xq, sx, stream));
-        DWDP_CUDA(ctx, launch_gather_fp8(xq, sx, (int)H, route->perm, (int)rows_r, (int)k, xp, sxp, stream));
+        DWDP_CUDA(ctx, launch_gather_fp8(xq, sx, (int)H, route->inv_perm, (int)T, (int)k, xp, sxp, stream));
     } else {
-        DWDP_CUDA(ctx, launch_gather(x, (int)H, route->perm, (int)rows_r, (int)k, xp, stream));
+        DWDP_CUDA(ctx, launch_gather(x, (int)H, route->inv_perm, (int)T, (int)k, xp, stream));
     }
     DWDP_CUDA(ctx, mark(ctx, 3, stream));
 

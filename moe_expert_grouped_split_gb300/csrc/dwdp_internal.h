@@ -93,12 +93,12 @@ cudaError_t launch_group(const int32_t* ids, int n, int E, int32_t* counts, int3
 size_t group_chunked_scratch_bytes(int n, int E);
 cudaError_t launch_group_chunked(const int32_t* ids, int n, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
                                  int32_t* inv, int32_t* scratch, cudaStream_t s);
-cudaError_t launch_gather(const void* x, int H, const int32_t* perm, int n_rows, int k, void* xp,
-                          cudaStream_t s);
+// Expert-ordered token rows: xp[inv[t k + j]] = x[t] for t < T, j < k.
+cudaError_t launch_gather(const void* x, int H, const int32_t* inv, int T, int k, void* xp, cudaStream_t s);
 // E4M3 rows: codes[r][:] and scale[r] of bf16 rows (scale = amax / 448).
 cudaError_t launch_quantize_rows(const void* in, int64_t rows, int cols, void* codes, float* scale, cudaStream_t s);
-// Gathered E4M3 rows: xp[r] = xq[perm[r] / k], sxp[r] = sx[perm[r] / k].
-cudaError_t launch_gather_fp8(const void* xq, const float* sx, int H, const int32_t* perm, int n_rows, int k,
+// Expert-ordered E4M3 rows: xp[inv[t k + j]] = xq[t], sxp[inv[t k + j]] = sx[t].
+cudaError_t launch_gather_fp8(const void* xq, const float* sx, int H, const int32_t* inv, int T, int k,
                               void* xp, float* sxp, cudaStream_t s);
 cudaError_t launch_combine(const void* y, int H, const int32_t* inv, const float* w, int T, int k,
                            int64_t shared_row0, bool has_shared, void* out, cudaStream_t s);

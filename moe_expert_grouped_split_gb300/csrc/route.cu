@@ -236,26 +236,74 @@ __global__ void __launch_bounds__(kChunk) chunk_place_kernel(const int32_t* __re
     }
 }
 
-// xp[r][:] = x[perm[r] / k][:]: one warp per row, 16-byte copies.
-__global__ void __launch_bounds__(256) gather_kernel(const uint4* __restrict__ x, int row_vecs,
-                                                     const int32_t* __restrict__ perm, int n_rows,
-                                                     int k, uint4* __restrict__ xp) {
+// Expert-ordered copies of the token rows: xp[inv[t k + j]][:] = x[t][:]
+// for every chosen expert j of token t (and sxp[inv[t k + j]] = sx[t] for
+// E4M3 rows).  One warp per token reads its row from HBM once and stores
+// it to its k slots, so the pass moves T rows in and T k rows out; walking
+// the permuted rows instead reads each token row k times at random
+// distances, which L2 does not hold.  The stores are streaming
+// (st.global.cs): the gate/up GEMM reads them long after they would have
+// left L2.  Each lane keeps four 16-byte loads in flight.  KC > 0 fixes k at
+// compile time so the k destinations stay in registers.
+template <int KC>
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const uint4* __restrict__ x, int row_vecs,
+                                                           const int32_t* __restrict__ inv, int T, int k,
+                                                           uint4* __restrict__ xp, const float* __restrict__ sx,
+                                                           float* __restrict__ sxp) {
     const int lane = threadIdx.x & 31;
-    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (r >= n_rows) return;
-    const int t = perm[r] / k;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int kk = KC > 0 ? KC : k;
+    const int32_t* it = inv + (int64_t)t * kk;
     const uint4* src = x + (int64_t)t * row_vecs;
-    uint4* dst = xp + (int64_t)r * row_vecs;
-    int i = lane;
-    for (; i + 96 < row_vecs; i += 128) {  // four 16-byte loads in flight per lane
-        const uint4 v0 = __ldg(src + i), v1 = __ldg(src + i + 32), v2 = __ldg(src + i + 64),
-                    v3 = __ldg(src + i + 96);
-        dst[i] = v0;
-        dst[i + 32] = v1;
-        dst[i + 64] = v2;
-        dst[i + 96] = v3;
+    if (sxp != nullptr)
+        for (int j = lane; j < kk; j += 32) sxp[it[j]] = sx[t];
+    if constexpr (KC > 0) {
+        int64_t dst[KC];
+#pragma unroll
+        for (int j = 0; j < KC; ++j) dst[j] = (int64_t)it[j] * row_vecs;
+        int i = lane;
+        for (; i + 96 < row_vecs; i += 128) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = __ldg(src + i + 32 * u);
+#pragma unroll
+            for (int j = 0; j < KC; ++j)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) __stcs(xp + dst[j] + i + 32 * u, v[u]);
+        }
+        for (; i < row_vecs; i += 32) {
+            const uint4 v = __ldg(src + i);
+#pragma unroll
+            for (int j = 0; j < KC; ++j) __stcs(xp + dst[j] + i, v);
+        }
+    } else {
+        for (int i = lane; i < row_vecs; i += 32) {
+            const uint4 v = __ldg(src + i);
+            for (int j = 0; j < kk; ++j) __stcs(xp + (int64_t)it[j] * row_vecs + i, v);
+        }
     }
-    for (; i < row_vecs; i += 32) dst[i] = __ldg(src + i);
+}
+
+template <int KC>
+void scatter_rows_launch(const uint4* x, int row_vecs, const int32_t* inv, int T, int k, uint4* xp,
+                         const float* sx, float* sxp, cudaStream_t s) {
+    const int warps = 8;
+    scatter_rows_kernel<KC><<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(x, row_vecs, inv, T, k, xp, sx, sxp);
+}
+
+cudaError_t scatter_rows(const void* x, int row_vecs, const int32_t* inv, int T, int k, void* xp, const float* sx,
+                         float* sxp, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    uint4* pv = reinterpret_cast<uint4*>(xp);
+    switch (k) {
+        case 2: scatter_rows_launch<2>(xv, row_vecs, inv, T, k, pv, sx, sxp, s); break;
+        case 4: scatter_rows_launch<4>(xv, row_vecs, inv, T, k, pv, sx, sxp, s); break;
+        case 8: scatter_rows_launch<8>(xv, row_vecs, inv, T, k, pv, sx, sxp, s); break;
+        default: scatter_rows_launch<0>(xv, row_vecs, inv, T, k, pv, sx, sxp, s);
+    }
+    return cudaGetLastError();
 }
 
 __device__ __forceinline__ void acc_bf16x8(float (&a)[8], uint4 q, float s) {
@@ -374,21 +422,6 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
     }
 }
 
-// xp[r][:] = xq[perm[r] / k][:] (E4M3 codes, H bytes per row), sxp[r] =
-// sx[perm[r] / k]: one warp per row, 16-byte copies.
-__global__ void __launch_bounds__(256) gather_fp8_kernel(const uint4* __restrict__ xq, const float* __restrict__ sx,
-                                                         int row_vecs, const int32_t* __restrict__ perm, int n_rows,
-                                                         int k, uint4* __restrict__ xp, float* __restrict__ sxp) {
-    const int lane = threadIdx.x & 31;
-    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (r >= n_rows) return;
-    const int t = perm[r] / k;
-    const uint4* src = xq + (int64_t)t * row_vecs;
-    uint4* dst = xp + (int64_t)r * row_vecs;
-    for (int i = lane; i < row_vecs; i += 32) dst[i] = __ldg(src + i);
-    if (lane == 0) sxp[r] = sx[t];
-}
-
 }  // namespace
 
 cudaError_t launch_quantize_rows(const void* in, int64_t rows, int cols, void* codes, float* scale, cudaStream_t s) {
@@ -399,13 +432,9 @@ cudaError_t launch_quantize_rows(const void* in, int64_t rows, int cols, void* c
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather_fp8(const void* xq, const float* sx, int H, const int32_t* perm, int n_rows, int k,
+cudaError_t launch_gather_fp8(const void* xq, const float* sx, int H, const int32_t* inv, int T, int k,
                               void* xp, float* sxp, cudaStream_t s) {
-    if (n_rows <= 0) return cudaSuccess;
-    const int warps = 8;
-    gather_fp8_kernel<<<(n_rows + warps - 1) / warps, 32 * warps, 0, s>>>(
-        reinterpret_cast<const uint4*>(xq), sx, H / 16, perm, n_rows, k, reinterpret_cast<uint4*>(xp), sxp);
-    return cudaGetLastError();
+    return scatter_rows(xq, H / 16, inv, T, k, xp, sx, sxp, s);
 }
 
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
@@ -446,13 +475,8 @@ cudaError_t launch_group_chunked(const int32_t* ids, int n, int E, int32_t* coun
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const void* x, int H, const int32_t* perm, int n_rows, int k, void* xp,
-                          cudaStream_t s) {
-    if (n_rows <= 0) return cudaSuccess;
-    const int warps = 8;
-    gather_kernel<<<(n_rows + warps - 1) / warps, 32 * warps, 0, s>>>(
-        reinterpret_cast<const uint4*>(x), H / 8, perm, n_rows, k, reinterpret_cast<uint4*>(xp));
-    return cudaGetLastError();
+cudaError_t launch_gather(const void* x, int H, const int32_t* inv, int T, int k, void* xp, cudaStream_t s) {
+    return scatter_rows(x, H / 8, inv, T, k, xp, nullptr, nullptr, s);
 }
 
 cudaError_t launch_combine(const void* y, int H, const int32_t* inv, const float* w, int T, int k,
