@@ -105,6 +105,19 @@ class Oracle:
             _U16P, _I64, _I64, _I64, _I64P, _I64, _I32P, _F64P,
             ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), _F32P, _F32P,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_float, ctypes.c_int, _F64P]
+        L.oracle_e2m1_to_double.restype = ctypes.c_double
+        L.oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
+        L.oracle_e2m1_encode.restype = ctypes.c_uint8
+        L.oracle_e2m1_encode.argtypes = [ctypes.c_double]
+        L.oracle_quantize_row_nvfp4.restype = None
+        L.oracle_quantize_row_nvfp4.argtypes = [_F32P, _I64, _U8P, _U8P, ctypes.POINTER(ctypes.c_float)]
+        L.oracle_moe_tokens_nvfp4.restype = None
+        vpp = ctypes.POINTER(ctypes.c_void_p)
+        L.oracle_moe_tokens_nvfp4.argtypes = [
+            _U16P, _I64, _I64, _I64, _I64P, _I64, _I32P, _F64P,
+            vpp, vpp, _F32P, vpp, vpp, _F32P,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+            ctypes.c_int, _F64P]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         self.lib = L
@@ -291,6 +304,73 @@ class Oracle:
                                        s13.ctypes.data if s13 is not None else None,
                                        s2.ctypes.data if s2 is not None else None,
                                        float(shared_s13), float(shared_s2), int(bool(mirrored)), out)
+        del keep
+        return out
+
+    # -- NVFP4 (E2M1 codes, E4M3 scales per 16-element block) ---------------
+    def e2m1_encode(self, v: float) -> int:
+        return int(self.lib.oracle_e2m1_encode(float(v)))
+
+    def e2m1_decode(self, code: int) -> float:
+        return self.lib.oracle_e2m1_to_double(int(code))
+
+    def quantize_row_nvfp4(self, row) -> tuple:
+        """(codes uint8 [n] one per element, block scales uint8 [n / 16],
+        row scale) of one row of binary32 values (n a multiple of 16)."""
+        r = np.ascontiguousarray(row, dtype=np.float32)
+        if r.size % 16:
+            raise ValueError("NVFP4 rows are whole 16-element blocks")
+        codes = np.zeros(r.size, dtype=np.uint8)
+        sf = np.zeros(r.size // 16, dtype=np.uint8)
+        s = ctypes.c_float()
+        self.lib.oracle_quantize_row_nvfp4(r, r.size, codes, sf, ctypes.byref(s))
+        return codes, sf, float(s.value)
+
+    def moe_tokens_nvfp4(self, x, tokens, ids, w, w13, w13_sf, w13_scale, w2, w2_sf, w2_scale,
+                         shared=None, mirrored: bool = True) -> np.ndarray:
+        """Layer output rows with NVFP4 expert weights.  Per expert e (None for
+        experts no selected token uses): w13[e] codes [2I][H] and w13_sf[e]
+        block scales [2I][H/16], w2[e] codes [H][I] and w2_sf[e] [H][I/16],
+        one code or E4M3 scale per byte; w13_scale / w2_scale [E] tensor
+        scales.  shared = (w13, w13_sf, s13, w2, w2_sf, s2) or None.
+        Activations are quantized per row; see dwdp_oracle.c."""
+        x = _u16(x)
+        T, H = x.shape
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        w = np.ascontiguousarray(w, dtype=np.float64)
+        k = ids.shape[1]
+        tok = np.ascontiguousarray(tokens, dtype=np.int64)
+        E = len(w13)
+        keep, I = [], None
+        ptrs = [(ctypes.c_void_p * E)() for _ in range(4)]
+        for e in range(E):
+            if w13[e] is None:
+                continue
+            arrs = [np.ascontiguousarray(a, dtype=np.uint8) for a in (w13[e], w13_sf[e], w2[e], w2_sf[e])]
+            I = arrs[0].shape[0] // 2
+            assert arrs[0].shape == (2 * I, H) and arrs[1].shape == (2 * I, H // 16)
+            assert arrs[2].shape == (H, I) and arrs[3].shape == (H, I // 16)
+            keep += arrs
+            for p, a in zip(ptrs, arrs):
+                p[e] = a.ctypes.data
+        for e in (np.unique(ids[tok]) if tok.size else []):
+            if ptrs[0][int(e)] is None:
+                raise ValueError(f"expert {int(e)} is routed to but has no weights")
+        sh = [None] * 4
+        ss13 = ss2 = 1.0
+        if shared is not None:
+            sh = [np.ascontiguousarray(shared[i], dtype=np.uint8) for i in (0, 1, 3, 4)]
+            ss13, ss2 = float(shared[2]), float(shared[5])
+            I = sh[0].shape[0] // 2
+        if H % 16 or (I is not None and I % 16):
+            raise ValueError("NVFP4 needs H and I multiples of 16")
+        sc13 = np.ascontiguousarray(w13_scale, dtype=np.float32)
+        sc2 = np.ascontiguousarray(w2_scale, dtype=np.float32)
+        out = np.zeros((tok.size, H), dtype=np.float64)
+        dp = lambda a: a.ctypes.data if a is not None else None
+        self.lib.oracle_moe_tokens_nvfp4(x, H, I, k, tok, tok.size, ids, w, ptrs[0], ptrs[1], sc13, ptrs[2], ptrs[3],
+                                         sc2, dp(sh[0]), dp(sh[1]), ss13, dp(sh[2]), dp(sh[3]), ss2,
+                                         int(bool(mirrored)), out)
         del keep
         return out
 

@@ -494,3 +494,191 @@ void oracle_moe_tokens_fp8(const uint16_t* x, int64_t H, int64_t I, int64_t k, c
         free(acc);
     }
 }
+
+/* ------------------------------------------------------------ NVFP4 -- */
+
+/* The NVFP4 path (the pages run DeepSeek-R1 with NVFP4 MoE weights, DWDP
+ * §5.1 Experimental Setup; they do not restate the format).  NVFP4 as
+ * publicly defined: each value is an E2M1 code times an E4M3 scale shared by
+ * a block of 16 consecutive elements along the contraction dimension, times
+ * one binary32 scale for the whole tensor (weights: one per expert tensor;
+ * activations here: one per row).
+ *
+ * E2M1: 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit; no infinities
+ * or NaN.  Exponent field 0 is subnormal (0 or 0.5); otherwise
+ * 2^(e-1) * (1 + m/2).  Magnitudes: 0, 0.5, 1, 1.5, 2, 3, 4, 6.  Codes are
+ * passed one per byte (0..15) in math layout [rows][K]; block scales as
+ * E4M3 codes [rows][K / 16]. */
+double oracle_e2m1_to_double(uint8_t c) {
+    int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -v : v;
+}
+
+/* Round to nearest E2M1 magnitude, ties to the even mantissa, saturating to
+ * +-6; the sign is kept (a negative value that rounds to 0 gives code 8). */
+uint8_t oracle_e2m1_encode(double v) {
+    uint8_t sign = signbit(v) ? 8 : 0;
+    double a = fabs(v);
+    /* quantum: 0.5 below 2, 1 in [2, 4), 2 from 4 up */
+    int q = (a < 2.0) ? -1 : (a < 4.0) ? 0 : 1;
+#if ORACLE_MUTANT == 16
+    double r = ldexp(round(ldexp(a, -q)), q);    /* planted: ties away from zero */
+#else
+    double r = ldexp(nearbyint(ldexp(a, -q)), q);
+#endif
+    if (r > 6.0) r = 6.0;
+    if (r == 0.0) return sign;
+    if (r == 0.5) return sign | 1;
+    int e = ilogb(r) + 1;                         /* 1 for 1..1.5, 2 for 2..3, 3 for 4..6 */
+    int m = (int)((r / ldexp(1.0, e - 1) - 1.0) * 2.0);
+    return sign | (uint8_t)(e << 1) | (uint8_t)m;
+}
+
+/* Quantize one row of n binary32 values (n a multiple of 16) to NVFP4:
+ *   s   = amax(row) / (6 * 448)           (1 for an all-zero row)
+ *   d   = 6 * s
+ *   sf  = E4M3(amax(block) / d)           per block of 16 (RNE, saturating)
+ *   eff = E4M3 value of sf * s
+ *   c   = E2M1(v / eff)                   (0 for every element when sf is 0)
+ * Every operation is one binary32 operation, as a kernel performs it, so
+ * each code is an integer decision taken in the kernel's precision.  The row's
+ * largest element lands on E2M1 +-6 with block scale 448. */
+void oracle_quantize_row_nvfp4(const float* v, int64_t n, uint8_t* codes, uint8_t* block_scales, float* scale) {
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i) {
+        float a = fabsf(v[i]);
+        if (a > amax) amax = a;
+    }
+#if ORACLE_MUTANT == 17
+    float s = amax > 0.0f ? amax / 448.0f : 1.0f;    /* planted: block range 6 forgotten */
+#else
+    float s = amax > 0.0f ? amax / 2688.0f : 1.0f;
+#endif
+    volatile float d = 6.0f * s;
+    for (int64_t b = 0; b < n / 16; ++b) {
+        float ab = 0.0f;
+        for (int i = 0; i < 16; ++i) {
+            float a = fabsf(v[b * 16 + i]);
+            if (a > ab) ab = a;
+        }
+        volatile float q = ab / d;
+        uint8_t sf = oracle_e4m3_encode((double)q);
+        block_scales[b] = sf;
+        double sfv = oracle_e4m3_to_double(sf);
+        volatile float eff = (float)sfv * s;
+        for (int i = 0; i < 16; ++i) {
+            if (sfv == 0.0) {
+                codes[b * 16 + i] = 0;
+            } else {
+                volatile float qq = v[b * 16 + i] / eff;
+                codes[b * 16 + i] = oracle_e2m1_encode((double)qq);
+            }
+        }
+    }
+    *scale = s;
+}
+
+/* Dequantized NVFP4 element: E2M1 code times its block's E4M3 scale (the
+ * tensor scale is applied by the caller). */
+static double nvfp4_elem(const uint8_t* codes, const uint8_t* sf, int64_t i) {
+#if ORACLE_MUTANT == 18
+    return oracle_e2m1_to_double(codes[i]) * oracle_e4m3_to_double(sf[i / 32]);   /* planted: 32-wide blocks */
+#else
+    return oracle_e2m1_to_double(codes[i]) * oracle_e4m3_to_double(sf[i / 16]);
+#endif
+}
+
+/* One expert on one token with NVFP4 weights: w13 codes [2I][H] with block
+ * scales w13sf [2I][H/16] and tensor scale s13, w2 codes [H][I] with w2sf
+ * [H][I/16] and s2.  The token's row arrives quantized (xq, xsf, sx).  g and u
+ * are fp64 sums of dequantized products times sx * s13; a = SiLU(g) * u
+ * (bf16 in mirrored mode) is quantized per row; y = fp64 sum times sa * s2
+ * (bf16 in mirrored mode). */
+static void expert_ffn_nvfp4(const uint8_t* xq, const uint8_t* xsf, float sx, int64_t H, int64_t I,
+                             const uint8_t* w13, const uint8_t* w13sf, float s13, const uint8_t* w2,
+                             const uint8_t* w2sf, float s2, int mirrored, float* a_tmp, uint8_t* aq, uint8_t* asf,
+                             double* y) {
+    for (int64_t i = 0; i < I; ++i) {
+        const uint8_t* wg = w13 + i * H;
+        const uint8_t* wu = w13 + (I + i) * H;
+        const uint8_t* sg = w13sf + i * (H / 16);
+        const uint8_t* su = w13sf + (I + i) * (H / 16);
+        double g = 0.0, u = 0.0;
+        for (int64_t h = 0; h < H; ++h) {
+            double xv = nvfp4_elem(xq, xsf, h);
+            g += xv * nvfp4_elem(wg, sg, h);
+            u += xv * nvfp4_elem(wu, su, h);
+        }
+        g *= (double)sx * (double)s13;
+        u *= (double)sx * (double)s13;
+        double a = g / (1.0 + exp(-g)) * u;
+        a_tmp[i] = (float)(mirrored ? rb(a) : a);
+    }
+    float sa;
+    oracle_quantize_row_nvfp4(a_tmp, I, aq, asf, &sa);
+    for (int64_t h = 0; h < H; ++h) {
+        const uint8_t* wd = w2 + h * I;
+        const uint8_t* sd = w2sf + h * (I / 16);
+        double s = 0.0;
+        for (int64_t i = 0; i < I; ++i) s += nvfp4_elem(aq, asf, i) * nvfp4_elem(wd, sd, i);
+#if ORACLE_MUTANT == 19
+        s *= (double)sa;                           /* planted: down-projection tensor scale dropped */
+#else
+        s *= (double)sa * (double)s2;
+#endif
+        y[h] = mirrored ? rb(s) : s;
+    }
+}
+
+/* The NVFP4 layer for n_sel tokens: as oracle_moe_tokens, with NVFP4 expert
+ * weights (codes, block scales and tensor scales per expert; shared_* for the
+ * shared expert, whose w13 may be NULL).  H and I are multiples of 16.  In
+ * strict mode (mirrored == 0) a is quantized from its fp64 value rounded once
+ * to binary32. */
+void oracle_moe_tokens_nvfp4(const uint16_t* x, int64_t H, int64_t I, int64_t k, const int64_t* tok,
+                             int64_t n_sel, const int32_t* ids, const double* w, const uint8_t* const* w13,
+                             const uint8_t* const* w13sf, const float* s13, const uint8_t* const* w2,
+                             const uint8_t* const* w2sf, const float* s2, const uint8_t* shared_w13,
+                             const uint8_t* shared_w13sf, float shared_s13, const uint8_t* shared_w2,
+                             const uint8_t* shared_w2sf, float shared_s2, int mirrored, double* out) {
+#pragma omp parallel
+    {
+        float* xr = (float*)malloc((size_t)H * sizeof(float));
+        uint8_t* xq = (uint8_t*)malloc((size_t)H);
+        uint8_t* xsf = (uint8_t*)malloc((size_t)H / 16 + 1);
+        float* a = (float*)malloc((size_t)I * sizeof(float));
+        uint8_t* aq = (uint8_t*)malloc((size_t)I);
+        uint8_t* asf = (uint8_t*)malloc((size_t)I / 16 + 1);
+        double* y = (double*)malloc((size_t)H * sizeof(double));
+        double* acc = (double*)malloc((size_t)H * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t s = 0; s < n_sel; ++s) {
+            int64_t t = tok[s];
+            for (int64_t h = 0; h < H; ++h) xr[h] = (float)oracle_bf16_to_double(x[t * H + h]);
+            float sx;
+            oracle_quantize_row_nvfp4(xr, H, xq, xsf, &sx);
+            for (int64_t h = 0; h < H; ++h) acc[h] = 0.0;
+            for (int64_t j = 0; j < k; ++j) {
+                int32_t e = ids[t * k + j];
+                expert_ffn_nvfp4(xq, xsf, sx, H, I, w13[e], w13sf[e], s13[e], w2[e], w2sf[e], s2[e], mirrored, a,
+                                 aq, asf, y);
+                for (int64_t h = 0; h < H; ++h) acc[h] += w[t * k + j] * y[h];
+            }
+            if (shared_w13) {
+                expert_ffn_nvfp4(xq, xsf, sx, H, I, shared_w13, shared_w13sf, shared_s13, shared_w2, shared_w2sf,
+                                 shared_s2, mirrored, a, aq, asf, y);
+                for (int64_t h = 0; h < H; ++h) acc[h] += y[h];
+            }
+            for (int64_t h = 0; h < H; ++h) out[s * H + h] = mirrored ? rb(acc[h]) : acc[h];
+        }
+        free(xr);
+        free(xq);
+        free(xsf);
+        free(a);
+        free(aq);
+        free(asf);
+        free(y);
+        free(acc);
+    }
+}

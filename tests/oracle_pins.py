@@ -467,3 +467,150 @@ def pin_fp8_dense(o):
 
 
 ALL_PINS += [pin_e4m3, pin_quantize_rows, pin_fp8_dense]
+
+
+# ---------------------------------------------------------------- NVFP4 --
+# E2M1 magnitudes of codes 0..7 by the format's definition (exponent field 0:
+# 0.5 * m; otherwise 2^(e-1) * (1 + m/2)); bit 3 is the sign.
+E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _e2m1_nearest(v: float) -> int:
+    """Brute force over the 8 magnitudes: nearest, ties to the even code
+    (mantissa bit 0), saturating at 6, sign kept."""
+    a = abs(v)
+    sign = 8 if math.copysign(1.0, v) < 0 else 0
+    if a >= 6.0:
+        return sign | 7
+    return sign | min(range(8), key=lambda c: (abs(a - E2M1_MAGNITUDES[c]), c & 1))
+
+
+def _nvfp4_decode(codes, sf):
+    """Dequantized values (without the row scale) of one-code-per-byte E2M1
+    codes and their E4M3 block scales, blocks of 16 along the last axis."""
+    codes = np.asarray(codes)
+    mag = np.array(E2M1_MAGNITUDES)[codes & 7] * np.where(codes & 8, -1.0, 1.0)
+    scale = np.repeat(_e4m3_decode_torch(np.asarray(sf)), 16, axis=-1)
+    return mag * scale
+
+
+def pin_e2m1(o):
+    for c in range(16):
+        want = E2M1_MAGNITUDES[c & 7] * (-1.0 if c & 8 else 1.0)
+        got = o.e2m1_decode(c)
+        assert got == want and math.copysign(1.0, got) == (-1.0 if c & 8 else 1.0), f"E2M1 decode of {c}"
+    grid = np.concatenate([np.arange(-8.0, 8.0, 1.0 / 64), [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -5.0, 6.5, 1e9]])
+    for v in grid:
+        assert o.e2m1_encode(float(v)) == _e2m1_nearest(float(v)), f"E2M1 encoding of {v}"
+
+
+def pin_quantize_rows_nvfp4(o):
+    rng = np.random.default_rng(16)
+    # 1) rows of exactly representable values come back with their own codes:
+    #    block b holds E2M1 magnitudes times 2^e_b with one element at 6 * 2^e_b
+    for n, spread in ((16, 0), (64, 3), (2048, 6)):
+        nb = n // 16
+        e = rng.integers(-spread, 1, size=nb) if spread else np.zeros(nb, dtype=int)
+        codes = rng.integers(0, 16, size=n).astype(np.uint8)
+        codes[np.arange(nb) * 16 + rng.integers(0, 16, size=nb)] = 7
+        vals = (np.array(E2M1_MAGNITUDES)[codes & 7] * np.where(codes & 8, -1.0, 1.0)
+                * np.repeat(2.0 ** e, 16) * 3.0).astype(np.float32)
+        got, sf, s = o.quantize_row_nvfp4(vals)
+        same = (got & 7) == (codes & 7)
+        nz = (codes & 7) != 0
+        assert same.all() and ((got[nz] & 8) == (codes[nz] & 8)).all(), "representable row did not round-trip"
+        assert np.allclose(_nvfp4_decode(got, sf) * s, vals, rtol=1e-6, atol=0)
+        assert (sf[e == 0] == 0x7E).all(), "blocks holding the row maximum take scale 448"
+    # 2) scaling a row by 2^j changes only the row scale
+    for n in (32, 512):
+        row = (rng.standard_normal(n) * 3.0).astype(np.float32)
+        c0, sf0, s0 = o.quantize_row_nvfp4(row)
+        for j in (-7, 5):
+            c1, sf1, s1 = o.quantize_row_nvfp4(row * np.float32(2.0 ** j))
+            assert np.array_equal(c0, c1) and np.array_equal(sf0, sf1) and s1 == s0 * 2.0 ** j
+    # 3) error bound: each value is within one E4M3-scaled step of its code
+    for n in (16, 256, 2048):
+        row = (rng.standard_normal(n) * rng.uniform(0.01, 50)).astype(np.float32)
+        row[rng.integers(0, n, size=n // 32)] *= 20            # outliers
+        c, sf, s = o.quantize_row_nvfp4(row)
+        deq = _nvfp4_decode(c, sf) * s
+        eff = np.repeat(_e4m3_decode_torch(sf), 16) * s
+        assert np.all(np.abs(deq - row) <= eff * 1.0 + 1e-30), "error above the coarsest half step"
+        i = int(np.argmax(np.abs(row)))
+        assert c[i] & 7 == 7 and sf[i // 16] == 0x7E, "the row maximum must map to +-6 with scale 448"
+        bmax = np.abs(row).reshape(-1, 16).max(axis=1)
+        assert np.all(np.abs(_e4m3_decode_torch(sf) * 6 * s - bmax) <= bmax * 2.0 ** -3), "block scale off"
+    # 4) zero row, zero block
+    c, sf, s = o.quantize_row_nvfp4(np.zeros(32, np.float32))
+    assert s == 1.0 and not c.any() and not sf.any()
+    row = rng.standard_normal(48).astype(np.float32)
+    row[16:32] = 0
+    c, sf, s = o.quantize_row_nvfp4(row)
+    assert sf[1] == 0 and not c[16:32].any()
+
+
+def _nvfp4_layer(rng, T, H, I, E, S):
+    x = _rand_bits(rng, (T, H), 1.0)
+    wr = _rand_bits(rng, (E, H), 0.3)
+    code = lambda shape: rng.integers(0, 16, size=shape).astype(np.uint8)
+    sfc = lambda shape: rng.integers(0x30, 0x48, size=shape).astype(np.uint8)   # E4M3 0.5 .. 4.0
+    mk = lambda: (code((2 * I, H)), sfc((2 * I, H // 16)), np.float32(rng.uniform(0.01, 0.02)),
+                  code((H, I)), sfc((H, I // 16)), np.float32(rng.uniform(0.01, 0.02)))
+    experts = [mk() for _ in range(E)]
+    return x, wr, experts, (mk() if S else None)
+
+
+def _dense_nvfp4(o, x, ids, w, experts, shared):
+    """Dense brute force of the NVFP4 layer: every expert on every token,
+    weights dequantized with numpy, fp64 matmuls; activation rows quantized
+    with the oracle's row quantizer (pinned above), a rounded once to binary32
+    (strict mode)."""
+    X32 = _decode(x).astype(np.float32)
+    T, H = X32.shape
+    E = len(experts)
+
+    def quant_rows(A32):
+        out = np.zeros(A32.shape)
+        for t in range(A32.shape[0]):
+            c, sf, s = o.quantize_row_nvfp4(A32[t])
+            out[t] = _nvfp4_decode(c, sf) * s
+        return out
+
+    XQ = quant_rows(X32)
+    G = np.zeros((T, E))
+    for t in range(T):
+        for j in range(ids.shape[1]):
+            G[t, ids[t, j]] += w[t, j]
+
+    def ffn(c13, sf13, s13, c2, sf2, s2):
+        W13 = _nvfp4_decode(c13, sf13) * np.float64(s13)
+        W2 = _nvfp4_decode(c2, sf2) * np.float64(s2)
+        I = W13.shape[0] // 2
+        A = (_silu(XQ @ W13[:I].T) * (XQ @ W13[I:].T)).astype(np.float32)
+        return quant_rows(A) @ W2.T
+
+    out = np.zeros((T, H))
+    for e in range(E):
+        out += G[:, e:e + 1] * ffn(*experts[e])
+    if shared is not None:
+        out += ffn(*shared)
+    return out
+
+
+def pin_nvfp4_dense(o):
+    rng = np.random.default_rng(17)
+    for (T, H, I, E, k, S) in [(10, 64, 32, 5, 2, 1), (6, 32, 48, 3, 3, 0)]:
+        x, wr, experts, shared = _nvfp4_layer(rng, T, H, I, E, S)
+        r = o.route(x, wr, None, k)
+        args = ([e[0] for e in experts], [e[1] for e in experts], [e[2] for e in experts],
+                [e[3] for e in experts], [e[4] for e in experts], [e[5] for e in experts])
+        got = o.moe_tokens_nvfp4(x, np.arange(T), r["ids"], r["w"], *args, shared=shared, mirrored=False)
+        ref = _dense_nvfp4(o, x, r["ids"], r["w"], experts, shared)
+        scale = np.sqrt((ref ** 2).mean())
+        assert np.max(np.abs(got - ref)) <= 1e-9 * max(1.0, scale), "NVFP4 layer != dense brute force"
+        m = o.moe_tokens_nvfp4(x, np.arange(T), r["ids"], r["w"], *args, shared=shared, mirrored=True)
+        assert np.array_equal(_decode(_bits_from_f32(m.astype(np.float32))), m)
+        assert np.sqrt(((m - got) ** 2).mean()) <= 0.1 * scale
+
+
+ALL_PINS += [pin_e2m1, pin_quantize_rows_nvfp4, pin_nvfp4_dense]

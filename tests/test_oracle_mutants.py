@@ -23,6 +23,10 @@ MUTANTS = {
     13: "E4M3 encoding truncates",
     14: "activation full-scale value 440 instead of 448",
     15: "FP8 activation scale dropped from the gate/up sums",
+    16: "E2M1 rounding ties away from zero",
+    17: "NVFP4 row scale without the block range 6",
+    18: "NVFP4 block scales indexed as 32-wide blocks",
+    19: "NVFP4 down-projection tensor scale dropped",
 }
 
 
