@@ -86,8 +86,9 @@ def parse(argv=None):
     p.add_argument("--workload", default="r1_moe_layer_8k", choices=sorted(WORKLOADS))
     p.add_argument("--chunk-mb", type=float, default=32.0)
     p.add_argument("--copy-streams", type=int, default=1)
-    p.add_argument("--dtype", default="bf16", choices=["bf16", "fp8"],
-                   help="expert weight type (fp8: E4M3 weights and activations, a next-row variant)")
+    p.add_argument("--dtype", default="bf16", choices=["bf16", "fp8", "nvfp4"],
+                   help="expert weight type (fp8: E4M3 weights and activations; nvfp4: E2M1 codes with E4M3 "
+                        "scales per 16-element block; next-row variants)")
     p.add_argument("--chunk-sweep", default="", help="comma-separated chunk sizes in MB (exposed copy per size)")
     p.add_argument("--merge-copy", action="store_true",
                    help="also time the merge-copy baseline (one contiguous weight buffer per layer)")
@@ -111,7 +112,7 @@ def g1_bytes(T, H, I, E_active, k, S, wb=2):
     """Gate/up grouped GEMM, algorithmic HBM bytes: every active expert's
     w13 once (2I*H elements of wb bytes), the gathered rows and x once (same
     element size), a written once (bf16)."""
-    return (E_active + S) * 2 * I * H * wb + T * (k + S) * H * wb + T * (k + S) * I * 2
+    return int((E_active + S) * 2 * I * H * wb + T * (k + S) * H * wb + T * (k + S) * I * 2)
 
 
 def step_bytes(T, H, I, E_active, k, S, R, wb=2):
@@ -123,9 +124,14 @@ def step_bytes(T, H, I, E_active, k, S, R, wb=2):
     a's quantization passes (codes written and read once)."""
     b = ((E_active + S) * 3 * H * I * wb + 2 * T * k * H * wb + 2 * T * (k + S) * I * 2
          + 2 * T * (k + S) * H * 2 + 2 * T * H * 2 + 2 * R * 3 * H * I * wb)
-    if wb == 1:
-        b += 2 * T * H + 2 * T * (k + S) * I
-    return b
+    if wb < 2:   # quantized: x's codes (shared expert) and a's codes, each written and read once
+        b += 2 * T * H * wb + 2 * T * (k + S) * I * wb
+    return int(b)
+
+
+# Bytes per weight (and quantized activation) element: NVFP4 is half a byte
+# of E2M1 code plus one E4M3 scale per 16 elements.
+WEIGHT_BYTES = {"bf16": 2, "fp8": 1, "nvfp4": 9 / 16}
 
 
 def measured_traffic(kernel_file: str):
@@ -233,7 +239,7 @@ class Workload:
     """n_layers R1-shaped layers with their pools, a Runtime, route buffers
     and per-layer token batches, all resident in HBM."""
 
-    def __init__(self, spec: Spec, chunk_bytes, n_copy_streams, n_layers=2, base_seed=0, fp8=False):
+    def __init__(self, spec: Spec, chunk_bytes, n_copy_streams, n_layers=2, base_seed=0, wdtype="bf16"):
         import torch
 
         from moe_expert_grouped_split_gb300 import binding as B
@@ -241,15 +247,15 @@ class Workload:
 
         self.B, self.I, self.torch = B, I, torch
         self.spec = spec
-        self.fp8 = fp8
+        self.wdtype = wdtype
         self.shape, self.placement = spec.shape, spec.placement
         sh = self.shape
         self.n_layers = n_layers
-        make = I.make_layer_fp8 if fp8 else I.make_layer
+        make = {"bf16": I.make_layer, "fp8": I.make_layer_fp8, "nvfp4": I.make_layer_nvfp4}[wdtype]
         self.layers = [make(sh, self.placement, base_seed, l, device="cuda", router_std=spec.router_std,
                             bias=spec.bias) for l in range(n_layers)]
         self.rt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, n_layers, self.placement.n_remote(),
-                            weight_dtype=B.DTYPE_E4M3 if fp8 else B.DTYPE_BF16)
+                            weight_dtype={"bf16": B.DTYPE_BF16, "fp8": B.DTYPE_E4M3, "nvfp4": B.DTYPE_NVFP4}[wdtype])
         for l, lw in enumerate(self.layers):
             self.rt.set_layer(l, lw)
         self.x = [I.make_tokens(sh.T, sh.H, base_seed, step=s, device="cuda") for s in range(n_layers)]
@@ -427,7 +433,7 @@ def run_layer_bench(args, world, local_rank, barrier):
     import torch
     torch.cuda.set_device(local_rank)
     spec = WORKLOADS[args.workload]()
-    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, fp8=args.dtype == "fp8")
+    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, wdtype=args.dtype)
     sh = wl.shape
     K, W = args.steps, args.warmup
     phases = [_events(torch, 7) for _ in range(K)]
@@ -518,8 +524,10 @@ def run_merge_baseline(wl, K, W):
         with torch.cuda.stream(wl.compute):
             wl.compute.wait_event(arrived[s])
             # the merge: resident experts into slots R.. of the stage's buffer
-            mrt.stage_w13[s][R:R + n_local].copy_(lw.local_w13[:n_local], non_blocking=True)
-            mrt.stage_w2[s][R:R + n_local].copy_(lw.local_w2[:n_local], non_blocking=True)
+            mrt.stage_w13[s][R:R + n_local].copy_(lw.local_w13[:n_local].view(torch.uint8).reshape(n_local, -1),
+                                                  non_blocking=True)
+            mrt.stage_w2[s][R:R + n_local].copy_(lw.local_w2[:n_local].view(torch.uint8).reshape(n_local, -1),
+                                                 non_blocking=True)
             mrt.route(x, lw.wr, lw.bias, wl.rb, wl.compute)
             mrt.moe(2 + 2 * l + s, s, x, wl.rb, wl.out, wl.compute)
             freed[s].record(wl.compute)
@@ -576,7 +584,7 @@ def run_pipeline_bench(args, world, local_rank, barrier):
 
     torch.cuda.set_device(local_rank)
     spec = WORKLOADS[args.workload]()
-    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, n_layers=4, fp8=args.dtype == "fp8")
+    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, n_layers=4, wdtype=args.dtype)
     sh = wl.shape
     steps = args.steps
     Ts = I.step_token_counts(steps + args.warmup, 6554, 8192, 0)
@@ -676,15 +684,20 @@ def cpu_baseline_sample(wl, target_s=15.0, max_tokens=512):
                 w13, w2 = lw.local_w13[pl.local_slot[e]], lw.local_w2[pl.local_slot[e]]
             else:
                 w13, w2 = lw.peer_w13[pl.peer_id[e]][pl.peer_slot[e]], lw.peer_w2[pl.peer_id[e]][pl.peer_slot[e]]
-            cache[e] = (conv(w13), conv(w2))
+            cache[e] = (conv13(w13), conv2(w2))
         w13s = [cache.get(e, (None, None))[0] for e in range(sh.E)]
         w2s = [cache.get(e, (None, None))[1] for e in range(sh.E)]
         return w13s, w2s
 
-    fp8 = getattr(wl, "fp8", False)
+    wdtype = getattr(wl, "wdtype", "bf16")
+    fp8, nvfp4 = wdtype == "fp8", wdtype == "nvfp4"
     conv = (lambda t: t.detach().contiguous().cpu().numpy().view(np.uint8)) if fp8 else I.bf16_bits
-    sw13 = conv(lw.shared_w13) if lw.shared_w13 is not None else None
-    sw2 = conv(lw.shared_w2) if lw.shared_w2 is not None else None
+    conv13 = conv2 = conv
+    if nvfp4:   # slots to math layout: (codes, block scales) of w13 / of w2
+        conv13 = lambda t: I.unpack_nvfp4(t.detach().cpu(), 2 * sh.I, sh.H)
+        conv2 = lambda t: I.unpack_nvfp4(t.detach().cpu(), sh.H, sh.I)
+    sw13 = conv13(lw.shared_w13) if lw.shared_w13 is not None else None
+    sw2 = conv2(lw.shared_w2) if lw.shared_w2 is not None else None
 
     def run(tokens):
         xs = np.ascontiguousarray(x[tokens])
@@ -692,7 +705,13 @@ def cpu_baseline_sample(wl, target_s=15.0, max_tokens=512):
         w13s, w2s = weights_for(r_pre["ids"])          # host copies of those experts (untimed)
         t0 = time.perf_counter()
         r = o.route(xs, wr, bias, sh.k)
-        if fp8:
+        if nvfp4:
+            sh_t = None if sw13 is None else (sw13[0], sw13[1], lw.shared_s13, sw2[0], sw2[1], lw.shared_s2)
+            o.moe_tokens_nvfp4(xs, np.arange(len(tokens)), r["ids"], r["w"],
+                               [None if a is None else a[0] for a in w13s], [None if a is None else a[1] for a in w13s],
+                               lw.w13_scale, [None if a is None else a[0] for a in w2s],
+                               [None if a is None else a[1] for a in w2s], lw.w2_scale, shared=sh_t, mirrored=True)
+        elif fp8:
             o.moe_tokens_fp8(xs, np.arange(len(tokens)), r["ids"], r["w"], w13s, w2s, lw.w13_scale, lw.w2_scale,
                              sw13, sw2, lw.shared_s13, lw.shared_s2, mirrored=True)
         else:
@@ -741,17 +760,19 @@ def main():
     sh = wl.shape
     peaks, src = measured_peaks()
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    fp8 = args.dtype == "fp8"
-    wb = 1 if fp8 else 2
+    wb = WEIGHT_BYTES[args.dtype]
     peak_note = f"{src} bf16_tflops_sustained (kernel timed inside a long step)"
-    if fp8:   # measured bf16 peak x the nominal dense fp8 / bf16 ratio (4.5 / 2.25)
+    if args.dtype == "fp8":   # measured bf16 peak x the nominal dense fp8 / bf16 ratio (4.5 / 2.25)
         peak = peak * 2.0
         peak_note = f"{src} bf16_tflops_sustained x 2 (nominal dense E4M3 / bf16 ratio), kernel inside a long step"
+    if args.dtype == "nvfp4":   # x the nominal dense fp4 / bf16 ratio (13.5 / 2.25)
+        peak = peak * 6.0
+        peak_note = f"{src} bf16_tflops_sustained x 6 (nominal dense FP4 / bf16 ratio), kernel inside a long step"
     hbm = peaks["hbm_gbs"]
     line = {
         "metric": METRIC, "value": round(res["value"], 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_step"], 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "nvfp4"}[args.dtype],
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights; R1 MoE layer shapes)",
         "config": {"workload": args.workload, "T": sh.T, "H": sh.H, "I": sh.I, "E": sh.E, "k": sh.k,
                    "shared": sh.S, "local_experts": int((wl.placement.local_slot >= 0).sum()),
@@ -778,7 +799,7 @@ def main():
         sb = step_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S, wl.placement.n_remote(), wb)
         layer_tflops = flops_layer / (res["ms_step"] / 1e3) / 1e12
         traffic = None
-        if args.workload == "r1_moe_layer_8k" and not fp8:
+        if args.workload == "r1_moe_layer_8k" and args.dtype == "bf16":
             traffic = measured_traffic(os.path.join(ROOT, "moe_expert_grouped_split_gb300", "csrc", "gemm.cu"))
         g1_s = res["phase_ms"]["gate_up_gemm"] / 1e3
         if g1 / g1b >= peak * 1e12 / (hbm * 1e9):     # arithmetic intensity at or above the ridge

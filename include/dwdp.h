@@ -38,8 +38,9 @@
  *   w2  of one expert : [H][I]   = W_down^T
  *   a pool            : w13 [n_slots][2I][H] and w2 [n_slots][H][I]
  *   router weight     : [E][H]   row e = column e of the H x E gate matrix
- * Expert weights are bf16, or 1-byte E4M3 codes in an E4M3 context; the
- * router weight and the activations passed in and out are always bf16.
+ * Expert weights are bf16, 1-byte E4M3 codes in an E4M3 context, or NVFP4
+ * slots (see DWDP_DTYPE_NVFP4) in an NVFP4 context; the router weight and
+ * the activations passed in and out are always bf16.
  */
 #ifndef DWDP_H_
 #define DWDP_H_
@@ -51,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DWDP_ABI_VERSION 2
+#define DWDP_ABI_VERSION 3
 #define DWDP_MAX_EXPERTS 1024
 #define DWDP_MAX_TOPK 32
 #define DWDP_MAX_LAYERS 256
@@ -72,15 +73,15 @@ typedef enum {
 } dwdp_status;
 
 typedef struct {
-    int32_t hidden;       /* H: multiple of 64 */
-    int32_t inter;        /* I: expert intermediate size, multiple of 64 */
+    int32_t hidden;       /* H: multiple of 64 (NVFP4: of 256) */
+    int32_t inter;        /* I: expert intermediate size, multiple of 64 (NVFP4: of 256) */
     int32_t n_experts;    /* E: routed experts, 1..DWDP_MAX_EXPERTS */
     int32_t top_k;        /* k: 1..min(E, DWDP_MAX_TOPK) */
     int32_t n_shared;     /* always-on shared experts: 0 or 1 */
     int32_t max_tokens;   /* largest T any call will pass */
     int32_t n_layers;     /* layers that get an expert map: 1..DWDP_MAX_LAYERS */
     int32_t stage_slots;  /* experts each staging buffer holds (0 = no staging) */
-    int32_t weight_dtype; /* DWDP_DTYPE_BF16, or DWDP_DTYPE_E4M3 (see below) */
+    int32_t weight_dtype; /* DWDP_DTYPE_BF16, DWDP_DTYPE_E4M3 or DWDP_DTYPE_NVFP4 */
 } dwdp_config;
 
 /* Expert weight types.  DWDP_DTYPE_E4M3 (an FP8 variant of the layer; the
@@ -92,8 +93,26 @@ typedef struct {
  * cores.  Routing stays bf16. */
 #define DWDP_DTYPE_BF16 0
 #define DWDP_DTYPE_E4M3 1
+/* DWDP_DTYPE_NVFP4 (the format the pages run DeepSeek-R1's MoE weights in,
+ * DWDP §5.1): a weight is an E2M1 code (4 bits) times an E4M3 scale shared by
+ * 16 consecutive elements along K, times one binary32 scale per expert tensor
+ * (dwdp_set_expert_scales).  One pool slot of a [rows][K] tensor (w13: rows =
+ * 2I, K = H; w2: rows = H, K = I) is rows * K * 9 / 16 bytes:
+ *   - codes [rows][K / 2] bytes, element 2i of a row in the low nibble of
+ *     byte i, 2i + 1 in the high nibble;
+ *   - then the block scales in 512-byte chunks, one per (row block rb of 128
+ *     rows, K step ks of 64 elements), chunk (rb, ks) at (rb * K / 64 + ks) *
+ *     512; in it the scale of row 128 rb + 32 m1 + m0 and 16-element block kb
+ *     of the step is byte 16 m0 + 4 m1 + kb.
+ * The layer quantizes its activations per row to NVFP4 before each expert
+ * GEMM (row scale = row amax / 2688 in binary32; block scale = E4M3 of block
+ * amax / (6 * row scale); code = E2M1 of v / (block scale * row scale), round
+ * to nearest even, saturating) and the GEMMs run on the block-scaled FP4
+ * tensor cores.  H and I must be multiples of 256. */
+#define DWDP_DTYPE_NVFP4 2
 
-/* One buffer of experts: w13 [n_slots][2I][H], w2 [n_slots][H][I] (device). */
+/* One buffer of experts: w13 [n_slots][2I][H], w2 [n_slots][H][I] (device;
+ * NVFP4: n_slots slots of the sizes given at DWDP_DTYPE_NVFP4). */
 typedef struct {
     const void* w13;
     const void* w2;
@@ -170,12 +189,13 @@ int32_t dwdp_set_expert_map(dwdp_ctx* ctx, int32_t layer, const dwdp_pool* local
                             const int32_t* peer_id, const int32_t* peer_slot,
                             const void* shared_w13, const void* shared_w2);
 
-/* Per-expert-tensor weight scales of layer `layer` for DWDP_DTYPE_E4M3
- * contexts: expert e's gate/up weights are w13 codes * w13_scale[e], its down
- * weights w2 codes * w2_scale[e] (host arrays [E]); shared_* for the shared
- * expert (ignored when n_shared == 0).  Required before dwdp_moe_layer on an
- * E4M3 context; kept until replaced.  Errors: INVALID_ARG (bf16 context, bad
- * layer, non-finite or non-positive scale). */
+/* Per-expert-tensor weight scales of layer `layer` for DWDP_DTYPE_E4M3 and
+ * DWDP_DTYPE_NVFP4 contexts: expert e's gate/up weights are the w13 codes'
+ * values * w13_scale[e], its down weights the w2 codes' values * w2_scale[e]
+ * (host arrays [E]; NVFP4: on top of the block scales); shared_* for the
+ * shared expert (ignored when n_shared == 0).  Required before
+ * dwdp_moe_layer on such a context; kept until replaced.  Errors:
+ * INVALID_ARG (bf16 context, bad layer, non-finite or non-positive scale). */
 int32_t dwdp_set_expert_scales(dwdp_ctx* ctx, int32_t layer, const float* w13_scale, const float* w2_scale,
                                float shared_w13_scale, float shared_w2_scale);
 
@@ -219,6 +239,20 @@ int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t 
 int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* x, int32_t T,
                        const dwdp_route_out* route, void* out, void* ws, size_t ws_bytes,
                        dwdp_stream_t stream);
+
+/* Activation quantization on its own, the same kernels and decisions as
+ * dwdp_moe_layer applies to x and to a: x [rows][K] bf16 (device) to
+ *   DWDP_DTYPE_E4M3: codes [rows][K] E4M3 bytes, row_scale [rows] fp32
+ *     (amax / 448; block_scales unused);
+ *   DWDP_DTYPE_NVFP4: codes [rows][K / 2] (two E2M1 codes per byte, element
+ *     2i in the low nibble), row_scale [rows] fp32 (amax / 2688) and
+ *     block_scales in the 512-byte chunk layout of DWDP_DTYPE_NVFP4 for a
+ *     tensor of ceil(rows / 128) * 128 rows (bytes of rows past `rows` are
+ *     not written).
+ * K a multiple of 64; rows < 2^31.  All pointers device, 16-byte aligned.
+ * Enqueued on `stream`; needs no context.  Errors: INVALID_ARG, CUDA. */
+int32_t dwdp_quantize_rows(int32_t weight_dtype, const void* x, int64_t rows, int32_t K, void* codes,
+                           void* block_scales, float* row_scale, dwdp_stream_t stream);
 
 /* Host-side bounded wait for stage `stage`'s last prefetch: returns OK when
  * it has finished, TIMEOUT after timeout_ms (>= 0), CUDA on a fault. */
@@ -294,10 +328,10 @@ int32_t dwdp_route_static(const void* x, int32_t T, int32_t hidden, int32_t n_ex
  * source and destination, cut into slices of chunk_bytes (the last one
  * short); slices are emitted round-robin over peers 0..n_peers-1.  Writes up
  * to max_out slices to out (may be NULL when max_out == 0) and the full count
- * to *n_out.  elem_bytes is the size of one weight element (2 for bf16, 1
- * for E4M3).  Errors: INVALID_ARG (bad map or a non-resident expert with no
+ * to *n_out.  weight_dtype (DWDP_DTYPE_*) sets the bytes of one expert
+ * tensor.  Errors: INVALID_ARG (bad map or a non-resident expert with no
  * peer copy). */
-int32_t dwdp_plan_prefetch(int32_t n_experts, int32_t hidden, int32_t inter, int32_t elem_bytes,
+int32_t dwdp_plan_prefetch(int32_t n_experts, int32_t hidden, int32_t inter, int32_t weight_dtype,
                            const int32_t* local_slot, const int32_t* peer_id,
                            const int32_t* peer_slot, int32_t n_peers, size_t chunk_bytes,
                            dwdp_copy_slice* out, int64_t max_out, int64_t* n_out);

@@ -18,7 +18,16 @@ DWDP_OK = 0
 STATUS = {0: "OK", -1: "INVALID_ARG", -2: "NOT_MAPPED", -3: "CUDA", -4: "TIMEOUT", -5: "UNSUPPORTED",
           -6: "DEVICE_CHECK"}
 EPI_BF16, EPI_SILU, EPI_F32 = 0, 1, 2
-DTYPE_BF16, DTYPE_E4M3 = 0, 1
+DTYPE_BF16, DTYPE_E4M3, DTYPE_NVFP4 = 0, 1, 2
+
+
+def weight_slot_bytes(rows: int, K: int, weight_dtype: int) -> int:
+    """Bytes of one [rows][K] expert tensor (one pool slot) in weight_dtype:
+    bf16 2 per element, E4M3 1, NVFP4 half a byte of E2M1 code plus 1/16
+    byte of E4M3 block scale (dwdp.h, DWDP_DTYPE_NVFP4)."""
+    if weight_dtype == DTYPE_NVFP4:
+        return rows * K // 2 + rows * K // 16
+    return rows * K * (1 if weight_dtype == DTYPE_E4M3 else 2)
 
 
 class DwdpError(RuntimeError):
@@ -75,6 +84,7 @@ SIGNATURES = [
     ("dwdp_grouped_gemm", _I32, [_VP, _I32, _VP, ctypes.c_int64, _I32, _I32, _VP, _I32, ctypes.POINTER(dwdp_pool),
                                  _I32, _I32P, _VP, _VP]),
     ("dwdp_route_static", _I32, [_VP, _I32, _I32, _I32, _I32, _VP, _VP, ctypes.POINTER(dwdp_route_out), _VP]),
+    ("dwdp_quantize_rows", _I32, [_I32, _VP, ctypes.c_int64, _I32, _VP, _VP, _VP, _VP]),
     ("dwdp_plan_prefetch", _I32, [_I32, _I32, _I32, _I32, _I32P, _I32P, _I32P, _I32, ctypes.c_size_t,
                                   ctypes.POINTER(dwdp_copy_slice), ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]),
 ]
@@ -233,6 +243,11 @@ def dwdp_route_static(x, T, hidden, n_experts, top_k, w_router, logit_bias, out:
                                          ctypes.byref(out), _stream(stream)))
 
 
+def dwdp_quantize_rows(weight_dtype, x, rows, K, codes, block_scales, row_scale, stream=None) -> None:
+    _check(None, lib().dwdp_quantize_rows(weight_dtype, _ptr(x), rows, K, _ptr(codes), _ptr(block_scales),
+                                          _ptr(row_scale), _stream(stream)))
+
+
 def dwdp_set_expert_scales(ctx, layer, w13_scale, w2_scale, shared_w13_scale=1.0, shared_w2_scale=1.0) -> None:
     s13 = np.ascontiguousarray(w13_scale, dtype=np.float32)
     s2 = np.ascontiguousarray(w2_scale, dtype=np.float32)
@@ -242,16 +257,16 @@ def dwdp_set_expert_scales(ctx, layer, w13_scale, w2_scale, shared_w13_scale=1.0
 
 
 def dwdp_plan_prefetch(n_experts, hidden, inter, local_slot, peer_id, peer_slot, n_peers, chunk_bytes,
-                       elem_bytes=2):
+                       weight_dtype=DTYPE_BF16):
     """The copy plan as a list of (peer, tensor, src_offset, dst_offset, nbytes)."""
     ls, lsp = _i32(local_slot)
     pi, pip = _i32(peer_id)
     ps, psp = _i32(peer_slot)
     n = ctypes.c_int64()
-    _check(None, lib().dwdp_plan_prefetch(n_experts, hidden, inter, elem_bytes, lsp, pip, psp, n_peers, chunk_bytes,
+    _check(None, lib().dwdp_plan_prefetch(n_experts, hidden, inter, weight_dtype, lsp, pip, psp, n_peers, chunk_bytes,
                                           None, 0, ctypes.byref(n)))
     arr = (dwdp_copy_slice * max(1, n.value))()
-    _check(None, lib().dwdp_plan_prefetch(n_experts, hidden, inter, elem_bytes, lsp, pip, psp, n_peers, chunk_bytes,
+    _check(None, lib().dwdp_plan_prefetch(n_experts, hidden, inter, weight_dtype, lsp, pip, psp, n_peers, chunk_bytes,
                                           arr, n.value, ctypes.byref(n)))
     return [(s.peer, s.tensor, s.src_offset, s.dst_offset, s.nbytes) for s in arr[: n.value]]
 
@@ -282,12 +297,14 @@ class Runtime:
     def __init__(self, hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots,
                  device="cuda", weight_dtype=DTYPE_BF16):
         import torch
-        bf = torch.uint8 if weight_dtype == DTYPE_E4M3 else torch.bfloat16
         self.cfg = dict(hidden=hidden, inter=inter, n_experts=n_experts, top_k=top_k, n_shared=n_shared,
                         max_tokens=max_tokens, n_layers=n_layers, stage_slots=stage_slots)
+        self.weight_dtype = weight_dtype
         if stage_slots > 0:
-            self.stage_w13 = [torch.empty((stage_slots, 2 * inter, hidden), dtype=bf, device=device) for _ in range(2)]
-            self.stage_w2 = [torch.empty((stage_slots, hidden, inter), dtype=bf, device=device) for _ in range(2)]
+            b13 = weight_slot_bytes(2 * inter, hidden, weight_dtype)
+            b2 = weight_slot_bytes(hidden, inter, weight_dtype)
+            self.stage_w13 = [torch.empty((stage_slots, b13), dtype=torch.uint8, device=device) for _ in range(2)]
+            self.stage_w2 = [torch.empty((stage_slots, b2), dtype=torch.uint8, device=device) for _ in range(2)]
         else:
             self.stage_w13 = [None, None]
             self.stage_w2 = [None, None]

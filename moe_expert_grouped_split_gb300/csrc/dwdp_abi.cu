@@ -75,27 +75,34 @@ namespace dwdp {
 
 // Rows x K matrix, row-major: a 2-D map with a [128 rows x 128 bytes] box,
 // 128-byte swizzle (the canonical K-major layout the MMA descriptors expect).
-bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, int elem_bytes) {
+// E4M3 and NVFP4 codes are mapped as bytes.
+bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, int fmt) {
     EncodeTiledFn fn = encode_fn();
     if (!fn || rows == 0) return false;
-    cuuint64_t dims[2] = {K, rows};
-    cuuint64_t strides[1] = {K * elem_bytes};
-    cuuint32_t box[2] = {(cuuint32_t)(BK_BYTES / elem_bytes), BM};
+    const bool bytes = fmt != FMT_BF16;
+    const uint64_t row_bytes = (uint64_t)operand_row_bytes((int64_t)K, fmt);
+    cuuint64_t dims[2] = {bytes ? row_bytes : K, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {(cuuint32_t)(bytes ? BK_BYTES : BK_BYTES / 2), BM};
     cuuint32_t es[2] = {1, 1};
-    return fn(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+    return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// A weight buffer [slots][rows][K]: a 3-D map, box [1 x 128 rows x 128 bytes].
-bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t rows, uint64_t K, int elem_bytes) {
+// A weight buffer [slots][rows][K]: a 3-D map, box [1 x 128 rows x 128 bytes];
+// slots are weight_slot_bytes apart (NVFP4: the codes of each slot, whose
+// block scales follow them).
+bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t rows, uint64_t K, int fmt) {
     EncodeTiledFn fn = encode_fn();
     if (!fn || rows == 0 || slots == 0) return false;
-    cuuint64_t dims[3] = {K, rows, slots};
-    cuuint64_t strides[2] = {K * elem_bytes, rows * K * elem_bytes};
-    cuuint32_t box[3] = {(cuuint32_t)(BK_BYTES / elem_bytes), BN / 2, 1};
+    const bool bytes = fmt != FMT_BF16;
+    const uint64_t row_bytes = (uint64_t)operand_row_bytes((int64_t)K, fmt);
+    cuuint64_t dims[3] = {bytes ? row_bytes : K, rows, slots};
+    cuuint64_t strides[2] = {row_bytes, (uint64_t)weight_slot_bytes((int64_t)rows, (int64_t)K, fmt)};
+    cuuint32_t box[3] = {(cuuint32_t)(bytes ? BK_BYTES : BK_BYTES / 2), BN / 2, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+    return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -108,7 +115,7 @@ struct dwdp_ctx {
     dwdp_config cfg{};
     int device = 0;
     int n_sms = 0;
-    int elem_bytes = 2;  // expert weight element size: 2 bf16, 1 E4M3
+    int fmt = FMT_BF16;  // expert weight format (weight_dtype)
     void* stage13[2] = {nullptr, nullptr};
     void* stage2[2] = {nullptr, nullptr};
     CUtensorMap stage_map13[2]{}, stage_map2[2]{};
@@ -152,16 +159,18 @@ struct WsLayout {
     size_t logits = 0;  // route: fp32 [T][E] when the caller does not keep logits
     size_t group = 0;   // route: scratch of the chunked grouping
     // moe offsets: gathered rows xp, activations a, expert outputs y; E4M3
-    // contexts also keep x's codes/scales (xq, sx), xp's scales (sxp) and
-    // a's codes/scales (aq, sa).
-    size_t xp = 0, a = 0, y = 0, xq = 0, sx = 0, sxp = 0, aq = 0, sa = 0;
+    // and NVFP4 contexts also keep x's codes/scales (xq, sx), xp's scales
+    // (sxp) and a's codes/scales (aq, sa); NVFP4 adds the block-scale chunks
+    // of the two GEMMs' A tiles (sfx, sfa).
+    size_t xp = 0, a = 0, y = 0, xq = 0, sx = 0, sxp = 0, aq = 0, sa = 0, sfx = 0, sfa = 0;
+    int64_t sf_tiles = 0;  // A tiles sfx / sfa have room for
     size_t route_bytes = 0, moe_bytes = 0;
 };
 
 WsLayout ws_layout(const dwdp_config& c, int64_t T) {
     WsLayout L;
     const int64_t H = c.hidden, I = c.inter, E = c.n_experts, k = c.top_k, S = c.n_shared;
-    const int64_t eb = (c.weight_dtype == DWDP_DTYPE_E4M3) ? 1 : 2;  // bytes of a GEMM operand element
+    const int fmt = c.weight_dtype;
     L.logits = 0;
     L.group = align_up((size_t)(T * E * 4), 256);
     L.route_bytes = L.group + align_up(group_chunked_scratch_bytes((int)(T * k), (int)E), 256);
@@ -171,15 +180,23 @@ WsLayout ws_layout(const dwdp_config& c, int64_t T) {
         o += align_up(bytes, 256);
         return at;
     };
-    L.xp = take((size_t)(T * k * H * eb));
+    L.xp = take((size_t)(T * k * operand_row_bytes(H, fmt)));
     L.a = take((size_t)(T * (k + S) * I * 2));
     L.y = take((size_t)(T * (k + S) * H * 2));
-    if (eb == 1) {
-        L.xq = take((size_t)(T * H));
+    if (fmt != FMT_BF16) {
+        L.xq = take((size_t)(T * operand_row_bytes(H, fmt)));
         L.sx = take((size_t)T * 4);
         L.sxp = take((size_t)(T * k) * 4);
-        L.aq = take((size_t)(T * (k + S) * I));
+        L.aq = take((size_t)(T * (k + S) * operand_row_bytes(I, fmt)));
         L.sa = take((size_t)(T * (k + S)) * 4);
+    }
+    if (fmt == FMT_NVFP4) {
+        // A tiles: sum over experts of ceil(rows / 128) <= (T k + 127 E) / 128,
+        // plus ceil(T / 128) shared tiles; a tile holds 128 x K / 16 = 8 K scales
+        const int64_t tiles = (T * k + 127 * E) / BM + (T + BM - 1) / BM;
+        L.sf_tiles = tiles;
+        L.sfx = take((size_t)(tiles * H * 8));
+        L.sfa = take((size_t)(tiles * I * 8));
     }
     L.moe_bytes = o;
     return L;
@@ -187,7 +204,7 @@ WsLayout ws_layout(const dwdp_config& c, int64_t T) {
 
 // The copy plan of [DWDP] §4.3.2 (see dwdp_plan_prefetch in dwdp.h for the
 // exact order).  Returns false on an invalid map.
-bool build_plan(int32_t E, int64_t H, int64_t I, int64_t elem, const int32_t* local_slot, const int32_t* peer_id,
+bool build_plan(int32_t E, int64_t H, int64_t I, int fmt, const int32_t* local_slot, const int32_t* peer_id,
                 const int32_t* peer_slot, int32_t n_peers, size_t chunk,
                 std::vector<dwdp_copy_slice>& plan, std::string& why) {
     plan.clear();
@@ -205,7 +222,7 @@ bool build_plan(int32_t E, int64_t H, int64_t I, int64_t elem, const int32_t* lo
             }
             sslot[e] = r++;
         }
-    const int64_t bytes[2] = {2 * I * H * elem, H * I * elem};
+    const int64_t bytes[2] = {weight_slot_bytes(2 * I, H, fmt), weight_slot_bytes(H, I, fmt)};
     std::vector<std::vector<dwdp_copy_slice>> per(n_peers > 0 ? n_peers : 0);
     for (int32_t p = 0; p < n_peers; ++p) {
         std::vector<dwdp_copy_slice> regions;
@@ -277,10 +294,13 @@ int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* cons
     const dwdp_config& c = *cfg;
     if (c.hidden <= 0 || c.inter <= 0 || c.n_experts <= 0 || c.top_k <= 0 || c.max_tokens < 0 ||
         c.n_layers <= 0 || c.stage_slots < 0 || c.n_shared < 0 ||
-        (c.weight_dtype != DWDP_DTYPE_BF16 && c.weight_dtype != DWDP_DTYPE_E4M3))
-        return fail(nullptr, DWDP_ERR_INVALID_ARG, "config has a non-positive size");
+        (c.weight_dtype != DWDP_DTYPE_BF16 && c.weight_dtype != DWDP_DTYPE_E4M3 &&
+         c.weight_dtype != DWDP_DTYPE_NVFP4))
+        return fail(nullptr, DWDP_ERR_INVALID_ARG, "config has a non-positive size or an unknown weight_dtype");
     if (c.hidden % 64 || c.inter % 64)
         return fail(nullptr, DWDP_ERR_UNSUPPORTED, "hidden and inter must be multiples of 64");
+    if (c.weight_dtype == DWDP_DTYPE_NVFP4 && (c.hidden % 256 || c.inter % 256))
+        return fail(nullptr, DWDP_ERR_UNSUPPORTED, "NVFP4: hidden and inter must be multiples of 256");
     if (c.n_experts > DWDP_MAX_EXPERTS || c.top_k > DWDP_MAX_TOPK || c.top_k > c.n_experts ||
         c.n_shared > 1 || c.n_layers > DWDP_MAX_LAYERS)
         return fail(nullptr, DWDP_ERR_UNSUPPORTED, "E <= %d, k <= min(E, %d), n_shared <= 1, layers <= %d",
@@ -295,7 +315,7 @@ int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* cons
     }
     std::unique_ptr<dwdp_ctx> ctx(new dwdp_ctx());
     ctx->cfg = c;
-    ctx->elem_bytes = (c.weight_dtype == DWDP_DTYPE_E4M3) ? 1 : 2;
+    ctx->fmt = c.weight_dtype;
     ctx->args.reset(new GemmArgs());
     cudaError_t e = cudaGetDevice(&ctx->device);
     if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDevice");
@@ -320,8 +340,8 @@ int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* cons
             ctx->stage13[s] = stage_w13[s];
             ctx->stage2[s] = stage_w2[s];
             if (!encode_slots(&ctx->stage_map13[s], stage_w13[s], c.stage_slots, 2ull * c.inter, c.hidden,
-                              ctx->elem_bytes) ||
-                !encode_slots(&ctx->stage_map2[s], stage_w2[s], c.stage_slots, c.hidden, c.inter, ctx->elem_bytes))
+                              ctx->fmt) ||
+                !encode_slots(&ctx->stage_map2[s], stage_w2[s], c.stage_slots, c.hidden, c.inter, ctx->fmt))
                 return fail(nullptr, DWDP_ERR_CUDA, "tensor map for a stage buffer");
         }
     }
@@ -398,16 +418,16 @@ int32_t dwdp_set_expert_map(dwdp_ctx* ctx, int32_t layer, const dwdp_pool* local
                     c.stage_slots);
     if (any_local) {
         m.local = *local;
-        if (!encode_slots(&m.local13, local->w13, local->n_slots, 2ull * c.inter, c.hidden, ctx->elem_bytes) ||
-            !encode_slots(&m.local2, local->w2, local->n_slots, c.hidden, c.inter, ctx->elem_bytes))
+        if (!encode_slots(&m.local13, local->w13, local->n_slots, 2ull * c.inter, c.hidden, ctx->fmt) ||
+            !encode_slots(&m.local2, local->w2, local->n_slots, c.hidden, c.inter, ctx->fmt))
             return fail(ctx, DWDP_ERR_CUDA, "tensor map for the local pool");
         m.has_local_map = true;
     }
     if (c.n_shared) {
         m.shared_w13 = shared_w13;
         m.shared_w2 = shared_w2;
-        if (!encode_slots(&m.shared13, shared_w13, 1, 2ull * c.inter, c.hidden, ctx->elem_bytes) ||
-            !encode_slots(&m.shared2, shared_w2, 1, c.hidden, c.inter, ctx->elem_bytes))
+        if (!encode_slots(&m.shared13, shared_w13, 1, 2ull * c.inter, c.hidden, ctx->fmt) ||
+            !encode_slots(&m.shared2, shared_w2, 1, c.hidden, c.inter, ctx->fmt))
             return fail(ctx, DWDP_ERR_CUDA, "tensor map for the shared expert");
     }
     m.bsrc.resize(E + c.n_shared);
@@ -428,7 +448,8 @@ int32_t dwdp_set_expert_scales(dwdp_ctx* ctx, int32_t layer, const float* w13_sc
                                float shared_w13_scale, float shared_w2_scale) {
     if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
     const dwdp_config& c = ctx->cfg;
-    if (c.weight_dtype != DWDP_DTYPE_E4M3) return fail(ctx, DWDP_ERR_INVALID_ARG, "scales apply to E4M3 contexts only");
+    if (c.weight_dtype == DWDP_DTYPE_BF16)
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "scales apply to E4M3 and NVFP4 contexts only");
     if (layer < 0 || layer >= c.n_layers) return fail(ctx, DWDP_ERR_INVALID_ARG, "layer %d out of range", layer);
     if (!w13_scale || !w2_scale) return fail(ctx, DWDP_ERR_INVALID_ARG, "scale arrays must not be NULL");
     std::vector<float> s13(w13_scale, w13_scale + c.n_experts), s2(w2_scale, w2_scale + c.n_experts);
@@ -444,17 +465,18 @@ int32_t dwdp_set_expert_scales(dwdp_ctx* ctx, int32_t layer, const float* w13_sc
     return DWDP_OK;
 }
 
-int32_t dwdp_plan_prefetch(int32_t n_experts, int32_t hidden, int32_t inter, int32_t elem_bytes,
+int32_t dwdp_plan_prefetch(int32_t n_experts, int32_t hidden, int32_t inter, int32_t weight_dtype,
                            const int32_t* local_slot,
                            const int32_t* peer_id, const int32_t* peer_slot, int32_t n_peers,
                            size_t chunk_bytes, dwdp_copy_slice* out, int64_t max_out, int64_t* n_out) {
-    if (n_experts <= 0 || hidden <= 0 || inter <= 0 || (elem_bytes != 1 && elem_bytes != 2) || !local_slot ||
+    if (n_experts <= 0 || hidden <= 0 || inter <= 0 || weight_dtype < DWDP_DTYPE_BF16 ||
+        weight_dtype > DWDP_DTYPE_NVFP4 || !local_slot ||
         !n_out || n_peers < 0 ||
         (max_out > 0 && !out))
         return fail(nullptr, DWDP_ERR_INVALID_ARG, "bad arguments to dwdp_plan_prefetch");
     std::vector<dwdp_copy_slice> plan;
     std::string why;
-    if (!build_plan(n_experts, hidden, inter, elem_bytes, local_slot, peer_id, peer_slot, n_peers, chunk_bytes, plan,
+    if (!build_plan(n_experts, hidden, inter, weight_dtype, local_slot, peer_id, peer_slot, n_peers, chunk_bytes, plan,
                     why))
         return fail(nullptr, DWDP_ERR_INVALID_ARG, "%s", why.c_str());
     *n_out = (int64_t)plan.size();
@@ -507,7 +529,7 @@ int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router
     a.col_bias = logit_bias;
     a.err = ctx->d_err;
     a.bsrc[0] = make_int2(0, 0);
-    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_F32, false, a, ctx->n_sms, stream));
+    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_F32, FMT_BF16, a, ctx->n_sms, stream));
     DWDP_CUDA(ctx, launch_topk(logits, nullptr, T, c.n_experts, c.top_k, out->topk_ids, out->topk_w, stream));
     DWDP_CUDA(ctx, launch_group_chunked(out->topk_ids, T * c.top_k, c.n_experts, out->counts, out->offsets,
                                         out->perm, out->inv_perm, group_scratch, stream));
@@ -530,7 +552,7 @@ int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t 
     if (it == m.plans.end()) {
         std::vector<dwdp_copy_slice> plan;
         std::string why;
-        if (!build_plan(c.n_experts, c.hidden, c.inter, ctx->elem_bytes, m.local_slot.data(), m.peer_id.data(),
+        if (!build_plan(c.n_experts, c.hidden, c.inter, ctx->fmt, m.local_slot.data(), m.peer_id.data(),
                         m.peer_slot.data(),
                         (int32_t)m.peers.size(), chunk_bytes, plan, why))
             return fail(ctx, DWDP_ERR_INVALID_ARG, "%s", why.c_str());
@@ -597,9 +619,10 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
         return fail(ctx, DWDP_ERR_INVALID_ARG, "workspace too small (%zu < %zu) or unaligned", ws_bytes, L.moe_bytes);
     const int64_t k = c.top_k, S = c.n_shared, H = c.hidden, I = c.inter, E = c.n_experts;
     const int64_t rows_r = (int64_t)T * k, rows_all = (int64_t)T * (k + S);
-    const bool f8 = ctx->elem_bytes == 1;
-    if (f8 && m.scale13.size() != m.bsrc.size())
-        return fail(ctx, DWDP_ERR_NOT_MAPPED, "layer %d has no E4M3 weight scales (dwdp_set_expert_scales)", layer);
+    const int fmt = ctx->fmt;
+    const bool scaled = fmt != FMT_BF16;
+    if (scaled && m.scale13.size() != m.bsrc.size())
+        return fail(ctx, DWDP_ERR_NOT_MAPPED, "layer %d has no weight scales (dwdp_set_expert_scales)", layer);
     char* w = static_cast<char*>(ws);
     void* xp = w + L.xp;
     void* act = w + L.a;
@@ -609,10 +632,19 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     float* sxp = reinterpret_cast<float*>(w + L.sxp);
     void* aq = w + L.aq;
     float* sa = reinterpret_cast<float*>(w + L.sa);
+    uint8_t* sfx = reinterpret_cast<uint8_t*>(w + L.sfx);
+    uint8_t* sfa = reinterpret_cast<uint8_t*>(w + L.sfa);
 
     if (m.n_remote > 0) DWDP_CUDA(ctx, cudaStreamWaitEvent(stream, ctx->ready[stage], 0));
     DWDP_CUDA(ctx, mark(ctx, 2, stream));
-    if (f8) {
+    if (fmt == FMT_NVFP4) {
+        // x rows to NVFP4 once per token, written to each chosen expert's row
+        if (!route->topk_ids || !aligned16(route->topk_ids))
+            return fail(ctx, DWDP_ERR_INVALID_ARG, "NVFP4 layers need route->topk_ids");
+        DWDP_CUDA(ctx, launch_quantize_x_nvfp4(x, (int)H, (int)T, (int)k, route->topk_ids, route->inv_perm,
+                                               route->offsets, (int)E, S > 0, xq, sx, xp, sxp, sfx, L.sf_tiles,
+                                               ctx->d_err, stream));
+    } else if (fmt == FMT_E4M3) {
         // x rows to E4M3 (per-token scales), then gathered into expert order
         DWDP_CUDA(ctx, launch_quantize_rows(x, T, (int)H, xq, sx, stream));
         DWDP_CUDA(ctx, launch_gather_fp8(xq, sx, (int)H, route->inv_perm, (int)T, (int)k, xp, sxp, stream));
@@ -630,14 +662,27 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
         a.tmB[1] = m.n_remote > 0 ? stg : *valid;
         a.tmB[2] = S ? shared : *valid;
     };
+    // NVFP4: where each buffer's slot 0 keeps its block scales (after its
+    // rows x K / 2 bytes of codes); buffers no group reads get nullptr.
+    auto set_bsf = [&](const void* local, const void* stg, const void* shared, int64_t rows, int64_t K) {
+        const int64_t codes = rows * K / 2;
+        auto at = [&](const void* base) { return base ? static_cast<const uint8_t*>(base) + codes : nullptr; };
+        a.bsf[0] = m.has_local_map ? at(local) : nullptr;
+        a.bsf[1] = m.n_remote > 0 ? at(stg) : nullptr;
+        a.bsf[2] = S ? at(shared) : nullptr;
+        a.b_slot_bytes = weight_slot_bytes(rows, K, fmt);
+    };
     // G1: a = SiLU(xp W_gate) * (xp W_up); the shared group reads x directly
     // (E4M3: xp / x codes, dequantized in the epilogue by row scale * weight scale).
-    if (!encode_rows(&a.tmA[0], xp, rows_r, H, ctx->elem_bytes) ||
-        !encode_rows(&a.tmA[1], f8 ? xq : x, T, H, ctx->elem_bytes))
+    if (!encode_rows(&a.tmA[0], xp, rows_r, H, fmt) || !encode_rows(&a.tmA[1], scaled ? xq : x, T, H, fmt))
         return fail(ctx, DWDP_ERR_CUDA, "tensor maps for the gate/up GEMM");
     a.row_scale[0] = sxp;
     a.row_scale[1] = sx;
     set_b(m.local13, ctx->stage_map13[m.n_remote > 0 ? stage : 0], m.shared13);
+    a.sfa = sfx;
+    a.sfa_tiles = L.sf_tiles;
+    if (fmt == FMT_NVFP4)
+        set_bsf(m.local.w13, ctx->stage13[m.n_remote > 0 ? stage : 0], m.shared_w13, 2 * I, H);
     a.row_offsets = route->offsets;
     a.n_routed = (int32_t)E;
     a.shared_rows = (int32_t)(T * S);
@@ -652,19 +697,25 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     a.err = ctx->d_err;
     for (size_t g = 0; g < m.bsrc.size(); ++g) {
         a.bsrc[g] = m.bsrc[g];
-        if (f8) a.gscale[g] = m.scale13[g];
+        if (scaled) a.gscale[g] = m.scale13[g];
     }
-    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_SILU, f8, a, ctx->n_sms, stream));
+    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_SILU, fmt, a, ctx->n_sms, stream));
     DWDP_CUDA(ctx, mark(ctx, 4, stream));
-    // G2: y = a W_down (E4M3: a's rows quantized first; this phase includes it).
-    if (f8) DWDP_CUDA(ctx, launch_quantize_rows(act, rows_all, (int)I, aq, sa, stream));
-    if (!encode_rows(&a.tmA[0], f8 ? aq : act, rows_all, I, ctx->elem_bytes))
+    // G2: y = a W_down (E4M3 / NVFP4: a's rows quantized first; this phase includes it).
+    if (fmt == FMT_E4M3) DWDP_CUDA(ctx, launch_quantize_rows(act, rows_all, (int)I, aq, sa, stream));
+    if (fmt == FMT_NVFP4)
+        DWDP_CUDA(ctx, launch_quantize_a_nvfp4(act, (int)I, rows_r, rows_all, route->offsets, (int)E, aq, sa, sfa,
+                                               L.sf_tiles, ctx->d_err, stream));
+    if (!encode_rows(&a.tmA[0], scaled ? aq : act, rows_all, I, fmt))
         return fail(ctx, DWDP_ERR_CUDA, "tensor map for the down GEMM");
     a.tmA[1] = a.tmA[0];
     a.row_scale[0] = a.row_scale[1] = sa;
-    if (f8)
+    if (scaled)
         for (size_t g = 0; g < m.bsrc.size(); ++g) a.gscale[g] = m.scale2[g];
     set_b(m.local2, ctx->stage_map2[m.n_remote > 0 ? stage : 0], m.shared2);
+    a.sfa = sfa;
+    if (fmt == FMT_NVFP4)
+        set_bsf(m.local.w2, ctx->stage2[m.n_remote > 0 ? stage : 0], m.shared_w2, H, I);
     a.shared_a_row = (int32_t)rows_r;
     a.shared_d_row = (int32_t)rows_r;
     a.K = (int32_t)I;
@@ -672,12 +723,33 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     a.ldd = H;
     a.d_rows = rows_all;
     a.D = y;
-    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_BF16, f8, a, ctx->n_sms, stream));
+    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_BF16, fmt, a, ctx->n_sms, stream));
     DWDP_CUDA(ctx, mark(ctx, 5, stream));
     // The stage's weights have been read: the next prefetch into it may start.
     if (m.n_remote > 0) DWDP_CUDA(ctx, cudaEventRecord(ctx->freed[stage], stream));
     DWDP_CUDA(ctx, launch_combine(y, (int)H, route->inv_perm, route->topk_w, T, (int)k, rows_r, S > 0, out, stream));
     DWDP_CUDA(ctx, mark(ctx, 6, stream));
+    return DWDP_OK;
+}
+
+int32_t dwdp_quantize_rows(int32_t weight_dtype, const void* x, int64_t rows, int32_t K, void* codes,
+                           void* block_scales, float* row_scale, dwdp_stream_t stream) {
+    if (weight_dtype != DWDP_DTYPE_E4M3 && weight_dtype != DWDP_DTYPE_NVFP4)
+        return fail(nullptr, DWDP_ERR_INVALID_ARG, "weight_dtype must be E4M3 or NVFP4");
+    if (rows < 0 || rows >= ((int64_t)1 << 31) || K <= 0 || K % 64)
+        return fail(nullptr, DWDP_ERR_INVALID_ARG, "rows in [0, 2^31), K a positive multiple of 64");
+    if (rows == 0) return DWDP_OK;
+    if (!x || !codes || !row_scale || !aligned16(x) || !aligned16(codes) || !aligned16(row_scale) ||
+        (weight_dtype == DWDP_DTYPE_NVFP4 && (!block_scales || !aligned16(block_scales))))
+        return fail(nullptr, DWDP_ERR_INVALID_ARG, "pointers must be non-NULL and 16-byte aligned");
+    cudaError_t e;
+    if (weight_dtype == DWDP_DTYPE_E4M3) {
+        e = launch_quantize_rows(x, rows, K, codes, row_scale, stream);
+    } else {
+        e = launch_quantize_a_nvfp4(x, K, 0, rows, nullptr, 0, codes, row_scale, static_cast<uint8_t*>(block_scales),
+                                    (rows + BM - 1) / BM, nullptr, stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "dwdp_quantize_rows");
     return DWDP_OK;
 }
 
@@ -761,7 +833,7 @@ int32_t dwdp_grouped_gemm(dwdp_ctx* ctx, int32_t epilogue, const void* a_ptr, in
     a.D = d;
     a.col_bias = nullptr;
     a.err = ctx->d_err;
-    DWDP_CUDA(ctx, launch_grouped_gemm(epilogue, false, a, ctx->n_sms, stream));
+    DWDP_CUDA(ctx, launch_grouped_gemm(epilogue, FMT_BF16, a, ctx->n_sms, stream));
     return DWDP_OK;
 }
 

@@ -16,9 +16,12 @@ constexpr int kMaxGroups = DWDP_MAX_EXPERTS + 1;  // routed experts + one shared
 
 enum Epilogue : int { EPI_BF16 = 0, EPI_SILU = 1, EPI_F32 = 2 };
 
+// GEMM operand formats (the weight_dtype values of dwdp.h).
+enum OperandFormat : int { FMT_BF16 = DWDP_DTYPE_BF16, FMT_E4M3 = DWDP_DTYPE_E4M3, FMT_NVFP4 = DWDP_DTYPE_NVFP4 };
+
 // Tile shape of the grouped GEMM: one CTA computes a 128 x 256 fp32
 // accumulator in tensor memory from K slices of 128 bytes per row staged by
-// TMA (64 bf16 or 128 E4M3 elements).
+// TMA (64 bf16, 128 E4M3 or 256 NVFP4 elements).
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;        // bf16 elements per K slice (128 bytes)
@@ -29,6 +32,29 @@ constexpr int kBBytes = BN * BK * 2;           // 32 KiB
 constexpr int kStageBytes = kABytes + kBBytes;  // 48 KiB
 constexpr int kGemmThreads = 192;              // producer, MMA, 4 epilogue warps
 constexpr int kClusterCtas = 2;                // CTAs per cluster (co-scheduled on one GPC)
+
+// NVFP4 block scales as the block-scaled MMA takes them: for a row block rb
+// (rows 128 rb .. 128 rb + 127) and a K step ks (elements 64 ks .. 64 ks + 63)
+// one 512-byte chunk; the E4M3 scale of row 128 rb + 32 m1 + m0 and
+// 16-element block kb of the step sits at byte 16 m0 + 4 m1 + kb.  Chunks
+// run K step fastest: chunk (rb, ks) starts at (rb * K / 64 + ks) * 512.
+// An activation operand's chunks are indexed by the GEMM's A tile instead
+// of rb (see GemmArgs::sfa).
+constexpr int kSfChunkBytes = 512;
+constexpr int kSfStageBytesA = 4 * kSfChunkBytes;        // 128 rows x 256 elements
+constexpr int kSfStageBytesB = 2 * kSfStageBytesA;       // 256 rows x 256 elements
+
+// Bytes of one [rows][K] weight tensor (one pool slot) in format fmt:
+// bf16 2 per element, E4M3 1, NVFP4 half a byte of code plus 1/16 byte of
+// block scale (codes first, then the scale chunks).
+inline int64_t weight_slot_bytes(int64_t rows, int64_t K, int fmt) {
+    if (fmt == FMT_NVFP4) return rows * K / 2 + rows * K / 16;
+    return rows * K * (fmt == FMT_E4M3 ? 1 : 2);
+}
+// Bytes of one row of GEMM operand codes in format fmt.
+inline int64_t operand_row_bytes(int64_t K, int fmt) {
+    return fmt == FMT_NVFP4 ? K / 2 : K * (fmt == FMT_E4M3 ? 1 : 2);
+}
 
 // Bits of the device error word (kernels OR them in; never trap).
 enum DeviceError : int {
@@ -61,27 +87,37 @@ struct GemmArgs {
     void* D;
     const float* col_bias;  // EPI_F32: added per column, may be null
     int* err;
-    // E4M3 operands only: the fp32 accumulator is multiplied by the A row's
-    // scale (routed rows: row_scale[0][A row], shared rows: row_scale[1][A row])
-    // and by the group's weight scale gscale[g].
+    // E4M3 and NVFP4 operands: the fp32 accumulator is multiplied by the A
+    // row's scale (routed rows: row_scale[0][A row], shared rows:
+    // row_scale[1][A row]) and by the group's weight scale gscale[g].
     const float* row_scale[2];
+    // NVFP4 only.  sfa: the A operand's block-scale chunks, indexed by A tile:
+    // the m-th 128-row tile of group g is A tile tile_start[g] / NT + m (groups
+    // in order, the shared group last), so its chunks for K step ks start at
+    // (atile * K / 64 + ks) * 512.  bsf[b]: start of slot 0's scale chunks in
+    // weight buffer b; slot s's chunks are b_slot_bytes further per slot.
+    const uint8_t* sfa;
+    int64_t sfa_tiles;  // A tiles sfa has room for (a larger tile index is flagged)
+    const uint8_t* bsf[3];
+    int64_t b_slot_bytes;
     int2 bsrc[kMaxGroups];
     float gscale[kMaxGroups];
 };
 
 // TMA tensor maps (dwdp_abi.cu): a rows x K matrix (box 128 rows x 128 B)
 // and a weight buffer [slots][rows][K] (box 1 x 128 rows x 128 B), both
-// 128 B swizzle; elem_bytes 2 = bf16, 1 = E4M3 codes.
-bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, int elem_bytes = 2);
+// 128 B swizzle.  K counts elements of format fmt (bf16, E4M3 codes or
+// NVFP4 codes, two per byte); a weight slot is weight_slot_bytes apart.
+bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, int fmt = FMT_BF16);
 bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t rows, uint64_t K,
-                  int elem_bytes = 2);
+                  int fmt = FMT_BF16);
 
 // Sets the text dwdp_last_error(NULL) returns on this thread (dwdp_abi.cu).
 void set_last_error(const char* msg);
 
 size_t gemm_smem_bytes(int n_groups);
 // fp8: both operands are E4M3 codes (K counted in elements = bytes).
-cudaError_t launch_grouped_gemm(int epi, bool fp8, const GemmArgs& args, int n_sms, cudaStream_t stream);
+cudaError_t launch_grouped_gemm(int epi, int fmt, const GemmArgs& args, int n_sms, cudaStream_t stream);
 
 // route.cu
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k,
@@ -100,6 +136,18 @@ cudaError_t launch_quantize_rows(const void* in, int64_t rows, int cols, void* c
 // Expert-ordered E4M3 rows: xp[inv[t k + j]] = xq[t], sxp[inv[t k + j]] = sx[t].
 cudaError_t launch_gather_fp8(const void* xq, const float* sx, int H, const int32_t* inv, int T, int k,
                               void* xp, float* sxp, cudaStream_t s);
+// NVFP4 activations (block scales in the GEMM's A-tile chunk layout): x
+// rows quantized once per token and written to the shared-expert copy (xq,
+// sx) and to each chosen expert's row of xp / sxp; a rows (routed rows in
+// group order, then rows_all - rows_r shared rows).
+// sf has room for sf_tiles A tiles; a row that would land beyond is flagged
+// in err and not written.
+cudaError_t launch_quantize_x_nvfp4(const void* x, int H, int T, int k, const int32_t* ids, const int32_t* inv,
+                                    const int32_t* offsets, int E, bool has_shared, void* xq, float* sx, void* xp,
+                                    float* sxp, uint8_t* sf, int64_t sf_tiles, int* err, cudaStream_t s);
+cudaError_t launch_quantize_a_nvfp4(const void* act, int I, int64_t rows_r, int64_t rows_all, const int32_t* offsets,
+                                    int E, void* aq, float* sa, uint8_t* sf, int64_t sf_tiles, int* err,
+                                    cudaStream_t s);
 cudaError_t launch_combine(const void* y, int H, const int32_t* inv, const float* w, int T, int k,
                            int64_t shared_row0, bool has_shared, void* out, cudaStream_t s);
 

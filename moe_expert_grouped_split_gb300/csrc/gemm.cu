@@ -8,10 +8,12 @@
 // feed the GEMM.
 //
 // Kernel organisation (one persistent CTA per SM, 192 threads):
-//   warp 0      TMA producer: A tile [128 x 64] + B tile [256 x 64] per stage,
-//               4-stage mbarrier ring in shared memory (128B swizzle).
-//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
-//               and issues tcgen05.mma (M=128, N=256, K=16) from one thread.
+//   warp 0      TMA producer: A tile [128 rows x 128 B] + B tile [256 rows x
+//               128 B] per stage, 4-stage mbarrier ring in shared memory
+//               (128B swizzle); NVFP4 adds the tiles' block-scale chunks.
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators;
+//               NVFP4: one accumulator and a ring of block scales) and issues
+//               tcgen05.mma (M=128, N=256, 32 bytes of K each) from one thread.
 //   warps 2..5  epilogue: tcgen05.ld the accumulator rows of their TMEM lane
 //               quarter, apply SiLU(gate)*up or plain conversion, store.
 // Tiles are enumerated group by group, n-tile by n-tile, m-tile fastest, and
@@ -32,10 +34,28 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitim
 // Instruction descriptors.  kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at bits
 // 17-22, M >> 4 at bits 24-28.  kind::f8f6f4: the same with A and B E4M3
-// (format 0).
+// (format 0).  kind::mxf4nvf4 (block-scaled, D always fp32): bits 4-5 and
+// 29-30 select the byte of the B / A scale word (0: scale_vec::4X uses all
+// four), A and B E2M1 (format 1), bit 23 = 0 for E4M3 scales, N and M as
+// above.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                             ((uint32_t)(BM >> 4) << 24);
 constexpr uint32_t kIdescE4M3 = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t kIdescNvfp4 = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+// Per-format constants.  NVFP4 keeps one accumulator (256 TMEM columns) so
+// that the other 256 columns can hold the block scales of the stages in
+// flight: per stage 4 K steps x (4 columns of A scales + 8 of B scales).
+template <int FMT>
+struct Fmt {
+    static constexpr int kKElems = FMT == FMT_NVFP4 ? 256 : FMT == FMT_E4M3 ? 128 : 64;  // K per 128-byte slice
+    static constexpr int kXPerSlice = FMT == FMT_BF16 ? 64 : 128;  // tensor-map x units (bf16 or bytes) per slice
+    static constexpr int kSfBytes = FMT == FMT_NVFP4 ? kSfStageBytesA + kSfStageBytesB : 0;
+    static constexpr int kStageTx = kStageBytes + kSfBytes;
+    static constexpr int kAccBufs = FMT == FMT_NVFP4 ? 1 : 2;
+};
+constexpr int kSfCol0 = BN;            // NVFP4: first TMEM column of the scale ring
+constexpr int kSfColsPerStage = 48;    // 4 K steps x (4 + 8) columns
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -134,6 +154,25 @@ __device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* 
         : "memory");
 }
 
+// Untiled bulk copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) into this CTA's shared memory, completing on bar.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"((uint64_t)src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// As bulk_load, into the same offset of every CTA in cta_mask.
+__device__ __forceinline__ void bulk_load_mc(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                             uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"((uint64_t)src), "r"(bytes), "r"(bar), "h"(cta_mask)
+        : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -164,6 +203,24 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory descriptor of one 512-byte block-scale chunk for
+// tcgen05.cp .32x128b: 32 rows of 16 bytes, no swizzle, 8-row core matrices
+// 128 B apart (stride byte offset).
+__device__ __forceinline__ uint64_t sf_chunk_desc(uint32_t saddr) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(128 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Copy one chunk into 32 TMEM lanes x 4 columns, replicated into all four
+// lane quarters: lane m0 of each quarter, column c + m1 then holds the four
+// scales of row 32 m1 + m0 for the K step.
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -171,11 +228,20 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// One 128 x 256 MMA step: K = 16 bf16 or K = 32 E4M3 elements (32 bytes).
-template <bool F8>
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t accumulate) {
-    if constexpr (F8) {
+// One 128 x 256 MMA step over 32 bytes of K: 16 bf16, 32 E4M3 or 64 NVFP4
+// elements (NVFP4: scaled by the E4M3 block scales at sfa / sfb in TMEM).
+template <int FMT>
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate,
+                                       uint32_t sfa = 0, uint32_t sfb = 0) {
+    if constexpr (FMT == FMT_NVFP4) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+                d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(kIdescNvfp4), "r"(accumulate), "r"(sfa), "r"(sfb)
+            : "memory");
+    } else if constexpr (FMT == FMT_E4M3) {
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
             "setp.ne.b32 p, %4, 0;\n\t"
@@ -247,32 +313,38 @@ __device__ __forceinline__ void store_bf16x32(void* p, const float* v) {
     }
 }
 
+template <int FMT>
 struct SmemLayout {
     // offsets from the 1024-aligned base
     static constexpr int kA = 0;
     static constexpr int kB = kStages * kABytes;
-    static constexpr int kBars = kB + kStages * kBBytes;  // full[S], empty[S], tfull[2], tempty[2], mdone
+    static constexpr int kSF = kB + kStages * kBBytes;    // NVFP4: A then B scale chunks per stage
+    static constexpr int kBars = kSF + kStages * Fmt<FMT>::kSfBytes;  // full[S], empty[S], tfull[2], tempty[2], mdone
     static constexpr int kNumBars = 2 * kStages + 5;
     static constexpr int kMisc = kBars + 8 * kNumBars;    // tmem base, abort flag
     static constexpr int kTileStart = kMisc + 16;         // int32[G+1]
 };
 
-template <int EPI, bool F8>
+template <int EPI, int FMT>
 __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
-    constexpr int KE = F8 ? BK_BYTES : BK;  // K elements per 128-byte slice
+    using SL = SmemLayout<FMT>;
+    using F = Fmt<FMT>;
+    constexpr int KE = F::kKElems;     // K elements per 128-byte slice
+    constexpr int KX = F::kXPerSlice;  // the slice's width in tensor-map x units
+    constexpr bool kScaled = FMT != FMT_BF16;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t bar0 = sbase + SmemLayout::kBars;
+    const uint32_t bar0 = sbase + SL::kBars;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
     const uint32_t mdone_bar = bar0 + 8u * (2 * kStages + 4);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SmemLayout::kMisc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::kMisc + 4);
-    int32_t* tile_start = reinterpret_cast<int32_t*>(smem + SmemLayout::kTileStart);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::kMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::kMisc + 4);
+    int32_t* tile_start = reinterpret_cast<int32_t*>(smem + SL::kTileStart);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -382,23 +454,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                 // the pair shares the weight tile when the peer's tile (tile ^ 1,
                 // same group) has the same n-tile
                 const bool share = paired && (((local ^ 1) / mt) == n);
+                int64_t atile = tile_start[g] / NT + m;  // NVFP4: the A tile's scale chunks
+                if (FMT == FMT_NVFP4 && atile >= p.sfa_tiles) {
+                    atomicOr(p.err, DERR_BAD_INDEX);  // inconsistent group rows: read tile 0's scales instead
+                    atile = 0;
+                }
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err, DERR_PRODUCER_WAIT)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, kStageBytes);
-                    const uint32_t sa = sbase + SmemLayout::kA + stage * kABytes;
-                    const uint32_t sb = sbase + SmemLayout::kB + stage * kBBytes;
-                    tma_load_2d(sa, ma, kb * KE, a_row, fb);
+                    mbar_arrive_expect_tx(fb, F::kStageTx);
+                    const uint32_t sa = sbase + SL::kA + stage * kABytes;
+                    const uint32_t sb = sbase + SL::kB + stage * kBBytes;
+                    tma_load_2d(sa, ma, kb * KX, a_row, fb);
                     if (share) {
                         // my half of the weight tile, into both CTAs' stages
                         const uint32_t off = crank ? (uint32_t)(kBBytes / 2) : 0u;
-                        tma_load_3d_mc(sb + off, mb, kb * KE, crank ? b_row1 : b_row0, src.y, fb, (uint16_t)0x3);
+                        tma_load_3d_mc(sb + off, mb, kb * KX, crank ? b_row1 : b_row0, src.y, fb, (uint16_t)0x3);
                     } else {
-                        tma_load_3d(sb, mb, kb * KE, b_row0, src.y, fb);
-                        tma_load_3d(sb + kBBytes / 2, mb, kb * KE, b_row1, src.y, fb);
+                        tma_load_3d(sb, mb, kb * KX, b_row0, src.y, fb);
+                        tma_load_3d(sb + kBBytes / 2, mb, kb * KX, b_row1, src.y, fb);
+                    }
+                    if constexpr (FMT == FMT_NVFP4) {
+                        // the tiles' block scales: 4 K steps of A's 128 rows, then
+                        // of B's two 128-row halves (multicast like the halves)
+                        const uint32_t ss = sbase + SL::kSF + stage * F::kSfBytes;
+                        const int64_t KS = p.K / 64;
+                        bulk_load(ss, p.sfa + (atile * KS + kb * 4) * kSfChunkBytes, kSfStageBytesA, fb);
+                        const uint8_t* bs = p.bsf[src.x] + (int64_t)src.y * p.b_slot_bytes;
+                        if (share) {
+                            const int64_t rb = (crank ? b_row1 : b_row0) / BM;
+                            bulk_load_mc(ss + kSfStageBytesA * (1 + crank), bs + (rb * KS + kb * 4) * kSfChunkBytes,
+                                         kSfStageBytesA, fb, (uint16_t)0x3);
+                        } else {
+                            bulk_load(ss + kSfStageBytesA, bs + ((int64_t)(b_row0 / BM) * KS + kb * 4) * kSfChunkBytes,
+                                      kSfStageBytesA, fb);
+                            bulk_load(ss + 2 * kSfStageBytesA,
+                                      bs + ((int64_t)(b_row1 / BM) * KS + kb * 4) * kSfChunkBytes, kSfStageBytesA, fb);
+                        }
                     }
                     pend[stage] = (int)phase;
                     if (++stage == kStages) {
@@ -428,20 +523,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);  // NVFP4: acc is always 0
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err, DERR_MMA_FULL_WAIT)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sw128_desc(sbase + SmemLayout::kA + stage * kABytes);
-                    const uint64_t bd = sw128_desc(sbase + SmemLayout::kB + stage * kBBytes);
+                    const uint64_t ad = sw128_desc(sbase + SL::kA + stage * kABytes);
+                    const uint64_t bd = sw128_desc(sbase + SL::kB + stage * kBBytes);
+                    if constexpr (FMT == FMT_NVFP4) {
+                        // block scales of this stage into its TMEM columns (the MMAs
+                        // that last read those columns finished before the stage was
+                        // refilled), then 4 block-scaled MMAs of 64 elements each
+                        const uint32_t ss = sbase + SL::kSF + stage * F::kSfBytes;
+                        const uint32_t tc = tmem_base + (uint32_t)(kSfCol0 + stage * kSfColsPerStage);
 #pragma unroll
-                    for (int kk = 0; kk < BK_BYTES / 32; ++kk) {
-                        // advance 32 bytes (16 bf16 / 32 E4M3) along K inside the swizzle atom
-                        tc_mma<F8>(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk),
-                               (kb > 0 || kk > 0) ? 1u : 0u);
+                        for (int j = 0; j < 4; ++j) {
+                            tc_cp_sf(tc + 4 * j, sf_chunk_desc(ss + j * kSfChunkBytes));
+                            tc_cp_sf(tc + 16 + 8 * j, sf_chunk_desc(ss + kSfStageBytesA + j * kSfChunkBytes));
+                            tc_cp_sf(tc + 20 + 8 * j, sf_chunk_desc(ss + 2 * kSfStageBytesA + j * kSfChunkBytes));
+                        }
+#pragma unroll
+                        for (int kk = 0; kk < BK_BYTES / 32; ++kk)
+                            tc_mma<FMT>(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk),
+                                        (kb > 0 || kk > 0) ? 1u : 0u, tc + 4 * kk, tc + 16 + 8 * kk);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < BK_BYTES / 32; ++kk) {
+                            // advance 32 bytes (16 bf16 / 32 E4M3) along K inside the swizzle atom
+                            tc_mma<FMT>(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk),
+                                        (kb > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     // Paired CTAs always free a stage in both CTAs, shared tile or not:
                     // if a pair could drift apart on unshared tiles, the first shared
@@ -457,7 +570,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                 }
                 if (!ok) break;
                 tc_commit(tfull_bar(acc));
-                if (++acc == 2) {
+                if (++acc == F::kAccBufs) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
@@ -488,9 +601,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                 atomicOr(p.err, DERR_BAD_INDEX);
                 valid = false;
             }
-            // E4M3: dequantize with the A row's scale times the group's weight scale
+            // E4M3 / NVFP4: dequantize with the A row's scale times the group's weight scale
             float sc = 1.0f;
-            if (F8 && valid) {
+            if (kScaled && valid) {
                 const int64_t arow = (routed ? (int64_t)p.row_offsets[g] : (int64_t)p.shared_a_row) + r;
                 sc = __ldg(p.row_scale[routed ? 0 : 1] + arow) * p.gscale[g];
             }
@@ -557,7 +670,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
-            if (++acc == 2) {
+            if (++acc == F::kAccBufs) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
@@ -577,28 +690,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 
 }  // namespace
 
+template <int FMT>
 size_t gemm_smem_bytes(int n_groups) {
-    return 1024 + SmemLayout::kTileStart + sizeof(int32_t) * (size_t)(n_groups + 1);
+    return 1024 + SmemLayout<FMT>::kTileStart + sizeof(int32_t) * (size_t)(n_groups + 1);
 }
 
-cudaError_t launch_grouped_gemm(int epi, bool fp8, const GemmArgs& args, int n_sms, cudaStream_t stream) {
+cudaError_t launch_grouped_gemm(int epi, int fmt, const GemmArgs& args, int n_sms, cudaStream_t stream) {
     const int G = args.n_routed + (args.shared_rows > 0 ? 1 : 0);
-    const size_t smem = gemm_smem_bytes(G);
-    const void* fn;
-    if (fp8) {
-        switch (epi) {
-            case EPI_SILU: fn = (const void*)grouped_gemm_kernel<EPI_SILU, true>; break;
-            case EPI_BF16: fn = (const void*)grouped_gemm_kernel<EPI_BF16, true>; break;
-            default: return cudaErrorInvalidValue;
-        }
-    } else {
-        switch (epi) {
-            case EPI_SILU: fn = (const void*)grouped_gemm_kernel<EPI_SILU, false>; break;
-            case EPI_BF16: fn = (const void*)grouped_gemm_kernel<EPI_BF16, false>; break;
-            case EPI_F32: fn = (const void*)grouped_gemm_kernel<EPI_F32, false>; break;
-            default: return cudaErrorInvalidValue;
-        }
+    size_t smem = 0;
+    const void* fn = nullptr;
+    if (fmt == FMT_NVFP4) {
+        smem = gemm_smem_bytes<FMT_NVFP4>(G);
+        if (epi == EPI_SILU) fn = (const void*)grouped_gemm_kernel<EPI_SILU, FMT_NVFP4>;
+        if (epi == EPI_BF16) fn = (const void*)grouped_gemm_kernel<EPI_BF16, FMT_NVFP4>;
+    } else if (fmt == FMT_E4M3) {
+        smem = gemm_smem_bytes<FMT_E4M3>(G);
+        if (epi == EPI_SILU) fn = (const void*)grouped_gemm_kernel<EPI_SILU, FMT_E4M3>;
+        if (epi == EPI_BF16) fn = (const void*)grouped_gemm_kernel<EPI_BF16, FMT_E4M3>;
+    } else if (fmt == FMT_BF16) {
+        smem = gemm_smem_bytes<FMT_BF16>(G);
+        if (epi == EPI_SILU) fn = (const void*)grouped_gemm_kernel<EPI_SILU, FMT_BF16>;
+        if (epi == EPI_BF16) fn = (const void*)grouped_gemm_kernel<EPI_BF16, FMT_BF16>;
+        if (epi == EPI_F32) fn = (const void*)grouped_gemm_kernel<EPI_F32, FMT_BF16>;
     }
+    if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);

@@ -422,7 +422,260 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
     }
 }
 
+// ------------------------------------------------------------- NVFP4 --
+// Activation rows to NVFP4 for the block-scaled GEMMs.  Per row of n bf16
+// values (n a multiple of 256): s = amax / 2688 (1 for an all-zero row),
+// d = 6 s; per 16-element block, its E4M3 scale sf = E4M3(amax_block / d)
+// (round to nearest even, saturating) and, with eff = value(sf) * s, each
+// element's E2M1 code of v / eff (round to nearest even, saturating; all
+// zero when sf is 0).  Every step is one binary32 operation, so the codes
+// are the same integer decisions whoever takes them in binary32.  Codes are
+// packed two per byte, element 2i in the low nibble.  Block scales go to the
+// chunk layout of the GEMM's A tiles (see kSfChunkBytes): a routed row r of
+// group g is row (r - offsets[g]) % 128 of A tile tb[g] + (r - offsets[g]) /
+// 128, where tb[g] counts the 128-row tiles of the groups before g; shared
+// row i is row i % 128 of A tile tb[E] + i / 128.
+
+// binary32 value of a non-negative E4M3 code (exact): exponent field 0 is
+// m * 2^-9, otherwise 2^(e-7) * (1 + m/8).
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+    return e == 0 ? (float)m * 0.001953125f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// Eight binary32 values to eight E2M1 codes (cvt.rn.satfinite), value i in
+// bits 4i .. 4i+3.
+__device__ __forceinline__ uint32_t e2m1x8(const float* v) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return r;
+}
+
+__device__ __forceinline__ void load_bf16x16(const uint4* src, float (&v)[16]) {
+    const uint4 q[2] = {__ldg(src), __ldg(src + 1)};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&q[h]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(p[j]);
+            v[8 * h + 2 * j] = f.x;
+            v[8 * h + 2 * j + 1] = f.y;
+        }
+    }
+}
+
+// The row scale s of one row of nb blocks (two uint4 per block), warp-wide.
+__device__ __forceinline__ float nvfp4_row_scale(const uint4* src, int nb, int lane) {
+    float amax = 0.0f;
+    for (int b = lane; b < nb; b += 32) {
+        float v[16];
+        load_bf16x16(src + 2 * b, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    return amax > 0.0f ? amax / 2688.0f : 1.0f;
+}
+
+// Block b of a row: its E4M3 scale code and 16 E2M1 codes (8 bytes).
+__device__ __forceinline__ uint32_t nvfp4_block(const uint4* src, int b, float s, float d, uint2& codes) {
+    float v[16];
+    load_bf16x16(src + 2 * b, v);
+    float ab = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(v[i]));
+    const uint32_t sf = __nv_cvt_float_to_fp8(ab / d, __NV_SATFINITE, __NV_E4M3);
+    const float eff = e4m3_value(sf) * s;
+    if (sf == 0) {
+        codes = make_uint2(0u, 0u);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = v[i] / eff;
+        codes = make_uint2(e2m1x8(v), e2m1x8(v + 8));
+    }
+    return sf;
+}
+
+__device__ __forceinline__ int64_t sf_byte(int64_t atile, int K, int b, int m) {
+    return (atile * (K / 64) + (b >> 2)) * kSfChunkBytes + (m & 31) * 16 + (m >> 5) * 4 + (b & 3);
+}
+
+// tb[g] for g <= E from the group offsets (warp 0), then a block barrier.
+// With no groups (offsets NULL, E = 0) tb[0] = 0.
+__device__ __forceinline__ void tile_bases(const int32_t* __restrict__ offsets, int E, int* tb, int* offs) {
+    if (offsets == nullptr) {
+        if (threadIdx.x == 0) tb[0] = offs[0] = 0;
+    } else if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int carry = 0;
+        for (int base = 0; base <= E; base += 32) {
+            const int g = base + lane;
+            int c = 0;
+            if (g <= E) offs[g] = offsets[g];
+            if (g < E) c = max(0, (offsets[g + 1] - offsets[g] + BM - 1) / BM);  // never negative
+            int v = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            if (g <= E) tb[g] = carry + v - c;  // exclusive
+            carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+    }
+    __syncthreads();
+}
+
+// x rows (one warp per token t): xq[t] and sx[t] for the shared expert (when
+// has_shared), and for each chosen expert j the row r = inv[t k + j] of xp /
+// sxp with its block scales, so x is read once.
+__global__ void __launch_bounds__(256) quantize_x_nvfp4_kernel(const uint4* __restrict__ x, int H, int T, int k,
+                                                               const int32_t* __restrict__ ids,
+                                                               const int32_t* __restrict__ inv,
+                                                               const int32_t* __restrict__ offsets, int E,
+                                                               int has_shared, uint2* __restrict__ xq,
+                                                               float* __restrict__ sx, uint2* __restrict__ xp,
+                                                               float* __restrict__ sxp, uint8_t* __restrict__ sf,
+                                                               int64_t sf_tiles, int* __restrict__ err) {
+    __shared__ int tb[DWDP_MAX_EXPERTS + 1], offs[DWDP_MAX_EXPERTS + 1];
+    tile_bases(offsets, E, tb, offs);
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int nb = H / 16;
+    const uint4* src = x + (int64_t)t * (H / 8);
+    const float s = nvfp4_row_scale(src, nb, lane);
+    const float d = 6.0f * s;
+    const int64_t n_rows = (int64_t)T * k;
+    // this token's destinations: lane j < k holds (row, A tile, row in tile) of choice j
+    int64_t my_r = -1, my_at = 0;
+    int my_m = 0;
+    if (lane < k) {
+        const int64_t r = inv[(int64_t)t * k + lane];
+        const int g = ids[(int64_t)t * k + lane];
+        if (r < 0 || r >= n_rows || g < 0 || g >= E || r < offs[g] || r >= offs[g + 1] ||
+            tb[g] + (r - offs[g]) / BM >= sf_tiles) {
+            atomicOr(err, DERR_BAD_INDEX);
+        } else {
+            my_r = r;
+            my_at = tb[g] + (r - offs[g]) / BM;
+            my_m = (int)((r - offs[g]) % BM);
+            sxp[r] = s;
+        }
+    }
+    if (has_shared && lane == 0) sx[t] = s;
+    const int64_t sh_at = tb[E] + t / BM;
+    if (has_shared && sh_at >= sf_tiles) {
+        if (lane == 0) atomicOr(err, DERR_BAD_INDEX);
+        has_shared = 0;
+    }
+    const int sh_m = t % BM;
+    // every lane runs every iteration: the shuffles below need the whole warp
+    for (int b0 = 0; b0 < nb; b0 += 32) {
+        const int b = b0 + lane;
+        const bool mine = b < nb;
+        uint2 c = make_uint2(0u, 0u);
+        uint32_t f = 0;
+        if (mine) {
+            f = nvfp4_block(src, b, s, d, c);
+            if (has_shared) {
+                xq[(int64_t)t * (H / 16) + b] = c;
+                sf[sf_byte(sh_at, H, b, sh_m)] = (uint8_t)f;
+            }
+        }
+        for (int j = 0; j < k; ++j) {
+            const int64_t r = __shfl_sync(0xffffffffu, my_r, j);
+            const int64_t at = __shfl_sync(0xffffffffu, my_at, j);
+            const int m = __shfl_sync(0xffffffffu, my_m, j);
+            if (r < 0 || !mine) continue;
+            xp[r * (H / 16) + b] = c;
+            sf[sf_byte(at, H, b, m)] = (uint8_t)f;
+        }
+    }
+}
+
+// a rows (one warp per row r of rows_all = routed rows then shared rows).
+// With rows_r = 0 and no groups this quantizes a plain [rows][I] matrix,
+// row r landing in row r % 128 of tile r / 128.
+__global__ void __launch_bounds__(256) quantize_a_nvfp4_kernel(const uint4* __restrict__ a, int I, int64_t rows_r,
+                                                               int64_t rows_all, const int32_t* __restrict__ offsets,
+                                                               int E, uint2* __restrict__ aq, float* __restrict__ sa,
+                                                               uint8_t* __restrict__ sf, int64_t sf_tiles,
+                                                               int* __restrict__ err) {
+    __shared__ int tb[DWDP_MAX_EXPERTS + 1], offs[DWDP_MAX_EXPERTS + 1];
+    tile_bases(offsets, E, tb, offs);
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (r >= rows_all) return;
+    int64_t at;
+    int m;
+    if (r < rows_r) {
+        // the group holding row r: the last g with offs[g] <= r (non-empty)
+        int lo = 0, hi = E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (offs[mid] <= r) lo = mid;
+            else hi = mid - 1;
+        }
+        if (r < offs[lo] || r >= offs[lo + 1]) {
+            if (lane == 0 && err) atomicOr(err, DERR_BAD_INDEX);
+            return;
+        }
+        at = tb[lo] + (r - offs[lo]) / BM;
+        m = (int)((r - offs[lo]) % BM);
+    } else {
+        at = tb[E] + (r - rows_r) / BM;
+        m = (int)((r - rows_r) % BM);
+    }
+    if (at >= sf_tiles) {
+        if (lane == 0 && err) atomicOr(err, DERR_BAD_INDEX);
+        return;
+    }
+    const int nb = I / 16;
+    const uint4* src = a + r * (I / 8);
+    const float s = nvfp4_row_scale(src, nb, lane);
+    const float d = 6.0f * s;
+    if (lane == 0) sa[r] = s;
+    for (int b = lane; b < nb; b += 32) {
+        uint2 c;
+        const uint32_t f = nvfp4_block(src, b, s, d, c);
+        aq[r * (I / 16) + b] = c;
+        sf[sf_byte(at, I, b, m)] = (uint8_t)f;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_x_nvfp4(const void* x, int H, int T, int k, const int32_t* ids, const int32_t* inv,
+                                    const int32_t* offsets, int E, bool has_shared, void* xq, float* sx, void* xp,
+                                    float* sxp, uint8_t* sf, int64_t sf_tiles, int* err, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    const int warps = 8;
+    quantize_x_nvfp4_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(
+        reinterpret_cast<const uint4*>(x), H, T, k, ids, inv, offsets, E, has_shared ? 1 : 0,
+        reinterpret_cast<uint2*>(xq), sx, reinterpret_cast<uint2*>(xp), sxp, sf, sf_tiles, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_a_nvfp4(const void* act, int I, int64_t rows_r, int64_t rows_all, const int32_t* offsets,
+                                    int E, void* aq, float* sa, uint8_t* sf, int64_t sf_tiles, int* err,
+                                    cudaStream_t s) {
+    if (rows_all <= 0) return cudaSuccess;
+    const int warps = 8;
+    quantize_a_nvfp4_kernel<<<(unsigned)((rows_all + warps - 1) / warps), 32 * warps, 0, s>>>(
+        reinterpret_cast<const uint4*>(act), I, rows_r, rows_all, offsets, E, reinterpret_cast<uint2*>(aq), sa, sf,
+        sf_tiles, err);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_rows(const void* in, int64_t rows, int cols, void* codes, float* scale, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;

@@ -113,7 +113,7 @@ extern "C" int32_t dwdp_route_static(const void* x, int32_t T, int32_t hidden, i
     a.col_bias = logit_bias;
     a.err = err;
     a.bsrc[0] = make_int2(0, 0);
-    e = launch_grouped_gemm(EPI_F32, false, a, n_sms, stream);
+    e = launch_grouped_gemm(EPI_F32, FMT_BF16, a, n_sms, stream);
     if (e == cudaSuccess) e = launch_topk(logits, nullptr, T, n_experts, top_k, out->topk_ids, out->topk_w, stream);
     if (e == cudaSuccess)
         e = launch_group(out->topk_ids, T * top_k, n_experts, out->counts, out->offsets, out->perm, out->inv_perm,

@@ -242,6 +242,101 @@ def make_layer_fp8(shape: LayerShape, placement: Placement, base_seed: int, laye
     return LayerWeightsFp8(shape, placement, wr, bt, lw13, lw2, pw13, pw2, sw13, sw2, s13, s2, ss13, ss2)
 
 
+# ----------------------------------------------------------------- NVFP4 --
+# Synthetic NVFP4 weights are drawn directly as codes: E2M1 magnitude codes
+# 0..7 with these probabilities (a bell-shaped spread over 0 .. 6) and a
+# uniform sign, E4M3 block-scale codes uniform in [0x30, 0x48) (0.5 .. 3.75),
+# and a tensor scale ~ 0.004 * U(0.8, 1.2), which puts the weights' spread
+# near the bf16 layers' 0.02.
+E2M1_CODE_P = (0.10, 0.18, 0.18, 0.15, 0.14, 0.12, 0.08, 0.05)
+
+
+@dataclass
+class LayerWeightsNvfp4(LayerWeights):
+    """As LayerWeights, with NVFP4 pool slots (uint8 [slots][slot bytes]:
+    packed codes then block-scale chunks, as dwdp.h lays them out) and one
+    tensor scale per expert tensor."""
+    w13_scale: np.ndarray | None = None   # [E] float32
+    w2_scale: np.ndarray | None = None    # [E] float32
+    shared_s13: float = 1.0
+    shared_s2: float = 1.0
+
+
+def nvfp4_codes(rows: int, K: int, seed: int, device="cpu") -> tuple:
+    """(codes uint8 [rows][K], one E2M1 code per byte; block scales uint8
+    [rows][K / 16], E4M3 codes) of one synthetic expert tensor."""
+    g = _gen(device, seed)
+    edges = torch.tensor(np.cumsum(E2M1_CODE_P)[:-1], dtype=torch.float32, device=device)
+    mag = torch.bucketize(torch.rand((rows, K), generator=g, device=device), edges).to(torch.uint8)
+    sign = (torch.rand((rows, K), generator=g, device=device) < 0.5).to(torch.uint8) << 3
+    sf = torch.randint(0x30, 0x48, (rows, K // 16), generator=g, device=device, dtype=torch.int32).to(torch.uint8)
+    return mag | sign, sf
+
+
+def pack_nvfp4(codes: torch.Tensor, sf: torch.Tensor) -> torch.Tensor:
+    """One pool slot (uint8, rows * K * 9 / 16 bytes) from math-layout codes
+    [rows][K] and block scales [rows][K / 16]: codes two per byte (element 2i
+    in the low nibble), then the scales in 512-byte chunks per (128-row block
+    rb, 64-element K step ks), row 128 rb + 32 m1 + m0 and block kb of the step
+    at byte 16 m0 + 4 m1 + kb.  rows a multiple of 128, K of 64."""
+    R, K = codes.shape
+    packed = codes[:, 0::2] | (codes[:, 1::2] << 4)
+    chunks = sf.reshape(R // 128, 4, 32, K // 64, 4).permute(0, 3, 2, 1, 4)
+    return torch.cat([packed.reshape(-1), chunks.reshape(-1)])
+
+
+def unpack_nvfp4(slot: torch.Tensor, rows: int, K: int) -> tuple:
+    """Inverse of pack_nvfp4: (codes uint8 [rows][K], block scales uint8
+    [rows][K / 16]) as numpy arrays from one slot's bytes."""
+    b = slot.reshape(-1).to(torch.uint8)
+    n = rows * K // 2
+    packed = b[:n].reshape(rows, K // 2)
+    codes = torch.stack([packed & 15, packed >> 4], dim=2).reshape(rows, K)
+    sf = b[n:n + rows * K // 16].reshape(rows // 128, K // 64, 32, 4, 4).permute(0, 3, 2, 1, 4)
+    return codes.numpy(), sf.reshape(rows, K // 16).numpy()
+
+
+def make_layer_nvfp4(shape: LayerShape, placement: Placement, base_seed: int, layer: int, device="cpu",
+                     router_std: float = 0.02, bias: np.ndarray | None = None) -> LayerWeightsNvfp4:
+    """One MoE layer with NVFP4 expert weights in the pools the placement
+    names.  Codes and scales depend only on (base seed, layer, expert)."""
+    H, I, E = shape.H, shape.I, shape.E
+    u8 = torch.uint8
+    b13, b2 = 2 * I * H * 9 // 16, H * I * 9 // 16
+    wr = randn_bf16((E, H), router_std, seed_for(base_seed, "Wr", layer), device)
+    lw13 = torch.empty((max(1, placement.n_local_slots), b13), dtype=u8, device=device)
+    lw2 = torch.empty((max(1, placement.n_local_slots), b2), dtype=u8, device=device)
+    pw13 = [torch.empty((placement.peer_slots, b13), dtype=u8, device=device) for _ in range(placement.n_peers)]
+    pw2 = [torch.empty((placement.peer_slots, b2), dtype=u8, device=device) for _ in range(placement.n_peers)]
+    for e in range(E):
+        d13, d2 = [], []
+        if placement.local_slot[e] >= 0:
+            d13.append(lw13[placement.local_slot[e]])
+            d2.append(lw2[placement.local_slot[e]])
+        if placement.peer_id[e] >= 0:
+            d13.append(pw13[placement.peer_id[e]][placement.peer_slot[e]])
+            d2.append(pw2[placement.peer_id[e]][placement.peer_slot[e]])
+        p13 = pack_nvfp4(*nvfp4_codes(2 * I, H, seed_for(base_seed, "W13f", layer, e), device))
+        p2 = pack_nvfp4(*nvfp4_codes(H, I, seed_for(base_seed, "W2f", layer, e), device))
+        for d in d13:
+            d.copy_(p13)
+        for d in d2:
+            d.copy_(p2)
+    rng = np.random.Generator(np.random.PCG64(seed_for(base_seed, "nvfp4_scales", layer)))
+    s13 = (0.004 * rng.uniform(0.8, 1.2, E)).astype(np.float32)
+    s2 = (0.004 * rng.uniform(0.8, 1.2, E)).astype(np.float32)
+    sw13 = sw2 = None
+    ss13 = ss2 = 1.0
+    if shape.S:
+        sw13 = pack_nvfp4(*nvfp4_codes(2 * I, H, seed_for(base_seed, "W13fs", layer), device))
+        sw2 = pack_nvfp4(*nvfp4_codes(H, I, seed_for(base_seed, "W2fs", layer), device))
+        ss13, ss2 = float(np.float32(0.004)), float(np.float32(0.0042))
+    bt = None
+    if bias is not None:
+        bt = torch.as_tensor(np.asarray(bias, dtype=np.float32)).to(device)
+    return LayerWeightsNvfp4(shape, placement, wr, bt, lw13, lw2, pw13, pw2, sw13, sw2, s13, s2, ss13, ss2)
+
+
 def make_tokens(T: int, H: int, base_seed: int, step: int = 0, device="cpu") -> torch.Tensor:
     """Activations x ~ N(0, 1) as bf16 [T, H]."""
     return randn_bf16((T, H), 1.0, seed_for(base_seed, "x", step), device)

@@ -39,11 +39,15 @@ def stage_slots(n_experts, local_slot):
 
 
 def plan_prefetch(n_experts, hidden, inter, local_slot, peer_id, peer_slot,
-                  n_peers, chunk_bytes, elem_bytes=2):
+                  n_peers, chunk_bytes, elem_bytes=2, tensor_bytes=None):
+    """tensor_bytes = (bytes of one expert's w13, of its w2) overrides
+    elem_bytes for formats that are not a whole number of bytes per element."""
     if chunk_bytes <= 0:
         raise ValueError("chunk_bytes must be positive")
     b13 = 2 * inter * hidden * elem_bytes
     b2 = hidden * inter * elem_bytes
+    if tensor_bytes is not None:
+        b13, b2 = tensor_bytes
     slot = stage_slots(n_experts, local_slot)
     per_peer = []
     for p in range(n_peers):

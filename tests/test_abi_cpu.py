@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), f"{n} not exported"
     bound = {s[0] for s in B.SIGNATURES}
     assert set(names) == bound, "binding and header disagree"
-    assert B.dwdp_version() == 2
+    assert B.dwdp_version() == 3
 
 
 def _random_map(rng, E, P, redundant=0.0):
@@ -64,9 +64,13 @@ def test_plan_matches_oracle(lib):
         I = 64 * int(rng.integers(1, 3))
         ls, pid, ps = _random_map(rng, E, P, redundant=0.2)
         chunk = int(rng.choice([1000, 4096, 65536, 10 ** 9, int(rng.integers(100, 300000))]))
-        eb = int(rng.choice([1, 2]))
-        got = B.dwdp_plan_prefetch(E, H, I, ls, pid, ps, P, chunk, elem_bytes=eb)
-        want = oracle.plan_prefetch(E, H, I, ls.tolist(), pid.tolist(), ps.tolist(), P, chunk, elem_bytes=eb)
+        dt = int(rng.choice([B.DTYPE_BF16, B.DTYPE_E4M3, B.DTYPE_NVFP4]))
+        got = B.dwdp_plan_prefetch(E, H, I, ls, pid, ps, P, chunk, weight_dtype=dt)
+        # bytes per expert tensor as dwdp.h states them: bf16 2 per element,
+        # E4M3 1, NVFP4 rows * K * 9 / 16 (codes + block scales)
+        tb = {B.DTYPE_BF16: (4 * I * H, 2 * H * I), B.DTYPE_E4M3: (2 * I * H, H * I),
+              B.DTYPE_NVFP4: (2 * I * H * 9 // 16, H * I * 9 // 16)}[dt]
+        want = oracle.plan_prefetch(E, H, I, ls.tolist(), pid.tolist(), ps.tolist(), P, chunk, tensor_bytes=tb)
         assert got == want, f"trial {trial}"
 
 

@@ -1,0 +1,192 @@
+"""The NVFP4 path through the C ABI against the oracle.
+
+* Activation quantization (dwdp_quantize_rows, the kernels the layer uses):
+  codes, E4M3 block scales and row scales bit-exact against the oracle's row
+  quantizer, which takes every decision in binary32 as the kernels do (E4M3
+  rows too).
+* The NVFP4 layer (mirrored mode): expert weights as E2M1 codes with E4M3
+  scales per 16-element block and a tensor scale per expert tensor,
+  activations quantized per row, block-scaled FP4 tcgen05 GEMMs.  x's codes
+  are the same on both sides; a's can differ where a one-ulp difference of
+  bf16 a (fp32 vs fp64 sums) straddles an E2M1 rounding boundary, so the
+  bar admits rare flips (gpu_helpers.assert_close_requantized).
+* The output does not depend on placement (DWDP section 2).
+
+Pool slots are read back into math layout here by plain index arithmetic
+from the layout dwdp.h states for DWDP_DTYPE_NVFP4."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import assert_close_requantized, to_f64
+from moe_expert_grouped_split_gb300 import binding as B
+from moe_expert_grouped_split_gb300 import inputs as I
+from moe_expert_grouped_split_gb300.build import build
+
+pytestmark = pytest.mark.gpu
+
+
+def _u8(t):
+    return t.detach().contiguous().cpu().numpy().view(np.uint8).ravel()
+
+
+def _sf_offsets(rows, K):
+    """Byte of the block scale of (row, 16-element block) in the chunk layout:
+    chunk (row // 128, block // 4) at (rb * K / 64 + ks) * 512, then
+    16 * (row % 32) + 4 * ((row % 128) // 32) + block % 4."""
+    r = np.arange(rows)[:, None]
+    b = np.arange(K // 16)[None, :]
+    return ((r // 128) * (K // 64) + b // 4) * 512 + 16 * (r % 32) + 4 * ((r % 128) // 32) + b % 4
+
+
+def _unpack_codes(packed, rows, K):
+    p = np.asarray(packed, dtype=np.uint8).reshape(rows, K // 2)
+    c = np.empty((rows, K), dtype=np.uint8)
+    c[:, 0::2] = p & 15
+    c[:, 1::2] = p >> 4
+    return c
+
+
+def _unpack_slot(blob, rows, K):
+    """(codes [rows][K], block scales [rows][K/16]) of one NVFP4 pool slot."""
+    blob = np.asarray(blob, dtype=np.uint8)
+    n = rows * K // 2
+    return _unpack_codes(blob[:n], rows, K), blob[n:][_sf_offsets(rows, K)]
+
+
+def _expert(lw, e):
+    pl, H, I_ = lw.placement, lw.shape.H, lw.shape.I
+    if pl.local_slot[e] >= 0:
+        b13, b2 = lw.local_w13[pl.local_slot[e]], lw.local_w2[pl.local_slot[e]]
+    else:
+        b13, b2 = lw.peer_w13[pl.peer_id[e]][pl.peer_slot[e]], lw.peer_w2[pl.peer_id[e]][pl.peer_slot[e]]
+    return _unpack_slot(_u8(b13), 2 * I_, H) + _unpack_slot(_u8(b2), H, I_)
+
+
+def _rows(rng, n, K):
+    v = rng.standard_normal((n, K)).astype(np.float32) * rng.uniform(0.01, 30, size=(n, 1)).astype(np.float32)
+    v[rng.random((n, K)) < 0.01] *= 40                        # outliers
+    v[3] = 0                                                  # an all-zero row
+    v[5, 16:48] = 0                                           # two zero blocks
+    v[7, :16] = -1e-30                                        # a block of negative near-zeros
+    return torch.from_numpy(v).to(torch.bfloat16)
+
+
+def test_quantize_rows_nvfp4_bit_exact():
+    build()
+    rng = np.random.default_rng(21)
+    rows, K = 300, 512
+    x = _rows(rng, rows, K)
+    pad = (rows + 127) // 128 * 128
+    codes = torch.empty(rows * K // 2, dtype=torch.uint8, device="cuda")
+    sf = torch.zeros(pad * K // 16, dtype=torch.uint8, device="cuda")
+    rs = torch.empty(rows, dtype=torch.float32, device="cuda")
+    B.dwdp_quantize_rows(B.DTYPE_NVFP4, x.cuda(), rows, K, codes, sf, rs)
+    torch.cuda.synchronize()
+    got_c = _unpack_codes(_u8(codes), rows, K)
+    got_sf = _u8(sf)[_sf_offsets(rows, K)]
+    got_s = rs.cpu().numpy()
+    o = oracle.default()
+    xf = x.float().numpy()
+    for r in range(rows):
+        c, f, s = o.quantize_row_nvfp4(xf[r])
+        assert np.float32(s) == got_s[r], f"row {r}: scale {got_s[r]} != {s}"
+        assert np.array_equal(f, got_sf[r]), f"row {r}: block scales differ"
+        assert np.array_equal(c, got_c[r]), f"row {r}: codes differ at {np.nonzero(c != got_c[r])[0][:8]}"
+
+
+def test_quantize_rows_e4m3_bit_exact():
+    build()
+    rng = np.random.default_rng(22)
+    rows, K = 130, 256
+    x = _rows(rng, rows, K)
+    codes = torch.empty((rows, K), dtype=torch.uint8, device="cuda")
+    rs = torch.empty(rows, dtype=torch.float32, device="cuda")
+    B.dwdp_quantize_rows(B.DTYPE_E4M3, x.cuda(), rows, K, codes, None, rs)
+    torch.cuda.synchronize()
+    o = oracle.default()
+    xf = x.float().numpy()
+    got_c, got_s = codes.cpu().numpy(), rs.cpu().numpy()
+    for r in range(rows):
+        c, s = o.quantize_row_e4m3(xf[r])
+        assert np.float32(s) == got_s[r] and np.array_equal(c, got_c[r]), f"row {r}"
+
+
+def test_quantize_rows_rejects_bad_arguments():
+    build()
+    x = torch.zeros((4, 96), dtype=torch.bfloat16, device="cuda")
+    c = torch.zeros(4 * 96, dtype=torch.uint8, device="cuda")
+    rs = torch.zeros(4, dtype=torch.float32, device="cuda")
+    with pytest.raises(B.DwdpError):    # K not a multiple of 64
+        B.dwdp_quantize_rows(B.DTYPE_NVFP4, x, 4, 96, c, c, rs)
+    with pytest.raises(B.DwdpError):    # bf16 is not a quantized type
+        B.dwdp_quantize_rows(B.DTYPE_BF16, x, 4, 64, c, c, rs)
+    with pytest.raises(B.DwdpError):    # NVFP4 needs block scales
+        B.dwdp_quantize_rows(B.DTYPE_NVFP4, x, 4, 64, c, None, rs)
+
+
+def _run(shape, placement, seed, tokens=None, router_std=0.02, chunk=1 << 20):
+    build()
+    lw = I.make_layer_nvfp4(shape, placement, seed, 0, device="cuda", router_std=router_std)
+    x = I.make_tokens(shape.T, shape.H, seed).cuda()
+    rt = B.Runtime(shape.H, shape.I, shape.E, shape.k, shape.S, shape.T, 1, max(1, placement.n_remote()),
+                   weight_dtype=B.DTYPE_NVFP4)
+    try:
+        rt.set_layer(0, lw)
+        rb = B.RouteBuffers(shape.T, shape.E, shape.k)
+        out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
+        if placement.n_remote() > 0:
+            rt.prefetch(0, 0, chunk, [torch.cuda.Stream()])
+        rt.route(x, lw.wr, None, rb)
+        rt.moe(0, 0, x, rb, out)
+        torch.cuda.synchronize()
+        assert rt.device_status() == 0
+        o = oracle.default()
+        tok = np.arange(shape.T) if tokens is None else np.asarray(tokens)
+        xs = I.bf16_bits(x)
+        ref = o.route(xs[tok], I.bf16_bits(lw.wr), None, shape.k)
+        ids = rb.topk_ids.cpu().numpy()[tok]
+        same = (ids == ref["ids"]).all(axis=1)
+        sub = np.nonzero(same)[0]
+        used = np.unique(ref["ids"][sub])
+        w = [[None] * shape.E for _ in range(4)]
+        for e in used:
+            for i, a in enumerate(_expert(lw, int(e))):
+                w[i][e] = a
+        shared = None
+        if shape.S:
+            c13, f13 = _unpack_slot(_u8(lw.shared_w13), 2 * shape.I, shape.H)
+            c2, f2 = _unpack_slot(_u8(lw.shared_w2), shape.H, shape.I)
+            shared = (c13, f13, lw.shared_s13, c2, f2, lw.shared_s2)
+        want = o.moe_tokens_nvfp4(xs[tok], sub, ref["ids"], ref["w"], w[0], w[1], lw.w13_scale, w[2], w[3],
+                                  lw.w2_scale, shared=shared, mirrored=True)
+        got = to_f64(out)[tok[sub]]
+        assert_close_requantized(got, want, what=f"NVFP4 layer output T={shape.T} H={shape.H} I={shape.I}")
+        return out.clone(), lw
+    finally:
+        rt.close()
+
+
+def test_nvfp4_small_layer_with_shared_expert():
+    _run(I.LayerShape(T=200, H=256, I=256, E=8, k=2, S=1), I.split_placement(8, 4, 1), seed=0)
+
+
+def test_nvfp4_ragged_several_k_blocks_and_n_tiles():
+    # K = 512 (two 256-element slices), G1 4 n-tiles, G2 2 n-tiles, 16 experts top-4
+    _run(I.LayerShape(T=333, H=512, I=512, E=16, k=4, S=0), I.split_placement(16, 5, 3), seed=1)
+
+
+def test_nvfp4_output_independent_of_placement():
+    shape = I.LayerShape(T=130, H=256, I=256, E=8, k=2, S=1)
+    a, _ = _run(shape, I.split_placement(8, 8, 0), seed=2)
+    b, _ = _run(shape, I.split_placement(8, 0, 2), seed=2)
+    c, _ = _run(shape, I.split_placement(8, 3, 2, redundant=[4, 6]), seed=2)
+    assert torch.equal(a, b) and torch.equal(a, c)
+
+
+def test_nvfp4_r1_layer_sample():
+    # full R1 shapes in the benchmark's launch configuration, 16 sampled tokens
+    shape, pl = I.r1_layer(8192)
+    rng = np.random.default_rng(4)
+    _run(shape, pl, seed=4, tokens=np.sort(rng.choice(8192, 16, replace=False)), chunk=32 << 20)

@@ -47,8 +47,9 @@ def test_stage_bytes_equal_sources(chunk, n_streams):
             assert B.dwdp_stage_layer(rt.ctx, stage) == layer
             e13, e2 = _expected_stage(lws[layer], pl)
             n = e13.shape[0]
-            assert torch.equal(rt.stage_w13[stage][:n], e13)
-            assert torch.equal(rt.stage_w2[stage][:n], e2)
+            # stage slots are raw bytes: compare byte for byte
+            assert torch.equal(rt.stage_w13[stage][:n], e13.view(torch.uint8).reshape(n, -1))
+            assert torch.equal(rt.stage_w2[stage][:n], e2.view(torch.uint8).reshape(n, -1))
     finally:
         rt.close()
 
