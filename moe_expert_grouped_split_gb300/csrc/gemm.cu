@@ -299,8 +299,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// SiLU(g) * u with the fast reciprocal (a few fp32 ulps; the result is
+// rounded to bf16).  For g below about -88, exp(-g) overflows to inf and the
+// reciprocal to 0, the limit of SiLU there.
 __device__ __forceinline__ float silu_mul(float g, float u) {
-    return g / (1.0f + __expf(-g)) * u;
+    return g * __frcp_rn(1.0f + __expf(-g)) * u;
 }
 
 // Store 32 bf16 values (64 bytes) at p (16-byte aligned).
@@ -614,36 +617,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             tc_fence_after();
             const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
 
+            // TMEM loads are issued two chunks (SiLU: two gate + two up chunks)
+            // ahead of one wait, so their latencies overlap
             if (EPI == EPI_SILU) {
                 __nv_bfloat16* D = reinterpret_cast<__nv_bfloat16*>(p.D);
 #pragma unroll 1
-                for (int c = 0; c < BN / 2 / 32; ++c) {
-                    uint32_t gv[32], uv[32];
-                    tmem_ld32(taddr + c * 32, gv);
-                    tmem_ld32(taddr + BN / 2 + c * 32, uv);
-                    tmem_wait_ld();
-                    const int col = n * (BN / 2) + c * 32;
-                    if (valid && col < p.N) {
-                        float o[32];
+                for (int c = 0; c < BN / 2 / 32; c += 2) {
+                    uint32_t gv[2][32], uv[2][32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            o[j] = silu_mul(__uint_as_float(gv[j]) * sc, __uint_as_float(uv[j]) * sc);
-                        store_bf16x32(D + grow * p.ldd + col, o);
+                    for (int h = 0; h < 2; ++h) {
+                        tmem_ld32(taddr + (c + h) * 32, gv[h]);
+                        tmem_ld32(taddr + BN / 2 + (c + h) * 32, uv[h]);
+                    }
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int col = n * (BN / 2) + (c + h) * 32;
+                        if (valid && col < p.N) {
+                            float o[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                o[j] = silu_mul(__uint_as_float(gv[h][j]) * sc, __uint_as_float(uv[h][j]) * sc);
+                            store_bf16x32(D + grow * p.ldd + col, o);
+                        }
                     }
                 }
             } else if (EPI == EPI_BF16) {
                 __nv_bfloat16* D = reinterpret_cast<__nv_bfloat16*>(p.D);
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(taddr + c * 32, v);
-                    tmem_wait_ld();
-                    const int col = n * BN + c * 32;
-                    if (valid && col < p.N) {
-                        float o[32];
+                for (int c = 0; c < BN / 32; c += 4) {
+                    uint32_t v[4][32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(v[j]) * sc;
-                        store_bf16x32(D + grow * p.ldd + col, o);
+                    for (int h = 0; h < 4; ++h) tmem_ld32(taddr + (c + h) * 32, v[h]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const int col = n * BN + (c + h) * 32;
+                        if (valid && col < p.N) {
+                            float o[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(v[h][j]) * sc;
+                            store_bf16x32(D + grow * p.ldd + col, o);
+                        }
                     }
                 }
             } else {
