@@ -92,6 +92,9 @@ def parse(argv=None):
     p.add_argument("--chunk-sweep", default="", help="comma-separated chunk sizes in MB (exposed copy per size)")
     p.add_argument("--merge-copy", action="store_true",
                    help="also time the merge-copy baseline (one contiguous weight buffer per layer)")
+    p.add_argument("--peer-pools", default="device", choices=["device", "host"],
+                   help="where the emulated peers' pools live (host: pinned host memory, copies over the "
+                        "host link, so only their writes use this GPU's HBM)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extras", action="store_true", help="skip compute-only / copy-only / e2e legs")
     return p.parse_args(argv)
@@ -239,7 +242,8 @@ class Workload:
     """n_layers R1-shaped layers with their pools, a Runtime, route buffers
     and per-layer token batches, all resident in HBM."""
 
-    def __init__(self, spec: Spec, chunk_bytes, n_copy_streams, n_layers=2, base_seed=0, wdtype="bf16"):
+    def __init__(self, spec: Spec, chunk_bytes, n_copy_streams, n_layers=2, base_seed=0, wdtype="bf16",
+                 peer_pools="device"):
         import torch
 
         from moe_expert_grouped_split_gb300 import binding as B
@@ -254,6 +258,16 @@ class Workload:
         make = {"bf16": I.make_layer, "fp8": I.make_layer_fp8, "nvfp4": I.make_layer_nvfp4}[wdtype]
         self.layers = [make(sh, self.placement, base_seed, l, device="cuda", router_std=spec.router_std,
                             bias=spec.bias) for l in range(n_layers)]
+        self.peer_pools = peer_pools
+        if peer_pools == "host":
+            # generated on the GPU, then moved to pinned host memory
+            for lw in self.layers:
+                for pools in (lw.peer_w13, lw.peer_w2):
+                    for i, t in enumerate(pools):
+                        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                        h.copy_(t)
+                        pools[i] = h
+            torch.cuda.empty_cache()
         self.rt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, n_layers, self.placement.n_remote(),
                             weight_dtype={"bf16": B.DTYPE_BF16, "fp8": B.DTYPE_E4M3, "nvfp4": B.DTYPE_NVFP4}[wdtype])
         for l, lw in enumerate(self.layers):
@@ -433,7 +447,7 @@ def run_layer_bench(args, world, local_rank, barrier):
     import torch
     torch.cuda.set_device(local_rank)
     spec = WORKLOADS[args.workload]()
-    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, wdtype=args.dtype)
+    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, wdtype=args.dtype, peer_pools=args.peer_pools)
     sh = wl.shape
     K, W = args.steps, args.warmup
     phases = [_events(torch, 7) for _ in range(K)]
@@ -778,6 +792,7 @@ def main():
                    "shared": sh.S, "local_experts": int((wl.placement.local_slot >= 0).sum()),
                    "remote_experts": wl.placement.n_remote(), "peer_pools": wl.placement.n_peers,
                    "chunk_mb": args.chunk_mb, "copy_streams": args.copy_streams, "expert_weights": args.dtype,
+                   "peer_pool_memory": args.peer_pools,
                    "layers": wl.n_layers,
                    "l2": "inputs larger than L2 (22.6 GB of expert weights + 16.9 GB of copies per layer)",
                    "parallelism": "replicas" if world > 1 else "single rank"},

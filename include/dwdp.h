@@ -179,7 +179,9 @@ size_t dwdp_workspace_bytes(const dwdp_ctx* ctx, int32_t T);
  *   otherwise peer_id[e] in [0, n_peers) and peer_slot[e] name its copy in
  *   peers[peer_id[e]], and it is staged by dwdp_prefetch_layer.
  * local_slot, peer_id, peer_slot are host arrays [E]; local and peers are host
- * structs describing device buffers.  shared_w13 [2I][H] / shared_w2 [H][I]
+ * structs describing device buffers (a peer pool may instead be pinned host
+ * memory: its slices then cross the host link, and only their writes land in
+ * this GPU's memory).  shared_w13 [2I][H] / shared_w2 [H][I]
  * (device) are the layer's shared expert, required iff n_shared == 1.  The
  * non-resident experts take stage slots 0, 1, ... in ascending id, at most
  * stage_slots of them.  Replaces any earlier map of the layer (the caller
@@ -214,7 +216,7 @@ int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router
 /* Pull layer `layer`'s non-resident experts from their peer pools into stage
  * buffer `stage` ([DWDP] §2: asynchronous prefetch of layer l+1 during layer
  * l, double-buffered; §4.3.2: fixed-size slices, round-robin over sources).
- * Each slice is one device-to-device memcpy node (copy engine, no SMs) of at
+ * Each slice is one memcpy node (copy engine, no SMs) of at
  * most chunk_bytes in a CUDA graph that the context builds on first use for
  * this (chunk_bytes, stage, n_copy_streams) and keeps until the layer's map
  * is replaced; slices from peer p form chain p % n_copy_streams of the graph

@@ -576,7 +576,7 @@ int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t 
             cudaGraphNode_t& t = tail[sl.peer % n_copy_streams];
             cudaGraphNode_t node;
             e = cudaGraphAddMemcpyNode1D(&node, g, t ? &t : nullptr, t ? 1 : 0, dst_base[sl.tensor] + sl.dst_offset,
-                                         src, (size_t)sl.nbytes, cudaMemcpyDeviceToDevice);
+                                         src, (size_t)sl.nbytes, cudaMemcpyDefault);
             if (e != cudaSuccess) break;
             t = node;
         }

@@ -177,6 +177,18 @@ def test_nvfp4_ragged_several_k_blocks_and_n_tiles():
     _run(I.LayerShape(T=333, H=512, I=512, E=16, k=4, S=0), I.split_placement(16, 5, 3), seed=1)
 
 
+def test_nvfp4_single_token_and_k_equals_e():
+    _run(I.LayerShape(T=1, H=256, I=256, E=4, k=2, S=1), I.split_placement(4, 2, 1), seed=5)
+    _run(I.LayerShape(T=70, H=256, I=256, E=4, k=4, S=0), I.split_placement(4, 1, 2), seed=6)
+
+
+def test_nvfp4_all_local_and_all_remote():
+    shape = I.LayerShape(T=129, H=256, I=512, E=8, k=2, S=1)
+    a, _ = _run(shape, I.split_placement(8, 8, 0), seed=7)
+    b, _ = _run(shape, I.split_placement(8, 0, 3), seed=7)
+    assert torch.equal(a, b)
+
+
 def test_nvfp4_output_independent_of_placement():
     shape = I.LayerShape(T=130, H=256, I=256, E=8, k=2, S=1)
     a, _ = _run(shape, I.split_placement(8, 8, 0), seed=2)

@@ -1,8 +1,8 @@
 """dwdp_prefetch_layer (DWDP §2 double-buffered prefetch, §4.3.2 round-robin
 slices): staged bytes equal their sources exactly, stage/layer bookkeeping
-is enforced, and the host-side bounded wait reports a timeout without
-faulting or hanging anything (the copy stream is held back by a short GPU
-sleep, then released)."""
+is enforced (device and pinned-host peer pools), and the host-side bounded
+wait reports a timeout without faulting or hanging anything (the copy stream
+is held back by a short GPU sleep, then released)."""
 import numpy as np
 import pytest
 import torch
@@ -52,6 +52,44 @@ def test_stage_bytes_equal_sources(chunk, n_streams):
             assert torch.equal(rt.stage_w2[stage][:n], e2.view(torch.uint8).reshape(n, -1))
     finally:
         rt.close()
+
+
+def test_stage_from_pinned_host_pools():
+    """Peer pools in pinned host memory: the slices cross the host link and
+    the staged bytes still equal their sources; the layer output is the same
+    as with device pools."""
+    build()
+    shape = I.LayerShape(T=64, H=256, I=128, E=12, k=2, S=1)
+    pl = I.split_placement(12, 3, 3)
+    lw = I.make_layer(shape, pl, 6, 0, device="cuda")
+    x = I.make_tokens(shape.T, shape.H, 1).cuda()
+    outs = []
+    for where in ("device", "host"):
+        if where == "host":
+            for pools in (lw.peer_w13, lw.peer_w2):
+                for i, t in enumerate(pools):
+                    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    h.copy_(t)
+                    pools[i] = h
+        rt = B.Runtime(shape.H, shape.I, shape.E, shape.k, shape.S, shape.T, 1, pl.n_remote())
+        try:
+            rt.set_layer(0, lw)
+            rt.prefetch(0, 0, 40_000, [torch.cuda.Stream()])
+            assert rt.wait_stage(0, 20_000) == 0
+            e13, e2 = _expected_stage(lw, pl)
+            n = e13.shape[0]
+            assert torch.equal(rt.stage_w13[0][:n].cpu(), e13.cpu().view(torch.uint8).reshape(n, -1))
+            assert torch.equal(rt.stage_w2[0][:n].cpu(), e2.cpu().view(torch.uint8).reshape(n, -1))
+            rb = B.RouteBuffers(shape.T, shape.E, shape.k)
+            out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
+            rt.route(x, lw.wr, None, rb)
+            rt.moe(0, 0, x, rb, out)
+            torch.cuda.synchronize()
+            assert rt.device_status() == 0
+            outs.append(out.clone())
+        finally:
+            rt.close()
+    assert torch.equal(outs[0], outs[1])
 
 
 def test_stage_must_hold_the_layer():
