@@ -739,9 +739,19 @@ def cpu_baseline_sample(wl, target_s=15.0, max_tokens=512):
     if n2 > n:
         dt = run(order[:n2])
         n = n2
-    return {"value": round(n / dt, 3), "unit": UNIT, "cores": o.num_threads(), "kind": "oracle",
+    cores = o.num_threads()
+    # the same oracle on one thread, on one or two of the sampled tokens
+    o.set_num_threads(1)
+    try:
+        n1 = 2 if per_tok * cores < 2.0 else 1
+        dt1 = run(order[:n1])
+    finally:
+        o.set_num_threads(cores)
+    return {"value": round(n / dt, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "value_1thread": round(n1 / dt1, 3),
             "sample": f"{n} seeded tokens of the {sh.T}-token R1-shaped layer (routing + {sh.k} routed experts"
-                      f"{' + shared expert' if sh.S else ''} per token, fp64, {dt:.1f} s)"}
+                      f"{' + shared expert' if sh.S else ''} per token, fp64, {dt:.1f} s; one thread: {n1} "
+                      f"tokens, {dt1:.1f} s)"}
 
 
 def main():
