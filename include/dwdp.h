@@ -236,7 +236,10 @@ int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t 
  * Each expert's weights come from the local pool or from stage `stage`, per
  * the layer's map; the stream first waits for that stage's "ready" event when
  * the layer has non-resident experts (per-layer arrival, [DWDP] §2).  route
- * holds dwdp_route's outputs for the same x.  out [T][H] bf16 (device).
+ * holds dwdp_route's outputs for the same x (offsets, inv_perm and topk_w are
+ * read; NVFP4 contexts also read topk_ids).  In E4M3 and NVFP4 contexts x
+ * and a are quantized per row first (see DWDP_DTYPE_*) and the GEMMs run on
+ * the codes.  out [T][H] bf16 (device).
  * Errors: INVALID_ARG, NOT_MAPPED, UNSUPPORTED, CUDA. */
 int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* x, int32_t T,
                        const dwdp_route_out* route, void* out, void* ws, size_t ws_bytes,
@@ -272,7 +275,7 @@ int32_t dwdp_device_status(dwdp_ctx* ctx);
  * caller-owned cudaEvent_t (or NULL to stop).  While set, dwdp_route records
  * events[0] at its start and events[1] at its end on its stream, and
  * dwdp_moe_layer records events[2] after waiting for its stage, events[3]
- * after the gather, events[4] after the gate/up GEMM, events[5] after the
+ * after x is in expert order (E4M3 / NVFP4: quantized), events[4] after the gate/up GEMM, events[5] after the
  * down GEMM and events[6] after the combine.  The context keeps the pointers
  * until the next call; the caller keeps the events alive.  Errors:
  * INVALID_ARG. */

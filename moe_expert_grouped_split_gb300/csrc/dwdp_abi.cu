@@ -645,7 +645,7 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
                                                route->offsets, (int)E, S > 0, xq, sx, xp, sxp, sfx, L.sf_tiles,
                                                ctx->d_err, stream));
     } else if (fmt == FMT_E4M3) {
-        // x rows to E4M3 (per-token scales), then gathered into expert order
+        // x rows to E4M3 (per-token scales), then copied into expert order
         DWDP_CUDA(ctx, launch_quantize_rows(x, T, (int)H, xq, sx, stream));
         DWDP_CUDA(ctx, launch_gather_fp8(xq, sx, (int)H, route->inv_perm, (int)T, (int)k, xp, sxp, stream));
     } else {

@@ -1,7 +1,8 @@
 // dwdp_internal.h: declarations shared by the translation units of libdwdp.so.
 //
 // Kernels live in gemm.cu (split-pointer grouped GEMM, tcgen05 + TMA) and
-// route.cu (top-k, grouping, gather, combine); dwdp_abi.cu is the C ABI.
+// route.cu (top-k, grouping, row scatter into expert order, combine, and the
+// E4M3 / NVFP4 activation quantizers); dwdp_abi.cu is the C ABI.
 #pragma once
 
 #include <cuda.h>  // CUtensorMap (type only; the driver is reached through an entry point)
@@ -115,8 +116,9 @@ bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t row
 // Sets the text dwdp_last_error(NULL) returns on this thread (dwdp_abi.cu).
 void set_last_error(const char* msg);
 
-size_t gemm_smem_bytes(int n_groups);
-// fp8: both operands are E4M3 codes (K counted in elements = bytes).
+// One grouped GEMM launch (gemm.cu) as 2-CTA clusters, one persistent CTA per
+// SM.  fmt: both operands bf16, both E4M3 codes, or both NVFP4 codes with
+// block scales (GemmArgs::sfa / bsf); K counts elements.  EPI_F32 is bf16 only.
 cudaError_t launch_grouped_gemm(int epi, int fmt, const GemmArgs& args, int n_sms, cudaStream_t stream);
 
 // route.cu

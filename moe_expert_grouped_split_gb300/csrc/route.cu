@@ -1,6 +1,7 @@
-// route.cu: routing, grouping, gather and combine kernels of the DWDP MoE
-// block (memory- and latency-bound; coalesced 16-byte accesses, warp-level
-// top-k, no atomics on any ordered output so every index is deterministic).
+// route.cu: routing, grouping, scatter into expert order, combine and the
+// activation quantizers (E4M3, NVFP4) of the DWDP MoE block (memory- and
+// latency-bound; coalesced 16-byte accesses, warp-level top-k, no atomics on
+// any ordered output so every index is deterministic).
 //
 // The pages do not print the router; these kernels implement the reading the
 // library documents in dwdp.h: fp32 logits, the k largest (ties to the lower
