@@ -275,8 +275,9 @@ int32_t dwdp_device_status(dwdp_ctx* ctx);
  * caller-owned cudaEvent_t (or NULL to stop).  While set, dwdp_route records
  * events[0] at its start and events[1] at its end on its stream, and
  * dwdp_moe_layer records events[2] after waiting for its stage, events[3]
- * after x is in expert order (E4M3 / NVFP4: quantized), events[4] after the gate/up GEMM, events[5] after the
- * down GEMM and events[6] after the combine.  The context keeps the pointers
+ * once x is in expert order (E4M3 / NVFP4: quantized), events[4] after the
+ * gate/up GEMM, events[5] after the down GEMM and events[6] after the
+ * combine.  The context keeps the pointers
  * until the next call; the caller keeps the events alive.  Errors:
  * INVALID_ARG. */
 #define DWDP_PHASE_EVENTS 7
