@@ -617,6 +617,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             tc_fence_after();
             const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
 
+            if constexpr (F::kAccBufs == 1 && EPI == EPI_BF16) {
+                // One accumulator (NVFP4): the next tile's MMAs wait for it, so
+                // the row's 256 results go to registers as packed bf16 first,
+                // the accumulator is released, and the stores follow.  (The
+                // SiLU epilogue keeps the interleaved path below: fully unrolled
+                // it ran slower.)
+                uint32_t packed[BN / 2];
+#pragma unroll
+                for (int c = 0; c < BN / 32; c += 2) {
+                    uint32_t v[2][32];
+                    tmem_ld32(taddr + c * 32, v[0]);
+                    tmem_ld32(taddr + (c + 1) * 32, v[1]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2)
+                            packed[(c + h) * 16 + j / 2] =
+                                pack_bf16(__uint_as_float(v[h][j]) * sc, __uint_as_float(v[h][j + 1]) * sc);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
+                __nv_bfloat16* D = reinterpret_cast<__nv_bfloat16*>(p.D);
+                const int col0 = n * BN;
+                if (valid) {
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        if (col0 + c * 32 >= p.N) break;
+                        uint4* q = reinterpret_cast<uint4*>(D + grow * p.ldd + col0 + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            q[i] = make_uint4(packed[c * 16 + 4 * i], packed[c * 16 + 4 * i + 1],
+                                              packed[c * 16 + 4 * i + 2], packed[c * 16 + 4 * i + 3]);
+                    }
+                }
+                if (++acc == F::kAccBufs) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+                continue;
+            }
             // TMEM loads are issued two chunks (SiLU: two gate + two up chunks)
             // ahead of one wait, so their latencies overlap
             if (EPI == EPI_SILU) {
