@@ -73,8 +73,9 @@ struct LayerMap {
 
 namespace dwdp {
 
-// Rows x K matrix, row-major: a 2-D map with a [128 rows x 128 bytes] box,
-// 128-byte swizzle (the canonical K-major layout the MMA descriptors expect).
+// Rows x K matrix, row-major: a 2-D map with a [128 rows x BK_BYTES] box and
+// the swizzle of that width (the canonical K-major layout the MMA
+// descriptors expect).
 // E4M3 and NVFP4 codes are mapped as bytes.
 bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, int fmt) {
     EncodeTiledFn fn = encode_fn();
@@ -86,11 +87,11 @@ bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, in
     cuuint32_t box[2] = {(cuuint32_t)(bytes ? BK_BYTES : BK_BYTES / 2), BM};
     cuuint32_t es[2] = {1, 1};
     return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, BK_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// A weight buffer [slots][rows][K]: a 3-D map, box [1 x 128 rows x 128 bytes];
+// A weight buffer [slots][rows][K]: a 3-D map, box [1 x 128 rows x BK_BYTES];
 // slots are weight_slot_bytes apart (NVFP4: the codes of each slot, whose
 // block scales follow them).
 bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t rows, uint64_t K, int fmt) {
@@ -103,7 +104,7 @@ bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t row
     cuuint32_t box[3] = {(cuuint32_t)(bytes ? BK_BYTES : BK_BYTES / 2), BN / 2, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, BK_BYTES == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -21,16 +21,20 @@ enum Epilogue : int { EPI_BF16 = 0, EPI_SILU = 1, EPI_F32 = 2 };
 enum OperandFormat : int { FMT_BF16 = DWDP_DTYPE_BF16, FMT_E4M3 = DWDP_DTYPE_E4M3, FMT_NVFP4 = DWDP_DTYPE_NVFP4 };
 
 // Tile shape of the grouped GEMM: one CTA computes a 128 x 256 fp32
-// accumulator in tensor memory from K slices of 128 bytes per row staged by
-// TMA (64 bf16, 128 E4M3 or 256 NVFP4 elements).
+// accumulator in tensor memory from K slices of BK_BYTES bytes per row staged
+// by TMA (128 bytes: 64 bf16, 128 E4M3 or 256 NVFP4 elements, 128-byte
+// swizzle, 4 stages; 64 bytes: half of that, 64-byte swizzle, 8 stages).
+#ifndef DWDP_SLICE_BYTES
+#define DWDP_SLICE_BYTES 128
+#endif
 constexpr int BM = 128;
 constexpr int BN = 256;
-constexpr int BK = 64;        // bf16 elements per K slice (128 bytes)
-constexpr int BK_BYTES = 128;
-constexpr int kStages = 4;
-constexpr int kABytes = BM * BK * 2;           // 16 KiB
-constexpr int kBBytes = BN * BK * 2;           // 32 KiB
-constexpr int kStageBytes = kABytes + kBBytes;  // 48 KiB
+constexpr int BK_BYTES = DWDP_SLICE_BYTES;
+constexpr int BK = BK_BYTES / 2;                // bf16 elements per K slice
+constexpr int kStages = 512 / BK_BYTES;         // 192 KiB of A + B stages either way
+constexpr int kABytes = BM * BK_BYTES;
+constexpr int kBBytes = BN * BK_BYTES;
+constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kGemmThreads = 192;              // producer, MMA, 4 epilogue warps
 constexpr int kClusterCtas = 2;                // CTAs per cluster (co-scheduled on one GPC)
 
@@ -42,8 +46,9 @@ constexpr int kClusterCtas = 2;                // CTAs per cluster (co-scheduled
 // An activation operand's chunks are indexed by the GEMM's A tile instead
 // of rb (see GemmArgs::sfa).
 constexpr int kSfChunkBytes = 512;
-constexpr int kSfStageBytesA = 4 * kSfChunkBytes;        // 128 rows x 256 elements
-constexpr int kSfStageBytesB = 2 * kSfStageBytesA;       // 256 rows x 256 elements
+constexpr int kSfStepsPerSlice = BK_BYTES / 32;          // 64-element K steps per K slice
+constexpr int kSfStageBytesA = kSfStepsPerSlice * kSfChunkBytes;  // 128 rows x one K slice
+constexpr int kSfStageBytesB = 2 * kSfStageBytesA;                // 256 rows x one K slice
 
 // Bytes of one [rows][K] weight tensor (one pool slot) in format fmt:
 // bf16 2 per element, E4M3 1, NVFP4 half a byte of code plus 1/16 byte of
@@ -105,9 +110,9 @@ struct GemmArgs {
     float gscale[kMaxGroups];
 };
 
-// TMA tensor maps (dwdp_abi.cu): a rows x K matrix (box 128 rows x 128 B)
-// and a weight buffer [slots][rows][K] (box 1 x 128 rows x 128 B), both
-// 128 B swizzle.  K counts elements of format fmt (bf16, E4M3 codes or
+// TMA tensor maps (dwdp_abi.cu): a rows x K matrix (box 128 rows x BK_BYTES)
+// and a weight buffer [slots][rows][K] (box 1 x 128 rows x BK_BYTES), both
+// swizzled to BK_BYTES.  K counts elements of format fmt (bf16, E4M3 codes or
 // NVFP4 codes, two per byte); a weight slot is weight_slot_bytes apart.
 bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t K, int fmt = FMT_BF16);
 bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t rows, uint64_t K,

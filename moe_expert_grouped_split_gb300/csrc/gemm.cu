@@ -48,14 +48,15 @@ constexpr uint32_t kIdescNvfp4 = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) <
 // flight: per stage 4 K steps x (4 columns of A scales + 8 of B scales).
 template <int FMT>
 struct Fmt {
-    static constexpr int kKElems = FMT == FMT_NVFP4 ? 256 : FMT == FMT_E4M3 ? 128 : 64;  // K per 128-byte slice
-    static constexpr int kXPerSlice = FMT == FMT_BF16 ? 64 : 128;  // tensor-map x units (bf16 or bytes) per slice
+    static constexpr int kKElems = FMT == FMT_NVFP4 ? 2 * BK_BYTES : FMT == FMT_E4M3 ? BK_BYTES : BK;  // K per slice
+    static constexpr int kXPerSlice = FMT == FMT_BF16 ? BK : BK_BYTES;  // tensor-map x units (bf16 or bytes) per slice
     static constexpr int kSfBytes = FMT == FMT_NVFP4 ? kSfStageBytesA + kSfStageBytesB : 0;
     static constexpr int kStageTx = kStageBytes + kSfBytes;
     static constexpr int kAccBufs = FMT == FMT_NVFP4 ? 1 : 2;
 };
-constexpr int kSfCol0 = BN;            // NVFP4: first TMEM column of the scale ring
-constexpr int kSfColsPerStage = 48;    // 4 K steps x (4 + 8) columns
+constexpr int kSfCol0 = BN;                             // NVFP4: first TMEM column of the scale ring
+constexpr int kSfColsPerStage = 12 * kSfStepsPerSlice;  // per K step: 4 columns of A scales, 8 of B
+static_assert(kSfCol0 + kStages * kSfColsPerStage <= 512, "NVFP4 scale ring must fit in TMEM");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -190,16 +191,17 @@ __device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
-// with 128-byte swizzle: rows of 128 B, 8-row atoms 1024 B apart (stride
-// byte offset), start address >> 4 in bits 0-13, leading byte offset unused
-// for this layout (1), descriptor version 1 at bits 46-47, swizzle mode 2
-// (128 B) at bits 61-63.  The tile base is 1024-byte aligned.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+// with the swizzle that matches the slice width: rows of BK_BYTES bytes,
+// 8-row atoms 8 * BK_BYTES apart (stride byte offset), start address >> 4 in
+// bits 0-13, leading byte offset unused for these layouts (1), descriptor
+// version 1 at bits 46-47, swizzle mode at bits 61-63 (2 = 128-byte, 4 =
+// 64-byte).  The tile base is 1024-byte aligned.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
     uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
     d |= (uint64_t)1 << 16;
-    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)((8 * BK_BYTES) >> 4) << 32;
     d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
+    d |= (uint64_t)(BK_BYTES == 128 ? 2 : 4) << 61;
     return d;
 }
 
@@ -485,17 +487,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                         // of B's two 128-row halves (multicast like the halves)
                         const uint32_t ss = sbase + SL::kSF + stage * F::kSfBytes;
                         const int64_t KS = p.K / 64;
-                        bulk_load(ss, p.sfa + (atile * KS + kb * 4) * kSfChunkBytes, kSfStageBytesA, fb);
+                        bulk_load(ss, p.sfa + (atile * KS + kb * kSfStepsPerSlice) * kSfChunkBytes, kSfStageBytesA, fb);
                         const uint8_t* bs = p.bsf[src.x] + (int64_t)src.y * p.b_slot_bytes;
                         if (share) {
                             const int64_t rb = (crank ? b_row1 : b_row0) / BM;
-                            bulk_load_mc(ss + kSfStageBytesA * (1 + crank), bs + (rb * KS + kb * 4) * kSfChunkBytes,
+                            bulk_load_mc(ss + kSfStageBytesA * (1 + crank), bs + (rb * KS + kb * kSfStepsPerSlice) * kSfChunkBytes,
                                          kSfStageBytesA, fb, (uint16_t)0x3);
                         } else {
-                            bulk_load(ss + kSfStageBytesA, bs + ((int64_t)(b_row0 / BM) * KS + kb * 4) * kSfChunkBytes,
+                            bulk_load(ss + kSfStageBytesA, bs + ((int64_t)(b_row0 / BM) * KS + kb * kSfStepsPerSlice) * kSfChunkBytes,
                                       kSfStageBytesA, fb);
                             bulk_load(ss + 2 * kSfStageBytesA,
-                                      bs + ((int64_t)(b_row1 / BM) * KS + kb * 4) * kSfChunkBytes, kSfStageBytesA, fb);
+                                      bs + ((int64_t)(b_row1 / BM) * KS + kb * kSfStepsPerSlice) * kSfChunkBytes, kSfStageBytesA, fb);
                         }
                     }
                     pend[stage] = (int)phase;
@@ -533,24 +535,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = sw128_desc(sbase + SL::kA + stage * kABytes);
-                    const uint64_t bd = sw128_desc(sbase + SL::kB + stage * kBBytes);
+                    const uint64_t ad = smem_desc(sbase + SL::kA + stage * kABytes);
+                    const uint64_t bd = smem_desc(sbase + SL::kB + stage * kBBytes);
                     if constexpr (FMT == FMT_NVFP4) {
                         // block scales of this stage into its TMEM columns (the MMAs
                         // that last read those columns finished before the stage was
                         // refilled), then 4 block-scaled MMAs of 64 elements each
                         const uint32_t ss = sbase + SL::kSF + stage * F::kSfBytes;
                         const uint32_t tc = tmem_base + (uint32_t)(kSfCol0 + stage * kSfColsPerStage);
+                        constexpr int kBCol = 4 * kSfStepsPerSlice;  // B scales follow A's columns
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
+                        for (int j = 0; j < kSfStepsPerSlice; ++j) {
                             tc_cp_sf(tc + 4 * j, sf_chunk_desc(ss + j * kSfChunkBytes));
-                            tc_cp_sf(tc + 16 + 8 * j, sf_chunk_desc(ss + kSfStageBytesA + j * kSfChunkBytes));
-                            tc_cp_sf(tc + 20 + 8 * j, sf_chunk_desc(ss + 2 * kSfStageBytesA + j * kSfChunkBytes));
+                            tc_cp_sf(tc + kBCol + 8 * j, sf_chunk_desc(ss + kSfStageBytesA + j * kSfChunkBytes));
+                            tc_cp_sf(tc + kBCol + 4 + 8 * j,
+                                     sf_chunk_desc(ss + 2 * kSfStageBytesA + j * kSfChunkBytes));
                         }
 #pragma unroll
                         for (int kk = 0; kk < BK_BYTES / 32; ++kk)
                             tc_mma<FMT>(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk),
-                                        (kb > 0 || kk > 0) ? 1u : 0u, tc + 4 * kk, tc + 16 + 8 * kk);
+                                        (kb > 0 || kk > 0) ? 1u : 0u, tc + 4 * kk, tc + kBCol + 8 * kk);
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < BK_BYTES / 32; ++kk) {
