@@ -132,6 +132,15 @@ def step_bytes(T, H, I, E_active, k, S, R, wb=2):
     return int(b)
 
 
+def kernels_per_layer(wdtype: str) -> int:
+    """This library's kernel launches per layer step: route = router GEMM,
+    top-k and the three grouping kernels; the layer = (quantizers,) scatter
+    into expert order (fused into the NVFP4 x quantizer), the two GEMMs and
+    the combine.  (The ncu launch lists in profiles/ show the same counts.)"""
+    layer = {"bf16": 4, "fp8": 6, "nvfp4": 5}[wdtype]
+    return 5 + layer
+
+
 # Bytes per weight (and quantized activation) element: NVFP4 is half a byte
 # of E2M1 code plus one E4M3 scale per 16 elements.
 WEIGHT_BYTES = {"bf16": 2, "fp8": 1, "nvfp4": 9 / 16}
@@ -815,7 +824,7 @@ def main():
         line["config"]["attention_standin"] = "bf16 GEMM T x 7168 x 7168 after every MoE layer"
         line["config"]["expert_weights"] = args.dtype
         line["tflops"] = round(flops / (res["ms_step"] / 1e3) / 1e12, 1)
-        line["gpu_launches"] = args.steps * 4 * 9
+        line["gpu_launches"] = args.steps * 4 * kernels_per_layer(args.dtype)
     else:
         flops_layer = layer_flops(sh.T, sh.H, sh.I, sh.E, sh.k, sh.S)
         g1 = g1_flops(sh.T, sh.H, sh.I, sh.k, sh.S)
@@ -847,7 +856,7 @@ def main():
                          "algorithmic_bytes_per_step": sb, "peak_source": f"{src} hbm_gbs"},
             "host_issue_ms_per_prefetch": res["issue_ms"],
             "merge_copy_baseline": res.get("merge_copy"),
-            "gpu_launches": 8 * args.steps,
+            "gpu_launches": kernels_per_layer(args.dtype) * args.steps,
         })
         if "chunk_sweep" in res:
             line["chunk_sweep"] = res["chunk_sweep"]
