@@ -35,8 +35,8 @@ def _run(dtype, shape, pl, lws, xs, overlapped, chunk):
             rt.set_layer(l, lw)
         compute = torch.cuda.Stream()
         copy = [torch.cuda.Stream()]
-        rbs = [B.RouteBuffers(shape.T, shape.E, shape.k) for _ in range(N_LAYERS)]
-        outs = [torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda") for _ in range(N_LAYERS)]
+        rbs = [B.RouteBuffers(x.shape[0], shape.E, shape.k) for x in xs]
+        outs = [torch.empty((x.shape[0], shape.H), dtype=torch.bfloat16, device="cuda") for x in xs]
         rt.prefetch(0, 0, chunk, copy)
         for l in range(N_LAYERS):
             s = l % 2
@@ -58,12 +58,16 @@ def _run(dtype, shape, pl, lws, xs, overlapped, chunk):
 
 
 @pytest.mark.parametrize("dtype", [B.DTYPE_BF16, B.DTYPE_NVFP4], ids=["bf16", "nvfp4"])
-def test_overlapped_layers_equal_serialised(dtype):
+@pytest.mark.parametrize("ragged", [False, True], ids=["fixed_T", "ragged_T"])
+def test_overlapped_layers_equal_serialised(dtype, ragged):
+    """ragged: each layer gets its own token count (one workspace sized for
+    the largest), as in the benchmark's 4-layer pipeline."""
     build()
     shape = I.LayerShape(T=300, H=512, I=256, E=12, k=2, S=1)
     pl = I.split_placement(12, 4, 2)
     lws = _layers(dtype, shape, pl)
-    xs = [I.make_tokens(shape.T, shape.H, 3, step=l).cuda() for l in range(N_LAYERS)]
+    Ts = [300, 257, 129, 1] if ragged else [shape.T] * N_LAYERS
+    xs = [I.make_tokens(Ts[l], shape.H, 3, step=l).cuda() for l in range(N_LAYERS)]
     ser, _ = _run(dtype, shape, pl, lws, xs, overlapped=False, chunk=1 << 20)
     for chunk in (50_000, 1 << 20):
         ovl, _ = _run(dtype, shape, pl, lws, xs, overlapped=True, chunk=chunk)
