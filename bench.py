@@ -49,18 +49,23 @@ Spec = namedtuple("Spec", "shape placement router_std bias")
 
 
 def _r1(T, zipf=False, router_std=0.02):
-    def make():
+    def make(group=4):
+        """group: DWDP group size N: E / N experts resident, the rest spread
+        over the N - 1 peers (N = 4: 64 local + 3 x 64, the default)."""
         from moe_expert_grouped_split_gb300 import inputs as I
-        shape, placement = I.r1_layer(T)
+        shape, _ = I.r1_layer(T)
+        n_local = shape.E // group
         bias = None
+        redundant = ()
         if zipf:
             bias = I.zipf_bias(shape.E, 1.2, I.seed_for(0, "zipf"))
-            placement = I.split_placement(shape.E, 64, 3, redundant=I.hottest_experts(bias, 16))
+            redundant = I.hottest_experts(bias, 16)
+        placement = I.split_placement(shape.E, n_local, group - 1, redundant=redundant)
         return Spec(shape, placement, router_std, bias)
     return make
 
 
-def _r1_small():
+def _r1_small(group=4):
     """R1 layer widths (H=7168, I=2048) with 16 routed experts, top-4, one
     shared expert and 1024 tokens (256 rows per expert, as at 8K tokens with
     256 experts and top-8): a few GB, for profiler captures."""
@@ -86,6 +91,8 @@ def parse(argv=None):
     p.add_argument("--workload", default="r1_moe_layer_8k", choices=sorted(WORKLOADS))
     p.add_argument("--chunk-mb", type=float, default=32.0)
     p.add_argument("--copy-streams", type=int, default=1)
+    p.add_argument("--group", type=int, default=4,
+                   help="DWDP group size N: E/N experts resident, the rest staged from N-1 peer pools")
     p.add_argument("--dtype", default="bf16", choices=["bf16", "fp8", "nvfp4"],
                    help="expert weight type (fp8: E4M3 weights and activations; nvfp4: E2M1 codes with E4M3 "
                         "scales per 16-element block; next-row variants)")
@@ -455,7 +462,7 @@ def run_layer_bench(args, world, local_rank, barrier):
     """The single-layer workloads (8K default, Zipf 16K, 256 tokens)."""
     import torch
     torch.cuda.set_device(local_rank)
-    spec = WORKLOADS[args.workload]()
+    spec = WORKLOADS[args.workload](group=args.group)
     wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, wdtype=args.dtype, peer_pools=args.peer_pools)
     sh = wl.shape
     K, W = args.steps, args.warmup
@@ -606,7 +613,7 @@ def run_pipeline_bench(args, world, local_rank, barrier):
     from moe_expert_grouped_split_gb300 import inputs as I
 
     torch.cuda.set_device(local_rank)
-    spec = WORKLOADS[args.workload]()
+    spec = WORKLOADS[args.workload](group=args.group)
     wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, n_layers=4, wdtype=args.dtype)
     sh = wl.shape
     steps = args.steps
@@ -813,7 +820,10 @@ def main():
                    "chunk_mb": args.chunk_mb, "copy_streams": args.copy_streams, "expert_weights": args.dtype,
                    "peer_pool_memory": args.peer_pools,
                    "layers": wl.n_layers,
-                   "l2": "inputs larger than L2 (22.6 GB of expert weights + 16.9 GB of copies per layer)",
+                   "dwdp_group": args.group,
+                   "l2": "inputs larger than L2 ({:.1f} GB of expert weights + {:.1f} GB of copies per layer)".format(
+                       (sh.E + sh.S) * 3 * sh.H * sh.I * WEIGHT_BYTES[args.dtype] / 1e9,
+                       wl.placement.n_remote() * 3 * sh.H * sh.I * WEIGHT_BYTES[args.dtype] / 1e9),
                    "parallelism": "replicas" if world > 1 else "single rank"},
         "clocks": res["clocks"],
     }
@@ -896,7 +906,7 @@ def main_reference(args, rank, world):
     import oracle
     from moe_expert_grouped_split_gb300 import inputs as I
 
-    spec = WORKLOADS[args.workload]()
+    spec = WORKLOADS[args.workload](group=args.group)
     shape = spec.shape
     T = shape.T
     dev = "cuda" if torch.cuda.is_available() else "cpu"
