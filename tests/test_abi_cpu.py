@@ -105,10 +105,21 @@ def test_host_validation_without_gpu(lib):
     assert lib.dwdp_create(ctypes.byref(cfg), None, None, ctypes.byref(out)) == -5
     cfg = B.dwdp_config(256, 128, 8, 9, 0, 64, 1, 0)          # k > E
     assert lib.dwdp_create(ctypes.byref(cfg), None, None, ctypes.byref(out)) == -5
+    cfg = B.dwdp_config(320, 256, 8, 2, 0, 64, 1, 0, B.DTYPE_NVFP4)   # NVFP4: H not a multiple of 256
+    assert lib.dwdp_create(ctypes.byref(cfg), None, None, ctypes.byref(out)) == -5
+    assert "256" in B.dwdp_last_error(None)
+    cfg = B.dwdp_config(256, 192, 8, 2, 0, 64, 1, 0, B.DTYPE_NVFP4)   # NVFP4: I not a multiple of 256
+    assert lib.dwdp_create(ctypes.byref(cfg), None, None, ctypes.byref(out)) == -5
     cfg = B.dwdp_config(256, 128, 8, 2, 0, 64, 1, 4)          # staging without buffers
     assert lib.dwdp_create(ctypes.byref(cfg), None, None, ctypes.byref(out)) == -1
     assert "stage" in B.dwdp_last_error(None)
     assert lib.dwdp_workspace_bytes(None, 10) == 0
+    # activation quantization: argument checks come before any CUDA call
+    x = ctypes.c_void_p(16)
+    assert lib.dwdp_quantize_rows(B.DTYPE_BF16, x, 4, 64, x, x, x, None) == -1      # not a quantized type
+    assert lib.dwdp_quantize_rows(B.DTYPE_NVFP4, x, 4, 96, x, x, x, None) == -1     # K not a multiple of 64
+    assert lib.dwdp_quantize_rows(B.DTYPE_NVFP4, x, 4, 64, x, None, x, None) == -1  # NVFP4 needs block scales
+    assert lib.dwdp_quantize_rows(B.DTYPE_NVFP4, x, 0, 64, None, None, None, None) == 0  # nothing to do
     assert lib.dwdp_stage_layer(None, 0) == -1
     if not torch.cuda.is_available():
         cfg = B.dwdp_config(256, 128, 8, 2, 0, 64, 1, 0)
