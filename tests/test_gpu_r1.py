@@ -12,7 +12,9 @@ round-robin slices, one shared expert, H=7168, I=2048, E=256, top-8):
 
 Workloads: 8192 tokens (N(0,1) activations, N(0,0.02) router), 16384 tokens
 with a Zipf(1.2) router bias over a seeded expert permutation and the 16
-hottest experts replicated locally, and 256 tokens with logits ~ N(0,1)."""
+hottest experts replicated locally, 256 tokens with logits ~ N(0,1), and
+32768 tokens (T (k + 1) = 294 912 expert rows) for the index arithmetic at
+scale."""
 import numpy as np
 import pytest
 import torch
@@ -30,6 +32,9 @@ def _workload(name):
     if name == "r1_8k":
         shape, pl = I.r1_layer(8192)
         return shape, pl, 0.02, None
+    if name == "r1_32k":
+        shape, pl = I.r1_layer(32768)
+        return shape, pl, 0.02, None
     if name == "r1_zipf_16k":
         shape, _ = I.r1_layer(16384)
         bias = I.zipf_bias(256, 1.2, I.seed_for(0, "zipf"))
@@ -41,7 +46,7 @@ def _workload(name):
     raise KeyError(name)
 
 
-@pytest.mark.parametrize("name", ["r1_8k", "r1_zipf_16k", "r1_256"])
+@pytest.mark.parametrize("name", ["r1_8k", "r1_zipf_16k", "r1_256", "r1_32k"])
 def test_full_size_layer(name):
     build()
     shape, pl, rstd, bias = _workload(name)
