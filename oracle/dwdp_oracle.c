@@ -178,7 +178,8 @@ void oracle_topk(const double* z, int64_t T, int64_t E, int64_t k, int decide_fp
  *   perm[r]     = flat index f = t*k + j of the pair at grouped row r
  *   inv[f]      = grouped row of pair f
  * Within an expert's rows, pairs keep ascending flat index (a stable counting
- * sort).  This ordering is this build's convention: the pages do not fix one. */
+ * sort).  The pages do not fix an order; this one is the library's documented
+ * order (dwdp_route_out.perm), so grouped rows compare bit for bit. */
 void oracle_group(const int32_t* ids, int64_t T, int64_t E, int64_t k,
                   int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv) {
     int64_t n = T * k;
