@@ -603,8 +603,8 @@ def run_merge_baseline(wl, K, W):
 def run_pipeline_bench(args, world, local_rank, barrier):
     """Four distinct R1 layers per step with an attention-sized GEMM
     stand-in (x . W_attn, T x 7168 x 7168, on this library's grouped GEMM)
-    after each MoE layer; layer l+1's experts are prefetched while layer l's
-    MoE block and layer l+1's stand-in run (DWDP §2).  T per step is
+    after each MoE layer; the copy of the next layer's experts overlaps the
+    current MoE layer and the stand-in that follows it (DWDP §2).  T per step is
     uniform in [6554, 8192] (0.8x-1.0x of 8K), 16 steps by default."""
     import numpy as np
     import torch
