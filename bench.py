@@ -518,7 +518,8 @@ def run_merge_baseline(wl, K, W):
     sh, pl = wl.shape, wl.placement
     if (pl.local_slot >= 0).sum() != pl.n_local_slots or pl.n_remote() + pl.n_local_slots != sh.E:
         return None   # redundant placements have no single merged layout
-    mrt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, 6, sh.E)
+    wd = {"bf16": B.DTYPE_BF16, "fp8": B.DTYPE_E4M3, "nvfp4": B.DTYPE_NVFP4}[wl.wdtype]
+    mrt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, 6, sh.E, weight_dtype=wd)
     stage_slot = [-1] * sh.E
     r = 0
     for e in range(sh.E):
@@ -533,8 +534,11 @@ def run_merge_baseline(wl, K, W):
             local = B.pool(mrt.stage_w13[s], mrt.stage_w2[s])
             B.dwdp_set_expert_map(mrt.ctx, 2 + 2 * l + s, local, [], merged_slot, [-1] * sh.E, [-1] * sh.E,
                                   lw.shared_w13, lw.shared_w2)
-    w13_bytes = 2 * sh.I * sh.H * 2
-    w2_bytes = sh.H * sh.I * 2
+            if getattr(lw, "w13_scale", None) is not None:
+                B.dwdp_set_expert_scales(mrt.ctx, 2 + 2 * l + s, lw.w13_scale, lw.w2_scale, lw.shared_s13,
+                                         lw.shared_s2)
+    w13_bytes = B.weight_slot_bytes(2 * sh.I, sh.H, wd)
+    w2_bytes = B.weight_slot_bytes(sh.H, sh.I, wd)
     n_local = pl.n_local_slots
     merge_bytes = n_local * (w13_bytes + w2_bytes)
     ev = lambda: torch.cuda.Event()
