@@ -911,7 +911,8 @@ def main():
 
 
 def main_reference(args, rank, world):
-    """The oracle as it stands, timed on host cores, same metric and unit."""
+    """The oracle as it stands, timed on host cores, same metric, unit and
+    expert weight format; each step is one seeded token per oracle thread."""
     if rank != 0:
         return
     import numpy as np
@@ -928,19 +929,39 @@ def main_reference(args, rank, world):
     x_all = I.bf16_bits(I.make_tokens(T, shape.H, 0, device=dev))
     wr = I.bf16_bits(I.randn_bf16((shape.E, shape.H), spec.router_std, I.seed_for(0, "Wr", 0), dev))
     rng = np.random.default_rng(99)
-    per_step = 4
+    per_step = max(1, o.num_threads())
+    wd = args.dtype
     cache = {}
+
+    def host(w):
+        """Math-layout host arrays of one expert as the oracle takes them."""
+        if wd == "bf16":
+            return I.bf16_bits(w[0]), I.bf16_bits(w[1])
+        if wd == "fp8":
+            return w[0].cpu().numpy(), w[1].cpu().numpy()
+        return tuple(t.cpu().numpy() for t in (*w[0], *w[1]))     # codes13, sf13, codes2, sf2
 
     def expert(e):
         if e not in cache:
-            cache[e] = (I.bf16_bits(I.randn_bf16((2 * shape.I, shape.H), 0.02, I.seed_for(0, "W13", 0, e), dev)),
-                        I.bf16_bits(I.randn_bf16((shape.H, shape.I), 0.02, I.seed_for(0, "W2", 0, e), dev)))
+            cache[e] = host(I.expert_weights(wd, shape, 0, 0, e, dev))
         return cache[e]
 
-    sw13 = sw2 = None
-    if shape.S:
-        sw13 = I.bf16_bits(I.randn_bf16((2 * shape.I, shape.H), 0.02, I.seed_for(0, "W13s", 0), dev))
-        sw2 = I.bf16_bits(I.randn_bf16((shape.H, shape.I), 0.02, I.seed_for(0, "W2s", 0), dev))
+    shared = host(I.expert_weights(wd, shape, 0, 0, None, dev)) if shape.S else None
+    scales = I.expert_scales(wd, 0, 0, shape.E) if wd != "bf16" else None
+
+    def layer(xs, r, n):
+        col = lambda i: [cache[e][i] if e in cache else None for e in range(shape.E)]
+        if wd == "bf16":
+            return o.moe_tokens(xs, np.arange(n), r["ids"], r["w"], col(0), col(1),
+                                *(shared if shared else (None, None)), mirrored=True)
+        s13, s2, ss13, ss2 = scales
+        if wd == "fp8":
+            kw = dict(shared_w13=shared[0], shared_w2=shared[1], shared_s13=ss13, shared_s2=ss2) if shared else {}
+            return o.moe_tokens_fp8(xs, np.arange(n), r["ids"], r["w"], col(0), col(1), s13, s2, mirrored=True, **kw)
+        sh = (shared[0], shared[1], ss13, shared[2], shared[3], ss2) if shared else None
+        return o.moe_tokens_nvfp4(xs, np.arange(n), r["ids"], r["w"], col(0), col(1), s13, col(2), col(3), s2,
+                                  shared=sh, mirrored=True)
+
     times = []
     ntok = 0
     for s in range(args.warmup + args.steps):
@@ -949,11 +970,9 @@ def main_reference(args, rank, world):
         pre = o.route(xs, wr, spec.bias, shape.k)
         for e in np.unique(pre["ids"]):
             expert(int(e))
-        w13s = [cache[e][0] if e in cache else None for e in range(shape.E)]
-        w2s = [cache[e][1] if e in cache else None for e in range(shape.E)]
         t0 = time.perf_counter()
         r = o.route(xs, wr, spec.bias, shape.k)
-        o.moe_tokens(xs, np.arange(per_step), r["ids"], r["w"], w13s, w2s, sw13, sw2, mirrored=True)
+        layer(xs, r, per_step)
         dt = time.perf_counter() - t0
         if s >= args.warmup:
             times.append(dt)
@@ -967,10 +986,11 @@ def main_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded, R1 MoE layer shapes)",
         "config": {"workload": args.workload, "T": T, "H": shape.H, "I": shape.I, "E": shape.E, "k": shape.k,
-                   "shared": shape.S},
+                   "shared": shape.S, "expert_weights": wd, "dwdp_group": args.group},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": o.num_threads(), "kind": "oracle",
-                         "sample": f"{per_step} seeded tokens per step of the {T}-token layer, {args.steps} "
-                                   f"timed steps ({total:.1f} s); ms_per_step extrapolates to {T} tokens"},
+                         "sample": f"{per_step} seeded tokens per step (one per oracle thread) of the {T}-token "
+                                   f"layer, {args.steps} timed steps ({total:.1f} s); ms_per_step extrapolates "
+                                   f"to {T} tokens"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -227,15 +227,12 @@ def make_layer_fp8(shape: LayerShape, placement: Placement, base_seed: int, laye
             d.copy_(d13[0])
         for d in d2[1:]:
             d.copy_(d2[0])
-    rng = np.random.Generator(np.random.PCG64(seed_for(base_seed, "fp8_scales", layer)))
-    s13 = (0.02 * rng.uniform(0.8, 1.2, E)).astype(np.float32)
-    s2 = (0.02 * rng.uniform(0.8, 1.2, E)).astype(np.float32)
+    s13, s2, ss13, ss2 = expert_scales("fp8", base_seed, layer, E)
     sw13 = sw2 = None
-    ss13 = ss2 = 1.0
     if shape.S:
-        sw13 = e4m3_codes((2 * I, H), seed_for(base_seed, "W13qs", layer), device)
-        sw2 = e4m3_codes((H, I), seed_for(base_seed, "W2qs", layer), device)
-        ss13, ss2 = float(np.float32(0.02)), float(np.float32(0.021))
+        sw13, sw2 = expert_weights("fp8", shape, base_seed, layer, None, device)
+    else:
+        ss13 = ss2 = 1.0
     bt = None
     if bias is not None:
         bt = torch.as_tensor(np.asarray(bias, dtype=np.float32)).to(device)
@@ -316,25 +313,54 @@ def make_layer_nvfp4(shape: LayerShape, placement: Placement, base_seed: int, la
         if placement.peer_id[e] >= 0:
             d13.append(pw13[placement.peer_id[e]][placement.peer_slot[e]])
             d2.append(pw2[placement.peer_id[e]][placement.peer_slot[e]])
-        p13 = pack_nvfp4(*nvfp4_codes(2 * I, H, seed_for(base_seed, "W13f", layer, e), device))
-        p2 = pack_nvfp4(*nvfp4_codes(H, I, seed_for(base_seed, "W2f", layer, e), device))
+        c13, c2 = expert_weights("nvfp4", shape, base_seed, layer, e, device)
+        p13, p2 = pack_nvfp4(*c13), pack_nvfp4(*c2)
         for d in d13:
             d.copy_(p13)
         for d in d2:
             d.copy_(p2)
-    rng = np.random.Generator(np.random.PCG64(seed_for(base_seed, "nvfp4_scales", layer)))
-    s13 = (0.004 * rng.uniform(0.8, 1.2, E)).astype(np.float32)
-    s2 = (0.004 * rng.uniform(0.8, 1.2, E)).astype(np.float32)
+    s13, s2, ss13, ss2 = expert_scales("nvfp4", base_seed, layer, E)
     sw13 = sw2 = None
-    ss13 = ss2 = 1.0
     if shape.S:
-        sw13 = pack_nvfp4(*nvfp4_codes(2 * I, H, seed_for(base_seed, "W13fs", layer), device))
-        sw2 = pack_nvfp4(*nvfp4_codes(H, I, seed_for(base_seed, "W2fs", layer), device))
-        ss13, ss2 = float(np.float32(0.004)), float(np.float32(0.0042))
+        c13, c2 = expert_weights("nvfp4", shape, base_seed, layer, None, device)
+        sw13, sw2 = pack_nvfp4(*c13), pack_nvfp4(*c2)
+    else:
+        ss13 = ss2 = 1.0
     bt = None
     if bias is not None:
         bt = torch.as_tensor(np.asarray(bias, dtype=np.float32)).to(device)
     return LayerWeightsNvfp4(shape, placement, wr, bt, lw13, lw2, pw13, pw2, sw13, sw2, s13, s2, ss13, ss2)
+
+
+def expert_weights(wdtype: str, shape: LayerShape, base_seed: int, layer: int, e=None, device="cpu"):
+    """One expert's weights in math layout, drawn exactly as the layer
+    builders draw them (e = None: the shared expert): bf16 (w13, w2) tensors
+    (the default weight spread 0.02); E4M3 (w13, w2) uint8 code tensors;
+    NVFP4 ((codes13, scales13), (codes2, scales2)) as nvfp4_codes returns."""
+    H, I = shape.H, shape.I
+    idx = (layer,) if e is None else (layer, e)
+    sfx = "s" if e is None else ""
+    if wdtype == "bf16":
+        return (randn_bf16((2 * I, H), 0.02, seed_for(base_seed, "W13" + sfx, *idx), device),
+                randn_bf16((H, I), 0.02, seed_for(base_seed, "W2" + sfx, *idx), device))
+    if wdtype == "fp8":
+        return (e4m3_codes((2 * I, H), seed_for(base_seed, "W13q" + sfx, *idx), device),
+                e4m3_codes((H, I), seed_for(base_seed, "W2q" + sfx, *idx), device))
+    if wdtype == "nvfp4":
+        return (nvfp4_codes(2 * I, H, seed_for(base_seed, "W13f" + sfx, *idx), device),
+                nvfp4_codes(H, I, seed_for(base_seed, "W2f" + sfx, *idx), device))
+    raise ValueError(wdtype)
+
+
+def expert_scales(wdtype: str, base_seed: int, layer: int, E: int) -> tuple:
+    """(w13 scales [E], w2 scales [E], shared w13 scale, shared w2 scale) of
+    an E4M3 or NVFP4 layer, as the layer builders draw them."""
+    base, tag, shared = {"fp8": (0.02, "fp8_scales", (0.02, 0.021)),
+                         "nvfp4": (0.004, "nvfp4_scales", (0.004, 0.0042))}[wdtype]
+    rng = np.random.Generator(np.random.PCG64(seed_for(base_seed, tag, layer)))
+    s13 = (base * rng.uniform(0.8, 1.2, E)).astype(np.float32)
+    s2 = (base * rng.uniform(0.8, 1.2, E)).astype(np.float32)
+    return s13, s2, float(np.float32(shared[0])), float(np.float32(shared[1]))
 
 
 def make_tokens(T: int, H: int, base_seed: int, step: int = 0, device="cpu") -> torch.Tensor:
