@@ -648,9 +648,9 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     } else if (fmt == FMT_E4M3) {
         // x rows to E4M3 (per-token scales), then copied into expert order
         DWDP_CUDA(ctx, launch_quantize_rows(x, T, (int)H, xq, sx, stream));
-        DWDP_CUDA(ctx, launch_gather_fp8(xq, sx, (int)H, route->inv_perm, (int)T, (int)k, xp, sxp, stream));
+        DWDP_CUDA(ctx, launch_gather_fp8(xq, sx, (int)H, route->inv_perm, (int)T, (int)k, xp, sxp, ctx->d_err, stream));
     } else {
-        DWDP_CUDA(ctx, launch_gather(x, (int)H, route->inv_perm, (int)T, (int)k, xp, stream));
+        DWDP_CUDA(ctx, launch_gather(x, (int)H, route->inv_perm, (int)T, (int)k, xp, ctx->d_err, stream));
     }
     DWDP_CUDA(ctx, mark(ctx, 3, stream));
 
@@ -728,7 +728,7 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     DWDP_CUDA(ctx, mark(ctx, 5, stream));
     // The stage's weights have been read: the next prefetch into it may start.
     if (m.n_remote > 0) DWDP_CUDA(ctx, cudaEventRecord(ctx->freed[stage], stream));
-    DWDP_CUDA(ctx, launch_combine(y, (int)H, route->inv_perm, route->topk_w, T, (int)k, rows_r, S > 0, out, stream));
+    DWDP_CUDA(ctx, launch_combine(y, (int)H, route->inv_perm, route->topk_w, T, (int)k, rows_r, S > 0, out, ctx->d_err, stream));
     DWDP_CUDA(ctx, mark(ctx, 6, stream));
     return DWDP_OK;
 }

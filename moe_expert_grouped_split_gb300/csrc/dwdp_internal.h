@@ -137,12 +137,15 @@ size_t group_chunked_scratch_bytes(int n, int E);
 cudaError_t launch_group_chunked(const int32_t* ids, int n, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
                                  int32_t* inv, int32_t* scratch, cudaStream_t s);
 // Expert-ordered token rows: xp[inv[t k + j]] = x[t] for t < T, j < k.
-cudaError_t launch_gather(const void* x, int H, const int32_t* inv, int T, int k, void* xp, cudaStream_t s);
+// Rows outside [0, T k) in inv are flagged in err (DERR_BAD_INDEX) and skipped,
+// here and in the combine.
+cudaError_t launch_gather(const void* x, int H, const int32_t* inv, int T, int k, void* xp, int* err,
+                          cudaStream_t s);
 // E4M3 rows: codes[r][:] and scale[r] of bf16 rows (scale = amax / 448).
 cudaError_t launch_quantize_rows(const void* in, int64_t rows, int cols, void* codes, float* scale, cudaStream_t s);
 // Expert-ordered E4M3 rows: xp[inv[t k + j]] = xq[t], sxp[inv[t k + j]] = sx[t].
 cudaError_t launch_gather_fp8(const void* xq, const float* sx, int H, const int32_t* inv, int T, int k,
-                              void* xp, float* sxp, cudaStream_t s);
+                              void* xp, float* sxp, int* err, cudaStream_t s);
 // NVFP4 activations (block scales in the GEMM's A-tile chunk layout): x
 // rows quantized once per token and written to the shared-expert copy (xq,
 // sx) and to each chosen expert's row of xp / sxp; a rows (routed rows in
@@ -156,6 +159,6 @@ cudaError_t launch_quantize_a_nvfp4(const void* act, int I, int64_t rows_r, int6
                                     int E, void* aq, float* sa, uint8_t* sf, int64_t sf_tiles, int* err,
                                     cudaStream_t s);
 cudaError_t launch_combine(const void* y, int H, const int32_t* inv, const float* w, int T, int k,
-                           int64_t shared_row0, bool has_shared, void* out, cudaStream_t s);
+                           int64_t shared_row0, bool has_shared, void* out, int* err, cudaStream_t s);
 
 }  // namespace dwdp

@@ -245,20 +245,29 @@ __global__ void __launch_bounds__(kChunk) chunk_place_kernel(const int32_t* __re
 // distances, which L2 does not hold.  The stores are streaming
 // (st.global.cs): the gate/up GEMM reads them long after they would have
 // left L2.  Each lane keeps four 16-byte loads in flight.  KC > 0 fixes k at
-// compile time so the k destinations stay in registers.
+// compile time so the k destinations stay in registers.  A destination row
+// outside [0, T k) is flagged in err and not written.
 template <int KC>
 __global__ void __launch_bounds__(256) scatter_rows_kernel(const uint4* __restrict__ x, int row_vecs,
                                                            const int32_t* __restrict__ inv, int T, int k,
                                                            uint4* __restrict__ xp, const float* __restrict__ sx,
-                                                           float* __restrict__ sxp) {
+                                                           float* __restrict__ sxp, int* __restrict__ err) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     const int kk = KC > 0 ? KC : k;
+    const int64_t n_rows = (int64_t)T * kk;
     const int32_t* it = inv + (int64_t)t * kk;
     const uint4* src = x + (int64_t)t * row_vecs;
+    uint32_t ok = 0;  // bit j: destination j is in range
+    for (int j = 0; j < kk; ++j) {
+        const int32_t r = it[j];
+        if (r >= 0 && r < n_rows) ok |= 1u << j;
+    }
+    if (ok != (kk == 32 ? 0xffffffffu : (1u << kk) - 1u) && lane == 0) atomicOr(err, DERR_BAD_INDEX);
     if (sxp != nullptr)
-        for (int j = lane; j < kk; j += 32) sxp[it[j]] = sx[t];
+        for (int j = lane; j < kk; j += 32)
+            if ((ok >> j) & 1u) sxp[it[j]] = sx[t];
     if constexpr (KC > 0) {
         int64_t dst[KC];
 #pragma unroll
@@ -270,39 +279,43 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const uint4* __restri
             for (int u = 0; u < 4; ++u) v[u] = __ldg(src + i + 32 * u);
 #pragma unroll
             for (int j = 0; j < KC; ++j)
+                if ((ok >> j) & 1u) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) __stcs(xp + dst[j] + i + 32 * u, v[u]);
+                    for (int u = 0; u < 4; ++u) __stcs(xp + dst[j] + i + 32 * u, v[u]);
+                }
         }
         for (; i < row_vecs; i += 32) {
             const uint4 v = __ldg(src + i);
 #pragma unroll
-            for (int j = 0; j < KC; ++j) __stcs(xp + dst[j] + i, v);
+            for (int j = 0; j < KC; ++j)
+                if ((ok >> j) & 1u) __stcs(xp + dst[j] + i, v);
         }
     } else {
         for (int i = lane; i < row_vecs; i += 32) {
             const uint4 v = __ldg(src + i);
-            for (int j = 0; j < kk; ++j) __stcs(xp + (int64_t)it[j] * row_vecs + i, v);
+            for (int j = 0; j < kk; ++j)
+                if ((ok >> j) & 1u) __stcs(xp + (int64_t)it[j] * row_vecs + i, v);
         }
     }
 }
 
 template <int KC>
 void scatter_rows_launch(const uint4* x, int row_vecs, const int32_t* inv, int T, int k, uint4* xp,
-                         const float* sx, float* sxp, cudaStream_t s) {
+                         const float* sx, float* sxp, int* err, cudaStream_t s) {
     const int warps = 8;
-    scatter_rows_kernel<KC><<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(x, row_vecs, inv, T, k, xp, sx, sxp);
+    scatter_rows_kernel<KC><<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(x, row_vecs, inv, T, k, xp, sx, sxp, err);
 }
 
 cudaError_t scatter_rows(const void* x, int row_vecs, const int32_t* inv, int T, int k, void* xp, const float* sx,
-                         float* sxp, cudaStream_t s) {
+                         float* sxp, int* err, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     const uint4* xv = reinterpret_cast<const uint4*>(x);
     uint4* pv = reinterpret_cast<uint4*>(xp);
     switch (k) {
-        case 2: scatter_rows_launch<2>(xv, row_vecs, inv, T, k, pv, sx, sxp, s); break;
-        case 4: scatter_rows_launch<4>(xv, row_vecs, inv, T, k, pv, sx, sxp, s); break;
-        case 8: scatter_rows_launch<8>(xv, row_vecs, inv, T, k, pv, sx, sxp, s); break;
-        default: scatter_rows_launch<0>(xv, row_vecs, inv, T, k, pv, sx, sxp, s);
+        case 2: scatter_rows_launch<2>(xv, row_vecs, inv, T, k, pv, sx, sxp, err, s); break;
+        case 4: scatter_rows_launch<4>(xv, row_vecs, inv, T, k, pv, sx, sxp, err, s); break;
+        case 8: scatter_rows_launch<8>(xv, row_vecs, inv, T, k, pv, sx, sxp, err, s); break;
+        default: scatter_rows_launch<0>(xv, row_vecs, inv, T, k, pv, sx, sxp, err, s);
     }
     return cudaGetLastError();
 }
@@ -323,7 +336,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
                                                       const int32_t* __restrict__ inv,
                                                       const float* __restrict__ w, int T, int k,
                                                       int64_t shared_row0, int has_shared,
-                                                      uint4* __restrict__ out) {
+                                                      uint4* __restrict__ out, int* __restrict__ err) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -332,10 +345,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint4* __restrict__ 
     for (int j = 0; j < k; ++j) {
         rows[j] = inv[(int64_t)t * k + j];
         ws[j] = w[(int64_t)t * k + j];
+        if (rows[j] < 0 || (int64_t)rows[j] >= (int64_t)T * k) {   // flagged; contributes nothing
+            if (lane == 0) atomicOr(err, DERR_BAD_INDEX);
+            rows[j] = -1;
+        }
     }
     for (int i = lane; i < row_vecs; i += 32) {
         float a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int j = 0; j < k; ++j) acc_bf16x8(a, __ldg(y + (int64_t)rows[j] * row_vecs + i), ws[j]);
+        for (int j = 0; j < k; ++j)
+            if (rows[j] >= 0) acc_bf16x8(a, __ldg(y + (int64_t)rows[j] * row_vecs + i), ws[j]);
         if (has_shared) acc_bf16x8(a, __ldg(y + (shared_row0 + t) * row_vecs + i), 1.0f);
         uint4 o;
         __nv_bfloat162* oh = reinterpret_cast<__nv_bfloat162*>(&o);
@@ -353,17 +371,24 @@ __global__ void __launch_bounds__(256) combine_kernel_k(const uint4* __restrict_
                                                         const int32_t* __restrict__ inv,
                                                         const float* __restrict__ w, int T,
                                                         int64_t shared_row0, int has_shared,
-                                                        uint4* __restrict__ out) {
+                                                        uint4* __restrict__ out, int* __restrict__ err) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     int64_t rows[KC];
     float ws[KC];
+    bool bad = false;
 #pragma unroll
     for (int j = 0; j < KC; ++j) {
-        rows[j] = (int64_t)inv[(int64_t)t * KC + j] * row_vecs;
-        ws[j] = w[(int64_t)t * KC + j];
+        const int32_t r = inv[(int64_t)t * KC + j];
+        const bool ok = r >= 0 && (int64_t)r < (int64_t)T * KC;
+        bad |= !ok;
+        // a row outside [0, T k) is flagged and read as row 0 with weight 0,
+        // so the loads stay unconditional and in bounds
+        rows[j] = ok ? (int64_t)r * row_vecs : 0;
+        ws[j] = ok ? w[(int64_t)t * KC + j] : 0.0f;
     }
+    if (bad && lane == 0) atomicOr(err, DERR_BAD_INDEX);
     const int64_t srow = (shared_row0 + t) * row_vecs;
     for (int i = lane; i < row_vecs; i += 32) {
         uint4 q[KC + 1];
@@ -687,8 +712,8 @@ cudaError_t launch_quantize_rows(const void* in, int64_t rows, int cols, void* c
 }
 
 cudaError_t launch_gather_fp8(const void* xq, const float* sx, int H, const int32_t* inv, int T, int k,
-                              void* xp, float* sxp, cudaStream_t s) {
-    return scatter_rows(xq, H / 16, inv, T, k, xp, sx, sxp, s);
+                              void* xp, float* sxp, int* err, cudaStream_t s) {
+    return scatter_rows(xq, H / 16, inv, T, k, xp, sx, sxp, err, s);
 }
 
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
@@ -729,12 +754,13 @@ cudaError_t launch_group_chunked(const int32_t* ids, int n, int E, int32_t* coun
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const void* x, int H, const int32_t* inv, int T, int k, void* xp, cudaStream_t s) {
-    return scatter_rows(x, H / 8, inv, T, k, xp, nullptr, nullptr, s);
+cudaError_t launch_gather(const void* x, int H, const int32_t* inv, int T, int k, void* xp, int* err,
+                          cudaStream_t s) {
+    return scatter_rows(x, H / 8, inv, T, k, xp, nullptr, nullptr, err, s);
 }
 
 cudaError_t launch_combine(const void* y, int H, const int32_t* inv, const float* w, int T, int k,
-                           int64_t shared_row0, bool has_shared, void* out, cudaStream_t s) {
+                           int64_t shared_row0, bool has_shared, void* out, int* err, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     const int warps = 8;
     const dim3 grid((T + warps - 1) / warps), block(32 * warps);
@@ -742,10 +768,10 @@ cudaError_t launch_combine(const void* y, int H, const int32_t* inv, const float
     uint4* ov = reinterpret_cast<uint4*>(out);
     const int hs = has_shared ? 1 : 0;
     switch (k) {
-        case 2: combine_kernel_k<2><<<grid, block, 0, s>>>(yv, H / 8, inv, w, T, shared_row0, hs, ov); break;
-        case 4: combine_kernel_k<4><<<grid, block, 0, s>>>(yv, H / 8, inv, w, T, shared_row0, hs, ov); break;
-        case 8: combine_kernel_k<8><<<grid, block, 0, s>>>(yv, H / 8, inv, w, T, shared_row0, hs, ov); break;
-        default: combine_kernel<<<grid, block, 0, s>>>(yv, H / 8, inv, w, T, k, shared_row0, hs, ov);
+        case 2: combine_kernel_k<2><<<grid, block, 0, s>>>(yv, H / 8, inv, w, T, shared_row0, hs, ov, err); break;
+        case 4: combine_kernel_k<4><<<grid, block, 0, s>>>(yv, H / 8, inv, w, T, shared_row0, hs, ov, err); break;
+        case 8: combine_kernel_k<8><<<grid, block, 0, s>>>(yv, H / 8, inv, w, T, shared_row0, hs, ov, err); break;
+        default: combine_kernel<<<grid, block, 0, s>>>(yv, H / 8, inv, w, T, k, shared_row0, hs, ov, err);
     }
     return cudaGetLastError();
 }

@@ -95,3 +95,32 @@ def test_empty_batch():
         assert (rb.counts.cpu() == 0).all() and (rb.offsets.cpu() == 0).all()
     finally:
         run.close()
+
+
+def test_bad_inverse_permutation_is_flagged():
+    """inv_perm comes from the caller, so the scatter and the combine check
+    every row it names: rows outside [0, T k) are not written or read, the
+    context's device error word reports DEVICE_CHECK (no fault), tokens that
+    do not use a bad row are unchanged, and the context stays usable."""
+    build()
+    shape, placement = I.tiny_layer()
+    lw = I.make_layer(shape, placement, 0, 0, device="cuda")
+    x = I.make_tokens(shape.T, shape.H, 0).cuda()
+    run = GpuLayerRun(shape, lw)
+    try:
+        rb, clean = run.run(x)
+        clean = clean.clone()
+        bad = rb.inv_perm.clone()
+        bad[5] = shape.T * shape.k + 100          # token 2's second slot
+        bad[7] = -3                               # token 3's second slot
+        rb.inv_perm.copy_(bad)
+        out = torch.empty_like(clean)
+        run.rt.moe(0, 0, x, rb, out)
+        torch.cuda.synchronize()
+        assert run.rt.device_status() == -6
+        keep = [t for t in range(shape.T) if t not in (2, 3)]
+        assert torch.equal(out[keep], clean[keep])
+        _, again = run.run(x)                     # clean inputs: no flag, same bytes
+        assert torch.equal(again, clean)
+    finally:
+        run.close()
