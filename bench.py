@@ -91,6 +91,8 @@ def parse(argv=None):
     p.add_argument("--workload", default="r1_moe_layer_8k", choices=sorted(WORKLOADS))
     p.add_argument("--chunk-mb", type=float, default=32.0)
     p.add_argument("--copy-streams", type=int, default=1)
+    p.add_argument("--prefetch-start", choices=["layer", "route"], default="route",
+                   help="when the next layer's copy may start: with the layer, or once its routing is done")
     p.add_argument("--group", type=int, default=4,
                    help="DWDP group size N: E/N experts resident, the rest staged from N-1 peer pools")
     p.add_argument("--dtype", default="bf16", choices=["bf16", "fp8", "nvfp4"],
@@ -259,7 +261,7 @@ class Workload:
     and per-layer token batches, all resident in HBM."""
 
     def __init__(self, spec: Spec, chunk_bytes, n_copy_streams, n_layers=2, base_seed=0, wdtype="bf16",
-                 peer_pools="device"):
+                 peer_pools="device", prefetch_start="route"):
         import torch
 
         from moe_expert_grouped_split_gb300 import binding as B
@@ -295,6 +297,10 @@ class Workload:
         self.copies = [torch.cuda.Stream() for _ in range(n_copy_streams)]
         self.chunk = int(chunk_bytes)
         self.issue_s = []
+        # "route": the copy streams wait for the current layer's routing, so
+        # the small latency-bound routing kernels run without the copy
+        self.prefetch_start = prefetch_start
+        self.routed = torch.cuda.Event()
 
     def layer_step(self, layer, stage, T=None, x=None, out=None):
         T = self.shape.T if T is None else T
@@ -302,10 +308,14 @@ class Workload:
         out = (self.out if out is None else out)[:T]
         with self.torch.cuda.stream(self.compute):
             self.rt.route(x, self.layers[layer].wr, self.layers[layer].bias, self.rb, self.compute)
+            self.routed.record(self.compute)
             self.rt.moe(layer, stage, x, self.rb, out, self.compute)
 
     def prefetch(self, layer, stage):
         t0 = time.perf_counter()
+        if self.prefetch_start == "route":
+            for c in self.copies:
+                c.wait_event(self.routed)
         self.rt.prefetch(layer, stage, self.chunk, self.copies)
         self.issue_s.append(time.perf_counter() - t0)
 
@@ -463,7 +473,8 @@ def run_layer_bench(args, world, local_rank, barrier):
     import torch
     torch.cuda.set_device(local_rank)
     spec = WORKLOADS[args.workload](group=args.group)
-    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, wdtype=args.dtype, peer_pools=args.peer_pools)
+    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, wdtype=args.dtype, peer_pools=args.peer_pools,
+                  prefetch_start=args.prefetch_start)
     sh = wl.shape
     K, W = args.steps, args.warmup
     phases = [_events(torch, 7) for _ in range(K)]
@@ -618,7 +629,8 @@ def run_pipeline_bench(args, world, local_rank, barrier):
 
     torch.cuda.set_device(local_rank)
     spec = WORKLOADS[args.workload](group=args.group)
-    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, n_layers=4, wdtype=args.dtype)
+    wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, n_layers=4, wdtype=args.dtype,
+                  prefetch_start=args.prefetch_start)
     sh = wl.shape
     steps = args.steps
     Ts = I.step_token_counts(steps + args.warmup, 6554, 8192, 0)
@@ -822,6 +834,7 @@ def main():
                    "shared": sh.S, "local_experts": int((wl.placement.local_slot >= 0).sum()),
                    "remote_experts": wl.placement.n_remote(), "peer_pools": wl.placement.n_peers,
                    "chunk_mb": args.chunk_mb, "copy_streams": args.copy_streams, "expert_weights": args.dtype,
+                   "prefetch_start": args.prefetch_start,
                    "peer_pool_memory": args.peer_pools,
                    "layers": wl.n_layers,
                    "dwdp_group": args.group,
