@@ -127,7 +127,11 @@ typedef struct {
  *   perm     [T*k]   flat index t*k+j of the pair at grouped row r; within an
  *                    expert, rows keep ascending flat index
  *   inv_perm [T*k]   grouped row of pair t*k+j
- *   logits   [T][E]  fp32 router logits x.Wr (+ bias); NULL = not returned */
+ *   logits   [T][E]  fp32 router logits x.Wr (+ bias); NULL = not returned.
+ *                    With few tokens the router GEMM splits K into up to 4
+ *                    parts summed in order: the logits are the ones the
+ *                    choice was made on, deterministic for a given device
+ *                    and shape. */
 typedef struct {
     int32_t* topk_ids;
     float* topk_w;
@@ -311,9 +315,11 @@ int32_t dwdp_grouped_gemm(dwdp_ctx* ctx, int32_t epilogue, const void* a, int64_
  * x [T][hidden], w_router [n_experts][hidden], logit_bias [n_experts] or
  * NULL, without a context or workspace; out->logits is ignored (the logits
  * stay in the scratch).  Its scratch is one file-scope device array of
- * DWDP_STATIC_SCRATCH_BYTES (16 MiB) of fp32 logits plus an error word,
- * held by every GPU that loads this library until the process exits, so
- * T * n_experts * 4 must not exceed DWDP_STATIC_SCRATCH_BYTES (else
+ * DWDP_STATIC_SCRATCH_BYTES (16 MiB) of fp32 logits, as much again for the
+ * router GEMM's partial sums (its K may be split into parts as in
+ * dwdp_route, which always fit on GPUs with up to 256 SMs) and an error
+ * word, held by every GPU that loads this library until the process exits,
+ * so T * n_experts * 4 must not exceed DWDP_STATIC_SCRATCH_BYTES (else
  * INVALID_ARG, nothing enqueued).  The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress) with that device
  * current; make that first call before any stream capture.  Every call on a

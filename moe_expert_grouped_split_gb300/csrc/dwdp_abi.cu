@@ -172,8 +172,8 @@ WsLayout ws_layout(const dwdp_config& c, int64_t T) {
     WsLayout L;
     const int64_t H = c.hidden, I = c.inter, E = c.n_experts, k = c.top_k, S = c.n_shared;
     const int fmt = c.weight_dtype;
-    L.logits = 0;
-    L.group = align_up((size_t)(T * E * 4), 256);
+    L.logits = 0;  // up to kRouterMaxSplit partial-sum planes of the router GEMM
+    L.group = align_up((size_t)(kRouterMaxSplit * T * E * 4), 256);
     L.route_bytes = L.group + align_up(group_chunked_scratch_bytes((int)(T * k), (int)E), 256);
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -507,8 +507,13 @@ int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router
     if (!ws || ws_bytes < L.route_bytes || !aligned16(ws))
         return fail(ctx, DWDP_ERR_INVALID_ARG, "workspace too small (%zu < %zu) or unaligned", ws_bytes,
                     L.route_bytes);
-    float* logits = out->logits;
-    if (!logits) logits = reinterpret_cast<float*>(static_cast<char*>(ws) + L.logits);
+    // K split: with fewer 128-token tiles than SMs the router GEMM's K is cut
+    // into parts, each a tile writing its own fp32 plane; the top-k kernel
+    // adds the planes in order (router_k_parts: deterministic per shape).
+    const int parts = router_k_parts(T, c.n_experts, c.hidden, ctx->n_sms,
+                                     (size_t)kRouterMaxSplit * T * c.n_experts * 4);
+    float* planes = reinterpret_cast<float*>(static_cast<char*>(ws) + L.logits);
+    float* logits = (out->logits && parts == 1) ? out->logits : planes;
     int32_t* group_scratch = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.group);
     DWDP_CUDA(ctx, mark(ctx, 0, stream));
     GemmArgs& a = *ctx->args;
@@ -528,10 +533,13 @@ int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router
     a.d_rows = T;
     a.D = logits;
     a.col_bias = logit_bias;
+    a.k_split = parts;
+    a.split_stride = (int64_t)T * c.n_experts;
     a.err = ctx->d_err;
     a.bsrc[0] = make_int2(0, 0);
     DWDP_CUDA(ctx, launch_grouped_gemm(EPI_F32, FMT_BF16, a, ctx->n_sms, stream));
-    DWDP_CUDA(ctx, launch_topk(logits, nullptr, T, c.n_experts, c.top_k, out->topk_ids, out->topk_w, stream));
+    DWDP_CUDA(ctx, launch_topk(logits, parts, (int64_t)T * c.n_experts, nullptr, T, c.n_experts, c.top_k,
+                               out->topk_ids, out->topk_w, parts > 1 ? out->logits : nullptr, stream));
     DWDP_CUDA(ctx, launch_group_chunked(out->topk_ids, T * c.top_k, c.n_experts, out->counts, out->offsets,
                                         out->perm, out->inv_perm, group_scratch, stream));
     DWDP_CUDA(ctx, mark(ctx, 1, stream));
@@ -695,6 +703,7 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     a.d_rows = rows_all;
     a.D = act;
     a.col_bias = nullptr;
+    a.k_split = 1;
     a.err = ctx->d_err;
     for (size_t g = 0; g < m.bsrc.size(); ++g) {
         a.bsrc[g] = m.bsrc[g];
@@ -833,6 +842,7 @@ int32_t dwdp_grouped_gemm(dwdp_ctx* ctx, int32_t epilogue, const void* a_ptr, in
     a.d_rows = a_rows;
     a.D = d;
     a.col_bias = nullptr;
+    a.k_split = 1;
     a.err = ctx->d_err;
     DWDP_CUDA(ctx, launch_grouped_gemm(epilogue, FMT_BF16, a, ctx->n_sms, stream));
     return DWDP_OK;

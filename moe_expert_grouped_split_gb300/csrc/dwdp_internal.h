@@ -14,6 +14,7 @@
 namespace dwdp {
 
 constexpr int kMaxGroups = DWDP_MAX_EXPERTS + 1;  // routed experts + one shared
+constexpr int kRouterMaxSplit = 4;                  // K parts of the router GEMM
 
 enum Epilogue : int { EPI_BF16 = 0, EPI_SILU = 1, EPI_F32 = 2 };
 
@@ -91,7 +92,12 @@ struct GemmArgs {
     int64_t ldd;    // D row stride, elements
     int64_t d_rows; // rows of D: stores at or beyond it are dropped and flagged
     void* D;
-    const float* col_bias;  // EPI_F32: added per column, may be null
+    const float* col_bias;  // EPI_F32: added per column (K part 0 only), may be null
+    // EPI_F32 only: K is cut into k_split contiguous parts of ceil(KB / k_split)
+    // k-blocks (every part non-empty), each a tile of its own; part s writes
+    // its partial sums to D + s * split_stride.  Other epilogues take 1.
+    int32_t k_split;
+    int64_t split_stride;  // elements
     int* err;
     // E4M3 and NVFP4 operands: the fp32 accumulator is multiplied by the A
     // row's scale (routed rows: row_scale[0][A row], shared rows:
@@ -126,9 +132,26 @@ void set_last_error(const char* msg);
 // block scales (GemmArgs::sfa / bsf); K counts elements.  EPI_F32 is bf16 only.
 cudaError_t launch_grouped_gemm(int epi, int fmt, const GemmArgs& args, int n_sms, cudaStream_t stream);
 
+// K parts of the router GEMM (bf16, K = H) for T tokens and E experts: with
+// fewer 128-token tiles than SMs, as many parts as still fit one wave of
+// n_sms CTAs, at most kRouterMaxSplit, none empty, and parts * T * E fp32
+// planes within max_bytes.  Depends only on its arguments, so two callers
+// with the same device and shapes split alike (and get the same logits).
+inline int router_k_parts(int64_t T, int64_t E, int64_t H, int n_sms, size_t max_bytes) {
+    const int64_t tiles = (T + BM - 1) / BM * ((E + BN - 1) / BN);
+    const int64_t kb = (H + BK - 1) / BK;
+    int parts = 1;
+    for (int q = 2; q <= kRouterMaxSplit; ++q)
+        if (tiles * q <= n_sms && (q - 1) * ((kb + q - 1) / q) < kb && (size_t)(q * T * E) * 4 <= max_bytes)
+            parts = q;
+    return parts;
+}
+
 // route.cu
-cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k,
-                        int32_t* ids, float* w, cudaStream_t s);
+// Top-k over logits given as `parts` fp32 planes [T][E] part_stride apart
+// (summed in plane order, then bias); z_out, if not null, receives the sums.
+cudaError_t launch_topk(const float* logits, int parts, int64_t part_stride, const float* bias, int T, int E,
+                        int k, int32_t* ids, float* w, float* z_out, cudaStream_t s);
 cudaError_t launch_group(const int32_t* ids, int n, int E, int32_t* counts, int32_t* offsets,
                          int32_t* perm, int32_t* inv, cudaStream_t s);
 // The same grouping in three passes over chunks of 1024 pairs; needs

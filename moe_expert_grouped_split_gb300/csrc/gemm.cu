@@ -358,6 +358,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     const int ntile_cols = (EPI == EPI_SILU) ? (BN / 2) : BN;  // output columns per tile
     const int NT = (p.N + ntile_cols - 1) / ntile_cols;
     const int KB = (p.K + KE - 1) / KE;
+    // EPI_F32 K split: a group's tiles are (K part, n-tile, m-tile), part-major
+    const int KSPLIT = (EPI == EPI_F32 && p.k_split > 1) ? p.k_split : 1;
+    const int NTV = NT * KSPLIT;
+    const int KB_PART = (KB + KSPLIT - 1) / KSPLIT;
     // Paired mode: the two CTAs of a cluster hold tiles 2p and 2p+1 (every
     // group has an even number of tiles when NT is even, so a pair never
     // straddles two groups).  When both tiles use the same weight tile (same
@@ -374,7 +378,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             atomicOr(p.err, DERR_BAD_INDEX);
             rows = 0;
         }
-        tile_start[g + 1] = ((rows + BM - 1) / BM) * NT;
+        tile_start[g + 1] = ((rows + BM - 1) / BM) * NTV;
     }
     if (threadIdx.x == 0) {
         tile_start[0] = 0;
@@ -440,9 +444,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 while (tile >= tile_start[g + 1]) ++g;
-                const int mt = (tile_start[g + 1] - tile_start[g]) / NT;
+                const int mt = (tile_start[g + 1] - tile_start[g]) / NTV;
                 const int local = tile - tile_start[g];
-                const int n = local / mt, m = local % mt;
+                const int nv = local / mt, m = local % mt;
+                const int part = nv / NT, n = nv - part * NT;
+                const int kb_begin = part * KB_PART, kb_end = min(KB, kb_begin + KB_PART);
                 const bool routed = g < n_routed;
                 const CUtensorMap* ma = routed ? &p.tmA[0] : &p.tmA[1];
                 const int a_row = (routed ? p.row_offsets[g] : p.shared_a_row) + m * BM;
@@ -459,12 +465,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                 // the pair shares the weight tile when the peer's tile (tile ^ 1,
                 // same group) has the same n-tile
                 const bool share = paired && (((local ^ 1) / mt) == n);
-                int64_t atile = tile_start[g] / NT + m;  // NVFP4: the A tile's scale chunks
+                int64_t atile = tile_start[g] / NTV + m;  // NVFP4: the A tile's scale chunks
                 if (FMT == FMT_NVFP4 && atile >= p.sfa_tiles) {
                     atomicOr(p.err, DERR_BAD_INDEX);  // inconsistent group rows: read tile 0's scales instead
                     atile = 0;
                 }
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err, DERR_PRODUCER_WAIT)) {
                         ok = false;
                         break;
@@ -522,14 +528,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
+            int g = 0;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                int nkb = KB;  // k-blocks of this tile (its K part's share when K is split)
+                if (KSPLIT > 1) {
+                    while (tile >= tile_start[g + 1]) ++g;
+                    const int mt = (tile_start[g + 1] - tile_start[g]) / NTV;
+                    const int part = ((tile - tile_start[g]) / mt) / NT;
+                    nkb = min(KB, (part + 1) * KB_PART) - part * KB_PART;
+                }
                 if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.err, DERR_MMA_TMEM_WAIT)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);  // NVFP4: acc is always 0
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err, DERR_MMA_FULL_WAIT)) {
                         ok = false;
                         break;
@@ -595,9 +609,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         int g = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             while (tile >= tile_start[g + 1]) ++g;
-            const int mt = (tile_start[g + 1] - tile_start[g]) / NT;
+            const int mt = (tile_start[g + 1] - tile_start[g]) / NTV;
             const int local = tile - tile_start[g];
-            const int n = local / mt, m = local % mt;
+            const int nv = local / mt, m = local % mt;
+            const int part = nv / NT, n = nv - part * NT;
             const bool routed = g < n_routed;
             const int rows = routed ? (p.row_offsets[g + 1] - p.row_offsets[g]) : p.shared_rows;
             const int64_t d_row0 = routed ? p.row_offsets[g] : p.shared_d_row;
@@ -708,7 +723,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                     }
                 }
             } else {
-                float* D = reinterpret_cast<float*>(p.D);
+                float* D = reinterpret_cast<float*>(p.D) + (int64_t)part * p.split_stride;
+                const float* bias = part == 0 ? p.col_bias : nullptr;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t v[32];
@@ -721,7 +737,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                             const int col = col0 + j;
                             if (col < p.N) {
                                 float o = __uint_as_float(v[j]);
-                                if (p.col_bias) o += p.col_bias[col];
+                                if (bias) o += bias[col];
                                 D[grow * p.ldd + col] = o;
                             }
                         }

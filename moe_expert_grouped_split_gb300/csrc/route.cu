@@ -18,70 +18,94 @@ namespace {
 
 constexpr int kMaxPerLane = DWDP_MAX_EXPERTS / 32;
 
-// One warp per token.  Lane l holds logits l, l+32, ...; k rounds of a warp
-// arg-max pick the chosen set (ties to the lower id), which is then listed in
-// ascending id.  w_j = exp(z_j - z_max) / sum_i exp(z_i - z_max) over the
-// chosen set (the full softmax denominator cancels in the renormalisation).
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits,
-                                                   const float* __restrict__ bias, int T, int E,
-                                                   int k, int32_t* __restrict__ ids,
-                                                   float* __restrict__ w) {
+// Order-preserving key of a logit: a > b as floats iff key(a) > key(b) as
+// unsigned (no NaN); -0 is folded into +0 so equal values tie.  Every finite
+// or infinite value has a key >= 0x007FFFFF, so 0 marks "no candidate".
+__device__ __forceinline__ uint32_t order_key(float x) {
+    const uint32_t u = __float_as_uint(x == 0.0f ? 0.0f : x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// One warp per token.  Lane l holds logits l, l+32, ... (PER of them: E <= 32
+// PER) and keeps the best of its own not yet chosen ones.  Each of the k
+// rounds takes the warp's largest key, then the lowest expert id holding it
+// (ties to the lower id), with two warp reductions; only the lane that owned
+// the pick rescans.  The chosen set is then listed in ascending id.
+// w_j = exp(z_j - z_max) / sum_i exp(z_i - z_max) over the chosen set (the
+// full softmax denominator cancels in the renormalisation).
+// The logits arrive as `parts` partial-sum planes part_stride apart (a
+// K-split router GEMM), added in plane order; with z_out the sums are stored.
+template <int PER>
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int parts,
+                                                   int64_t part_stride, const float* __restrict__ bias,
+                                                   int T, int E, int k, int32_t* __restrict__ ids,
+                                                   float* __restrict__ w, float* __restrict__ z_out) {
+    constexpr int kNone = 0x7fffffff;
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     const float* z = logits + (int64_t)t * E;
-    float v[kMaxPerLane];
-    const int per = (E + 31) >> 5;
+    uint32_t key[PER];
 #pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j) {
+    for (int j = 0; j < PER; ++j) {
         const int e = lane + 32 * j;
-        v[j] = -INFINITY;
-        if (j < per && e < E) v[j] = z[e] + (bias ? bias[e] : 0.0f);
+        key[j] = 0u;
+        if (e < E) {
+            float v = z[e];
+            for (int q = 1; q < parts; ++q) v += z[q * part_stride + e];
+            if (bias) v += bias[e];
+            if (z_out) z_out[(int64_t)t * E + e] = v;
+            key[j] = order_key(v);
+        }
     }
-    uint32_t taken = 0;  // bit j: v[j] already chosen
-    int my_id = -1;      // lane s < k ends up holding the s-th chosen id
+    // this lane's best remaining candidate (largest key, lowest id on ties)
+    auto best = [&](uint32_t& bk, int& bi) {
+        bk = 0u;
+        bi = kNone;
+#pragma unroll
+        for (int j = 0; j < PER; ++j)
+            if (key[j] > bk) {
+                bk = key[j];
+                bi = lane + 32 * j;
+            }
+    };
+    uint32_t lk;
+    int li;
+    best(lk, li);
+    int my_id = -1;  // lane s < k ends up holding the s-th chosen id
     float my_val = 0.0f;
     for (int s = 0; s < k; ++s) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < kMaxPerLane; ++j) {
-            const int e = lane + 32 * j;
-            if (j < per && e < E && !(taken >> j & 1u)) {
-                if (v[j] > bv || (v[j] == bv && e < bi) || bi == 0x7fffffff) {
-                    bv = v[j];
-                    bi = e;
-                }
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        const uint32_t gk = __reduce_max_sync(0xffffffffu, lk);
+        const int gi = __reduce_min_sync(0xffffffffu, (lk == gk && gk != 0u) ? li : kNone);
+        if (gi == kNone) break;  // fewer than k candidates (k <= E is checked on the host)
         if (lane == s) {
-            my_id = bi;
-            my_val = bv;
+            my_id = gi;
+            my_val = key_value(gk);
+        }
+        if ((gi & 31) == lane) {
+#pragma unroll
+            for (int j = 0; j < PER; ++j)  // (a constant index keeps key[] in registers)
+                if (j == (gi >> 5)) key[j] = 0u;
+            best(lk, li);
         }
     }
     // rank of my id among the chosen ids -> ascending-id slot
     int rank = 0;
     for (int s = 0; s < k; ++s) {
         const int other = __shfl_sync(0xffffffffu, my_id, s);
-        if (lane < k && other < my_id) ++rank;
+        if (lane < k && my_id >= 0 && other >= 0 && other < my_id) ++rank;
     }
     // z_max is the first pick
     const float zmax = __shfl_sync(0xffffffffu, my_val, 0);
-    const float ex = (lane < k) ? __expf(my_val - zmax) : 0.0f;
+    const float ex = (lane < k && my_id >= 0) ? __expf(my_val - zmax) : 0.0f;
     float sum = ex;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane < k) {
+    if (lane < k && my_id >= 0) {
         ids[(int64_t)t * k + rank] = my_id;
         w[(int64_t)t * k + rank] = ex / sum;
     }
@@ -716,11 +740,21 @@ cudaError_t launch_gather_fp8(const void* xq, const float* sx, int H, const int3
     return scatter_rows(xq, H / 16, inv, T, k, xp, sx, sxp, err, s);
 }
 
-cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
-                        float* w, cudaStream_t s) {
+cudaError_t launch_topk(const float* logits, int parts, int64_t part_stride, const float* bias, int T, int E,
+                        int k, int32_t* ids, float* w, float* z_out, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     const int warps = 8;
-    topk_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(logits, bias, T, E, k, ids, w);
+    const dim3 grid((T + warps - 1) / warps), block(32 * warps);
+    static_assert(kMaxPerLane == 32, "dispatch covers up to 32 logits per lane");
+#define DWDP_TOPK(PER) \
+    topk_kernel<PER><<<grid, block, 0, s>>>(logits, parts, part_stride, bias, T, E, k, ids, w, z_out)
+    if (E <= 32) DWDP_TOPK(1);
+    else if (E <= 64) DWDP_TOPK(2);
+    else if (E <= 128) DWDP_TOPK(4);
+    else if (E <= 256) DWDP_TOPK(8);
+    else if (E <= 512) DWDP_TOPK(16);
+    else DWDP_TOPK(32);
+#undef DWDP_TOPK
     return cudaGetLastError();
 }
 

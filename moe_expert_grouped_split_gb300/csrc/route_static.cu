@@ -16,7 +16,10 @@
 namespace {
 
 constexpr size_t kErrBytes = 256;  // error word, padded so the logits stay aligned
-__device__ __align__(256) unsigned char g_route_scratch[kErrBytes + DWDP_STATIC_SCRATCH_BYTES];
+// the logits, plus as much again for the router GEMM's K-split partial sums
+// (dwdp_route's split always fits on GPUs with up to 256 SMs)
+constexpr size_t kPlaneBytes = 2 * (size_t)DWDP_STATIC_SCRATCH_BYTES;
+__device__ __align__(256) unsigned char g_route_scratch[kErrBytes + kPlaneBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
@@ -109,12 +112,18 @@ extern "C" int32_t dwdp_route_static(const void* x, int32_t T, int32_t hidden, i
     a.N = n_experts;
     a.ldd = n_experts;
     a.d_rows = T;
+    // the same K split as dwdp_route, so the same logits
+    const int parts = router_k_parts(T, n_experts, hidden, n_sms, kPlaneBytes);
     a.D = logits;
     a.col_bias = logit_bias;
+    a.k_split = parts;
+    a.split_stride = (int64_t)T * n_experts;
     a.err = err;
     a.bsrc[0] = make_int2(0, 0);
     e = launch_grouped_gemm(EPI_F32, FMT_BF16, a, n_sms, stream);
-    if (e == cudaSuccess) e = launch_topk(logits, nullptr, T, n_experts, top_k, out->topk_ids, out->topk_w, stream);
+    if (e == cudaSuccess)
+        e = launch_topk(logits, parts, (int64_t)T * n_experts, nullptr, T, n_experts, top_k, out->topk_ids,
+                        out->topk_w, nullptr, stream);
     if (e == cudaSuccess)
         e = launch_group(out->topk_ids, T * top_k, n_experts, out->counts, out->offsets, out->perm, out->inv_perm,
                          stream);
