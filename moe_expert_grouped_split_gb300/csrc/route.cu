@@ -11,12 +11,16 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <algorithm>
+#include <atomic>
+
 #include "dwdp_internal.h"
 
 namespace dwdp {
 namespace {
 
 constexpr int kMaxPerLane = DWDP_MAX_EXPERTS / 32;
+constexpr int kQuantWarps = 8;  // warps per block of the NVFP4 quantizers
 
 // Order-preserving key of a logit: a > b as floats iff key(a) > key(b) as
 // unsigned (no NaN); -0 is folded into +0 so equal values tie.  Every finite
@@ -525,6 +529,7 @@ __device__ __forceinline__ void load_bf16x16(const uint4* src, float (&v)[16]) {
 // The row scale s of one row of nb blocks (two uint4 per block), warp-wide.
 __device__ __forceinline__ float nvfp4_row_scale(const uint4* src, int nb, int lane) {
     float amax = 0.0f;
+#pragma unroll 4
     for (int b = lane; b < nb; b += 32) {
         float v[16];
         load_bf16x16(src + 2 * b, v);
@@ -534,6 +539,20 @@ __device__ __forceinline__ float nvfp4_row_scale(const uint4* src, int nb, int l
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     return amax > 0.0f ? amax / 2688.0f : 1.0f;
+}
+
+// a / b rounded to nearest even, given y = RN(1/b): Markstein's one-step
+// correction (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with
+// q = RN(a y), the remainder r = a - b q is exact in one FMA and RN(q + r y)
+// is the correctly rounded quotient, for b, 1/b and a/b in the normal range.
+// The caller keeps b within [2^-100, 2^100]; a quotient below the normal
+// range then has |a| below it too and lies far below 0.25, where every
+// rounding gives E2M1 code 0; copysign keeps the sign of a zero quotient.
+__device__ __forceinline__ float div_rn_markstein(float a, float b, float y) {
+    const float q = __fmul_rn(a, y);
+    const float r = fmaf(-q, b, a);
+    return copysignf(fmaf(r, y, q), a);
 }
 
 // Block b of a row: its E4M3 scale code and 16 E2M1 codes (8 bytes).
@@ -548,11 +567,29 @@ __device__ __forceinline__ uint32_t nvfp4_block(const uint4* src, int b, float s
     if (sf == 0) {
         codes = make_uint2(0u, 0u);
     } else {
+        if (eff >= 0x1p-100f && eff <= 0x1p100f) {
+            // the 16 quotients v / eff, correctly rounded, from one reciprocal
+            const float y = __frcp_rn(eff);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = v[i] / eff;
+            for (int i = 0; i < 16; ++i) v[i] = div_rn_markstein(v[i], eff, y);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = v[i] / eff;
+        }
         codes = make_uint2(e2m1x8(v), e2m1x8(v + 8));
     }
     return sf;
+}
+
+// Blocks b and b + 1 of a row (b even): their scale codes (block b in the
+// low byte) and 32 E2M1 codes (16 bytes), so a lane stores 16 bytes of codes
+// and 2 adjacent scale bytes at once.
+__device__ __forceinline__ uint32_t nvfp4_block_pair(const uint4* src, int b, float s, float d, uint4& codes) {
+    uint2 c0, c1;
+    const uint32_t f0 = nvfp4_block(src, b, s, d, c0);
+    const uint32_t f1 = nvfp4_block(src, b + 1, s, d, c1);
+    codes = make_uint4(c0.x, c0.y, c1.x, c1.y);
+    return f0 | (f1 << 8);
 }
 
 __device__ __forceinline__ int64_t sf_byte(int64_t atile, int K, int b, int m) {
@@ -597,30 +634,34 @@ __global__ void __launch_bounds__(256) quantize_x_nvfp4_kernel(const uint4* __re
                                                                float* __restrict__ sxp, uint8_t* __restrict__ sf,
                                                                int64_t sf_tiles, int* __restrict__ err) {
     __shared__ int tb[DWDP_MAX_EXPERTS + 1], offs[DWDP_MAX_EXPERTS + 1];
+    // per warp: the token's destination rows (-1: flagged, skipped) and the
+    // byte of block 0's scale in each one's A tile
+    __shared__ int32_t dst_row[kQuantWarps][DWDP_MAX_TOPK];
+    __shared__ int64_t dst_sf[kQuantWarps][DWDP_MAX_TOPK];
     tile_bases(offsets, E, tb, offs);
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int t = blockIdx.x * (blockDim.x >> 5) + wib;
     if (t >= T) return;
     const int nb = H / 16;
     const uint4* src = x + (int64_t)t * (H / 8);
     const float s = nvfp4_row_scale(src, nb, lane);
     const float d = 6.0f * s;
     const int64_t n_rows = (int64_t)T * k;
-    // this token's destinations: lane j < k holds (row, A tile, row in tile) of choice j
-    int64_t my_r = -1, my_at = 0;
-    int my_m = 0;
     if (lane < k) {
         const int64_t r = inv[(int64_t)t * k + lane];
         const int g = ids[(int64_t)t * k + lane];
+        int32_t row = -1;
+        int64_t base = 0;
         if (r < 0 || r >= n_rows || g < 0 || g >= E || r < offs[g] || r >= offs[g + 1] ||
             tb[g] + (r - offs[g]) / BM >= sf_tiles) {
             atomicOr(err, DERR_BAD_INDEX);
         } else {
-            my_r = r;
-            my_at = tb[g] + (r - offs[g]) / BM;
-            my_m = (int)((r - offs[g]) % BM);
+            row = (int32_t)r;
+            base = sf_byte(tb[g] + (r - offs[g]) / BM, H, 0, (int)((r - offs[g]) % BM));
             sxp[r] = s;
         }
+        dst_row[wib][lane] = row;
+        dst_sf[wib][lane] = base;
     }
     if (has_shared && lane == 0) sx[t] = s;
     const int64_t sh_at = tb[E] + t / BM;
@@ -628,44 +669,33 @@ __global__ void __launch_bounds__(256) quantize_x_nvfp4_kernel(const uint4* __re
         if (lane == 0) atomicOr(err, DERR_BAD_INDEX);
         has_shared = 0;
     }
-    const int sh_m = t % BM;
-    // every lane runs every iteration: the shuffles below need the whole warp
-    for (int b0 = 0; b0 < nb; b0 += 32) {
-        const int b = b0 + lane;
-        const bool mine = b < nb;
-        uint2 c = make_uint2(0u, 0u);
-        uint32_t f = 0;
-        if (mine) {
-            f = nvfp4_block(src, b, s, d, c);
-            if (has_shared) {
-                xq[(int64_t)t * (H / 16) + b] = c;
-                sf[sf_byte(sh_at, H, b, sh_m)] = (uint8_t)f;
-            }
+    const int64_t sh_sf = has_shared ? sf_byte(sh_at, H, 0, t % BM) : 0;
+    __syncwarp();
+    // two blocks per lane (nb is a multiple of 4): 16 bytes of codes and two
+    // adjacent scale bytes per destination
+    uint4* xq4 = reinterpret_cast<uint4*>(xq);
+    uint4* xp4 = reinterpret_cast<uint4*>(xp);
+    for (int b = 2 * lane; b < nb; b += 64) {
+        uint4 c;
+        const uint16_t f = (uint16_t)nvfp4_block_pair(src, b, s, d, c);
+        const int64_t sf_off = (int64_t)(b >> 2) * kSfChunkBytes + (b & 3);  // block b within a row's chunks
+        if (has_shared) {
+            xq4[(int64_t)t * (H / 32) + b / 2] = c;
+            *reinterpret_cast<uint16_t*>(sf + sh_sf + sf_off) = f;
         }
         for (int j = 0; j < k; ++j) {
-            const int64_t r = __shfl_sync(0xffffffffu, my_r, j);
-            const int64_t at = __shfl_sync(0xffffffffu, my_at, j);
-            const int m = __shfl_sync(0xffffffffu, my_m, j);
-            if (r < 0 || !mine) continue;
-            xp[r * (H / 16) + b] = c;
-            sf[sf_byte(at, H, b, m)] = (uint8_t)f;
+            const int32_t r = dst_row[wib][j];
+            if (r < 0) continue;
+            xp4[(int64_t)r * (H / 32) + b / 2] = c;
+            *reinterpret_cast<uint16_t*>(sf + dst_sf[wib][j] + sf_off) = f;
         }
     }
 }
 
-// a rows (one warp per row r of rows_all = routed rows then shared rows).
-// With rows_r = 0 and no groups this quantizes a plain [rows][I] matrix,
-// row r landing in row r % 128 of tile r / 128.
-__global__ void __launch_bounds__(256) quantize_a_nvfp4_kernel(const uint4* __restrict__ a, int I, int64_t rows_r,
-                                                               int64_t rows_all, const int32_t* __restrict__ offsets,
-                                                               int E, uint2* __restrict__ aq, float* __restrict__ sa,
-                                                               uint8_t* __restrict__ sf, int64_t sf_tiles,
-                                                               int* __restrict__ err) {
-    __shared__ int tb[DWDP_MAX_EXPERTS + 1], offs[DWDP_MAX_EXPERTS + 1];
-    tile_bases(offsets, E, tb, offs);
-    const int lane = threadIdx.x & 31;
-    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (r >= rows_all) return;
+__device__ __forceinline__ void quantize_a_row(const uint4* __restrict__ a, int I, int64_t r, int64_t rows_r,
+                                               const int* offs, const int* tb, int E, uint2* __restrict__ aq,
+                                               float* __restrict__ sa, uint8_t* __restrict__ sf, int64_t sf_tiles,
+                                               int* __restrict__ err, int lane) {
     int64_t at;
     int m;
     if (r < rows_r) {
@@ -695,13 +725,34 @@ __global__ void __launch_bounds__(256) quantize_a_nvfp4_kernel(const uint4* __re
     const float s = nvfp4_row_scale(src, nb, lane);
     const float d = 6.0f * s;
     if (lane == 0) sa[r] = s;
-    for (int b = lane; b < nb; b += 32) {
-        uint2 c;
-        const uint32_t f = nvfp4_block(src, b, s, d, c);
-        aq[r * (I / 16) + b] = c;
-        sf[sf_byte(at, I, b, m)] = (uint8_t)f;
+    const int64_t base = sf_byte(at, I, 0, m);
+    uint4* aq4 = reinterpret_cast<uint4*>(aq);
+    for (int b = 2 * lane; b < nb; b += 64) {  // two blocks per lane, as for x
+        uint4 c;
+        const uint16_t f = (uint16_t)nvfp4_block_pair(src, b, s, d, c);
+        aq4[r * (I / 32) + b / 2] = c;
+        *reinterpret_cast<uint16_t*>(sf + base + (int64_t)(b >> 2) * kSfChunkBytes + (b & 3)) = f;
     }
 }
+
+// a rows (one warp per row r of rows_all = routed rows then shared rows).
+// With rows_r = 0 and no groups this quantizes a plain [rows][I] matrix,
+// row r landing in row r % 128 of tile r / 128.
+__global__ void __launch_bounds__(256) quantize_a_nvfp4_kernel(const uint4* __restrict__ a, int I, int64_t rows_r,
+                                                               int64_t rows_all, const int32_t* __restrict__ offsets,
+                                                               int E, uint2* __restrict__ aq, float* __restrict__ sa,
+                                                               uint8_t* __restrict__ sf, int64_t sf_tiles,
+                                                               int* __restrict__ err) {
+    __shared__ int tb[DWDP_MAX_EXPERTS + 1], offs[DWDP_MAX_EXPERTS + 1];
+    tile_bases(offsets, E, tb, offs);
+    const int lane = threadIdx.x & 31;
+    // persistent: each warp takes rows warp, warp + all warps, ... (the tile
+    // bases above are computed once per block)
+    const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows_all; r += n_warps)
+        quantize_a_row(a, I, r, rows_r, offs, tb, E, aq, sa, sf, sf_tiles, err, lane);
+}
+
 
 }  // namespace
 
@@ -709,19 +760,41 @@ cudaError_t launch_quantize_x_nvfp4(const void* x, int H, int T, int k, const in
                                     const int32_t* offsets, int E, bool has_shared, void* xq, float* sx, void* xp,
                                     float* sxp, uint8_t* sf, int64_t sf_tiles, int* err, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    const int warps = 8;
+    const int warps = kQuantWarps;  // the kernel's per-warp destination tables assume it
     quantize_x_nvfp4_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(
         reinterpret_cast<const uint4*>(x), H, T, k, ids, inv, offsets, E, has_shared ? 1 : 0,
         reinterpret_cast<uint2*>(xq), sx, reinterpret_cast<uint2*>(xp), sxp, sf, sf_tiles, err);
     return cudaGetLastError();
 }
 
+// Blocks of quantize_a_nvfp4_kernel resident at once on the current device
+// (its persistent grid), looked up once per device.
+static int quantize_a_blocks() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        int sms = 0, per_sm = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_a_nvfp4_kernel, 32 * kQuantWarps, 0) !=
+                cudaSuccess)
+            return 0;
+        n = sms * (per_sm > 0 ? per_sm : 1);
+        cached[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 cudaError_t launch_quantize_a_nvfp4(const void* act, int I, int64_t rows_r, int64_t rows_all, const int32_t* offsets,
                                     int E, void* aq, float* sa, uint8_t* sf, int64_t sf_tiles, int* err,
                                     cudaStream_t s) {
     if (rows_all <= 0) return cudaSuccess;
-    const int warps = 8;
-    quantize_a_nvfp4_kernel<<<(unsigned)((rows_all + warps - 1) / warps), 32 * warps, 0, s>>>(
+    const int warps = kQuantWarps;
+    const int cap = quantize_a_blocks();
+    if (cap <= 0) return cudaErrorInvalidDevice;
+    const int64_t blocks = std::min<int64_t>((rows_all + warps - 1) / warps, cap);
+    quantize_a_nvfp4_kernel<<<(unsigned)blocks, 32 * warps, 0, s>>>(
         reinterpret_cast<const uint4*>(act), I, rows_r, rows_all, offsets, E, reinterpret_cast<uint2*>(aq), sa, sf,
         sf_tiles, err);
     return cudaGetLastError();

@@ -96,6 +96,58 @@ def test_quantize_rows_nvfp4_bit_exact():
         assert np.array_equal(c, got_c[r]), f"row {r}: codes differ at {np.nonzero(c != got_c[r])[0][:8]}"
 
 
+def _bf16_step(v, up):
+    """The bf16 neighbour of float32 v (exactly representable in bf16)."""
+    b = np.array([v], dtype=np.float32).view(np.uint32)[0] >> 16
+    b = b + 1 if (up == (v >= 0)) else b - 1
+    return np.array([b << 16], dtype=np.uint32).view(np.float32)[0]
+
+
+def test_quantize_rows_nvfp4_rounding_boundaries():
+    """Rows whose quotients v / eff land exactly on the E2M1 rounding
+    thresholds (0.25, 0.75, ..., 5: ties to even) and one bf16 step either
+    side.  The row amax is 2688 * 2^j, so s = 2^j and each block's scale
+    (block amax 6 * e * 2^j) is the E4M3 value e exactly; every value is
+    bf16-representable.  Codes, scales and row scales must match the oracle
+    (binary32 division) bit for bit."""
+    build()
+    rng = np.random.default_rng(24)
+    rows, K = 256, 512
+    thresholds = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], dtype=np.float32)
+    mant = np.array([1, 1.125, 1.25, 1.375, 1.5, 1.625, 1.75, 1.875], dtype=np.float32)
+    x = np.zeros((rows, K), dtype=np.float32)
+    for r in range(rows):
+        s = np.float32(2.0 ** int(rng.integers(-30, 30)))
+        x[r, 0] = np.float32(2688.0) * s                              # the row amax: s = 2^j
+        for b in range(1, K // 16):
+            e = mant[rng.integers(0, 8)] * np.float32(2.0 ** int(rng.integers(-6, 6)))
+            blk = np.empty(16, dtype=np.float32)
+            blk[0] = np.float32(6.0) * e * s                          # the block amax: scale code = e
+            for i in range(1, 16):
+                v = thresholds[rng.integers(0, 7)] * e * s
+                step = rng.integers(0, 3)                             # on the threshold, or one bf16 step off
+                if step:
+                    v = _bf16_step(v, step == 1)
+                blk[i] = v if rng.random() < 0.5 else -v
+            x[r, 16 * b:16 * b + 16] = blk
+    xt = torch.from_numpy(x).to(torch.bfloat16)
+    assert torch.equal(xt.float(), torch.from_numpy(x)), "test rows must be bf16-representable"
+    pad = (rows + 127) // 128 * 128
+    codes = torch.empty(rows * K // 2, dtype=torch.uint8, device="cuda")
+    sf = torch.zeros(pad * K // 16, dtype=torch.uint8, device="cuda")
+    rs = torch.empty(rows, dtype=torch.float32, device="cuda")
+    B.dwdp_quantize_rows(B.DTYPE_NVFP4, xt.cuda(), rows, K, codes, sf, rs)
+    torch.cuda.synchronize()
+    got_c = _unpack_codes(_u8(codes), rows, K)
+    got_sf = _u8(sf)[_sf_offsets(rows, K)]
+    o = oracle.default()
+    for r in range(rows):
+        c, f, sc = o.quantize_row_nvfp4(x[r])
+        assert np.float32(sc) == rs.cpu().numpy()[r], f"row {r}: scale"
+        assert np.array_equal(f, got_sf[r]), f"row {r}: block scales differ"
+        assert np.array_equal(c, got_c[r]), f"row {r}: codes differ at {np.nonzero(c != got_c[r])[0][:8]}"
+
+
 def test_quantize_rows_e4m3_bit_exact():
     build()
     rng = np.random.default_rng(22)
