@@ -512,8 +512,8 @@ __device__ __forceinline__ uint32_t e2m1x8(const float* v) {
     return r;
 }
 
-__device__ __forceinline__ void load_bf16x16(const uint4* src, float (&v)[16]) {
-    const uint4 q[2] = {__ldg(src), __ldg(src + 1)};
+// 16 bf16 values (two uint4) as binary32.
+__device__ __forceinline__ void bf16x16_to_float(const uint4* q, float (&v)[16]) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&q[h]);
@@ -524,6 +524,11 @@ __device__ __forceinline__ void load_bf16x16(const uint4* src, float (&v)[16]) {
             v[8 * h + 2 * j + 1] = f.y;
         }
     }
+}
+
+__device__ __forceinline__ void load_bf16x16(const uint4* src, float (&v)[16]) {
+    const uint4 q[2] = {__ldg(src), __ldg(src + 1)};
+    bf16x16_to_float(q, v);
 }
 
 // The row scale s of one row of nb blocks (two uint4 per block), warp-wide.
@@ -555,10 +560,11 @@ __device__ __forceinline__ float div_rn_markstein(float a, float b, float y) {
     return copysignf(fmaf(r, y, q), a);
 }
 
-// Block b of a row: its E4M3 scale code and 16 E2M1 codes (8 bytes).
-__device__ __forceinline__ uint32_t nvfp4_block(const uint4* src, int b, float s, float d, uint2& codes) {
+// One 16-element block (its two uint4 of bf16 in q): its E4M3 scale code and
+// 16 E2M1 codes (8 bytes).
+__device__ __forceinline__ uint32_t nvfp4_block(const uint4* q, float s, float d, uint2& codes) {
     float v[16];
-    load_bf16x16(src + 2 * b, v);
+    bf16x16_to_float(q, v);
     float ab = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) ab = fmaxf(ab, fabsf(v[i]));
@@ -581,15 +587,21 @@ __device__ __forceinline__ uint32_t nvfp4_block(const uint4* src, int b, float s
     return sf;
 }
 
-// Blocks b and b + 1 of a row (b even): their scale codes (block b in the
-// low byte) and 32 E2M1 codes (16 bytes), so a lane stores 16 bytes of codes
-// and 2 adjacent scale bytes at once.
-__device__ __forceinline__ uint32_t nvfp4_block_pair(const uint4* src, int b, float s, float d, uint4& codes) {
+// Two adjacent blocks (their four uint4 of bf16 in q): their scale codes
+// (the first block's in the low byte) and 32 E2M1 codes (16 bytes), so a
+// lane stores 16 bytes of codes and 2 adjacent scale bytes at once.
+__device__ __forceinline__ uint32_t nvfp4_block_pair(const uint4 (&q)[4], float s, float d, uint4& codes) {
     uint2 c0, c1;
-    const uint32_t f0 = nvfp4_block(src, b, s, d, c0);
-    const uint32_t f1 = nvfp4_block(src, b + 1, s, d, c1);
+    const uint32_t f0 = nvfp4_block(q, s, d, c0);
+    const uint32_t f1 = nvfp4_block(q + 2, s, d, c1);
     codes = make_uint4(c0.x, c0.y, c1.x, c1.y);
     return f0 | (f1 << 8);
+}
+
+// A row's blocks b, b + 1 (b even) as four uint4, or zeros past the row end.
+__device__ __forceinline__ void load_block_pair(const uint4* src, int b, int nb, uint4 (&q)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = b < nb ? __ldg(src + 2 * b + i) : make_uint4(0u, 0u, 0u, 0u);
 }
 
 __device__ __forceinline__ int64_t sf_byte(int64_t atile, int K, int b, int m) {
@@ -675,9 +687,16 @@ __global__ void __launch_bounds__(256) quantize_x_nvfp4_kernel(const uint4* __re
     // adjacent scale bytes per destination
     uint4* xq4 = reinterpret_cast<uint4*>(xq);
     uint4* xp4 = reinterpret_cast<uint4*>(xp);
+    // the next pair's loads are issued before this pair is converted
+    uint4 nxt[4];
+    load_block_pair(src, 2 * lane, nb, nxt);
     for (int b = 2 * lane; b < nb; b += 64) {
+        uint4 cur[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+        load_block_pair(src, b + 64, nb, nxt);
         uint4 c;
-        const uint16_t f = (uint16_t)nvfp4_block_pair(src, b, s, d, c);
+        const uint16_t f = (uint16_t)nvfp4_block_pair(cur, s, d, c);
         const int64_t sf_off = (int64_t)(b >> 2) * kSfChunkBytes + (b & 3);  // block b within a row's chunks
         if (has_shared) {
             xq4[(int64_t)t * (H / 32) + b / 2] = c;
@@ -727,9 +746,15 @@ __device__ __forceinline__ void quantize_a_row(const uint4* __restrict__ a, int 
     if (lane == 0) sa[r] = s;
     const int64_t base = sf_byte(at, I, 0, m);
     uint4* aq4 = reinterpret_cast<uint4*>(aq);
-    for (int b = 2 * lane; b < nb; b += 64) {  // two blocks per lane, as for x
+    uint4 nxt[4];
+    load_block_pair(src, 2 * lane, nb, nxt);
+    for (int b = 2 * lane; b < nb; b += 64) {  // two blocks per lane, next pair loaded ahead, as for x
+        uint4 cur[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+        load_block_pair(src, b + 64, nb, nxt);
         uint4 c;
-        const uint16_t f = (uint16_t)nvfp4_block_pair(src, b, s, d, c);
+        const uint16_t f = (uint16_t)nvfp4_block_pair(cur, s, d, c);
         aq4[r * (I / 32) + b / 2] = c;
         *reinterpret_cast<uint16_t*>(sf + base + (int64_t)(b >> 2) * kSfChunkBytes + (b & 3)) = f;
     }
