@@ -210,34 +210,83 @@ __global__ void __launch_bounds__(kChunk) chunk_count_kernel(const int32_t* __re
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = h[e];
 }
 
-// One block of >= E threads: thread e walks the chunks of expert e.
+// One block of 1024 threads; P = 1024 / (E rounded up to a power of two)
+// threads per expert: thread (e, q) owns the q-th run of consecutive chunks
+// of expert e.  Pass 1 sums the run, the runs' sums are scanned per expert
+// and the experts' totals across experts, and pass 2 rewrites the run's
+// counts as bases.  The loads and stores of a run go four at a time, so a
+// thread waits on memory a few times instead of once per chunk.
 __global__ void __launch_bounds__(1024) chunk_scan_kernel(int32_t* __restrict__ hist, int n_chunks, int E,
                                                           int32_t* __restrict__ counts,
                                                           int32_t* __restrict__ offsets) {
-    __shared__ int scan[1024];
-    const int e = threadIdx.x;
+    __shared__ int part[1024];  // per thread: its run's sum, then the run's offset within its expert
+    __shared__ int scan[1024];  // per expert: inclusive scan of the totals
+    int ep = 1;
+    while (ep < E) ep <<= 1;
+    const int P = 1024 / ep;  // E <= 1024, so P >= 1
+    const int tid = threadIdx.x;
+    const int e = tid / P, q = tid % P;
+    const bool active = e < E;
+    const int per = (n_chunks + P - 1) / P;
+    const int c0 = min(n_chunks, q * per), c1 = min(n_chunks, c0 + per);
+    int sum = 0;
+    if (active) {
+        int c = c0;
+        for (; c + 4 <= c1; c += 4) {
+            int v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = hist[(int64_t)(c + u) * E + e];
+            sum += v[0] + v[1] + v[2] + v[3];
+        }
+        for (; c < c1; ++c) sum += hist[(int64_t)c * E + e];
+    }
+    part[tid] = sum;
+    __syncthreads();
+    // per expert: exclusive offsets of its P runs, and its total
     int c_e = 0;
-    if (e < E)
-        for (int c = 0; c < n_chunks; ++c) {
-            const int v = hist[(int64_t)c * E + e];
-            hist[(int64_t)c * E + e] = c_e;  // pairs of e before chunk c
+    if (active && q == 0) {
+        for (int r = 0; r < P; ++r) {
+            const int v = part[tid + r];
+            part[tid + r] = c_e;
             c_e += v;
         }
-    scan[e] = (e < E) ? c_e : 0;
+    }
+    scan[tid] = 0;
+    __syncthreads();
+    if (active && q == 0) scan[e] = c_e;
     __syncthreads();
     // inclusive scan over experts (Hillis-Steele in shared memory)
     for (int o = 1; o < 1024; o <<= 1) {
-        const int v = (e >= o) ? scan[e - o] : 0;
+        const int v = (tid >= o) ? scan[tid - o] : 0;
         __syncthreads();
-        scan[e] += v;
+        scan[tid] += v;
         __syncthreads();
     }
-    if (e < E) {
-        const int base = scan[e] - c_e;
-        counts[e] = c_e;
-        offsets[e] = base;
-        if (e == E - 1) offsets[E] = scan[e];
-        for (int c = 0; c < n_chunks; ++c) hist[(int64_t)c * E + e] += base;
+    if (active) {
+        const int total = scan[e] - (e > 0 ? scan[e - 1] : 0);
+        const int base = scan[e] - total;  // pairs of experts before e
+        if (q == 0) {
+            counts[e] = total;
+            offsets[e] = base;
+            if (e == E - 1) offsets[E] = scan[e];
+        }
+        int running = base + part[tid];
+        int c = c0;
+        for (; c + 4 <= c1; c += 4) {
+            int v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = hist[(int64_t)(c + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                hist[(int64_t)(c + u) * E + e] = running;
+                running += v[u];
+            }
+        }
+        for (; c < c1; ++c) {
+            const int v = hist[(int64_t)c * E + e];
+            hist[(int64_t)c * E + e] = running;
+            running += v;
+        }
     }
 }
 
