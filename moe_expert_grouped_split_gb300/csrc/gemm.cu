@@ -529,6 +529,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             uint32_t acc_phase = 0;
             bool ok = true;
             int g = 0;
+            const uint64_t ad0 = smem_desc(sbase + SL::kA), bd0 = smem_desc(sbase + SL::kB);
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 int nkb = KB;  // k-blocks of this tile (its K part's share when K is split)
                 if (KSPLIT > 1) {
@@ -549,8 +550,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = smem_desc(sbase + SL::kA + stage * kABytes);
-                    const uint64_t bd = smem_desc(sbase + SL::kB + stage * kBBytes);
+                    // stage s's tiles sit s * k{A,B}Bytes past stage 0's: add to the
+                    // start-address field (address / 16; no carry, as below)
+                    const uint64_t ad = ad0 + (uint64_t)(stage * (kABytes / 16));
+                    const uint64_t bd = bd0 + (uint64_t)(stage * (kBBytes / 16));
                     if constexpr (FMT == FMT_NVFP4) {
                         // block scales of this stage into its TMEM columns (the MMAs
                         // that last read those columns finished before the stage was
@@ -558,12 +561,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                         const uint32_t ss = sbase + SL::kSF + stage * F::kSfBytes;
                         const uint32_t tc = tmem_base + (uint32_t)(kSfCol0 + stage * kSfColsPerStage);
                         constexpr int kBCol = 4 * kSfStepsPerSlice;  // B scales follow A's columns
+                        // the chunk o bytes past ss has descriptor sd + o / 16: the
+                        // start-address field holds address / 16 and shared memory
+                        // addresses stay below its 2^14 limit, so the add never carries
+                        const uint64_t sd = sf_chunk_desc(ss);
 #pragma unroll
                         for (int j = 0; j < kSfStepsPerSlice; ++j) {
-                            tc_cp_sf(tc + 4 * j, sf_chunk_desc(ss + j * kSfChunkBytes));
-                            tc_cp_sf(tc + kBCol + 8 * j, sf_chunk_desc(ss + kSfStageBytesA + j * kSfChunkBytes));
+                            tc_cp_sf(tc + 4 * j, sd + (uint64_t)(j * kSfChunkBytes / 16));
+                            tc_cp_sf(tc + kBCol + 8 * j, sd + (uint64_t)((kSfStageBytesA + j * kSfChunkBytes) / 16));
                             tc_cp_sf(tc + kBCol + 4 + 8 * j,
-                                     sf_chunk_desc(ss + 2 * kSfStageBytesA + j * kSfChunkBytes));
+                                     sd + (uint64_t)((2 * kSfStageBytesA + j * kSfChunkBytes) / 16));
                         }
 #pragma unroll
                         for (int kk = 0; kk < BK_BYTES / 32; ++kk)
