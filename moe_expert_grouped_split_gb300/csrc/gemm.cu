@@ -687,6 +687,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             }
             // TMEM loads are issued two chunks (SiLU: two gate + two up chunks)
             // ahead of one wait, so their latencies overlap
+            bool released = false;
             if (EPI == EPI_SILU) {
                 __nv_bfloat16* D = reinterpret_cast<__nv_bfloat16*>(p.D);
 #pragma unroll 1
@@ -698,6 +699,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                         tmem_ld32(taddr + BN / 2 + (c + h) * 32, uv[h]);
                     }
                     tmem_wait_ld();
+                    if (c + 2 >= BN / 2 / 32) {
+                        // the last chunks are in registers: hand the accumulator
+                        // back now, so the next tile's MMAs overlap this math
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tempty_bar(acc));
+                        released = true;
+                    }
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int col = n * (BN / 2) + (c + h) * 32;
@@ -751,9 +760,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            if (!released) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(acc));
+            }
             if (++acc == F::kAccBufs) {
                 acc = 0;
                 acc_phase ^= 1u;
