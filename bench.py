@@ -93,6 +93,9 @@ def parse(argv=None):
                    help="prefetch slice size in MB (default 16 for the 4-layer pipeline, as that workload "
                         "specifies, else 32: the fastest single-destination setting measured)")
     p.add_argument("--copy-streams", type=int, default=1)
+    p.add_argument("--stages", type=int, default=2,
+                   help="staging buffers (2: the pages' double buffering; 3: the copy of layer l+2 may start "
+                        "while layer l computes)")
     p.add_argument("--prefetch-start", choices=["layer", "route"], default="route",
                    help="when the next layer's copy may start: with the layer, or once its routing is done")
     p.add_argument("--group", type=int, default=4,
@@ -266,7 +269,7 @@ class Workload:
     and per-layer token batches, all resident in HBM."""
 
     def __init__(self, spec: Spec, chunk_bytes, n_copy_streams, n_layers=2, base_seed=0, wdtype="bf16",
-                 peer_pools="device", prefetch_start="route"):
+                 peer_pools="device", prefetch_start="route", n_stages=2):
         import torch
 
         from moe_expert_grouped_split_gb300 import binding as B
@@ -291,8 +294,12 @@ class Workload:
                         h.copy_(t)
                         pools[i] = h
             torch.cuda.empty_cache()
+        if n_stages < 2:
+            raise ValueError("the benchmark overlaps the copy: it needs at least 2 stages")
+        self.n_stages = n_stages
         self.rt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, n_layers, self.placement.n_remote(),
-                            weight_dtype={"bf16": B.DTYPE_BF16, "fp8": B.DTYPE_E4M3, "nvfp4": B.DTYPE_NVFP4}[wdtype])
+                            weight_dtype={"bf16": B.DTYPE_BF16, "fp8": B.DTYPE_E4M3, "nvfp4": B.DTYPE_NVFP4}[wdtype],
+                            n_stages=n_stages)
         for l, lw in enumerate(self.layers):
             self.rt.set_layer(l, lw)
         self.x = [I.make_tokens(sh.T, sh.H, base_seed, step=s, device="cuda") for s in range(n_layers)]
@@ -325,15 +332,23 @@ class Workload:
         self.issue_s.append(time.perf_counter() - t0)
 
     def step(self, i, prefetch_next=True, x=None, out=None):
-        """Step i of the two-layer alternation: layer i%2 from stage i%2, and
-        the prefetch of layer (i+1)%2 into the other stage."""
+        """Step i of the layer alternation: layer i % n_layers from stage
+        i % S, then the prefetch of step i + S - 1's layer into its stage
+        (S = 2: the next layer into the other stage).  Without prefetch_next
+        every layer is already staged at stage = layer."""
         l = i % self.n_layers
-        self.layer_step(l, i % 2, x=x, out=out)
-        if prefetch_next:
-            self.prefetch((i + 1) % self.n_layers, (i + 1) % 2)
+        if not prefetch_next:
+            self.layer_step(l, l, x=x, out=out)
+            return
+        S = self.n_stages
+        self.layer_step(l, i % S, x=x, out=out)
+        j = i + S - 1
+        self.prefetch(j % self.n_layers, j % S)
 
     def prologue(self):
-        self.prefetch(0, 0)
+        """The copies of steps 0 .. S-2, before step 0."""
+        for j in range(self.n_stages - 1):
+            self.prefetch(j % self.n_layers, j)
 
     def sync(self):
         self.torch.cuda.synchronize()
@@ -479,7 +494,7 @@ def run_layer_bench(args, world, local_rank, barrier):
     torch.cuda.set_device(local_rank)
     spec = WORKLOADS[args.workload](group=args.group)
     wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, wdtype=args.dtype, peer_pools=args.peer_pools,
-                  prefetch_start=args.prefetch_start)
+                  prefetch_start=args.prefetch_start, n_stages=args.stages)
     sh = wl.shape
     K, W = args.steps, args.warmup
     phases = [_events(torch, 7) for _ in range(K)]
@@ -635,7 +650,8 @@ def run_pipeline_bench(args, world, local_rank, barrier):
     torch.cuda.set_device(local_rank)
     spec = WORKLOADS[args.workload](group=args.group)
     wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, n_layers=4, wdtype=args.dtype,
-                  prefetch_start=args.prefetch_start)
+                  prefetch_start=args.prefetch_start, n_stages=args.stages)
+    S = wl.n_stages
     sh = wl.shape
     steps = args.steps
     Ts = I.step_token_counts(steps + args.warmup, 6554, 8192, 0)
@@ -656,16 +672,17 @@ def run_pipeline_bench(args, world, local_rank, barrier):
         for s in range(s_from, s_to):
             for l in range(4):
                 lay = layer_of(g)
-                stage = g % 2 if with_copies else lay % 2
+                stage = g % S if with_copies else lay % 2
                 wl.layer_step(lay, stage, T=Ts[s])
-                if with_copies:
-                    wl.prefetch(layer_of(g + 1), (g + 1) % 2)
+                if with_copies:   # the layer S - 1 ahead into its stage
+                    wl.prefetch(layer_of(g + S - 1), (g + S - 1) % S)
                 attn_standin(layer_of(g + 1), s)
                 g += 1
 
     ev = lambda: _events(torch, 2)
-    # overlapped: prologue (layer 0 into stage 0) outside the timed steps
-    wl.prefetch(0, 0)
+    # overlapped: prologue (the first S - 1 layers into their stages) outside the timed steps
+    for j in range(S - 1):
+        wl.prefetch(j, j)
     run(0, args.warmup, True)
     wl.sync()
     barrier()
@@ -839,7 +856,7 @@ def main():
                    "shared": sh.S, "local_experts": int((wl.placement.local_slot >= 0).sum()),
                    "remote_experts": wl.placement.n_remote(), "peer_pools": wl.placement.n_peers,
                    "chunk_mb": args.chunk_mb, "copy_streams": args.copy_streams, "expert_weights": args.dtype,
-                   "prefetch_start": args.prefetch_start,
+                   "prefetch_start": args.prefetch_start, "stages": args.stages,
                    "peer_pool_memory": args.peer_pools,
                    "layers": wl.n_layers,
                    "dwdp_group": args.group,

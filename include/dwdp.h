@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define DWDP_ABI_VERSION 3
+#define DWDP_ABI_VERSION 4
 #define DWDP_MAX_EXPERTS 1024
 #define DWDP_MAX_TOPK 32
 #define DWDP_MAX_LAYERS 256
@@ -82,7 +82,10 @@ typedef struct {
     int32_t n_layers;     /* layers that get an expert map: 1..DWDP_MAX_LAYERS */
     int32_t stage_slots;  /* experts each staging buffer holds (0 = no staging) */
     int32_t weight_dtype; /* DWDP_DTYPE_BF16, DWDP_DTYPE_E4M3 or DWDP_DTYPE_NVFP4 */
+    int32_t n_stages;     /* staging buffers: 0 = 2 (the pages' double buffering); 1..DWDP_MAX_STAGES */
 } dwdp_config;
+
+#define DWDP_MAX_STAGES 4
 
 /* Expert weight types.  DWDP_DTYPE_E4M3 (an FP8 variant of the layer; the
  * pages run NVFP4 expert weights, DWDP §5.1): pools and stage buffers hold
@@ -157,11 +160,14 @@ typedef struct {
 int32_t dwdp_version(void);
 
 /* Create a context on the current CUDA device.  stage_w13[s] / stage_w2[s]
- * (s = 0, 1) are the caller's two staging buffers ([DWDP] §2: double
- * buffering), each [stage_slots][2I][H] / [stage_slots][H][I] bf16; they may
- * be NULL when cfg->stage_slots == 0.  On success *out owns the events and
- * descriptors listed above.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
-int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* const stage_w2[2],
+ * (s = 0 .. n_stages - 1, n_stages = cfg->n_stages or 2 when that is 0) are
+ * the caller's staging buffers ([DWDP] §2: double buffering; a third stage
+ * lets the copy of layer l + 2 start while layer l computes, so the copy
+ * stream can run back to back), each [stage_slots][2I][H] /
+ * [stage_slots][H][I] in the weight format; they may be NULL when
+ * cfg->stage_slots == 0.  On success *out owns the events and descriptors
+ * listed above.  Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[], void* const stage_w2[],
                     dwdp_ctx** out);
 
 /* Destroy a context (waits for nothing; the caller synchronises first). */

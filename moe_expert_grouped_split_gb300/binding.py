@@ -39,7 +39,8 @@ class DwdpError(RuntimeError):
 class dwdp_config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
-                ("n_layers", ctypes.c_int32), ("stage_slots", ctypes.c_int32), ("weight_dtype", ctypes.c_int32)]
+                ("n_layers", ctypes.c_int32), ("stage_slots", ctypes.c_int32), ("weight_dtype", ctypes.c_int32),
+                ("n_stages", ctypes.c_int32)]
 
 
 class dwdp_pool(ctypes.Structure):
@@ -141,10 +142,13 @@ def dwdp_version() -> int:
 
 
 def dwdp_create(hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots,
-                stage_w13=(None, None), stage_w2=(None, None), weight_dtype=DTYPE_BF16) -> int:
-    cfg = dwdp_config(hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots, weight_dtype)
-    s13 = (_VP * 2)(_ptr(stage_w13[0]), _ptr(stage_w13[1]))
-    s2 = (_VP * 2)(_ptr(stage_w2[0]), _ptr(stage_w2[1]))
+                stage_w13=(None, None), stage_w2=(None, None), weight_dtype=DTYPE_BF16, n_stages=0) -> int:
+    """n_stages 0 means 2; stage_w13 / stage_w2 hold one buffer (or None) per stage."""
+    cfg = dwdp_config(hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots, weight_dtype,
+                      n_stages)
+    n = max(len(stage_w13), len(stage_w2), n_stages or 2)
+    s13 = (_VP * n)(*[_ptr(stage_w13[i]) if i < len(stage_w13) else None for i in range(n)])
+    s2 = (_VP * n)(*[_ptr(stage_w2[i]) if i < len(stage_w2) else None for i in range(n)])
     out = _VP()
     _check(None, lib().dwdp_create(ctypes.byref(cfg), s13, s2, ctypes.byref(out)))
     return out.value
@@ -291,25 +295,27 @@ class RouteBuffers:
 
 
 class Runtime:
-    """One dwdp context with its two stage buffers and a workspace (torch
-    allocations); methods forward to the C ABI."""
+    """One dwdp context with its stage buffers (two by default) and a
+    workspace (torch allocations); methods forward to the C ABI."""
 
     def __init__(self, hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots,
-                 device="cuda", weight_dtype=DTYPE_BF16):
+                 device="cuda", weight_dtype=DTYPE_BF16, n_stages=2):
         import torch
         self.cfg = dict(hidden=hidden, inter=inter, n_experts=n_experts, top_k=top_k, n_shared=n_shared,
                         max_tokens=max_tokens, n_layers=n_layers, stage_slots=stage_slots)
         self.weight_dtype = weight_dtype
+        self.n_stages = n_stages
         if stage_slots > 0:
             b13 = weight_slot_bytes(2 * inter, hidden, weight_dtype)
             b2 = weight_slot_bytes(hidden, inter, weight_dtype)
-            self.stage_w13 = [torch.empty((stage_slots, b13), dtype=torch.uint8, device=device) for _ in range(2)]
-            self.stage_w2 = [torch.empty((stage_slots, b2), dtype=torch.uint8, device=device) for _ in range(2)]
+            self.stage_w13 = [torch.empty((stage_slots, b13), dtype=torch.uint8, device=device)
+                              for _ in range(n_stages)]
+            self.stage_w2 = [torch.empty((stage_slots, b2), dtype=torch.uint8, device=device) for _ in range(n_stages)]
         else:
-            self.stage_w13 = [None, None]
-            self.stage_w2 = [None, None]
+            self.stage_w13 = [None] * n_stages
+            self.stage_w2 = [None] * n_stages
         self.ctx = dwdp_create(hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots,
-                               self.stage_w13, self.stage_w2, weight_dtype)
+                               self.stage_w13, self.stage_w2, weight_dtype, n_stages)
         self.ws_bytes = max(256, dwdp_workspace_bytes(self.ctx, max_tokens))
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
         self._keep = {}

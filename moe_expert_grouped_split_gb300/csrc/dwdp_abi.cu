@@ -117,18 +117,28 @@ struct dwdp_ctx {
     int device = 0;
     int n_sms = 0;
     int fmt = FMT_BF16;  // expert weight format (weight_dtype)
-    void* stage13[2] = {nullptr, nullptr};
-    void* stage2[2] = {nullptr, nullptr};
-    CUtensorMap stage_map13[2]{}, stage_map2[2]{};
-    cudaEvent_t ready[2] = {nullptr, nullptr};
-    cudaEvent_t freed[2] = {nullptr, nullptr};
-    int stage_layer[2] = {-1, -1};
+    int n_stages = 2;
+    void* stage13[DWDP_MAX_STAGES] = {};
+    void* stage2[DWDP_MAX_STAGES] = {};
+    CUtensorMap stage_map13[DWDP_MAX_STAGES]{}, stage_map2[DWDP_MAX_STAGES]{};
+    cudaEvent_t ready[DWDP_MAX_STAGES] = {};
+    cudaEvent_t freed[DWDP_MAX_STAGES] = {};
+    int stage_layer[DWDP_MAX_STAGES] = {-1, -1, -1, -1};
     std::vector<LayerMap> layers;
     int* d_err = nullptr;
-    cudaEvent_t phase[DWDP_PHASE_EVENTS] = {};
+    cudaEvent_t phase[DWDP_PHASE_EVENTS] = {};  // the caller's (dwdp_set_phase_events)
     bool phases_on = false;
     std::string err;
     std::unique_ptr<GemmArgs> args;
+    // frees what the context made, also after a dwdp_create that failed half-way
+    ~dwdp_ctx() {
+        for (int s = 0; s < DWDP_MAX_STAGES; ++s) {
+            if (ready[s]) cudaEventDestroy(ready[s]);
+            if (freed[s]) cudaEventDestroy(freed[s]);
+        }
+        for (LayerMap& m : layers) m.release();
+        if (d_err) cudaFree(d_err);
+    }
 };
 
 namespace {
@@ -288,7 +298,7 @@ const char* dwdp_last_error(const dwdp_ctx* ctx) {
     return ctx ? ctx->err.c_str() : g_last_error.c_str();
 }
 
-int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* const stage_w2[2],
+int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[], void* const stage_w2[],
                     dwdp_ctx** out) {
     if (!cfg || !out) return fail(nullptr, DWDP_ERR_INVALID_ARG, "cfg and out must not be NULL");
     *out = nullptr;
@@ -308,14 +318,18 @@ int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* cons
                     DWDP_MAX_EXPERTS, DWDP_MAX_TOPK, DWDP_MAX_LAYERS);
     if ((int64_t)c.max_tokens * (c.top_k + c.n_shared) >= (int64_t)1 << 31)
         return fail(nullptr, DWDP_ERR_UNSUPPORTED, "max_tokens * (k + n_shared) must stay below 2^31");
+    const int n_stages = c.n_stages == 0 ? 2 : c.n_stages;
+    if (n_stages < 1 || n_stages > DWDP_MAX_STAGES)
+        return fail(nullptr, DWDP_ERR_INVALID_ARG, "n_stages must be 0 (= 2) or 1..%d", DWDP_MAX_STAGES);
     if (c.stage_slots > 0) {
-        for (int s = 0; s < 2; ++s)
+        for (int s = 0; s < n_stages; ++s)
             if (!stage_w13 || !stage_w2 || !stage_w13[s] || !stage_w2[s] || !aligned16(stage_w13[s]) ||
                 !aligned16(stage_w2[s]))
                 return fail(nullptr, DWDP_ERR_INVALID_ARG, "stage buffers must be non-NULL, 16-byte aligned");
     }
     std::unique_ptr<dwdp_ctx> ctx(new dwdp_ctx());
     ctx->cfg = c;
+    ctx->n_stages = n_stages;
     ctx->fmt = c.weight_dtype;
     ctx->args.reset(new GemmArgs());
     cudaError_t e = cudaGetDevice(&ctx->device);
@@ -328,7 +342,7 @@ int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* cons
                     prop.major, prop.minor);
     ctx->n_sms = prop.multiProcessorCount;
     if (!encode_fn()) return fail(nullptr, DWDP_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < n_stages; ++s) {
         e = cudaEventCreateWithFlags(&ctx->ready[s], cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->freed[s], cudaEventDisableTiming);
         if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaEventCreate");
@@ -337,7 +351,7 @@ int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* cons
     if (e == cudaSuccess) e = cudaMemset(ctx->d_err, 0, 256);
     if (e != cudaSuccess) return cuda_fail(nullptr, e, "error word");
     if (c.stage_slots > 0) {
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < n_stages; ++s) {
             ctx->stage13[s] = stage_w13[s];
             ctx->stage2[s] = stage_w2[s];
             if (!encode_slots(&ctx->stage_map13[s], stage_w13[s], c.stage_slots, 2ull * c.inter, c.hidden,
@@ -352,16 +366,7 @@ int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[2], void* cons
     return DWDP_OK;
 }
 
-void dwdp_destroy(dwdp_ctx* ctx) {
-    if (!ctx) return;
-    for (int s = 0; s < 2; ++s) {
-        if (ctx->ready[s]) cudaEventDestroy(ctx->ready[s]);
-        if (ctx->freed[s]) cudaEventDestroy(ctx->freed[s]);
-    }
-    for (LayerMap& m : ctx->layers) m.release();
-    if (ctx->d_err) cudaFree(ctx->d_err);
-    delete ctx;
-}
+void dwdp_destroy(dwdp_ctx* ctx) { delete ctx; }
 
 size_t dwdp_workspace_bytes(const dwdp_ctx* ctx, int32_t T) {
     if (!ctx || T < 0) return 0;
@@ -440,7 +445,7 @@ int32_t dwdp_set_expert_map(dwdp_ctx* ctx, int32_t layer, const dwdp_pool* local
     m.scale2 = ctx->layers[layer].scale2;
     ctx->layers[layer].release();
     ctx->layers[layer] = std::move(m);
-    for (int s = 0; s < 2; ++s)
+    for (int s = 0; s < ctx->n_stages; ++s)
         if (ctx->stage_layer[s] == layer) ctx->stage_layer[s] = -1;  // staged bytes follow the old map
     return DWDP_OK;
 }
@@ -551,7 +556,8 @@ int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t 
     if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
     const dwdp_config& c = ctx->cfg;
     if (layer < 0 || layer >= c.n_layers) return fail(ctx, DWDP_ERR_INVALID_ARG, "layer %d out of range", layer);
-    if (stage < 0 || stage > 1) return fail(ctx, DWDP_ERR_INVALID_ARG, "stage must be 0 or 1");
+    if (stage < 0 || stage >= ctx->n_stages)
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "stage %d outside [0, %d)", stage, ctx->n_stages);
     if (chunk_bytes == 0) return fail(ctx, DWDP_ERR_INVALID_ARG, "chunk_bytes must be positive");
     if (!copy_streams || n_copy_streams < 1 || n_copy_streams > DWDP_MAX_PEERS)
         return fail(ctx, DWDP_ERR_INVALID_ARG, "need 1..%d copy streams", DWDP_MAX_PEERS);
@@ -612,7 +618,8 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     LayerMap& m = ctx->layers[layer];
     if (!m.mapped) return fail(ctx, DWDP_ERR_NOT_MAPPED, "layer %d has no expert map", layer);
     if (m.n_remote > 0) {
-        if (stage < 0 || stage > 1) return fail(ctx, DWDP_ERR_INVALID_ARG, "stage must be 0 or 1");
+        if (stage < 0 || stage >= ctx->n_stages)
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "stage %d outside [0, %d)", stage, ctx->n_stages);
         if (ctx->stage_layer[stage] != layer)
             return fail(ctx, DWDP_ERR_NOT_MAPPED, "stage %d holds layer %d, not layer %d", stage,
                         ctx->stage_layer[stage], layer);
@@ -765,7 +772,8 @@ int32_t dwdp_quantize_rows(int32_t weight_dtype, const void* x, int64_t rows, in
 
 int32_t dwdp_wait_stage(dwdp_ctx* ctx, int32_t stage, int32_t timeout_ms) {
     if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
-    if (stage < 0 || stage > 1 || timeout_ms < 0) return fail(ctx, DWDP_ERR_INVALID_ARG, "bad stage or timeout");
+    if (stage < 0 || stage >= ctx->n_stages || timeout_ms < 0)
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "bad stage or timeout");
     const auto t0 = std::chrono::steady_clock::now();
     for (;;) {
         cudaError_t e = cudaEventQuery(ctx->ready[stage]);
@@ -778,7 +786,7 @@ int32_t dwdp_wait_stage(dwdp_ctx* ctx, int32_t stage, int32_t timeout_ms) {
 }
 
 int32_t dwdp_stage_layer(const dwdp_ctx* ctx, int32_t stage) {
-    if (!ctx || stage < 0 || stage > 1) return -1;
+    if (!ctx || stage < 0 || stage >= ctx->n_stages) return -1;
     return ctx->stage_layer[stage];
 }
 

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), f"{n} not exported"
     bound = {s[0] for s in B.SIGNATURES}
     assert set(names) == bound, "binding and header disagree"
-    assert B.dwdp_version() == 3
+    assert B.dwdp_version() == 4
 
 
 def _random_map(rng, E, P, redundant=0.0):
@@ -113,6 +113,14 @@ def test_host_validation_without_gpu(lib):
     cfg = B.dwdp_config(256, 128, 8, 2, 0, 64, 1, 4)          # staging without buffers
     assert lib.dwdp_create(ctypes.byref(cfg), None, None, ctypes.byref(out)) == -1
     assert "stage" in B.dwdp_last_error(None)
+    for n_stages in (5, -1):                                    # stage count outside 0 (= 2), 1..4
+        cfg = B.dwdp_config(256, 128, 8, 2, 0, 64, 1, 0, B.DTYPE_BF16, n_stages)
+        assert lib.dwdp_create(ctypes.byref(cfg), None, None, ctypes.byref(out)) == -1
+        assert "n_stages" in B.dwdp_last_error(None)
+    # three stages, one missing buffer
+    cfg = B.dwdp_config(256, 128, 8, 2, 0, 64, 1, 4, B.DTYPE_BF16, 3)
+    bufs = (ctypes.c_void_p * 3)(256, 512, None)
+    assert lib.dwdp_create(ctypes.byref(cfg), bufs, bufs, ctypes.byref(out)) == -1
     assert lib.dwdp_workspace_bytes(None, 10) == 0
     # activation quantization: argument checks come before any CUDA call
     x = ctypes.c_void_p(16)

@@ -27,9 +27,13 @@ def _layers(dtype, shape, pl):
     return [make(shape, pl, 11, l, device="cuda") for l in range(N_LAYERS)]
 
 
-def _run(dtype, shape, pl, lws, xs, overlapped, chunk):
+def _run(dtype, shape, pl, lws, xs, overlapped, chunk, n_stages=2):
+    """Layer l reads stage l % S; after it is enqueued, layer l + S - 1 is
+    prefetched into stage (l + S - 1) % S, which layer l - 1 read (S = 2:
+    the next layer into the other stage)."""
+    S = n_stages
     rt = B.Runtime(shape.H, shape.I, shape.E, shape.k, shape.S, shape.T, N_LAYERS, pl.n_remote(),
-                   weight_dtype=dtype)
+                   weight_dtype=dtype, n_stages=S)
     try:
         for l, lw in enumerate(lws):
             rt.set_layer(l, lw)
@@ -37,19 +41,20 @@ def _run(dtype, shape, pl, lws, xs, overlapped, chunk):
         copy = [torch.cuda.Stream()]
         rbs = [B.RouteBuffers(x.shape[0], shape.E, shape.k) for x in xs]
         outs = [torch.empty((x.shape[0], shape.H), dtype=torch.bfloat16, device="cuda") for x in xs]
-        rt.prefetch(0, 0, chunk, copy)
+        for j in range(min(S - 1, N_LAYERS)):
+            rt.prefetch(j, j, chunk, copy)
         for l in range(N_LAYERS):
-            s = l % 2
+            s = l % S
             if not overlapped:
                 assert rt.wait_stage(s, 20_000) == 0
             rt.route(xs[l], lws[l].wr, None, rbs[l], compute)
             rt.moe(l, s, xs[l], rbs[l], outs[l], compute)
             if not overlapped:
                 compute.synchronize()
-            if l + 1 < N_LAYERS:
-                # into the other stage, which layer l-1 read: the context makes
-                # the copy wait for that layer's down GEMM
-                rt.prefetch(l + 1, 1 - s, chunk, copy)
+            if l + S - 1 < N_LAYERS:
+                # the context makes the copy wait for the down GEMM of the
+                # last layer that read that stage
+                rt.prefetch(l + S - 1, (l + S - 1) % S, chunk, copy)
         torch.cuda.synchronize()
         assert rt.device_status() == 0
         return [o.clone() for o in outs], rbs
@@ -61,7 +66,8 @@ def _run(dtype, shape, pl, lws, xs, overlapped, chunk):
 @pytest.mark.parametrize("ragged", [False, True], ids=["fixed_T", "ragged_T"])
 def test_overlapped_layers_equal_serialised(dtype, ragged):
     """ragged: each layer gets its own token count (one workspace sized for
-    the largest), as in the benchmark's 4-layer pipeline."""
+    the largest), as in the benchmark's 4-layer pipeline.  Two stages (the
+    pages' double buffering) and three (copies two layers ahead)."""
     build()
     shape = I.LayerShape(T=300, H=512, I=256, E=12, k=2, S=1)
     pl = I.split_placement(12, 4, 2)
@@ -69,10 +75,11 @@ def test_overlapped_layers_equal_serialised(dtype, ragged):
     Ts = [300, 257, 129, 1] if ragged else [shape.T] * N_LAYERS
     xs = [I.make_tokens(Ts[l], shape.H, 3, step=l).cuda() for l in range(N_LAYERS)]
     ser, _ = _run(dtype, shape, pl, lws, xs, overlapped=False, chunk=1 << 20)
-    for chunk in (50_000, 1 << 20):
-        ovl, _ = _run(dtype, shape, pl, lws, xs, overlapped=True, chunk=chunk)
+    for n_stages, chunk in ((2, 50_000), (2, 1 << 20), (3, 50_000), (4, 1 << 20)):
+        ovl, _ = _run(dtype, shape, pl, lws, xs, overlapped=True, chunk=chunk, n_stages=n_stages)
         for l in range(N_LAYERS):
-            assert torch.equal(ovl[l], ser[l]), f"layer {l} differs from the serialised run (chunk {chunk})"
+            assert torch.equal(ovl[l], ser[l]), \
+                f"layer {l} differs from the serialised run ({n_stages} stages, chunk {chunk})"
 
 
 def test_overlapped_layers_match_oracle():

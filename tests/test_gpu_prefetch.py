@@ -1,8 +1,9 @@
 """dwdp_prefetch_layer (DWDP §2 double-buffered prefetch, §4.3.2 round-robin
 slices): staged bytes equal their sources exactly, stage/layer bookkeeping
-is enforced (device and pinned-host peer pools), and the host-side bounded
-wait reports a timeout without faulting or hanging anything (the copy stream
-is held back by a short GPU sleep, then released)."""
+is enforced (device and pinned-host peer pools, two or three stages), and
+the host-side bounded wait reports a timeout without faulting or hanging
+anything (the copy stream is held back by a short GPU sleep, then
+released)."""
 import numpy as np
 import pytest
 import torch
@@ -14,12 +15,13 @@ from moe_expert_grouped_split_gb300.build import build
 pytestmark = pytest.mark.gpu
 
 
-def _setup(n_layers=2):
+def _setup(n_layers=2, n_stages=2):
     build()
     shape = I.LayerShape(T=64, H=256, I=128, E=12, k=2, S=1)
     pl = I.split_placement(12, 3, 3)
     lws = [I.make_layer(shape, pl, 5, l, device="cuda") for l in range(n_layers)]
-    rt = B.Runtime(shape.H, shape.I, shape.E, shape.k, shape.S, shape.T, n_layers, pl.n_remote())
+    rt = B.Runtime(shape.H, shape.I, shape.E, shape.k, shape.S, shape.T, n_layers, pl.n_remote(),
+                   n_stages=n_stages)
     for l, lw in enumerate(lws):
         rt.set_layer(l, lw)
     return shape, pl, lws, rt
@@ -110,6 +112,43 @@ def test_stage_must_hold_the_layer():
         rt.moe(0, 1, x, rb, out)                       # stage 1 holds layer 0
         torch.cuda.synchronize()
         assert rt.device_status() == 0
+    finally:
+        rt.close()
+
+
+def test_stage_count():
+    """A context has n_stages staging buffers (2 by default): stage indexes
+    outside [0, n_stages) are rejected before anything is enqueued; with
+    three, stage 2 holds a layer like the others."""
+    shape, pl, lws, rt = _setup()
+    try:
+        s = torch.cuda.Stream()
+        with pytest.raises(B.DwdpError) as ei:
+            rt.prefetch(0, 2, 1 << 20, [s])
+        assert ei.value.code == -1 and "stage 2" in str(ei.value)
+        assert B.dwdp_stage_layer(rt.ctx, 2) == -1
+    finally:
+        rt.close()
+    shape, pl, lws, rt = _setup(n_stages=3)
+    try:
+        x = I.make_tokens(shape.T, shape.H, 0).cuda()
+        rb = B.RouteBuffers(shape.T, shape.E, shape.k)
+        out2 = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
+        out0 = torch.empty_like(out2)
+        rt.prefetch(1, 2, 1 << 20, [torch.cuda.Stream()])
+        rt.prefetch(1, 0, 1 << 20, [torch.cuda.Stream()])
+        assert rt.wait_stage(2, 20_000) == 0 and B.dwdp_stage_layer(rt.ctx, 2) == 1
+        e13, e2 = _expected_stage(lws[1], pl)
+        n = e13.shape[0]
+        assert torch.equal(rt.stage_w13[2][:n], e13.view(torch.uint8).reshape(n, -1))
+        rt.route(x, lws[1].wr, None, rb)
+        rt.moe(1, 2, x, rb, out2)
+        rt.moe(1, 0, x, rb, out0)
+        torch.cuda.synchronize()
+        assert rt.device_status() == 0 and torch.equal(out2, out0)
+        with pytest.raises(B.DwdpError) as ei:
+            rt.moe(1, 3, x, rb, out2)
+        assert ei.value.code == -1
     finally:
         rt.close()
 
