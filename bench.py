@@ -96,8 +96,9 @@ def parse(argv=None):
     p.add_argument("--stages", type=int, default=2,
                    help="staging buffers (2: the pages' double buffering; 3: the copy of layer l+2 may start "
                         "while layer l computes)")
-    p.add_argument("--prefetch-start", choices=["layer", "route"], default="route",
-                   help="when the next layer's copy may start: with the layer, or once its routing is done")
+    p.add_argument("--prefetch-start", choices=["layer", "route", "gate_up"], default="route",
+                   help="when a layer's copy may start, besides its stage being free: with the current layer, "
+                        "once its routing is done, or once its gate/up GEMM is done (best with --stages 3)")
     p.add_argument("--group", type=int, default=4,
                    help="DWDP group size N: E/N experts resident, the rest staged from N-1 peer pools")
     p.add_argument("--dtype", default="bf16", choices=["bf16", "fp8", "nvfp4"],
@@ -310,9 +311,17 @@ class Workload:
         self.chunk = int(chunk_bytes)
         self.issue_s = []
         # "route": the copy streams wait for the current layer's routing, so
-        # the small latency-bound routing kernels run without the copy
+        # the small latency-bound routing kernels run without the copy;
+        # "gate_up": for its gate/up GEMM (the library's phase event 4), so
+        # the copy overlaps the down GEMM, the combine and the next layer's
+        # routing first
         self.prefetch_start = prefetch_start
         self.routed = torch.cuda.Event()
+        self.gate_ev = [torch.cuda.Event() for _ in range(B.DWDP_PHASE_EVENTS)]
+        for e in self.gate_ev:       # torch creates the CUDA event on its first record
+            e.record()
+        self.gated_by = None      # the phase events of the last layer step
+        self._phases_set = False
 
     def layer_step(self, layer, stage, T=None, x=None, out=None):
         T = self.shape.T if T is None else T
@@ -323,20 +332,34 @@ class Workload:
             self.routed.record(self.compute)
             self.rt.moe(layer, stage, x, self.rb, out, self.compute)
 
+    def set_phases(self, events):
+        """Phase events for the following layer steps (None: none)."""
+        if events is not None or self._phases_set:
+            self.B.dwdp_set_phase_events(self.rt.ctx, events)
+        self._phases_set = events is not None
+
     def prefetch(self, layer, stage):
         t0 = time.perf_counter()
         if self.prefetch_start == "route":
             for c in self.copies:
                 c.wait_event(self.routed)
+        elif self.prefetch_start == "gate_up" and self.gated_by is not None:
+            for c in self.copies:
+                c.wait_event(self.gated_by[4])
         self.rt.prefetch(layer, stage, self.chunk, self.copies)
         self.issue_s.append(time.perf_counter() - t0)
 
-    def step(self, i, prefetch_next=True, x=None, out=None):
+    def step(self, i, prefetch_next=True, x=None, out=None, phases=None):
         """Step i of the layer alternation: layer i % n_layers from stage
         i % S, then the prefetch of step i + S - 1's layer into its stage
         (S = 2: the next layer into the other stage).  Without prefetch_next
-        every layer is already staged at stage = layer."""
+        every layer is already staged at stage = layer.  phases: the timing
+        events of this step, or None."""
         l = i % self.n_layers
+        gate = self.prefetch_start == "gate_up" and prefetch_next
+        ev = phases if phases is not None else (self.gate_ev if gate else None)
+        self.set_phases(ev)
+        self.gated_by = ev
         if not prefetch_next:
             self.layer_step(l, l, x=x, out=out)
             return
@@ -384,11 +407,9 @@ def run_overlapped(wl, K, W, world, phases, clocks_index=0, barrier=lambda: None
         for c in wl.copies:
             c.wait_stream(wl.compute)
         for i in range(K):
-            if phases is not None:
-                B.dwdp_set_phase_events(wl.rt.ctx, phases[i])
-            wl.step(n)
+            wl.step(n, phases=phases[i] if phases is not None else None)
             n += 1
-        B.dwdp_set_phase_events(wl.rt.ctx, None)
+        wl.set_phases(None)
         for c in wl.copies:
             wl.compute.wait_stream(c)
         stop.record(wl.compute)
@@ -411,10 +432,8 @@ def run_compute_only(wl, K, phases=None):
     a, b = _events(torch, 2)
     a.record(wl.compute)
     for i in range(K):
-        if phases is not None:
-            B.dwdp_set_phase_events(wl.rt.ctx, phases[i])
-        wl.step(i, prefetch_next=False)
-    B.dwdp_set_phase_events(wl.rt.ctx, None)
+        wl.step(i, prefetch_next=False, phases=phases[i] if phases is not None else None)
+    wl.set_phases(None)
     b.record(wl.compute)
     b.synchronize()
     return a.elapsed_time(b) / K
@@ -669,6 +688,9 @@ def run_pipeline_bench(args, world, local_rank, barrier):
 
     def run(s_from, s_to, with_copies, layer_of=lambda g: g % 4):
         g = s_from * 4
+        gate = with_copies and wl.prefetch_start == "gate_up"
+        wl.set_phases(wl.gate_ev if gate else None)
+        wl.gated_by = wl.gate_ev if gate else None
         for s in range(s_from, s_to):
             for l in range(4):
                 lay = layer_of(g)
