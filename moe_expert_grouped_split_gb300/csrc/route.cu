@@ -196,7 +196,8 @@ __global__ void __launch_bounds__(1024) place_kernel(const int32_t* __restrict__
 //   chunk_place:  pair f of chunk c with expert e goes to row base[c][e] +
 //                 (pairs of e earlier in the chunk), ranked with warp
 //                 match_any inside a warp and per-warp counts across warps.
-// Every row is the stable (ascending flat index) position, as before.
+// Every row is the stable (ascending flat index) position, the one
+// count_kernel + place_kernel give.
 constexpr int kChunk = 1024;
 
 __global__ void __launch_bounds__(kChunk) chunk_count_kernel(const int32_t* __restrict__ ids, int n, int E,
@@ -527,7 +528,8 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
 
 // ------------------------------------------------------------- NVFP4 --
 // Activation rows to NVFP4 for the block-scaled GEMMs.  Per row of n bf16
-// values (n a multiple of 256): s = amax / 2688 (1 for an all-zero row),
+// values (n a multiple of 64; a lane takes two adjacent blocks at a time):
+// s = amax / 2688 (1 for an all-zero row),
 // d = 6 s; per 16-element block, its E4M3 scale sf = E4M3(amax_block / d)
 // (round to nearest even, saturating) and, with eff = value(sf) * s, each
 // element's E2M1 code of v / eff (round to nearest even, saturating; all
