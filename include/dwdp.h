@@ -9,9 +9,9 @@
  *   [news] the thecoregrid.dev news summary of the same paper.
  *
  * One rank runs one MoE block per layer.  Some experts of each layer are
- * resident ("local"); the others live on peers and are pulled into one of two
- * staging buffers by asynchronous copies while the previous layer computes
- * ([DWDP] §2 Methodology Overview).  The grouped GEMM reads each expert from
+ * resident ("local"); the others live on peers and are pulled into one of the
+ * staging buffers (two by default: double buffering) by asynchronous copies
+ * while the previous layer computes ([DWDP] §2 Methodology Overview).  The grouped GEMM reads each expert from
  * whichever buffer holds it through a per-expert table, with no merge copy
  * ([DWDP] §4.2).  Copies are cut into fixed-size slices issued round-robin
  * over the sources ([DWDP] §4.3.2; [news]).  On one GPU the peers are emulated
@@ -249,7 +249,10 @@ int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t 
  * holds dwdp_route's outputs for the same x (offsets, inv_perm and topk_w are
  * read; NVFP4 contexts also read topk_ids).  In E4M3 and NVFP4 contexts x
  * and a are quantized per row first (see DWDP_DTYPE_*) and the GEMMs run on
- * the codes.  out [T][H] bf16 (device).
+ * the codes.  out [T][H] bf16 (device).  An inv_perm entry outside
+ * [0, T*k) is not followed: the kernels skip it (the token's output then
+ * lacks that expert) and set the device error word, which
+ * dwdp_device_status reports as DEVICE_CHECK.
  * Errors: INVALID_ARG, NOT_MAPPED, UNSUPPORTED, CUDA. */
 int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* x, int32_t T,
                        const dwdp_route_out* route, void* out, void* ws, size_t ws_bytes,
