@@ -15,11 +15,16 @@
 //               NVFP4: one accumulator and a ring of block scales) and issues
 //               tcgen05.mma (M=128, N=256, 32 bytes of K each) from one thread.
 //   warps 2..5  epilogue: tcgen05.ld the accumulator rows of their TMEM lane
-//               quarter, apply SiLU(gate)*up or plain conversion, store.
+//               quarter, hand the accumulator back to warp 1 as soon as the
+//               last loads land, apply SiLU(gate)*up or plain conversion,
+//               store.
 // Tiles are enumerated group by group, n-tile by n-tile, m-tile fastest, and
-// dealt to CTAs round-robin: CTAs running side by side share weight tiles in
-// L2.  Every wait is bounded (global timer); a wait that runs out sets a bit
-// in the device error word and the CTA drains its copies and exits.
+// dealt to CTAs round-robin; CTAs 2c and 2c+1 form a cluster, and when their
+// tiles are sibling m-tiles of one weight tile each loads half of it and
+// multicasts it to both.  EPI_F32 (the router) may also split K into parts,
+// each a tile with its own output plane.  Every wait is bounded (global
+// timer); a wait that runs out sets a bit in the device error word and the
+// CTA drains its copies and exits.
 #include <cuda_bf16.h>
 
 #include <algorithm>
