@@ -153,6 +153,35 @@ def test_stage_count():
         rt.close()
 
 
+def test_single_stage_serialises_layers():
+    """n_stages = 1: layer 1's copy into the only stage waits for layer 0's
+    down GEMM (the stage's free event), so the two layers run one after the
+    other, and their outputs equal those of a two-stage context."""
+    outs = {}
+    for n_stages in (1, 2):
+        shape, pl, lws, rt = _setup(n_stages=n_stages)
+        try:
+            copy = [torch.cuda.Stream()]
+            compute = torch.cuda.Stream()
+            res = []
+            for layer in (0, 1):
+                stage = 0 if n_stages == 1 else layer
+                x = I.make_tokens(shape.T, shape.H, 7, step=layer).cuda()
+                rb = B.RouteBuffers(shape.T, shape.E, shape.k)
+                out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
+                rt.prefetch(layer, stage, 50_000, copy)
+                rt.route(x, lws[layer].wr, None, rb, compute)
+                rt.moe(layer, stage, x, rb, out, compute)
+                res.append(out)
+            torch.cuda.synchronize()
+            assert rt.device_status() == 0
+            outs[n_stages] = [o.clone() for o in res]
+        finally:
+            rt.close()
+    for a, b in zip(outs[1], outs[2]):
+        assert torch.equal(a, b)
+
+
 def test_unmapped_layer_and_bad_arguments():
     build()
     rt = B.Runtime(256, 128, 8, 2, 0, 64, 2, 4)
