@@ -1,0 +1,50 @@
+"""The benchmark's algorithmic work per layer, against the figures the
+hot-path scope states for the 8192-token R1 layer (T = 8192, H = 7168,
+I = 2048, E = 256 routed experts all active, top-8, one shared expert,
+192 experts staged): 6.49 TFLOP of expert FLOPs plus 3.0e10 for the
+router, 4.33e12 FLOPs and 16.45 GB for the gate/up GEMM (w13 of 257
+experts, 58.72 MB each, plus the rows in and a out), 22.64 GB of expert
+weights read once (88.08 MB per expert), and the prefetch moving 16.91 GB
+read plus 16.91 GB written.  The roofline fractions the bench prints
+divide these by measured times, so a wrong term would misstate them."""
+import pytest
+
+import bench
+
+T, H, I, E, K, S, R = 8192, 7168, 2048, 256, 8, 1, 192
+MB = 1e6
+
+
+def test_layer_and_gate_up_flops():
+    router = 2 * T * H * E
+    assert router == pytest.approx(3.0e10, rel=0.01)
+    assert bench.layer_flops(T, H, I, E, K, S) - router == pytest.approx(6.49e12, rel=1e-3)
+    assert bench.g1_flops(T, H, I, K, S) == pytest.approx(4.33e12, rel=1e-3)
+
+
+def test_gate_up_bytes():
+    w13 = 2 * I * H * 2                      # one expert's gate/up weights, bf16
+    assert w13 / MB == pytest.approx(58.72, rel=1e-3)
+    assert bench.g1_bytes(T, H, I, E, K, S) / 1e9 == pytest.approx(16.45, rel=2e-3)
+    # E4M3 weights and rows: one byte per element, a still written in bf16
+    assert bench.g1_bytes(T, H, I, E, K, S, wb=1) == (E + S) * w13 // 2 + T * (K + S) * H + T * (K + S) * I * 2
+
+
+def test_step_bytes_terms():
+    expert = 3 * H * I * 2
+    assert expert / MB == pytest.approx(88.08, rel=1e-3)
+    weights = (E + S) * expert
+    assert weights / 1e9 == pytest.approx(22.64, rel=1e-3)
+    prefetch = 2 * R * expert                # read + written on this GPU's memory
+    assert prefetch / 2 / 1e9 == pytest.approx(16.91, rel=1e-3)
+    xp, a, y, x_out = 2 * T * K * H * 2, 2 * T * (K + S) * I * 2, 2 * T * (K + S) * H * 2, 2 * T * H * 2
+    assert bench.step_bytes(T, H, I, E, K, S, R) == weights + xp + a + y + x_out + prefetch
+    # with no staged experts the copy term vanishes
+    assert bench.step_bytes(T, H, I, E, K, S, 0) == weights + xp + a + y + x_out
+
+
+def test_kernels_per_step_match_the_launch_lists():
+    # profiles/launches_r1_moe_layer_8k*.md: 9 (bf16), 11 (E4M3), 10 (NVFP4) kernels per step
+    assert bench.kernels_per_layer("bf16") == 9
+    assert bench.kernels_per_layer("fp8") == 11
+    assert bench.kernels_per_layer("nvfp4") == 10
