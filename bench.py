@@ -24,8 +24,12 @@ routing, 16 hottest experts replicated), r1_moe_layer_256 (decode-like;
 [6554, 8192], 16 steps) and r1_small_profile (for profiler captures).
 
 --impl reference runs the same metric with the CPU oracle on host cores.
-Multi-GPU: replicas only (each rank runs the same independent workload on
-its own GPU; no data-path collective); the timing is max over ranks.
+
+One GPU only: the DWDP rank's hot path runs on one GPU (its peers are
+emulated by device pools), and its grouped GEMM shares weight tiles between
+the two CTAs of a cluster with multicast loads, which are kept to one-GPU
+runs.  With --gpus > 1 or WORLD_SIZE > 1 the benchmark prints one JSON line
+saying so ("unavailable") and exits before building or loading the library.
 """
 from __future__ import annotations
 
@@ -106,7 +110,9 @@ def parse(argv=None):
                         "scales per 16-element block; next-row variants)")
     p.add_argument("--chunk-sweep", default="", help="comma-separated chunk sizes in MB (exposed copy per size)")
     p.add_argument("--merge-copy", action="store_true",
-                   help="also time the merge-copy baseline (one contiguous weight buffer per layer)")
+                   help="also time the merge-copy baseline (one contiguous weight buffer per layer); on by "
+                        "default for the 8K-token layer")
+    p.add_argument("--no-merge-copy", action="store_true", help="skip the merge-copy baseline")
     p.add_argument("--peer-pools", default="device", choices=["device", "host"],
                    help="where the emulated peers' pools live (host: pinned host memory, copies over the "
                         "host link, so only their writes use this GPU's HBM)")
@@ -115,6 +121,10 @@ def parse(argv=None):
     args = p.parse_args(argv)
     if args.chunk_mb is None:
         args.chunk_mb = 16.0 if args.workload == "r1_pipeline_4layer" else 32.0
+    if args.workload == "r1_moe_layer_8k" and not args.no_extras and args.group == 4:
+        args.merge_copy = True
+    if args.no_merge_copy:
+        args.merge_copy = False
     return args
 
 
@@ -244,21 +254,55 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def max_over_ranks(v: float, world: int, device="cuda") -> float:
-    """Max of a per-rank timing over all ranks (replicas: the job ends when
-    the slowest rank does)."""
-    if world <= 1:
-        return v
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+# nominal dense tensor-core throughput of each operand type relative to bf16
+# (2.25 / 4.5 / 13.5 PFLOP/s for bf16 / FP8 / FP4 on GB300)
+TC_RATIO = {"bf16": 1.0, "fp8": 2.0, "nvfp4": 6.0}
 
 
-def whole_job_rate(units_per_rank_step: int, steps: int, world: int, ms_max: float) -> float:
-    """Units processed by all ranks per second, timed by the slowest rank."""
-    return world * steps * units_per_rank_step / (ms_max / 1e3)
+def roofline_peaks(peaks: dict, src: str, wdtype: str):
+    """(tensor peak TFLOP/s, HBM peak GB/s, note) for the benchmark's GEMMs.
+    The burst bf16 figure applies: every timed kernel runs inside a timed
+    region of well under a second at full SM clock, while the sustained
+    figure was taken over seconds under the power cap at a lower clock.
+    FP8 / FP4 take the measured bf16 burst peak times the nominal ratio."""
+    r = TC_RATIO[wdtype]
+    tc = peaks["bf16_tflops"] * r
+    note = f"{src} bf16_tflops (burst)" + (f" x {r:g} (nominal dense {wdtype} / bf16 ratio)" if r != 1 else "")
+    return tc, peaks["hbm_gbs"], note
+
+
+def roofline_entry(kernel: str, flops: float, nbytes: float, seconds: float, tc_peak: float, hbm_peak: float,
+                   tc_note: str, hbm_note: str) -> dict:
+    """The kernel against the roof its arithmetic intensity puts it under:
+    intensity (FLOP per algorithmic HBM byte) at or above the ridge
+    tc_peak / hbm_peak -> tensor-bound, achieved TFLOP/s against tc_peak;
+    below it -> HBM-bound, achieved algorithmic GB/s against hbm_peak."""
+    ai = flops / nbytes
+    ridge = tc_peak * 1e12 / (hbm_peak * 1e9)
+    if ai >= ridge:
+        ach = flops / seconds / 1e12
+        return {"kernel": kernel, "bound": "tensor", "achieved": round(ach, 1), "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": round(ach / tc_peak, 4), "peak_source": tc_note, "arithmetic_intensity": round(ai, 1),
+                "ridge": round(ridge, 1)}
+    ach = nbytes / seconds / 1e9
+    return {"kernel": kernel, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(ach / hbm_peak, 4), "peak_source": hbm_note, "arithmetic_intensity": round(ai, 1),
+            "ridge": round(ridge, 1)}
+
+
+def whole_job_rate(units_per_step: int, steps: int, ms_total: float) -> float:
+    """Units processed per second over the timed steps."""
+    return steps * units_per_step / (ms_total / 1e3)
+
+
+def single_gpu_refusal(args, world: int):
+    """The JSON line printed instead of a measurement when more than one GPU
+    is asked for, or None for a one-GPU run."""
+    if world <= 1 and args.gpus <= 1:
+        return None
+    return {"metric": METRIC, "unit": UNIT, "n_gpus": max(world, args.gpus), "higher_is_better": True,
+            "unavailable": "single-GPU path: one DWDP rank on one GPU (peers emulated by device pools); its "
+                           "grouped GEMM's cluster-multicast loads are kept to one-GPU runs"}
 
 
 PHASES = ["route", "wait_stage", "gather", "gate_up_gemm", "down_gemm", "combine"]
@@ -390,9 +434,9 @@ def _phase_avg(phases, K):
     return {n_: round(sum(p[j] for p in ph) / K, 4) for j, n_ in enumerate(PHASES)}
 
 
-def run_overlapped(wl, K, W, world, phases, clocks_index=0, barrier=lambda: None):
+def run_overlapped(wl, K, W, phases, clocks_index=0):
     """K timed steps (after W warm-up steps) of the two-layer alternation with
-    the next layer's prefetch overlapped; max over ranks."""
+    the next layer's prefetch overlapped."""
     torch, B = wl.torch, wl.B
     wl.prologue()
     n = 0
@@ -400,7 +444,6 @@ def run_overlapped(wl, K, W, world, phases, clocks_index=0, barrier=lambda: None
         wl.step(n)
         n += 1
     wl.sync()
-    barrier()
     start, stop = _events(torch, 2)
     with ClockSampler(clocks_index) as clk:
         start.record(wl.compute)
@@ -415,7 +458,7 @@ def run_overlapped(wl, K, W, world, phases, clocks_index=0, barrier=lambda: None
         stop.record(wl.compute)
         stop.synchronize()
     assert wl.rt.device_status() == 0
-    ms_total = max_over_ranks(start.elapsed_time(stop), world)
+    ms_total = start.elapsed_time(stop)
     return ms_total, clk.summary()
 
 
@@ -453,7 +496,7 @@ def run_copy_only(wl, K):
     return a.elapsed_time(b) / K
 
 
-def run_e2e(wl, K, world, barrier=lambda: None):
+def run_e2e(wl, K):
     """The metric through the public API with host buffers: each step copies
     its tokens in from pinned host memory and its output back to pinned host
     memory, inside the timed region.  The copies run on their own streams,
@@ -490,7 +533,6 @@ def run_e2e(wl, K, world, barrier=lambda: None):
     for i in range(2):
         step(i)
     wl.sync()
-    barrier()
     a, b = _events(torch, 2)
     a.record(wl.compute)
     for s_ in wl.copies + [h2d, d2h]:
@@ -502,24 +544,23 @@ def run_e2e(wl, K, world, barrier=lambda: None):
     b.record(wl.compute)
     b.synchronize()
     assert wl.rt.device_status() == 0
-    e2e_ms = max_over_ranks(a.elapsed_time(b), world)
-    return {"value": round(whole_job_rate(T, K, world, e2e_ms), 1), "unit": UNIT,
+    e2e_ms = a.elapsed_time(b)
+    return {"value": round(whole_job_rate(T, K, e2e_ms), 1), "unit": UNIT,
             "h2d_bytes_per_step": T * sh.H * 2, "d2h_bytes_per_step": T * sh.H * 2}
 
 
-def run_layer_bench(args, world, local_rank, barrier):
+def run_layer_bench(args):
     """The single-layer workloads (8K default, Zipf 16K, 256 tokens)."""
     import torch
-    torch.cuda.set_device(local_rank)
+    torch.cuda.set_device(0)
     spec = WORKLOADS[args.workload](group=args.group)
     wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, wdtype=args.dtype, peer_pools=args.peer_pools,
                   prefetch_start=args.prefetch_start, n_stages=args.stages)
     sh = wl.shape
     K, W = args.steps, args.warmup
     phases = [_events(torch, 7) for _ in range(K)]
-    ms_total, clocks = run_overlapped(wl, K, W, world, phases, local_rank, barrier)
-    barrier()
-    res = {"ms_step": ms_total / K, "value": whole_job_rate(sh.T, K, world, ms_total),
+    ms_total, clocks = run_overlapped(wl, K, W, phases)
+    res = {"ms_step": ms_total / K, "value": whole_job_rate(sh.T, K, ms_total),
            "phase_ms": _phase_avg(phases, K), "clocks": clocks,
            "issue_ms": round(1e3 * sum(wl.issue_s) / max(1, len(wl.issue_s)), 3)}
     e_active = int((wl.rb.counts[: sh.E] > 0).sum().item())
@@ -528,14 +569,14 @@ def run_layer_bench(args, world, local_rank, barrier):
         res["compute_only_ms"] = run_compute_only(wl, K, phases)
         res["compute_only_phase_ms"] = _phase_avg(phases, K)
         res["copy_only_ms"] = run_copy_only(wl, K)
-        res["e2e"] = run_e2e(wl, K, world, barrier)
+        res["e2e"] = run_e2e(wl, K)
     if args.chunk_sweep:
         sweep = []
         comp = res.get("compute_only_ms") or run_compute_only(wl, K)
         for mb in [float(v) for v in args.chunk_sweep.split(",") if v]:
             wl.chunk = int(mb * (1 << 20))
             wl.issue_s = []
-            ms, _ = run_overlapped(wl, K, W, world, None, local_rank, barrier)
+            ms, _ = run_overlapped(wl, K, W, None)
             issue = 1e3 * sum(wl.issue_s) / max(1, len(wl.issue_s))
             copy = run_copy_only(wl, K)
             over = ms / K
@@ -554,72 +595,98 @@ def run_layer_bench(args, world, local_rank, barrier):
     return res
 
 
-def run_merge_baseline(wl, K, W):
+class MergeCopyLayer:
     """The pages' baseline before split-weight management (DWDP §4.2): the
-    grouped GEMM reads ONE contiguous [E] weight buffer, so after the
-    non-resident experts arrive the resident ones are merged into it with a
-    device-to-device copy on the critical path.  Built from the public ABI
-    only, in the variant most favourable to the baseline: the prefetch lands
-    directly in the merged buffer (stage slots 0..R-1) and only the resident
-    experts are copied (slots R..E-1), then the same kernels run on a map
-    in which every expert is resident in that buffer.  Returns ms per step
-    (overlapped and with every expert already staged) and the merge bytes."""
-    torch, B = wl.torch, wl.B
-    sh, pl = wl.shape, wl.placement
-    if (pl.local_slot >= 0).sum() != pl.n_local_slots or pl.n_remote() + pl.n_local_slots != sh.E:
-        return None   # redundant placements have no single merged layout
-    wd = {"bf16": B.DTYPE_BF16, "fp8": B.DTYPE_E4M3, "nvfp4": B.DTYPE_NVFP4}[wl.wdtype]
-    mrt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, 6, sh.E, weight_dtype=wd)
-    stage_slot = [-1] * sh.E
-    r = 0
-    for e in range(sh.E):
-        if pl.local_slot[e] < 0:
-            stage_slot[e] = r
-            r += 1
-    R = r
-    merged_slot = [stage_slot[e] if pl.local_slot[e] < 0 else R + int(pl.local_slot[e]) for e in range(sh.E)]
-    for l, lw in enumerate(wl.layers):
-        mrt.set_layer(l, lw)                               # layers 0, 1: where the prefetch reads from
-        for s in (0, 1):                                   # layers 2+2l+s: everything resident in merged[s]
-            local = B.pool(mrt.stage_w13[s], mrt.stage_w2[s])
-            B.dwdp_set_expert_map(mrt.ctx, 2 + 2 * l + s, local, [], merged_slot, [-1] * sh.E, [-1] * sh.E,
-                                  lw.shared_w13, lw.shared_w2)
-            if getattr(lw, "w13_scale", None) is not None:
-                B.dwdp_set_expert_scales(mrt.ctx, 2 + 2 * l + s, lw.w13_scale, lw.w2_scale, lw.shared_s13,
-                                         lw.shared_s2)
-    w13_bytes = B.weight_slot_bytes(2 * sh.I, sh.H, wd)
-    w2_bytes = B.weight_slot_bytes(sh.H, sh.I, wd)
-    n_local = pl.n_local_slots
-    merge_bytes = n_local * (w13_bytes + w2_bytes)
-    ev = lambda: torch.cuda.Event()
-    arrived = [ev(), ev()]
-    freed = [ev(), ev()]
+    grouped GEMM reads ONE contiguous [E] weight buffer per layer, so after
+    the non-resident experts arrive the resident ones are merged into it
+    with a device-to-device copy on the critical path.  Built from the
+    public ABI only, in the variant most favourable to the baseline: the
+    prefetch lands directly in the merged buffer (its slots 0..R-1, the
+    stage slots of the non-resident experts in ascending id) and only the
+    resident experts are copied (to slots R..E-1), then the same kernels run
+    on a map in which every expert is resident in that buffer.  Merged
+    buffer s (a staging buffer of a context with E stage slots) serves
+    layer l of `layers` at step parity s: maps 2 + 2 l + s."""
 
-    def prefetch(l, s, copies=True):
-        wl.copies[0].wait_event(freed[s])
-        if copies:
-            mrt.prefetch(l, s, wl.chunk, wl.copies)
-        arrived[s].record(wl.copies[0])
+    def __init__(self, B, torch, shape, placement, layers, wdtype: str, max_tokens=None):
+        sh, pl = shape, placement
+        if (pl.local_slot >= 0).sum() != pl.n_local_slots or pl.n_remote() + pl.n_local_slots != sh.E:
+            raise ValueError("a redundant placement has no single merged layout")
+        self.B, self.torch, self.shape, self.pl, self.layers = B, torch, sh, pl, layers
+        wd = {"bf16": B.DTYPE_BF16, "fp8": B.DTYPE_E4M3, "nvfp4": B.DTYPE_NVFP4}[wdtype]
+        self.rt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, max_tokens or sh.T, 2 + 2 * len(layers), sh.E,
+                            weight_dtype=wd)
+        stage_slot = [-1] * sh.E
+        r = 0
+        for e in range(sh.E):
+            if pl.local_slot[e] < 0:
+                stage_slot[e] = r
+                r += 1
+        self.R = r
+        self.merged_slot = [stage_slot[e] if pl.local_slot[e] < 0 else r + int(pl.local_slot[e]) for e in range(sh.E)]
+        for l, lw in enumerate(layers):
+            self.rt.set_layer(l, lw)                          # layers 0, 1: where the prefetch reads from
+            for s in (0, 1):                                  # maps 2+2l+s: everything resident in merged[s]
+                local = B.pool(self.rt.stage_w13[s], self.rt.stage_w2[s])
+                B.dwdp_set_expert_map(self.rt.ctx, 2 + 2 * l + s, local, [], self.merged_slot, [-1] * sh.E,
+                                      [-1] * sh.E, lw.shared_w13, lw.shared_w2)
+                if getattr(lw, "w13_scale", None) is not None:
+                    B.dwdp_set_expert_scales(self.rt.ctx, 2 + 2 * l + s, lw.w13_scale, lw.w2_scale, lw.shared_s13,
+                                             lw.shared_s2)
+        self.w13_bytes = B.weight_slot_bytes(2 * sh.I, sh.H, wd)
+        self.w2_bytes = B.weight_slot_bytes(sh.H, sh.I, wd)
+        self.n_local = pl.n_local_slots
+        self.merge_bytes = self.n_local * (self.w13_bytes + self.w2_bytes)
+        self.arrived = [torch.cuda.Event(), torch.cuda.Event()]
+        self.freed = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def prefetch(self, l, s, chunk, copies):
+        """Layer l's non-resident experts into merged buffer s (slots 0..R-1)."""
+        copies[0].wait_event(self.freed[s])
+        self.rt.prefetch(l, s, chunk, copies)
+        self.arrived[s].record(copies[0])
+
+    def merge(self, l, s, stream):
+        """The D2D merge: layer l's resident experts into slots R.. of buffer s."""
+        lw, n = self.layers[l], self.n_local
+        with self.torch.cuda.stream(stream):
+            stream.wait_event(self.arrived[s])
+            self.rt.stage_w13[s][self.R:self.R + n].copy_(lw.local_w13[:n].view(self.torch.uint8).reshape(n, -1),
+                                                          non_blocking=True)
+            self.rt.stage_w2[s][self.R:self.R + n].copy_(lw.local_w2[:n].view(self.torch.uint8).reshape(n, -1),
+                                                         non_blocking=True)
+
+    def layer(self, l, s, x, rb, out, stream):
+        """Merge, route and the MoE layer on the merged buffer."""
+        self.merge(l, s, stream)
+        lw = self.layers[l]
+        with self.torch.cuda.stream(stream):
+            self.rt.route(x, lw.wr, lw.bias, rb, stream)
+            self.rt.moe(2 + 2 * l + s, s, x, rb, out, stream)
+            self.freed[s].record(stream)
+
+    def close(self):
+        self.rt.close()
+
+
+def run_merge_baseline(wl, K, W):
+    """The merge-copy baseline (MergeCopyLayer) timed like the split-pointer
+    step: ms per step overlapped with the next layer's prefetch, and with
+    every expert already staged (merge + compute only), plus the merge bytes."""
+    torch = wl.torch
+    try:
+        mc = MergeCopyLayer(wl.B, torch, wl.shape, wl.placement, wl.layers, wl.wdtype)
+    except ValueError:
+        return None
 
     def step(i, prefetch_next=True):
-        l, s = i % 2, i % 2
-        lw = wl.layers[l]
-        x = wl.x[l]
-        with torch.cuda.stream(wl.compute):
-            wl.compute.wait_event(arrived[s])
-            # the merge: resident experts into slots R.. of the stage's buffer
-            mrt.stage_w13[s][R:R + n_local].copy_(lw.local_w13[:n_local].view(torch.uint8).reshape(n_local, -1),
-                                                  non_blocking=True)
-            mrt.stage_w2[s][R:R + n_local].copy_(lw.local_w2[:n_local].view(torch.uint8).reshape(n_local, -1),
-                                                 non_blocking=True)
-            mrt.route(x, lw.wr, lw.bias, wl.rb, wl.compute)
-            mrt.moe(2 + 2 * l + s, s, x, wl.rb, wl.out, wl.compute)
-            freed[s].record(wl.compute)
+        l = s = i % 2
+        mc.layer(l, s, wl.x[l], wl.rb, wl.out, wl.compute)
         if prefetch_next:
-            prefetch((i + 1) % 2, (i + 1) % 2)
+            mc.prefetch((i + 1) % 2, (i + 1) % 2, wl.chunk, wl.copies)
 
     wl.sync()
-    prefetch(0, 0)
+    mc.prefetch(0, 0, wl.chunk, wl.copies)
     for i in range(W):
         step(i)
     wl.sync()
@@ -637,7 +704,7 @@ def run_merge_baseline(wl, K, W):
     # every expert already staged: merge + compute only
     wl.sync()
     for l in (0, 1):
-        prefetch(l, l)
+        mc.prefetch(l, l, wl.chunk, wl.copies)
     wl.sync()
     for i in range(2):
         step(i, prefetch_next=False)
@@ -648,13 +715,14 @@ def run_merge_baseline(wl, K, W):
     b.record(wl.compute)
     b.synchronize()
     comp = a.elapsed_time(b) / K
-    assert mrt.device_status() == 0
-    mrt.close()
+    assert mc.rt.device_status() == 0
+    merge_bytes, n_local = mc.merge_bytes, mc.n_local
+    mc.close()
     return {"overlapped_ms": round(over, 4), "compute_only_ms": round(comp, 4),
             "merge_bytes_per_layer": merge_bytes, "merged_experts_copied": n_local}
 
 
-def run_pipeline_bench(args, world, local_rank, barrier):
+def run_pipeline_bench(args):
     """Four distinct R1 layers per step with an attention-sized GEMM
     stand-in (x . W_attn, T x 7168 x 7168, on this library's grouped GEMM)
     after each MoE layer; the copy of the next layer's experts overlaps the
@@ -666,7 +734,7 @@ def run_pipeline_bench(args, world, local_rank, barrier):
     from moe_expert_grouped_split_gb300 import binding as B
     from moe_expert_grouped_split_gb300 import inputs as I
 
-    torch.cuda.set_device(local_rank)
+    torch.cuda.set_device(0)
     spec = WORKLOADS[args.workload](group=args.group)
     wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, n_layers=4, wdtype=args.dtype,
                   prefetch_start=args.prefetch_start, n_stages=args.stages)
@@ -707,9 +775,8 @@ def run_pipeline_bench(args, world, local_rank, barrier):
         wl.prefetch(j, j)
     run(0, args.warmup, True)
     wl.sync()
-    barrier()
     a, b = ev()
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(0) as clk:
         a.record(wl.compute)
         for c in wl.copies:
             c.wait_stream(wl.compute)
@@ -719,9 +786,9 @@ def run_pipeline_bench(args, world, local_rank, barrier):
         b.record(wl.compute)
         b.synchronize()
     assert wl.rt.device_status() == 0
-    ms = max_over_ranks(a.elapsed_time(b), world)
+    ms = a.elapsed_time(b)
     tokens = 4 * sum(Ts[args.warmup:])
-    res = {"ms_step": ms / steps, "value": world * tokens / (ms / 1e3), "clocks": clk.summary()}
+    res = {"ms_step": ms / steps, "value": tokens / (ms / 1e3), "clocks": clk.summary()}
     if not args.no_extras:
         # compute only: the same sequence with layers 0 and 1 (staged once)
         # standing in for 2 and 3 (same shapes, same routing statistics)
@@ -834,43 +901,27 @@ def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return main_reference(args, rank, world)
+    refusal = single_gpu_refusal(args, world)
+    if refusal is not None:
+        # nothing is built or loaded: no kernel of this library runs on more than one GPU
+        if rank == 0:
+            print(json.dumps(refusal), flush=True)
+        return
 
-    import torch
-
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl")
     from moe_expert_grouped_split_gb300.build import build
-    if rank == 0 or world == 1:
-        build()
-
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-    barrier()
+    build()
     pipeline = args.workload == "r1_pipeline_4layer"
-    res = (run_pipeline_bench if pipeline else run_layer_bench)(args, world, local_rank, barrier)
+    res = (run_pipeline_bench if pipeline else run_layer_bench)(args)
     wl = res.pop("wl")
     sh = wl.shape
     peaks, src = measured_peaks()
-    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    tc_peak, hbm, tc_note = roofline_peaks(peaks, src, args.dtype)
+    hbm_note = f"{src} hbm_gbs"
     wb = WEIGHT_BYTES[args.dtype]
-    peak_note = f"{src} bf16_tflops_sustained (kernel timed inside a long step)"
-    if args.dtype == "fp8":   # measured bf16 peak x the nominal dense fp8 / bf16 ratio (4.5 / 2.25)
-        peak = peak * 2.0
-        peak_note = f"{src} bf16_tflops_sustained x 2 (nominal dense E4M3 / bf16 ratio), kernel inside a long step"
-    if args.dtype == "nvfp4":   # x the nominal dense fp4 / bf16 ratio (13.5 / 2.25)
-        peak = peak * 6.0
-        peak_note = f"{src} bf16_tflops_sustained x 6 (nominal dense FP4 / bf16 ratio), kernel inside a long step"
-    hbm = peaks["hbm_gbs"]
     line = {
-        "metric": METRIC, "value": round(res["value"], 1), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": round(res["value"], 1), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_step"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "nvfp4"}[args.dtype],
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights; R1 MoE layer shapes)",
@@ -885,7 +936,7 @@ def main():
                    "l2": "inputs larger than L2 ({:.1f} GB of expert weights + {:.1f} GB of copies per layer)".format(
                        (sh.E + sh.S) * 3 * sh.H * sh.I * WEIGHT_BYTES[args.dtype] / 1e9,
                        wl.placement.n_remote() * 3 * sh.H * sh.I * WEIGHT_BYTES[args.dtype] / 1e9),
-                   "parallelism": "replicas" if world > 1 else "single rank"},
+                   "parallelism": "single rank"},
         "clocks": res["clocks"],
     }
     if pipeline:
@@ -899,32 +950,25 @@ def main():
     else:
         flops_layer = layer_flops(sh.T, sh.H, sh.I, sh.E, sh.k, sh.S)
         g1 = g1_flops(sh.T, sh.H, sh.I, sh.k, sh.S)
-        g1_tflops = g1 / (res["phase_ms"]["gate_up_gemm"] / 1e3) / 1e12
         g1b = g1_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S, wb)
         sb = step_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S, wl.placement.n_remote(), wb)
         layer_tflops = flops_layer / (res["ms_step"] / 1e3) / 1e12
         traffic = None
         if args.workload == "r1_moe_layer_8k" and args.dtype == "bf16":
             traffic = measured_traffic(os.path.join(ROOT, "moe_expert_grouped_split_gb300", "csrc", "gemm.cu"))
-        g1_s = res["phase_ms"]["gate_up_gemm"] / 1e3
-        if g1 / g1b >= peak * 1e12 / (hbm * 1e9):     # arithmetic intensity at or above the ridge
-            roof = {"kernel": "gate_up_grouped_gemm", "bound": "tensor", "achieved": round(g1_tflops, 1),
-                    "peak": peak, "unit": "TFLOP/s", "frac": round(g1_tflops / peak, 4),
-                    "peak_source": peak_note}
-        else:
-            gbs = g1b / g1_s / 1e9
-            roof = {"kernel": "gate_up_grouped_gemm", "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
-                    "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_source": f"{src} hbm_gbs"}
+        roof = roofline_entry("gate_up_grouped_gemm", g1, g1b, res["phase_ms"]["gate_up_gemm"] / 1e3, tc_peak, hbm,
+                              tc_note, hbm_note)
         roof.update({"traffic": traffic, "algorithmic_flops_per_launch": g1, "algorithmic_bytes_per_launch": g1b,
-                     "arithmetic_intensity": round(g1 / g1b, 1)})
+                     "timed": "CUDA events around the kernel on the compute stream, inside the overlapped step"})
         line.update({
             "tflops": round(layer_tflops, 1),
-            "tc_peak_frac": round(layer_tflops / peak, 4),
+            "tc_peak_frac": round(layer_tflops / tc_peak, 4),
+            "tc_peak": {"value": tc_peak, "unit": "TFLOP/s", "source": tc_note},
             "phase_ms": res["phase_ms"],
             "roofline": roof,
             "step_hbm": {"bound": "hbm", "achieved": round(sb / (res["ms_step"] / 1e3) / 1e9, 1), "peak": hbm,
                          "unit": "GB/s", "frac": round(sb / (res["ms_step"] / 1e3) / 1e9 / hbm, 4),
-                         "algorithmic_bytes_per_step": sb, "peak_source": f"{src} hbm_gbs"},
+                         "algorithmic_bytes_per_step": sb, "peak_source": hbm_note},
             "host_issue_ms_per_prefetch": res["issue_ms"],
             "merge_copy_baseline": res.get("merge_copy"),
             "gpu_launches": kernels_per_layer(args.dtype) * args.steps,
@@ -946,25 +990,19 @@ def main():
             pre["interference"] = {n_: round(res["phase_ms"][n_] / max(res["compute_only_phase_ms"][n_], 1e-9), 3)
                                    for n_ in PHASES if n_ != "wait_stage"}
             # the roofline kernel again, timed in the compute-only leg (no copy
-            # sharing the memory system), against the same peak
+            # sharing the memory system), against the same roof
             r = line["roofline"]
-            g1_alone = res["compute_only_phase_ms"]["gate_up_gemm"] / 1e3
-            if r["unit"] == "TFLOP/s":
-                ach = r["algorithmic_flops_per_launch"] / g1_alone / 1e12
-            else:
-                ach = r["algorithmic_bytes_per_launch"] / g1_alone / 1e9
-            line["roofline_alone"] = {"kernel": r["kernel"], "bound": r["bound"], "achieved": round(ach, 1),
-                                      "peak": r["peak"], "unit": r["unit"], "frac": round(ach / r["peak"], 4)}
+            alone = roofline_entry(r["kernel"], r["algorithmic_flops_per_launch"], r["algorithmic_bytes_per_launch"],
+                                   res["compute_only_phase_ms"]["gate_up_gemm"] / 1e3, tc_peak, hbm, tc_note,
+                                   hbm_note)
+            alone["timed"] = "CUDA events around the kernel on the compute stream, compute-only leg (no copy)"
+            line["roofline_alone"] = alone
         line["prefetch"] = pre
     if "e2e" in res:
         line["e2e"] = res["e2e"]
-    if rank == 0 and not args.no_cpu_baseline and not pipeline:
+    if not args.no_cpu_baseline and not pipeline:
         line["cpu_baseline"] = cpu_baseline_sample(wl)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    print(json.dumps(line), flush=True)
 
 
 def main_reference(args, rank, world):
@@ -1036,18 +1074,19 @@ def main_reference(args, rank, world):
             ntok += per_step
     total = sum(times)
     value = ntok / total
-    ms_step = T / value * 1e3
+    ms_step = total / len(times) * 1e3     # one timed step = one bounded token sample
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 1),
+        "ms_per_layer_extrapolated": round(T / value * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded, R1 MoE layer shapes)",
         "config": {"workload": args.workload, "T": T, "H": shape.H, "I": shape.I, "E": shape.E, "k": shape.k,
                    "shared": shape.S, "expert_weights": wd, "dwdp_group": args.group},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": o.num_threads(), "kind": "oracle",
                          "sample": f"{per_step} seeded tokens per step (one per oracle thread) of the {T}-token "
-                                   f"layer, {args.steps} timed steps ({total:.1f} s); ms_per_step extrapolates "
-                                   f"to {T} tokens"},
+                                   f"layer, {args.steps} timed steps ({total:.1f} s); ms_per_step is one such "
+                                   f"step, ms_per_layer_extrapolated the whole {T}-token layer at this rate"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

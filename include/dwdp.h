@@ -22,7 +22,13 @@
  *     with no padding between rows.
  *   - "device" pointers point into the current CUDA device's global memory
  *     and must be 16-byte aligned; the caller owns every buffer it passes and
- *     keeps it alive until the work enqueued on it has finished.
+ *     keeps it alive until the work enqueued on it has finished.  Buffers
+ *     the GEMMs read through TMA tensor maps (x, the workspace, the router
+ *     weight, the local pool, the shared expert, the staging buffers) are
+ *     checked to be device memory of the context's (current) device, else
+ *     INVALID_ARG: the kernels never read another GPU's or the host's memory
+ *     through a tensor map.  Only peer pools, which are copied from and
+ *     never read by a kernel, may live elsewhere.
  *   - The context owns its CUDA events, tensor-map descriptors, its small
  *     device tables and error word, and the copy plans.  Use one context from
  *     one host thread at a time.
@@ -52,7 +58,7 @@
 extern "C" {
 #endif
 
-#define DWDP_ABI_VERSION 4
+#define DWDP_ABI_VERSION 5
 #define DWDP_MAX_EXPERTS 1024
 #define DWDP_MAX_TOPK 32
 #define DWDP_MAX_LAYERS 256
@@ -182,6 +188,36 @@ const char* dwdp_last_error(const dwdp_ctx* ctx);
  * order on one stream). */
 size_t dwdp_workspace_bytes(const dwdp_ctx* ctx, int32_t T);
 
+/* Where dwdp_moe_layer keeps each intermediate of a T-token layer in its
+ * workspace (instrumentation: after the layer has run, and until the next
+ * call that uses the workspace, the caller may read them back).  Regions,
+ * with rows_r = T k routed rows in expert order (dwdp_route's grouped rows)
+ * and rows_all = T (k + n_shared) (the shared expert's rows after them):
+ *   DWDP_WS_XP  [rows_r][H] x in expert order (bf16, E4M3 or NVFP4 codes)
+ *   DWDP_WS_A   [rows_all][I] bf16 a = SiLU(gate) * up
+ *   DWDP_WS_Y   [rows_all][H] bf16 expert outputs y
+ *   DWDP_WS_XQ  [T][H] x's codes (E4M3 / NVFP4 contexts)
+ *   DWDP_WS_SX, DWDP_WS_SXP  fp32 row scales of x by token / in expert order
+ *   DWDP_WS_AQ  [rows_all][I] a's codes; DWDP_WS_SA [rows_all] fp32 a's row scales
+ *   DWDP_WS_SFX, DWDP_WS_SFA  NVFP4 block scales of the gate/up and down
+ *     GEMMs' A operands in the 512-byte chunk layout, chunk (tile, ks) at
+ *     (tile * K / 64 + ks) * 512, where the A tiles are numbered expert by
+ *     expert (ceil(rows_e / 128) tiles each, in expert order), then the
+ *     shared expert's ceil(T / 128) tiles.
+ * Writes the byte offset from ws and the region's size (0 when the context's
+ * weight type has no such region).  Errors: INVALID_ARG. */
+#define DWDP_WS_XP 0
+#define DWDP_WS_A 1
+#define DWDP_WS_Y 2
+#define DWDP_WS_XQ 3
+#define DWDP_WS_SX 4
+#define DWDP_WS_SXP 5
+#define DWDP_WS_AQ 6
+#define DWDP_WS_SA 7
+#define DWDP_WS_SFX 8
+#define DWDP_WS_SFA 9
+int32_t dwdp_workspace_region(const dwdp_ctx* ctx, int32_t T, int32_t region, size_t* offset, size_t* bytes);
+
 /* Placement of layer `layer` ([DWDP] §2: experts partitioned across peers,
  * placement need not be disjoint; a redundant expert is read from its local
  * copy).  For each routed expert e:
@@ -217,7 +253,12 @@ int32_t dwdp_set_expert_scales(dwdp_ctx* ctx, int32_t layer, const float* w13_sc
  * choice.  The chosen experts are the k largest logits (softmax is
  * monotone), ties to the lower id, decided on the fp32 logits; weights are
  * exp(z_j - z_max) / sum over the chosen set.  ws (device, ws_bytes >=
- * dwdp_workspace_bytes) is scratch.  Enqueued on `stream`.
+ * dwdp_workspace_bytes) is scratch.  Enqueued on `stream`.  A token with
+ * a logit that is not finite (NaN or +-inf, e.g. from a NaN in x) has no
+ * defined choice: it still gets k distinct experts, but its ids and weights
+ * are unspecified and the device error word is set (dwdp_device_status:
+ * DEVICE_CHECK).  x and w_router must be device memory of the context's
+ * device (they are read through TMA tensor maps).
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router,
                    const float* logit_bias, const dwdp_route_out* out, void* ws, size_t ws_bytes,
@@ -281,7 +322,9 @@ int32_t dwdp_wait_stage(dwdp_ctx* ctx, int32_t stage, int32_t timeout_ms);
 int32_t dwdp_stage_layer(const dwdp_ctx* ctx, int32_t stage);
 
 /* Read and clear the device error word (synchronises the device).  OK, or
- * DEVICE_CHECK with the failing check described by dwdp_last_error. */
+ * DEVICE_CHECK with the failing check described by dwdp_last_error: bits
+ * 0-5 a bounded wait inside the grouped GEMM ran out, bit 6 an index outside
+ * its buffer was skipped, bit 7 a router logit was not finite. */
 int32_t dwdp_device_status(dwdp_ctx* ctx);
 
 /* Optional phase timing.  events is a host array of DWDP_PHASE_EVENTS
@@ -324,23 +367,39 @@ int32_t dwdp_grouped_gemm(dwdp_ctx* ctx, int32_t epilogue, const void* a, int64_
  * x [T][hidden], w_router [n_experts][hidden], logit_bias [n_experts] or
  * NULL, without a context or workspace; out->logits is ignored (the logits
  * stay in the scratch).  Its scratch is one file-scope device array of
- * DWDP_STATIC_SCRATCH_BYTES (16 MiB) of fp32 logits, as much again for the
- * router GEMM's partial sums (its K may be split into parts as in
- * dwdp_route, which always fit on GPUs with up to 256 SMs) and an error
- * word, held by every GPU that loads this library until the process exits,
- * so T * n_experts * 4 must not exceed DWDP_STATIC_SCRATCH_BYTES (else
- * INVALID_ARG, nothing enqueued).  The first call on each device looks up
- * the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.  Every call on a
- * device shares the one array and it keeps the last call's contents (the
- * error word is cleared on `stream` at the start of each call): calls whose
- * work overlaps on the GPU (other streams, other threads) race on it.  Calls
- * no cudaMalloc, cudaFree or other allocating routine.  Errors (text in
+ * 32 MiB + 256 bytes: DWDP_STATIC_SCRATCH_BYTES (16 MiB) of fp32 logits, as
+ * much again for the router GEMM's partial sums (its K may be split into
+ * parts as in dwdp_route, which always fit on GPUs with up to 256 SMs) and a
+ * 256-byte error word, held by every GPU that loads this library until the
+ * process exits, so T * n_experts * 4 must not exceed
+ * DWDP_STATIC_SCRATCH_BYTES (else INVALID_ARG, nothing enqueued).  The first
+ * call on each device (of this entry point or of dwdp_route_static_status)
+ * looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current and keeps it for the life of the process; make that first
+ * call before any stream capture, and do not use these two calls on a
+ * device after cudaDeviceReset (the address belonged to the context the
+ * reset destroyed).  Every call on a device shares the one array and it
+ * keeps the last call's contents (the error word is cleared on `stream` at
+ * the start of each call): calls whose work overlaps on the GPU (other
+ * streams, other threads) race on it.  Device-side failures (a non-finite
+ * logit as in dwdp_route, a bounded wait that ran out) set the array's
+ * error word: read it with dwdp_route_static_status.  Calls no cudaMalloc,
+ * cudaFree or other allocating routine.  Errors (text in
  * dwdp_last_error(NULL)): INVALID_ARG, UNSUPPORTED, CUDA. */
 #define DWDP_STATIC_SCRATCH_BYTES (16u << 20)
 int32_t dwdp_route_static(const void* x, int32_t T, int32_t hidden, int32_t n_experts, int32_t top_k,
                           const void* w_router, const float* logit_bias, const dwdp_route_out* out,
                           dwdp_stream_t stream);
+
+/* The device error word of dwdp_route_static on the current device (no
+ * counterpart in the paper; dwdp_route_static has no context whose
+ * dwdp_device_status could report it).  Waits for the work already enqueued
+ * on `stream` (not allowed while `stream` is being captured), reads the word
+ * and, when it is non-zero, clears it on `stream`.  *bits (may be NULL)
+ * receives the raw bits (as for dwdp_device_status).  Returns OK for a zero
+ * word, DEVICE_CHECK otherwise (text in dwdp_last_error(NULL)).  Allocates
+ * nothing.  Errors: CUDA, UNSUPPORTED. */
+int32_t dwdp_route_static_status(dwdp_stream_t stream, int32_t* bits);
 
 /* Host-only (no GPU needed): the prefetch copy plan dwdp_prefetch_layer
  * issues for a map ([DWDP] §4.3.2).  The non-resident experts (local_slot <

@@ -86,6 +86,9 @@ SIGNATURES = [
     ("dwdp_grouped_gemm", _I32, [_VP, _I32, _VP, ctypes.c_int64, _I32, _I32, _VP, _I32, ctypes.POINTER(dwdp_pool),
                                  _I32, _I32P, _VP, _VP]),
     ("dwdp_route_static", _I32, [_VP, _I32, _I32, _I32, _I32, _VP, _VP, ctypes.POINTER(dwdp_route_out), _VP]),
+    ("dwdp_route_static_status", _I32, [_VP, _I32P]),
+    ("dwdp_workspace_region", _I32, [_VP, _I32, _I32, ctypes.POINTER(ctypes.c_size_t),
+                                     ctypes.POINTER(ctypes.c_size_t)]),
     ("dwdp_quantize_rows", _I32, [_I32, _VP, ctypes.c_int64, _I32, _VP, _VP, _VP, _VP]),
     ("dwdp_plan_prefetch", _I32, [_I32, _I32, _I32, _I32, _I32P, _I32P, _I32P, _I32, ctypes.c_size_t,
                                   ctypes.POINTER(dwdp_copy_slice), ctypes.c_int64, ctypes.POINTER(ctypes.c_int64)]),
@@ -248,6 +251,30 @@ def dwdp_route_static(x, T, hidden, n_experts, top_k, w_router, logit_bias, out:
                                          ctypes.byref(out), _stream(stream)))
 
 
+def dwdp_route_static_status(stream=None) -> int:
+    """The error bits dwdp_route_static left on the current device (read and
+    cleared after the stream's work); raises DwdpError (DEVICE_CHECK) when
+    they are non-zero, with the bits in ``.bits``."""
+    bits = ctypes.c_int32(0)
+    rc = lib().dwdp_route_static_status(_stream(stream), ctypes.byref(bits))
+    if rc != 0:
+        err = DwdpError(rc, dwdp_last_error(None))
+        err.bits = bits.value
+        raise err
+    return bits.value
+
+
+WS_REGIONS = {"xp": 0, "a": 1, "y": 2, "xq": 3, "sx": 4, "sxp": 5, "aq": 6, "sa": 7, "sfx": 8, "sfa": 9}
+
+
+def dwdp_workspace_region(ctx, T, region) -> tuple:
+    """(byte offset, bytes) of a named intermediate in dwdp_moe_layer's workspace."""
+    off, n = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(ctx, lib().dwdp_workspace_region(ctx, T, WS_REGIONS[region] if isinstance(region, str) else region,
+                                            ctypes.byref(off), ctypes.byref(n)))
+    return off.value, n.value
+
+
 def dwdp_quantize_rows(weight_dtype, x, rows, K, codes, block_scales, row_scale, stream=None) -> None:
     _check(None, lib().dwdp_quantize_rows(weight_dtype, _ptr(x), rows, K, _ptr(codes), _ptr(block_scales),
                                           _ptr(row_scale), _stream(stream)))
@@ -340,6 +367,12 @@ class Runtime:
 
     def prefetch(self, layer, stage, chunk_bytes, copy_streams) -> None:
         dwdp_prefetch_layer(self.ctx, layer, stage, chunk_bytes, copy_streams)
+
+    def ws_region(self, T: int, region: str):
+        """The bytes of one intermediate of the last T-token layer in the
+        workspace (a uint8 view, no copy)."""
+        off, n = dwdp_workspace_region(self.ctx, T, region)
+        return self.ws[off:off + n]
 
     def wait_stage(self, stage, timeout_ms) -> int:
         return dwdp_wait_stage(self.ctx, stage, timeout_ms)

@@ -342,6 +342,11 @@ int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[], void* const
                     prop.major, prop.minor);
     ctx->n_sms = prop.multiProcessorCount;
     if (!encode_fn()) return fail(nullptr, DWDP_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+    if (c.stage_slots > 0)
+        for (int s = 0; s < n_stages; ++s)
+            if (!is_device_memory_of(stage_w13[s], ctx->device) || !is_device_memory_of(stage_w2[s], ctx->device))
+                return fail(nullptr, DWDP_ERR_INVALID_ARG,
+                            "stage buffer %d must be device memory of the current device (%d)", s, ctx->device);
     for (int s = 0; s < n_stages; ++s) {
         e = cudaEventCreateWithFlags(&ctx->ready[s], cudaEventDisableTiming);
         if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ctx->freed[s], cudaEventDisableTiming);
@@ -372,6 +377,33 @@ size_t dwdp_workspace_bytes(const dwdp_ctx* ctx, int32_t T) {
     if (!ctx || T < 0) return 0;
     const WsLayout L = ws_layout(ctx->cfg, T);
     return std::max(L.route_bytes, L.moe_bytes);
+}
+
+int32_t dwdp_workspace_region(const dwdp_ctx* ctx, int32_t T, int32_t region, size_t* offset, size_t* bytes) {
+    if (!ctx || T < 0 || !offset || !bytes)
+        return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx, offset and bytes must not be NULL; T >= 0");
+    const dwdp_config& c = ctx->cfg;
+    const WsLayout L = ws_layout(c, T);
+    const int64_t H = c.hidden, I = c.inter, k = c.top_k, S = c.n_shared;
+    const int fmt = c.weight_dtype;
+    const bool q = fmt != FMT_BF16, f4 = fmt == FMT_NVFP4;
+    size_t o = 0, n = 0;
+    switch (region) {
+        case DWDP_WS_XP: o = L.xp; n = (size_t)(T * k * operand_row_bytes(H, fmt)); break;
+        case DWDP_WS_A: o = L.a; n = (size_t)(T * (k + S) * I * 2); break;
+        case DWDP_WS_Y: o = L.y; n = (size_t)(T * (k + S) * H * 2); break;
+        case DWDP_WS_XQ: o = L.xq; n = q ? (size_t)(T * operand_row_bytes(H, fmt)) : 0; break;
+        case DWDP_WS_SX: o = L.sx; n = q ? (size_t)T * 4 : 0; break;
+        case DWDP_WS_SXP: o = L.sxp; n = q ? (size_t)(T * k) * 4 : 0; break;
+        case DWDP_WS_AQ: o = L.aq; n = q ? (size_t)(T * (k + S) * operand_row_bytes(I, fmt)) : 0; break;
+        case DWDP_WS_SA: o = L.sa; n = q ? (size_t)(T * (k + S)) * 4 : 0; break;
+        case DWDP_WS_SFX: o = L.sfx; n = f4 ? (size_t)(L.sf_tiles * H * 8) : 0; break;
+        case DWDP_WS_SFA: o = L.sfa; n = f4 ? (size_t)(L.sf_tiles * I * 8) : 0; break;
+        default: return fail(nullptr, DWDP_ERR_INVALID_ARG, "unknown workspace region %d", region);
+    }
+    *offset = n ? o : 0;
+    *bytes = n;
+    return DWDP_OK;
 }
 
 int32_t dwdp_set_expert_map(dwdp_ctx* ctx, int32_t layer, const dwdp_pool* local, const dwdp_pool* peers,
@@ -407,6 +439,14 @@ int32_t dwdp_set_expert_map(dwdp_ctx* ctx, int32_t layer, const dwdp_pool* local
         return fail(ctx, DWDP_ERR_INVALID_ARG, "local pool pointers must be non-NULL, 16-byte aligned");
     if (c.n_shared && (!shared_w13 || !shared_w2 || !aligned16(shared_w13) || !aligned16(shared_w2)))
         return fail(ctx, DWDP_ERR_INVALID_ARG, "the shared expert's weights are required");
+    // the GEMM reads the local pool and the shared expert through tensor maps:
+    // they must live in this GPU's memory (peer pools are only copied from)
+    if (any_local && (!is_device_memory_of(local->w13, ctx->device) || !is_device_memory_of(local->w2, ctx->device)))
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "the local pool must be device memory of the context's device (%d)",
+                    ctx->device);
+    if (c.n_shared && (!is_device_memory_of(shared_w13, ctx->device) || !is_device_memory_of(shared_w2, ctx->device)))
+        return fail(ctx, DWDP_ERR_INVALID_ARG,
+                    "the shared expert must be device memory of the context's device (%d)", ctx->device);
     LayerMap m;
     m.local_slot.assign(local_slot, local_slot + E);
     m.peer_id.assign(E, -1);
@@ -508,6 +548,9 @@ int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router
     }
     if (!x || !w_router || !aligned16(x) || !aligned16(w_router))
         return fail(ctx, DWDP_ERR_INVALID_ARG, "x and w_router must be non-NULL, 16-byte aligned");
+    if (!is_device_memory_of(x, ctx->device) || !is_device_memory_of(w_router, ctx->device))
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "x and w_router must be device memory of the context's device (%d)",
+                    ctx->device);
     const WsLayout L = ws_layout(c, T);
     if (!ws || ws_bytes < L.route_bytes || !aligned16(ws))
         return fail(ctx, DWDP_ERR_INVALID_ARG, "workspace too small (%zu < %zu) or unaligned", ws_bytes,
@@ -544,7 +587,8 @@ int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router
     a.bsrc[0] = make_int2(0, 0);
     DWDP_CUDA(ctx, launch_grouped_gemm(EPI_F32, FMT_BF16, a, ctx->n_sms, stream));
     DWDP_CUDA(ctx, launch_topk(logits, parts, (int64_t)T * c.n_experts, nullptr, T, c.n_experts, c.top_k,
-                               out->topk_ids, out->topk_w, parts > 1 ? out->logits : nullptr, stream));
+                               out->topk_ids, out->topk_w, parts > 1 ? out->logits : nullptr, ctx->d_err,
+                               stream));
     DWDP_CUDA(ctx, launch_group_chunked(out->topk_ids, T * c.top_k, c.n_experts, out->counts, out->offsets,
                                         out->perm, out->inv_perm, group_scratch, stream));
     DWDP_CUDA(ctx, mark(ctx, 1, stream));
@@ -633,6 +677,10 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     const WsLayout L = ws_layout(c, T);
     if (!ws || ws_bytes < L.moe_bytes || !aligned16(ws))
         return fail(ctx, DWDP_ERR_INVALID_ARG, "workspace too small (%zu < %zu) or unaligned", ws_bytes, L.moe_bytes);
+    // x and the workspace (xp, a and their codes) are read through tensor maps
+    if (!is_device_memory_of(x, ctx->device) || !is_device_memory_of(ws, ctx->device))
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "x and ws must be device memory of the context's device (%d)",
+                    ctx->device);
     const int64_t k = c.top_k, S = c.n_shared, H = c.hidden, I = c.inter, E = c.n_experts;
     const int64_t rows_r = (int64_t)T * k, rows_all = (int64_t)T * (k + S);
     const int fmt = ctx->fmt;
@@ -827,6 +875,9 @@ int32_t dwdp_grouped_gemm(dwdp_ctx* ctx, int32_t epilogue, const void* a_ptr, in
     for (int b = 0; b < n_bufs; ++b) {
         if (!bufs[b].w13 || !aligned16(bufs[b].w13) || bufs[b].n_slots < 1)
             return fail(ctx, DWDP_ERR_INVALID_ARG, "buffer %d: base must be non-NULL, aligned, n_slots >= 1", b);
+        if (!is_device_memory_of(bufs[b].w13, ctx->device))
+            return fail(ctx, DWDP_ERR_INVALID_ARG, "buffer %d must be device memory of the context's device (%d)", b,
+                        ctx->device);
         if (!encode_slots(&a.tmB[b], bufs[b].w13, bufs[b].n_slots, brows, K))
             return fail(ctx, DWDP_ERR_CUDA, "tensor map for buffer %d", b);
     }
@@ -837,6 +888,8 @@ int32_t dwdp_grouped_gemm(dwdp_ctx* ctx, int32_t epilogue, const void* a_ptr, in
             return fail(ctx, DWDP_ERR_INVALID_ARG, "group %d: (buffer %d, slot %d) out of range", g, b, s);
         a.bsrc[g] = make_int2(b, s);
     }
+    if (!is_device_memory_of(a_ptr, ctx->device))
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "a must be device memory of the context's device (%d)", ctx->device);
     if (!encode_rows(&a.tmA[0], a_ptr, (uint64_t)a_rows, K)) return fail(ctx, DWDP_ERR_CUDA, "tensor map for A");
     a.tmA[1] = a.tmA[0];
     a.row_offsets = row_offsets;

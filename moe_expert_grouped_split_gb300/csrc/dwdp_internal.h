@@ -72,6 +72,7 @@ enum DeviceError : int {
     DERR_DRAIN_WAIT = 1 << 4,
     DERR_MMA_DONE_WAIT = 1 << 5,
     DERR_BAD_INDEX = 1 << 6,
+    DERR_NONFINITE_LOGIT = 1 << 7,  // a router logit is NaN or infinite
 };
 
 // Everything one grouped-GEMM launch needs; passed by value (grid constant).
@@ -127,6 +128,20 @@ bool encode_slots(CUtensorMap* m, const void* base, uint64_t slots, uint64_t row
 // Sets the text dwdp_last_error(NULL) returns on this thread (dwdp_abi.cu).
 void set_last_error(const char* msg);
 
+// True when p points into device memory of device `dev` (cudaMalloc or
+// virtual-memory allocations; not host, managed or another GPU's memory).
+// Every buffer a TMA tensor map covers is checked with it before the map is
+// encoded, so the GEMM's loads, including the loads it shares between the
+// two CTAs of a cluster, only ever read this GPU's own memory.
+inline bool is_device_memory_of(const void* p, int dev) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();  // an unknown pointer leaves no sticky error behind
+        return false;
+    }
+    return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
+
 // One grouped GEMM launch (gemm.cu) as 2-CTA clusters, one persistent CTA per
 // SM.  fmt: both operands bf16, both E4M3 codes, or both NVFP4 codes with
 // block scales (GemmArgs::sfa / bsf); K counts elements.  EPI_F32 is bf16 only.
@@ -150,8 +165,9 @@ inline int router_k_parts(int64_t T, int64_t E, int64_t H, int n_sms, size_t max
 // route.cu
 // Top-k over logits given as `parts` fp32 planes [T][E] part_stride apart
 // (summed in plane order, then bias); z_out, if not null, receives the sums.
+// A token with a non-finite logit sets DERR_NONFINITE_LOGIT in err.
 cudaError_t launch_topk(const float* logits, int parts, int64_t part_stride, const float* bias, int T, int E,
-                        int k, int32_t* ids, float* w, float* z_out, cudaStream_t s);
+                        int k, int32_t* ids, float* w, float* z_out, int* err, cudaStream_t s);
 cudaError_t launch_group(const int32_t* ids, int n, int E, int32_t* counts, int32_t* offsets,
                          int32_t* perm, int32_t* inv, cudaStream_t s);
 // The same grouping in three passes over chunks of 1024 pairs; needs

@@ -23,9 +23,12 @@ constexpr int kMaxPerLane = DWDP_MAX_EXPERTS / 32;
 constexpr int kQuantWarps = 8;  // warps per block of the NVFP4 quantizers
 
 // Order-preserving key of a logit: a > b as floats iff key(a) > key(b) as
-// unsigned (no NaN); -0 is folded into +0 so equal values tie.  Every finite
-// or infinite value has a key >= 0x007FFFFF, so 0 marks "no candidate".
+// unsigned; -0 is folded into +0 so equal values tie.  Every finite or
+// infinite value has a key >= 0x007FFFFF, so 0 marks "no candidate".  Every
+// NaN, whatever its sign or payload, gets the one key 0xFFFFFFFF (above
+// +inf), so a token with NaN logits still gets k distinct picks.
 __device__ __forceinline__ uint32_t order_key(float x) {
+    if (x != x) return 0xFFFFFFFFu;
     const uint32_t u = __float_as_uint(x == 0.0f ? 0.0f : x);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
@@ -43,17 +46,22 @@ __device__ __forceinline__ float key_value(uint32_t key) {
 // full softmax denominator cancels in the renormalisation).
 // The logits arrive as `parts` partial-sum planes part_stride apart (a
 // K-split router GEMM), added in plane order; with z_out the sums are stored.
+// A token with a logit that is not finite (NaN or +-inf) has no defined
+// choice or weights: it is still routed (some k distinct experts) and
+// DERR_NONFINITE_LOGIT is set in err.
 template <int PER>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int parts,
                                                    int64_t part_stride, const float* __restrict__ bias,
                                                    int T, int E, int k, int32_t* __restrict__ ids,
-                                                   float* __restrict__ w, float* __restrict__ z_out) {
+                                                   float* __restrict__ w, float* __restrict__ z_out,
+                                                   int* __restrict__ err) {
     constexpr int kNone = 0x7fffffff;
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     const float* z = logits + (int64_t)t * E;
     uint32_t key[PER];
+    bool finite = true;
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
         const int e = lane + 32 * j;
@@ -63,9 +71,11 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
             for (int q = 1; q < parts; ++q) v += z[q * part_stride + e];
             if (bias) v += bias[e];
             if (z_out) z_out[(int64_t)t * E + e] = v;
+            finite &= isfinite(v);
             key[j] = order_key(v);
         }
     }
+    if (!__all_sync(0xffffffffu, finite) && lane == 0) atomicOr(err, DERR_NONFINITE_LOGIT);
     // this lane's best remaining candidate (largest key, lowest id on ties)
     auto best = [&](uint32_t& bk, int& bi) {
         bk = 0u;
@@ -890,13 +900,13 @@ cudaError_t launch_gather_fp8(const void* xq, const float* sx, int H, const int3
 }
 
 cudaError_t launch_topk(const float* logits, int parts, int64_t part_stride, const float* bias, int T, int E,
-                        int k, int32_t* ids, float* w, float* z_out, cudaStream_t s) {
+                        int k, int32_t* ids, float* w, float* z_out, int* err, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     const int warps = 8;
     const dim3 grid((T + warps - 1) / warps), block(32 * warps);
     static_assert(kMaxPerLane == 32, "dispatch covers up to 32 logits per lane");
 #define DWDP_TOPK(PER) \
-    topk_kernel<PER><<<grid, block, 0, s>>>(logits, parts, part_stride, bias, T, E, k, ids, w, z_out)
+    topk_kernel<PER><<<grid, block, 0, s>>>(logits, parts, part_stride, bias, T, E, k, ids, w, z_out, err)
     if (E <= 32) DWDP_TOPK(1);
     else if (E <= 64) DWDP_TOPK(2);
     else if (E <= 128) DWDP_TOPK(4);

@@ -9,6 +9,7 @@
 // entry point needs neither.  Its only scratch (the logits and an error
 // word) is the file-scope device array below, which every GPU that loads
 // this library holds until the process exits.
+#include <cstdio>
 #include <mutex>
 
 #include "dwdp_internal.h"
@@ -92,6 +93,8 @@ extern "C" int32_t dwdp_route_static(const void* x, int32_t T, int32_t hidden, i
     }
     if (!x || !w_router || !aligned16(x) || !aligned16(w_router))
         return fail_static(DWDP_ERR_INVALID_ARG, "x and w_router must be non-NULL, 16-byte aligned");
+    if (!is_device_memory_of(x, dev) || !is_device_memory_of(w_router, dev))
+        return fail_static(DWDP_ERR_INVALID_ARG, "x and w_router must be device memory of the current device");
     int* err = reinterpret_cast<int*>(scratch);
     float* logits = reinterpret_cast<float*>(scratch + kErrBytes);
     // the error word keeps the previous call's bits: clear it on this stream
@@ -123,9 +126,41 @@ extern "C" int32_t dwdp_route_static(const void* x, int32_t T, int32_t hidden, i
     e = launch_grouped_gemm(EPI_F32, FMT_BF16, a, n_sms, stream);
     if (e == cudaSuccess)
         e = launch_topk(logits, parts, (int64_t)T * n_experts, nullptr, T, n_experts, top_k, out->topk_ids,
-                        out->topk_w, nullptr, stream);
+                        out->topk_w, nullptr, err, stream);
     if (e == cudaSuccess)
         e = launch_group(out->topk_ids, T * top_k, n_experts, out->counts, out->offsets, out->perm, out->inv_perm,
                          stream);
     return e == cudaSuccess ? DWDP_OK : fail_static(DWDP_ERR_CUDA, cudaGetErrorString(e));
+}
+
+extern "C" int32_t dwdp_route_static_status(dwdp_stream_t stream, int32_t* bits) {
+    using namespace dwdp;
+    if (bits) *bits = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_static(DWDP_ERR_CUDA, cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail_static(DWDP_ERR_UNSUPPORTED, "device index too large");
+    unsigned char* scratch = nullptr;
+    int n_sms = 0;
+    const int32_t rc = setup_device(dev, &scratch, &n_sms);
+    if (rc != DWDP_OK) return rc;
+    int* err = reinterpret_cast<int*>(scratch);
+    int h = 0;
+    // read the word after everything already enqueued on the stream, then
+    // clear it there, so the next call on this stream starts from zero
+    e = cudaMemcpyAsync(&h, err, sizeof h, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess && h != 0) {
+        e = cudaMemsetAsync(err, 0, sizeof h, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    }
+    if (e != cudaSuccess) return fail_static(DWDP_ERR_CUDA, cudaGetErrorString(e));
+    if (bits) *bits = h;
+    if (h != 0) {
+        char buf[160];
+        snprintf(buf, sizeof buf, "dwdp_route_static: device check failed: error bits 0x%x%s", h,
+                 (h & DERR_NONFINITE_LOGIT) ? " (a router logit is not finite)" : "");
+        return fail_static(DWDP_ERR_DEVICE_CHECK, buf);
+    }
+    return DWDP_OK;
 }

@@ -683,3 +683,42 @@ void oracle_moe_tokens_nvfp4(const uint16_t* x, int64_t H, int64_t I, int64_t k,
         free(acc);
     }
 }
+
+/* One NVFP4 linear layer on rows that arrive already quantized (the second
+ * half of expert_ffn_nvfp4 on its own, and its first half with
+ * epilogue 1), so a caller can check each GEMM of the NVFP4 layer given
+ * the codes its input rows really had:
+ *   epilogue 0:  out[r][c] = (sum_k A[r][k] W[c][k]) * row_scale[r] * w_scale
+ *   epilogue 1:  g = the same with W's row c, u = with W's row N + c,
+ *                out[r][c] = SiLU(g) * u                  (W has 2N rows)
+ * with A[r][k] = E2M1(codes[r][k]) * E4M3(sf[r][k / 16]) and W likewise
+ * (w codes [N or 2N][K], wsf [.][K / 16]); fp64 sums, rounded to bf16 in
+ * mirrored mode. */
+void oracle_nvfp4_linear(const uint8_t* codes, const uint8_t* sf, const float* row_scale, int64_t n, int64_t K,
+                         const uint8_t* w, const uint8_t* wsf, float w_scale, int64_t N, int epilogue, int mirrored,
+                         double* out) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n; ++r) {
+        const uint8_t* a = codes + r * K;
+        const uint8_t* as = sf + r * (K / 16);
+#if ORACLE_MUTANT == 20
+        const double sc = (double)w_scale;                        /* planted: row scale dropped */
+#else
+        const double sc = (double)row_scale[r] * (double)w_scale;
+#endif
+        for (int64_t c = 0; c < N; ++c) {
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k) s += nvfp4_elem(a, as, k) * nvfp4_elem(w + c * K, wsf + c * (K / 16), k);
+            s *= sc;
+            if (epilogue == 1) {
+                double u = 0.0;
+                const uint8_t* wu = w + (N + c) * K;
+                const uint8_t* su = wsf + (N + c) * (K / 16);
+                for (int64_t k = 0; k < K; ++k) u += nvfp4_elem(a, as, k) * nvfp4_elem(wu, su, k);
+                u *= sc;
+                s = s / (1.0 + exp(-s)) * u;
+            }
+            out[r * N + c] = mirrored ? rb(s) : s;
+        }
+    }
+}

@@ -139,3 +139,60 @@ class GpuLayerRun:
 
     def close(self):
         self.rt.close()
+
+
+def assert_route_same_logits(o, rb, T: int, k: int, E: int):
+    """The oracle's steps after the logits (top-k on fp32 decisions, weights,
+    grouping) fed the GPU's own fp32 logits for every token: expert ids,
+    counts, offsets, perm and inv_perm must then be identical, bit for bit,
+    and the weights equal within fp32 softmax rounding.  (The GPU's logits
+    themselves are checked against the oracle's fp64 logits separately.)
+    Returns the oracle's (ids, w) for those logits."""
+    z = rb.logits.cpu().numpy()[:T].astype(np.float64)
+    ids_o, w_o = o.topk(z, k, decide_fp32=True)
+    counts, offsets, perm, inv = o.group(ids_o, E)
+    ids = rb.topk_ids.cpu().numpy()[:T]
+    bad = np.nonzero((ids != ids_o).any(axis=1))[0]
+    assert bad.size == 0, f"{bad.size} of {T} tokens choose other experts than the oracle on the same logits " \
+                          f"(first: token {bad[:5].tolist()})"
+    assert np.array_equal(rb.counts.cpu().numpy(), counts)
+    assert np.array_equal(rb.offsets.cpu().numpy(), offsets)
+    assert np.array_equal(rb.perm.cpu().numpy()[: T * k], perm)
+    assert np.array_equal(rb.inv_perm.cpu().numpy()[: T * k], inv)
+    w = rb.topk_w.cpu().numpy()[:T].astype(np.float64)
+    dw = np.abs(w - w_o).max()
+    assert dw <= 2e-6, f"weights differ by {dw:.3e}"
+    return ids_o, w_o
+
+
+def last_tile_tokens(perm, offsets, k: int, T: int, eligible, n_shared: int = 0, bm: int = 128):
+    """A small set of tokens that between them own at least one row of
+    every routed expert's last (ragged) 128-row m-tile, and (n_shared) of
+    the shared expert's last m-tile, chosen greedily from the tokens in
+    `eligible` (a boolean mask over tokens).  Returns (sorted tokens,
+    experts whose last tile has no eligible token)."""
+    E = offsets.size - 1
+    cover = {}
+    missed = []
+    for e in range(E):
+        c = int(offsets[e + 1] - offsets[e])
+        if c == 0:
+            continue
+        start = int(offsets[e]) + bm * ((c - 1) // bm)
+        toks = {int(t) for t in perm[start:offsets[e + 1]] // k if eligible[t]}
+        if not toks:
+            missed.append(e)
+            continue
+        for t in toks:
+            cover.setdefault(t, set()).add(e)
+    left = set(e for s in cover.values() for e in s)
+    chosen = []
+    while left:
+        t = max(cover, key=lambda u: (len(cover[u] & left), -u))
+        chosen.append(t)
+        left -= cover.pop(t)
+    if n_shared:
+        tail = [t for t in range(bm * ((T - 1) // bm), T) if eligible[t]]
+        if tail and not any(t >= bm * ((T - 1) // bm) for t in chosen):
+            chosen.append(tail[-1])
+    return np.array(sorted(chosen), dtype=np.int64), missed

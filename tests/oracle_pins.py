@@ -614,3 +614,36 @@ def pin_nvfp4_dense(o):
 
 
 ALL_PINS += [pin_e2m1, pin_quantize_rows_nvfp4, pin_nvfp4_dense]
+
+
+def pin_nvfp4_linear(o):
+    """The NVFP4 linear layer on given codes against numpy: the rows and the
+    weights dequantized with the format tables, an fp64 matmul times the row
+    and tensor scales (epilogue 0), and SiLU(gate) * up of the two halves
+    (epilogue 1); mirrored mode is torch's bf16 rounding of that."""
+    rng = np.random.default_rng(18)
+    for (n, K, N) in [(7, 64, 5), (3, 256, 16)]:
+        codes = rng.integers(0, 16, size=(n, K)).astype(np.uint8)
+        sf = rng.integers(0x28, 0x50, size=(n, K // 16)).astype(np.uint8)
+        rs = rng.uniform(0.001, 3.0, size=n).astype(np.float32)
+        for epi in (0, 1):
+            rows = 2 * N if epi else N
+            w = rng.integers(0, 16, size=(rows, K)).astype(np.uint8)
+            wsf = rng.integers(0x28, 0x50, size=(rows, K // 16)).astype(np.uint8)
+            ws = np.float32(rng.uniform(0.005, 0.02))
+            A = _nvfp4_decode(codes, sf) * rs[:, None].astype(np.float64)
+            W = _nvfp4_decode(w, wsf) * np.float64(ws)
+            if epi == 0:
+                ref = A @ W.T
+            else:
+                g, u = A @ W[:N].T, A @ W[N:].T
+                ref = _silu(g) * u
+            got = o.nvfp4_linear(codes, sf, rs, w, wsf, ws, epilogue=epi, mirrored=False)
+            scale = max(1.0, np.abs(ref).max())
+            assert np.max(np.abs(got - ref)) <= 1e-12 * scale, f"NVFP4 linear (epilogue {epi}) != numpy"
+            # mirrored: bf16 values within half a bf16 step (at most 2^-8 relative) of the exact result
+            m = o.nvfp4_linear(codes, sf, rs, w, wsf, ws, epilogue=epi, mirrored=True)
+            assert np.array_equal(_decode(_bits_from_f32(m.astype(np.float32))), m)
+            assert np.all(np.abs(m - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30)
+
+ALL_PINS += [pin_nvfp4_linear]

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), f"{n} not exported"
     bound = {s[0] for s in B.SIGNATURES}
     assert set(names) == bound, "binding and header disagree"
-    assert B.dwdp_version() == 4
+    assert B.dwdp_version() == 5
 
 
 def _random_map(rng, E, P, redundant=0.0):

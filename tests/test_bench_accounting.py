@@ -44,7 +44,34 @@ def test_step_bytes_terms():
 
 
 def test_kernels_per_step_match_the_launch_lists():
-    # profiles/launches_r1_moe_layer_8k*.md: 9 (bf16), 11 (E4M3), 10 (NVFP4) kernels per step
+    # the ncu launch lists of one step show 9 (bf16), 11 (E4M3) and 10 (NVFP4)
+    # of this library's kernels
     assert bench.kernels_per_layer("bf16") == 9
     assert bench.kernels_per_layer("fp8") == 11
     assert bench.kernels_per_layer("nvfp4") == 10
+
+
+PEAKS = {"hbm_gbs": 6792.7, "bf16_tflops": 1928.3, "bf16_tflops_sustained": 1712.7}
+
+
+def test_roofline_bound_follows_the_ridge():
+    """The gate/up GEMM at 8192 tokens does 4.33e12 FLOP over 16.45 GB of
+    algorithmic bytes: 263 FLOP/B, below the burst ridge 1928.3 TFLOP/s /
+    6792.7 GB/s = 284 FLOP/B, so it is HBM-bound and its fraction is
+    bytes / time / HBM peak."""
+    tc, hbm, note = bench.roofline_peaks(PEAKS, "measured", "bf16")
+    assert tc == 1928.3 and hbm == 6792.7 and "burst" in note
+    g1, g1b = bench.g1_flops(T, H, I, K, S), bench.g1_bytes(T, H, I, E, K, S)
+    r = bench.roofline_entry("g1", g1, g1b, 5.8134e-3, tc, hbm, note, "hbm")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["ridge"] == pytest.approx(283.9, abs=0.1)
+    assert r["achieved"] == pytest.approx(g1b / 5.8134e-3 / 1e9, rel=1e-3)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6792.7, abs=1e-4)
+    assert 0.41 < r["frac"] < 0.43
+    # twice the FLOPs per byte crosses the ridge: tensor-bound, FLOP/s against the tensor peak
+    r2 = bench.roofline_entry("g1", 2 * g1, g1b, 5.8134e-3, tc, hbm, note, "hbm")
+    assert r2["bound"] == "tensor" and r2["frac"] == pytest.approx(2 * g1 / 5.8134e-3 / 1e12 / tc, abs=1e-4)
+
+
+def test_low_precision_peaks_scale_the_measured_bf16_burst():
+    assert bench.roofline_peaks(PEAKS, "measured", "fp8")[0] == pytest.approx(2 * 1928.3)
+    assert bench.roofline_peaks(PEAKS, "measured", "nvfp4")[0] == pytest.approx(6 * 1928.3)

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import assert_close, to_f64
+from gpu_helpers import assert_close, last_tile_tokens, to_f64
 from moe_expert_grouped_split_gb300 import binding as B
 from moe_expert_grouped_split_gb300 import inputs as I
 from moe_expert_grouped_split_gb300.build import build
@@ -45,8 +45,17 @@ def _run(shape, placement, seed, tokens=None, router_std=0.02, chunk=1 << 20):
         torch.cuda.synchronize()
         assert rt.device_status() == 0
         o = oracle.default()
-        tok = np.arange(shape.T) if tokens is None else np.asarray(tokens)
         xs = I.bf16_bits(x)
+        if isinstance(tokens, str) and tokens == "last_tiles":
+            # tokens that own a row of every expert's last m-tile (and of the
+            # shared expert's), among those the oracle routes the same way
+            full = o.route(xs, I.bf16_bits(lw.wr), None, shape.k)
+            agree = (rb.topk_ids.cpu().numpy()[: shape.T] == full["ids"]).all(axis=1)
+            tokens, missed = last_tile_tokens(rb.perm.cpu().numpy()[: shape.T * shape.k], rb.offsets.cpu().numpy(),
+                                              shape.k, shape.T, agree, n_shared=shape.S)
+            assert not missed, f"experts {missed}: no token of their last m-tile routes like the oracle"
+            print(f"\n{len(tokens)} tokens cover every expert's last m-tile")
+        tok = np.arange(shape.T) if tokens is None else np.asarray(tokens)
         ref = o.route(xs[tok], I.bf16_bits(lw.wr), None, shape.k)
         ids = rb.topk_ids.cpu().numpy()[tok]
         same = (ids == ref["ids"]).all(axis=1)
@@ -85,7 +94,7 @@ def test_fp8_output_independent_of_placement():
 
 
 def test_fp8_r1_layer_sample():
-    # full R1 shapes in the benchmark's launch configuration, 24 sampled tokens
+    # full R1 shapes in the benchmark's launch configuration; the output of
+    # tokens covering every expert's last m-tile
     shape, pl = I.r1_layer(8192)
-    rng = np.random.default_rng(3)
-    _run(shape, pl, seed=3, tokens=np.sort(rng.choice(8192, 24, replace=False)), chunk=32 << 20)
+    _run(shape, pl, seed=3, tokens="last_tiles", chunk=32 << 20)

@@ -19,7 +19,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import assert_close_requantized, to_f64
+from gpu_helpers import assert_close, assert_close_requantized, last_tile_tokens, to_f64
 from moe_expert_grouped_split_gb300 import binding as B
 from moe_expert_grouped_split_gb300 import inputs as I
 from moe_expert_grouped_split_gb300.build import build
@@ -195,8 +195,17 @@ def _run(shape, placement, seed, tokens=None, router_std=0.02, chunk=1 << 20):
         torch.cuda.synchronize()
         assert rt.device_status() == 0
         o = oracle.default()
-        tok = np.arange(shape.T) if tokens is None else np.asarray(tokens)
         xs = I.bf16_bits(x)
+        if isinstance(tokens, str) and tokens == "last_tiles":
+            # tokens that own a row of every expert's last m-tile (and of the
+            # shared expert's), among those the oracle routes the same way
+            full = o.route(xs, I.bf16_bits(lw.wr), None, shape.k)
+            agree = (rb.topk_ids.cpu().numpy()[: shape.T] == full["ids"]).all(axis=1)
+            tokens, missed = last_tile_tokens(rb.perm.cpu().numpy()[: shape.T * shape.k], rb.offsets.cpu().numpy(),
+                                              shape.k, shape.T, agree, n_shared=shape.S)
+            assert not missed, f"experts {missed}: no token of their last m-tile routes like the oracle"
+            print(f"\n{len(tokens)} tokens cover every expert's last m-tile")
+        tok = np.arange(shape.T) if tokens is None else np.asarray(tokens)
         ref = o.route(xs[tok], I.bf16_bits(lw.wr), None, shape.k)
         ids = rb.topk_ids.cpu().numpy()[tok]
         same = (ids == ref["ids"]).all(axis=1)
@@ -249,8 +258,129 @@ def test_nvfp4_output_independent_of_placement():
     assert torch.equal(a, b) and torch.equal(a, c)
 
 
-def test_nvfp4_r1_layer_sample():
-    # full R1 shapes in the benchmark's launch configuration, 16 sampled tokens
+def _a_tiles(offsets, rows_r, rows_all):
+    """A tile and row-in-tile of every row of the down GEMM's A operand:
+    expert by expert, ceil(rows / 128) tiles each, then the shared rows."""
+    E = offsets.size - 1
+    tile = np.empty(rows_all, dtype=np.int64)
+    base = 0
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        r = np.arange(lo, hi)
+        tile[lo:hi] = base + (r - lo) // 128
+        base += (hi - lo + 127) // 128
+    r = np.arange(rows_r, rows_all)
+    tile[rows_r:] = base + (r - rows_r) // 128
+    within = np.empty(rows_all, dtype=np.int64)
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        within[lo:hi] = (np.arange(lo, hi) - lo) % 128
+    within[rows_r:] = (np.arange(rows_r, rows_all) - rows_r) % 128
+    return tile, within
+
+
+def _down_path_case(shape, placement, seed, n_gate_rows, chunk):
+    """The NVFP4 layer split at its quantized intermediate, each stage held
+    to the plain bars (no allowance for requantization flips):
+      1. gate/up: the GPU's bf16 a of sampled rows against the oracle's
+         SiLU(gate) * up of the same token's x codes (the oracle quantizes x
+         itself) and the row's expert weights;
+      2. a's codes: every row of the GPU's bf16 a quantized by the oracle's
+         row quantizer gives, bit for bit, the codes, E4M3 block scales (at
+         their A-tile chunk positions) and row scale the down GEMM read;
+      3. down: the GPU's y of sampled rows (the last row of every expert's
+         group, in its last m-tile, and of the shared rows) against the
+         oracle's product of those codes with the expert's w2.
+    The layer output itself keeps the end-to-end check of _run."""
+    build()
+    sh = shape
+    lw = I.make_layer_nvfp4(sh, placement, seed, 0, device="cuda")
+    x = I.make_tokens(sh.T, sh.H, seed).cuda()
+    rt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, 1, max(1, placement.n_remote()), weight_dtype=B.DTYPE_NVFP4)
+    try:
+        rt.set_layer(0, lw)
+        rb = B.RouteBuffers(sh.T, sh.E, sh.k)
+        out = torch.empty((sh.T, sh.H), dtype=torch.bfloat16, device="cuda")
+        if placement.n_remote() > 0:
+            rt.prefetch(0, 0, chunk, [torch.cuda.Stream()])
+        rt.route(x, lw.wr, None, rb)
+        rt.moe(0, 0, x, rb, out)
+        torch.cuda.synchronize()
+        assert rt.device_status() == 0
+        T, k, H, I_, E = sh.T, sh.k, sh.H, sh.I, sh.E
+        rows_r, rows_all = T * k, T * (k + sh.S)
+        a_gpu = rt.ws_region(T, "a").view(torch.bfloat16).reshape(rows_all, I_).float().cpu().numpy()
+        aq = _unpack_codes(_u8(rt.ws_region(T, "aq")), rows_all, I_)
+        sa = rt.ws_region(T, "sa").view(torch.float32).cpu().numpy()
+        sfa = _u8(rt.ws_region(T, "sfa"))
+        y_gpu = rt.ws_region(T, "y").view(torch.bfloat16).reshape(rows_all, H).float().cpu().numpy()
+        offsets = rb.offsets.cpu().numpy()
+        perm = rb.perm.cpu().numpy()[:rows_r]
+        o = oracle.default()
+
+        # 2. a's codes, every row
+        tile, within = _a_tiles(offsets, rows_r, rows_all)
+        blk = np.arange(I_ // 16)
+        for r in range(rows_all):
+            c, f, s_ = o.quantize_row_nvfp4(a_gpu[r])
+            assert np.float32(s_) == sa[r], f"row {r}: row scale {sa[r]} != {s_}"
+            assert np.array_equal(c, aq[r]), f"row {r}: codes differ at {np.nonzero(c != aq[r])[0][:8]}"
+            m = within[r]
+            at = (tile[r] * (I_ // 64) + blk // 4) * 512 + 16 * (m % 32) + 4 * (m // 32) + blk % 4
+            assert np.array_equal(f, sfa[at]), f"row {r}: block scales differ"
+
+        def weights(g):
+            """(w13 codes, sf, scale, w2 codes, sf, scale) of group g (E: shared)."""
+            if g == E:
+                c13, f13 = _unpack_slot(_u8(lw.shared_w13), 2 * I_, H)
+                c2, f2 = _unpack_slot(_u8(lw.shared_w2), H, I_)
+                return c13, f13, lw.shared_s13, c2, f2, lw.shared_s2
+            c13, f13, c2, f2 = _expert(lw, g)
+            return c13, f13, lw.w13_scale[g], c2, f2, lw.w2_scale[g]
+
+        groups = [(e, int(offsets[e + 1]) - 1) for e in range(E) if offsets[e + 1] > offsets[e]]
+        if sh.S:
+            groups.append((E, rows_all - 1))
+        xb = x.float().cpu().numpy()
+        rng = np.random.default_rng(seed)
+        gate_rows = set(rng.choice(len(groups), size=min(n_gate_rows, len(groups)), replace=False).tolist())
+        a_want, a_got, y_want, y_got = [], [], [], []
+        for i, (g, r) in enumerate(groups):
+            c13, f13, s13, c2, f2, s2 = weights(g)
+            if i in gate_rows:
+                # 1. gate/up from the token's own x codes
+                t = (int(perm[r]) // k) if r < rows_r else r - rows_r
+                xc, xf, xs = o.quantize_row_nvfp4(xb[t])
+                a_want.append(o.nvfp4_linear(xc[None], xf[None], np.array([xs], np.float32), c13, f13, s13,
+                                             epilogue=1)[0])
+                a_got.append(a_gpu[r])
+            # 3. down from the codes the GPU's a quantized to
+            at = (tile[r] * (I_ // 64) + blk // 4) * 512 + 16 * (within[r] % 32) + 4 * (within[r] // 32) + blk % 4
+            y_want.append(o.nvfp4_linear(aq[r][None], sfa[at][None], sa[r:r + 1], c2, f2, s2)[0])
+            y_got.append(y_gpu[r])
+        ra, ma = assert_close(np.array(a_got), np.array(a_want), what="NVFP4 gate/up output a")
+        ry, my = assert_close(np.array(y_got), np.array(y_want), what="NVFP4 down output y")
+        print(f"\nNVFP4 T={T}: {rows_all} a rows requantized bit-exact; a vs oracle max rel {ra:.2e} MAE {ma:.2e} "
+              f"({len(a_got)} rows); y vs oracle max rel {ry:.2e} MAE {my:.2e} ({len(y_got)} rows)")
+    finally:
+        rt.close()
+
+
+def test_nvfp4_down_path_exact_a_codes_small():
+    # ragged groups, two K slices for both GEMMs, the shared expert
+    _down_path_case(I.LayerShape(T=333, H=512, I=512, E=16, k=4, S=1), I.split_placement(16, 5, 3), seed=8,
+                    n_gate_rows=17, chunk=1 << 20)
+
+
+def test_nvfp4_down_path_exact_a_codes_r1():
+    # the 8192-token R1 layer: all 73 728 a rows' codes, down output of every
+    # expert's last row, gate/up output of 64 of them
     shape, pl = I.r1_layer(8192)
-    rng = np.random.default_rng(4)
-    _run(shape, pl, seed=4, tokens=np.sort(rng.choice(8192, 16, replace=False)), chunk=32 << 20)
+    _down_path_case(shape, pl, seed=4, n_gate_rows=64, chunk=32 << 20)
+
+
+def test_nvfp4_r1_layer_sample():
+    # full R1 shapes in the benchmark's launch configuration; the output of
+    # tokens covering every expert's last m-tile
+    shape, pl = I.r1_layer(8192)
+    _run(shape, pl, seed=4, tokens="last_tiles", chunk=32 << 20)

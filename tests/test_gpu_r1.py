@@ -2,13 +2,17 @@
 times (64 local experts, 192 staged from three peer pools in 32 MB
 round-robin slices, one shared expert, H=7168, I=2048, E=256, top-8):
 
-  * routing: fp32 logits of a token sample against the oracle, expert choice
-    bit-exact away from near-ties, and the grouping of ALL T*k pairs checked
-    for the properties that define it (stable counting sort by expert);
-  * layer output: a seeded token sample against the oracle's mirrored layer
-    (the graded comparison), and against its strict layer (fp64 throughout,
-    no intermediate bf16 rounding), where the GPU may be no further off than
-    the mirrored rounding points themselves put the oracle.
+  * routing, every token: the oracle's top-k and grouping fed the GPU's own
+    fp32 logits give the same expert ids, counts, offsets, perm and inv_perm
+    bit for bit (and the same weights within fp32 rounding); independently,
+    the GPU's logits match the oracle's fp64 logits and the oracle's own
+    routing chooses the same experts for every token that is not a near-tie;
+  * layer output: tokens chosen so that between them they own a row of every
+    routed expert's last (ragged) 128-row m-tile and of the shared expert's
+    last m-tile, against the oracle's mirrored layer (the graded comparison),
+    and against its strict layer (fp64 throughout, no intermediate bf16
+    rounding), where the GPU may be no further off than the mirrored rounding
+    points themselves put the oracle.
 
 Workloads: 8192 tokens (N(0,1) activations, N(0,0.02) router), 16384 tokens
 with a Zipf(1.2) router bias over a seeded expert permutation and the 16
@@ -20,8 +24,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import (GpuLayerRun, assert_close, check_choice_valid, check_grouping_properties,
-                         near_tie_tokens, rel_metrics, to_f64)
+from gpu_helpers import (GpuLayerRun, assert_close, assert_route_same_logits, check_choice_valid,
+                         last_tile_tokens, near_tie_tokens, rel_metrics, to_f64)
 from moe_expert_grouped_split_gb300 import inputs as I
 from moe_expert_grouped_split_gb300.build import build
 
@@ -46,6 +50,20 @@ def _workload(name):
     raise KeyError(name)
 
 
+def expert_weights_host(lw, pl, experts, E, conv=I.bf16_bits):
+    """Host copies of the given experts' weights, resolved through the
+    placement (local slot, else its peer pool's slot)."""
+    w13s, w2s = [None] * E, [None] * E
+    for e in experts:
+        e = int(e)
+        if pl.local_slot[e] >= 0:
+            a, b = lw.local_w13[pl.local_slot[e]], lw.local_w2[pl.local_slot[e]]
+        else:
+            a, b = lw.peer_w13[pl.peer_id[e]][pl.peer_slot[e]], lw.peer_w2[pl.peer_id[e]][pl.peer_slot[e]]
+        w13s[e], w2s[e] = conv(a), conv(b)
+    return w13s, w2s
+
+
 @pytest.mark.parametrize("name", ["r1_8k", "r1_zipf_16k", "r1_256", "r1_32k"])
 def test_full_size_layer(name):
     build()
@@ -56,49 +74,44 @@ def test_full_size_layer(name):
     try:
         rb, out = run.run(x, chunk_bytes=32 << 20)
         T, k, E = shape.T, shape.k, shape.E
+        o = oracle.default()
+        # routing of every token, bit for bit, on the GPU's own logits
+        assert_route_same_logits(o, rb, T, k, E)
         ids = rb.topk_ids.cpu().numpy()[:T]
         counts = rb.counts.cpu().numpy()
         offsets = rb.offsets.cpu().numpy()
         perm = rb.perm.cpu().numpy()[: T * k]
-        inv = rb.inv_perm.cpu().numpy()[: T * k]
-        check_grouping_properties(ids, counts, offsets, perm, inv, E)
         if bias is not None:
             # heavy skew really reaches the grouped GEMM
             assert counts.max() > 8 * counts.mean()
 
-        o = oracle.default()
-        rng = np.random.default_rng(7)
-        sample = np.sort(rng.choice(T, size=min(T, 256), replace=False))
-        xs = I.bf16_bits(x)[sample]
+        # the oracle's own routing of every token, from its fp64 logits
+        xs = I.bf16_bits(x)
         ref = o.route(xs, I.bf16_bits(lw.wr), bias, k)
-        z_gpu = rb.logits.cpu().numpy()[sample].astype(np.float64)
+        z_gpu = rb.logits.cpu().numpy()[:T].astype(np.float64)
         err = np.abs(z_gpu - ref["logits"]).max()
         assert err <= 1e-5 * max(1.0, np.abs(ref["logits"]).max()) + 1e-5, f"logit error {err}"
         tie = near_tie_tokens(ref["logits"], k)
-        same = (ids[sample] == ref["ids"]).all(axis=1)
-        assert same[~tie].all()
-        check_choice_valid(ref["logits"], ids[sample], k)
+        same = (ids == ref["ids"]).all(axis=1)
+        assert same[~tie].all(), f"{(~same & ~tie).sum()} tokens differ without a near-tie"
+        check_choice_valid(ref["logits"], ids, k)
+        print(f"\n{name}: {tie.sum()} near-tie tokens, {(~same).sum()} chose differently from the oracle's "
+              f"fp64 logits")
 
-        # layer output on a smaller sample (the oracle's FFN is the slow part)
-        sub = np.nonzero(same)[0][:24]
-        used = np.unique(ref["ids"][sub])
-        w13s, w2s = [None] * E, [None] * E
-        for e in used:
-            if pl.local_slot[e] >= 0:
-                a, b = lw.local_w13[pl.local_slot[e]], lw.local_w2[pl.local_slot[e]]
-            else:
-                a, b = lw.peer_w13[pl.peer_id[e]][pl.peer_slot[e]], lw.peer_w2[pl.peer_id[e]][pl.peer_slot[e]]
-            w13s[e], w2s[e] = I.bf16_bits(a), I.bf16_bits(b)
-        want = o.moe_tokens(xs, sub, ref["ids"], ref["w"], w13s, w2s, I.bf16_bits(lw.shared_w13),
-                            I.bf16_bits(lw.shared_w2), mirrored=True)
-        got = to_f64(out[torch.from_numpy(sample[sub]).cuda()])
+        # layer output on tokens that cover every expert's last m-tile
+        sub, missed = last_tile_tokens(perm, offsets, k, T, same, n_shared=shape.S)
+        assert not missed, f"experts {missed}: no token of their last m-tile routes like the oracle"
+        w13s, w2s = expert_weights_host(lw, pl, np.unique(ref["ids"][sub]), E)
+        sw13, sw2 = I.bf16_bits(lw.shared_w13), I.bf16_bits(lw.shared_w2)
+        want = o.moe_tokens(xs, sub, ref["ids"], ref["w"], w13s, w2s, sw13, sw2, mirrored=True)
+        got = to_f64(out[torch.from_numpy(sub).cuda()])
         r_m, mae_m = assert_close(got, want, what=f"{name} layer output")
-        strict = o.moe_tokens(xs, sub, ref["ids"], ref["w"], w13s, w2s, I.bf16_bits(lw.shared_w13),
-                              I.bf16_bits(lw.shared_w2), mirrored=False)
+        strict = o.moe_tokens(xs, sub, ref["ids"], ref["w"], w13s, w2s, sw13, sw2, mirrored=False)
         r_s, mae_s = rel_metrics(got, strict)
         r_o, mae_o = rel_metrics(want, strict)
-        print(f"\n{name}: vs mirrored max rel {r_m:.3e} MAE {mae_m:.3e}; vs strict max rel {r_s:.3e} "
-              f"MAE {mae_s:.3e}; oracle mirrored vs strict max rel {r_o:.3e} MAE {mae_o:.3e}")
+        print(f"{name}: {sub.size} tokens covering {int((counts > 0).sum())} experts' last m-tiles: vs mirrored "
+              f"max rel {r_m:.3e} MAE {mae_m:.3e}; vs strict max rel {r_s:.3e} MAE {mae_s:.3e}; oracle mirrored "
+              f"vs strict max rel {r_o:.3e} MAE {mae_o:.3e}")
         assert mae_s <= 2.0 * mae_o + 1e-4, (mae_s, mae_o)
         assert r_s <= 2.0 * r_o + 2e-2, (r_s, r_o)
     finally:

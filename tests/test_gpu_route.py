@@ -91,3 +91,60 @@ def test_equal_logits_tie_to_lower_id():
 
 def test_single_token():
     _route_case(1, 256, 8, 2, seed=7)
+
+
+def test_non_finite_logit_is_reported_and_routing_stays_valid():
+    """A NaN in one token's row makes every one of its logits NaN: that
+    token still gets k distinct experts, every other token is routed as the
+    oracle routes it, the grouping stays consistent, and the context's error
+    word reports the non-finite logit (DEVICE_CHECK) once."""
+    build()
+    T, H, E, k = 200, 256, 16, 4
+    rt = B.Runtime(H, 128, E, k, 0, T, 1, 0)
+    try:
+        x = I.make_tokens(T, H, 9).cuda()
+        x[17, 3] = float("nan")
+        wr = I.randn_bf16((E, H), 0.05, I.seed_for(9, "Wr")).cuda()
+        rb = B.RouteBuffers(T, E, k)
+        rt.route(x, wr, None, rb)
+        torch.cuda.synchronize()
+        with pytest.raises(B.DwdpError) as ei:
+            rt.device_status()
+        assert ei.value.code == -6 and "0x80" in str(ei.value)
+        assert rt.device_status() == 0
+        ids = rb.topk_ids.cpu().numpy()
+        assert len(set(ids[17].tolist())) == k
+        good = np.arange(T) != 17
+        o = oracle.default()
+        xs = I.bf16_bits(x)[good]
+        ref = o.route(xs, I.bf16_bits(wr), None, k, decide_fp32=True)
+        tie = near_tie_tokens(ref["logits"], k)
+        same = (ids[good] == ref["ids"]).all(axis=1)
+        assert same[~tie].all()
+        check_grouping_properties(ids, rb.counts.cpu().numpy(), rb.offsets.cpu().numpy(),
+                                  rb.perm.cpu().numpy()[: T * k], rb.inv_perm.cpu().numpy()[: T * k], E)
+    finally:
+        rt.close()
+
+
+def test_tensor_mapped_inputs_must_be_this_devices_memory():
+    """x and the router weight are read through TMA tensor maps: pinned host
+    memory (which the GPU could reach) is refused on the host, before
+    anything is enqueued."""
+    build()
+    T, H, E, k = 8, 256, 8, 2
+    rt = B.Runtime(H, 128, E, k, 0, T, 1, 0)
+    try:
+        x_host = I.make_tokens(T, H, 1).pin_memory()
+        wr = I.randn_bf16((E, H), 0.02, I.seed_for(1, "Wr")).cuda()
+        rb = B.RouteBuffers(T, E, k)
+        with pytest.raises(B.DwdpError) as ei:
+            rt.route(x_host, wr, None, rb)
+        assert ei.value.code == -1 and "device memory" in str(ei.value)
+        with pytest.raises(B.DwdpError) as ei:
+            B.dwdp_route_static(x_host, T, H, E, k, wr, None, rb.c)
+        assert ei.value.code == -1 and "device memory" in str(ei.value)
+        torch.cuda.synchronize()
+        assert rt.device_status() == 0
+    finally:
+        rt.close()

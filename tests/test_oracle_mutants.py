@@ -27,6 +27,7 @@ MUTANTS = {
     17: "NVFP4 row scale without the block range 6",
     18: "NVFP4 block scales indexed as 32-wide blocks",
     19: "NVFP4 down-projection tensor scale dropped",
+    20: "NVFP4 linear layer drops the row scale",
 }
 
 
