@@ -108,9 +108,8 @@ def test_non_finite_logit_is_reported_and_routing_stays_valid():
         rb = B.RouteBuffers(T, E, k)
         rt.route(x, wr, None, rb)
         torch.cuda.synchronize()
-        with pytest.raises(B.DwdpError) as ei:
-            rt.device_status()
-        assert ei.value.code == -6 and "0x80" in str(ei.value)
+        assert rt.device_status() == -6                      # DEVICE_CHECK, read and cleared
+        assert "0x80" in B.dwdp_last_error(rt.ctx)
         assert rt.device_status() == 0
         ids = rb.topk_ids.cpu().numpy()
         assert len(set(ids[17].tolist())) == k
