@@ -48,6 +48,9 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN 
 constexpr uint32_t kIdescE4M3 = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 constexpr uint32_t kIdescNvfp4 = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
+#ifndef DWDP_SF_WARP
+#define DWDP_SF_WARP 1
+#endif
 // Per-format constants.  NVFP4 keeps one accumulator (256 TMEM columns) so
 // that the other 256 columns can hold the block scales of the stages in
 // flight: per stage 4 K steps x (4 columns of A scales + 8 of B scales).
@@ -58,6 +61,10 @@ struct Fmt {
     static constexpr int kSfBytes = FMT == FMT_NVFP4 ? kSfStageBytesA + kSfStageBytesB : 0;
     static constexpr int kStageTx = kStageBytes + kSfBytes;
     static constexpr int kAccBufs = FMT == FMT_NVFP4 ? 1 : 2;
+    // NVFP4: a seventh warp copies each stage's block scales into TMEM, so
+    // the MMA warp's one thread issues only the MMAs
+    static constexpr bool kSfWarp = FMT == FMT_NVFP4 && DWDP_SF_WARP;
+    static constexpr int kThreads = kGemmThreads + (kSfWarp ? 32 : 0);
 };
 constexpr int kSfCol0 = BN;                             // NVFP4: first TMEM column of the scale ring
 constexpr int kSfColsPerStage = 12 * kSfStepsPerSlice;  // per K step: 4 columns of A scales, 8 of B
@@ -228,6 +235,22 @@ __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
+// The twelve chunks of one stage into its TMEM scale columns starting at tc:
+// per 64-element K step j, A's 128 rows at tc + 4 j, B's two 128-row halves
+// at tc + 16 + 8 j and tc + 20 + 8 j (sd: descriptor of the stage's first
+// chunk; chunk o bytes further has descriptor sd + o / 16, since the
+// start-address field holds address / 16 and shared memory addresses stay
+// below its 2^14 limit, so the add never carries).
+__device__ __forceinline__ void copy_stage_scales(uint32_t tc, uint64_t sd) {
+    constexpr int kBCol = 4 * kSfStepsPerSlice;  // B scales follow A's columns
+#pragma unroll
+    for (int j = 0; j < kSfStepsPerSlice; ++j) {
+        tc_cp_sf(tc + 4 * j, sd + (uint64_t)(j * kSfChunkBytes / 16));
+        tc_cp_sf(tc + kBCol + 8 * j, sd + (uint64_t)((kSfStageBytesA + j * kSfChunkBytes) / 16));
+        tc_cp_sf(tc + kBCol + 4 + 8 * j, sd + (uint64_t)((2 * kSfStageBytesA + j * kSfChunkBytes) / 16));
+    }
+}
+
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -329,14 +352,15 @@ struct SmemLayout {
     static constexpr int kA = 0;
     static constexpr int kB = kStages * kABytes;
     static constexpr int kSF = kB + kStages * kBBytes;    // NVFP4: A then B scale chunks per stage
-    static constexpr int kBars = kSF + kStages * Fmt<FMT>::kSfBytes;  // full[S], empty[S], tfull[2], tempty[2], mdone
-    static constexpr int kNumBars = 2 * kStages + 5;
+    // full[S], empty[S], tfull[2], tempty[2], mdone, sf_full[S], cpdone
+    static constexpr int kBars = kSF + kStages * Fmt<FMT>::kSfBytes;
+    static constexpr int kNumBars = 3 * kStages + 6;
     static constexpr int kMisc = kBars + 8 * kNumBars;    // tmem base, abort flag
     static constexpr int kTileStart = kMisc + 16;         // int32[G+1]
 };
 
 template <int EPI, int FMT>
-__global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
+__global__ void __launch_bounds__(Fmt<FMT>::kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
     using SL = SmemLayout<FMT>;
     using F = Fmt<FMT>;
     constexpr int KE = F::kKElems;     // K elements per 128-byte slice
@@ -352,6 +376,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
     const uint32_t mdone_bar = bar0 + 8u * (2 * kStages + 4);
+    auto sf_full_bar = [&](int s) { return bar0 + 8u * (2 * kStages + 5 + s); };  // scales of stage s in TMEM
+    const uint32_t cpdone_bar = bar0 + 8u * (3 * kStages + 5);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::kMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::kMisc + 4);
     int32_t* tile_start = reinterpret_cast<int32_t*>(smem + SL::kTileStart);
@@ -397,6 +423,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             mbar_init(tempty_bar(a), 4);
         }
         mbar_init(mdone_bar, 1);
+        for (int s = 0; s < kStages; ++s) mbar_init(sf_full_bar(s), 1);
+        mbar_init(cpdone_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -550,7 +578,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);  // NVFP4: acc is always 0
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err, DERR_MMA_FULL_WAIT)) {
+                    // with the scale warp, its commit for this stage also means the
+                    // stage's operands have landed (it waited for them first)
+                    const uint32_t ready = F::kSfWarp ? sf_full_bar(stage) : full_bar(stage);
+                    if (!mbar_wait(ready, phase, abort_flag, p.err, DERR_MMA_FULL_WAIT)) {
                         ok = false;
                         break;
                     }
@@ -562,21 +593,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
                     if constexpr (FMT == FMT_NVFP4) {
                         // block scales of this stage into its TMEM columns (the MMAs
                         // that last read those columns finished before the stage was
-                        // refilled), then 4 block-scaled MMAs of 64 elements each
+                        // refilled; with the scale warp it has copied them already),
+                        // then 4 block-scaled MMAs of 64 elements each
                         const uint32_t ss = sbase + SL::kSF + stage * F::kSfBytes;
                         const uint32_t tc = tmem_base + (uint32_t)(kSfCol0 + stage * kSfColsPerStage);
                         constexpr int kBCol = 4 * kSfStepsPerSlice;  // B scales follow A's columns
-                        // the chunk o bytes past ss has descriptor sd + o / 16: the
-                        // start-address field holds address / 16 and shared memory
-                        // addresses stay below its 2^14 limit, so the add never carries
-                        const uint64_t sd = sf_chunk_desc(ss);
-#pragma unroll
-                        for (int j = 0; j < kSfStepsPerSlice; ++j) {
-                            tc_cp_sf(tc + 4 * j, sd + (uint64_t)(j * kSfChunkBytes / 16));
-                            tc_cp_sf(tc + kBCol + 8 * j, sd + (uint64_t)((kSfStageBytesA + j * kSfChunkBytes) / 16));
-                            tc_cp_sf(tc + kBCol + 4 + 8 * j,
-                                     sd + (uint64_t)((2 * kSfStageBytesA + j * kSfChunkBytes) / 16));
-                        }
+                        if constexpr (!F::kSfWarp) copy_stage_scales(tc, sf_chunk_desc(ss));
 #pragma unroll
                         for (int kk = 0; kk < BK_BYTES / 32; ++kk)
                             tc_mma<FMT>(d_tmem, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk),
@@ -611,6 +633,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
             // all issued MMAs complete before TMEM is released
             tc_commit(mdone_bar);
             mbar_wait_drain(mdone_bar, 0, p.err, DERR_MMA_DONE_WAIT);
+        }
+    } else if (F::kSfWarp && warp == kGemmThreads / 32) {
+        // ------------------------------------------------ scale copies ----
+        // Stage by stage in the MMA warp's order: once a stage's operands have
+        // landed, copy its twelve block-scale chunks into the stage's TMEM
+        // scale columns and commit to sf_full[stage], on which the MMA warp
+        // waits.  The columns are free again by then: the stage was refilled
+        // only after the MMAs that last read them had completed.
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err, DERR_MMA_FULL_WAIT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ss = sbase + SL::kSF + stage * F::kSfBytes;
+                    copy_stage_scales(tmem_base + (uint32_t)(kSfCol0 + stage * kSfColsPerStage), sf_chunk_desc(ss));
+                    tc_commit(sf_full_bar(stage));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // every copy issued has completed before TMEM is released
+            tc_commit(cpdone_bar);
+            mbar_wait_drain(cpdone_bar, 0, p.err, DERR_MMA_DONE_WAIT);
         }
     } else {
         // ------------------------------------------------ epilogue --------
@@ -829,7 +882,7 @@ cudaError_t launch_grouped_gemm(int epi, int fmt, const GemmArgs& args, int n_sm
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kGemmThreads);
+    cfg.blockDim = dim3(fmt == FMT_NVFP4 ? Fmt<FMT_NVFP4>::kThreads : kGemmThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
