@@ -113,6 +113,10 @@ def parse(argv=None):
                    help="also time the merge-copy baseline (one contiguous weight buffer per layer); on by "
                         "default for the 8K-token layer")
     p.add_argument("--no-merge-copy", action="store_true", help="skip the merge-copy baseline")
+    p.add_argument("--variants", default=None,
+                   help="comma-separated weight types (fp8, nvfp4) also measured on the same workload after the "
+                        "main line, each summarised under 'variants' (default for the 8K-token bf16 layer: "
+                        "fp8,nvfp4)")
     p.add_argument("--peer-pools", default="device", choices=["device", "host"],
                    help="where the emulated peers' pools live (host: pinned host memory, copies over the "
                         "host link, so only their writes use this GPU's HBM)")
@@ -125,6 +129,9 @@ def parse(argv=None):
         args.merge_copy = True
     if args.no_merge_copy:
         args.merge_copy = False
+    if args.variants is None:
+        default = args.workload == "r1_moe_layer_8k" and args.dtype == "bf16" and not args.no_extras
+        args.variants = "fp8,nvfp4" if default and args.group == 4 else ""
     return args
 
 
@@ -897,6 +904,49 @@ def cpu_baseline_sample(wl, target_s=15.0, max_tokens=512):
                       f"tokens, {dt1:.1f} s)"}
 
 
+def variant_summary(args, wdtype: str) -> dict:
+    """The same workload with other expert weights (E4M3 or NVFP4), timed
+    like the main line (overlapped steps, compute-only and copy-only legs,
+    end to end with host buffers), in compact form."""
+    import copy as _copy
+
+    import torch
+    a = _copy.copy(args)
+    a.dtype, a.merge_copy, a.chunk_sweep = wdtype, False, ""
+    res = run_layer_bench(a)
+    wl = res.pop("wl")
+    sh = wl.shape
+    peaks, src = measured_peaks()
+    tc_peak, hbm, tc_note = roofline_peaks(peaks, src, wdtype)
+    wb = WEIGHT_BYTES[wdtype]
+    g1 = g1_flops(sh.T, sh.H, sh.I, sh.k, sh.S)
+    g1b = g1_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S, wb)
+    comp, copy_ms = res["compute_only_ms"], res["copy_only_ms"]
+    exposed = max(0.0, res["ms_step"] - comp)
+    out = {
+        "expert_weights": wdtype, "value": round(res["value"], 1), "unit": UNIT,
+        "ms_per_step": round(res["ms_step"], 4), "e2e": res["e2e"],
+        "tflops": round(layer_flops(sh.T, sh.H, sh.I, sh.E, sh.k, sh.S) / (res["ms_step"] / 1e3) / 1e12, 1),
+        "phase_ms": res["phase_ms"], "compute_only_phase_ms": res["compute_only_phase_ms"],
+        "prefetch": {"compute_only_ms": round(comp, 4), "copy_only_ms": round(copy_ms, 4),
+                     "exposed_ms": round(exposed, 4),
+                     "hidden_frac": round(max(0.0, 1.0 - exposed / copy_ms), 4) if copy_ms > 0 else None},
+        "roofline": roofline_entry("gate_up_grouped_gemm", g1, g1b, res["phase_ms"]["gate_up_gemm"] / 1e3, tc_peak,
+                                   hbm, tc_note, f"{src} hbm_gbs"),
+        "roofline_alone": roofline_entry("gate_up_grouped_gemm", g1, g1b,
+                                         res["compute_only_phase_ms"]["gate_up_gemm"] / 1e3, tc_peak, hbm, tc_note,
+                                         f"{src} hbm_gbs"),
+        "step_hbm_frac": round(step_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S, wl.placement.n_remote(), wb)
+                               / (res["ms_step"] / 1e3) / 1e9 / hbm, 4),
+        "clocks": res["clocks"], "gpu_launches": kernels_per_layer(wdtype) * args.steps,
+    }
+    wl.rt.close()
+    del wl, res
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -1002,6 +1052,13 @@ def main():
         line["e2e"] = res["e2e"]
     if not args.no_cpu_baseline and not pipeline:
         line["cpu_baseline"] = cpu_baseline_sample(wl)
+    if args.variants and not pipeline:
+        import torch
+        wl.rt.close()
+        del wl, res
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["variants"] = {v: variant_summary(args, v) for v in args.variants.split(",") if v}
     print(json.dumps(line), flush=True)
 
 
