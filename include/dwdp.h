@@ -416,6 +416,25 @@ int32_t dwdp_plan_prefetch(int32_t n_experts, int32_t hidden, int32_t inter, int
                            const int32_t* peer_slot, int32_t n_peers, size_t chunk_bytes,
                            dwdp_copy_slice* out, int64_t max_out, int64_t* n_out);
 
+/* Host-only (no GPU needed): the expert map of rank `rank` in a DWDP group
+ * of n_ranks ranks ([DWDP] §2: each rank keeps a partition of the experts
+ * and pulls the rest from its peers; §4.3.1-§4.3.2: the pulls of several
+ * destinations from one source contend, so slices are issued round-robin).
+ * Rank q hosts experts [floor(q E / N), floor((q + 1) E / N)) in slots
+ * 0, 1, ... of its pool.  Fills local_slot [E] (the slot for this rank's own
+ * experts, else -1), and for the others peer_id [E] and peer_slot [E] (-1 for
+ * own experts), numbering this rank's peers from the next rank on: peer p
+ * is rank (rank + 1 + p) mod n_ranks, so the peers array given to
+ * dwdp_set_expert_map lists the other ranks' pools in that order.  With this
+ * numbering the round-robin of dwdp_plan_prefetch has every rank, at the
+ * same step of its plan, pulling from a different source (when every rank
+ * hosts the same number of experts), so no source serves two destinations
+ * at once.  A map for placement only: the pulls themselves are copy-engine
+ * memcpy nodes whose source may be any memory the copy engine reaches.
+ * Errors: INVALID_ARG. */
+int32_t dwdp_group_map(int32_t n_experts, int32_t n_ranks, int32_t rank, int32_t* local_slot, int32_t* peer_id,
+                       int32_t* peer_slot);
+
 #ifdef __cplusplus
 }
 #endif

@@ -87,6 +87,7 @@ SIGNATURES = [
                                  _I32, _I32P, _VP, _VP]),
     ("dwdp_route_static", _I32, [_VP, _I32, _I32, _I32, _I32, _VP, _VP, ctypes.POINTER(dwdp_route_out), _VP]),
     ("dwdp_route_static_status", _I32, [_VP, _I32P]),
+    ("dwdp_group_map", _I32, [_I32, _I32, _I32, _I32P, _I32P, _I32P]),
     ("dwdp_workspace_region", _I32, [_VP, _I32, _I32, ctypes.POINTER(ctypes.c_size_t),
                                      ctypes.POINTER(ctypes.c_size_t)]),
     ("dwdp_quantize_rows", _I32, [_I32, _VP, ctypes.c_int64, _I32, _VP, _VP, _VP, _VP]),
@@ -286,6 +287,17 @@ def dwdp_set_expert_scales(ctx, layer, w13_scale, w2_scale, shared_w13_scale=1.0
     fp = ctypes.POINTER(ctypes.c_float)
     _check(ctx, lib().dwdp_set_expert_scales(ctx, layer, s13.ctypes.data_as(fp), s2.ctypes.data_as(fp),
                                              float(shared_w13_scale), float(shared_w2_scale)))
+
+
+def dwdp_group_map(n_experts, n_ranks, rank):
+    """(local_slot, peer_id, peer_slot) int32 arrays [E] of rank `rank` in a
+    DWDP group of n_ranks ranks (host only)."""
+    ls = np.empty(n_experts, dtype=np.int32)
+    pid = np.empty(n_experts, dtype=np.int32)
+    ps = np.empty(n_experts, dtype=np.int32)
+    _check(None, lib().dwdp_group_map(n_experts, n_ranks, rank, ls.ctypes.data_as(_I32P), pid.ctypes.data_as(_I32P),
+                                      ps.ctypes.data_as(_I32P)))
+    return ls, pid, ps
 
 
 def dwdp_plan_prefetch(n_experts, hidden, inter, local_slot, peer_id, peer_slot, n_peers, chunk_bytes,

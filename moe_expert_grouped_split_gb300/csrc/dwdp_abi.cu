@@ -530,6 +530,31 @@ int32_t dwdp_plan_prefetch(int32_t n_experts, int32_t hidden, int32_t inter, int
     return DWDP_OK;
 }
 
+int32_t dwdp_group_map(int32_t n_experts, int32_t n_ranks, int32_t rank, int32_t* local_slot, int32_t* peer_id,
+                       int32_t* peer_slot) {
+    if (n_experts <= 0 || n_ranks < 1 || n_ranks > DWDP_MAX_PEERS + 1 || n_ranks > n_experts || rank < 0 ||
+        rank >= n_ranks || !local_slot || !peer_id || !peer_slot)
+        return fail(nullptr, DWDP_ERR_INVALID_ARG, "need 1 <= n_ranks <= min(E, %d), 0 <= rank < n_ranks and "
+                    "non-NULL arrays", DWDP_MAX_PEERS + 1);
+    // contiguous blocks: rank q hosts experts [q E / N, (q + 1) E / N)
+    auto first = [&](int64_t q) { return (int32_t)(q * n_experts / n_ranks); };
+    int32_t home = 0;
+    for (int32_t e = 0; e < n_experts; ++e) {
+        while (e >= first(home + 1)) ++home;
+        const int32_t slot = e - first(home);
+        if (home == rank) {
+            local_slot[e] = slot;
+            peer_id[e] = -1;
+            peer_slot[e] = -1;
+        } else {
+            local_slot[e] = -1;
+            peer_id[e] = ((home - rank - 1) % n_ranks + n_ranks) % n_ranks;  // peer p is rank (rank + 1 + p) mod N
+            peer_slot[e] = slot;
+        }
+    }
+    return DWDP_OK;
+}
+
 int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router, const float* logit_bias,
                    const dwdp_route_out* out, void* ws, size_t ws_bytes, dwdp_stream_t stream) {
     if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");

@@ -29,7 +29,7 @@ from pathlib import Path
 
 import numpy as np
 
-from .prefetch_plan import plan_prefetch, stage_slots  # noqa: F401
+from .prefetch_plan import group_map, plan_prefetch, stage_slots  # noqa: F401
 
 _HERE = Path(__file__).resolve().parent
 _SRC = _HERE / "dwdp_oracle.c"

@@ -90,3 +90,31 @@ def plan_prefetch(n_experts, hidden, inter, local_slot, peer_id, peer_slot,
             break
         c += 1
     return plan
+
+
+def group_map(n_experts, n_ranks, rank):
+    """Placement of rank `rank` in a DWDP group of n_ranks ranks (DWDP §2:
+    the experts are partitioned over the ranks, each pulls the others'
+    experts from their homes).  Readings: rank q hosts the contiguous block
+    of experts [floor(q E / N), floor((q + 1) E / N)) in slots 0, 1, ...;
+    a rank numbers its peers from the next rank on (peer p = rank
+    (rank + 1 + p) mod N), so that the round-robin over peers of
+    ``plan_prefetch`` starts every rank at a different source (DWDP §4.3.1:
+    many destinations pulling from one source contend).  Returns
+    (local_slot, peer_id, peer_slot) lists."""
+    homes = []
+    for q in range(n_ranks):
+        lo, hi = q * n_experts // n_ranks, (q + 1) * n_experts // n_ranks
+        homes += [(q, e - lo) for e in range(lo, hi)]
+    local_slot, peer_id, peer_slot = [], [], []
+    for e in range(n_experts):
+        q, slot = homes[e]
+        if q == rank:
+            local_slot.append(slot)
+            peer_id.append(-1)
+            peer_slot.append(-1)
+        else:
+            local_slot.append(-1)
+            peer_id.append((q - rank - 1) % n_ranks)
+            peer_slot.append(slot)
+    return local_slot, peer_id, peer_slot

@@ -133,3 +133,14 @@ def test_host_validation_without_gpu(lib):
         cfg = B.dwdp_config(256, 128, 8, 2, 0, 64, 1, 0)
         rc = lib.dwdp_create(ctypes.byref(cfg), None, None, ctypes.byref(out))
         assert rc == -3, B.dwdp_last_error(None)               # no CUDA device here
+
+
+def test_group_map_matches_oracle(lib):
+    for E in (1, 7, 16, 256):
+        for N in range(1, min(E, 9) + 1):
+            for r in range(N):
+                got = [a.tolist() for a in B.dwdp_group_map(E, N, r)]
+                assert got == [list(v) for v in oracle.group_map(E, N, r)], (E, N, r)
+    for bad in ((8, 0, 0), (8, 3, 3), (8, 9, 0), (0, 1, 0)):
+        with pytest.raises(B.DwdpError):
+            B.dwdp_group_map(*bad)

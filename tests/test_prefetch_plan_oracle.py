@@ -86,3 +86,32 @@ def test_r1_split_counts():
     total = sum(x[4] for x in plan)
     assert total == 192 * 3 * H * I * 2
     assert len(plan) == 3 * (-(-64 * 2 * I * H * 2 // (16 << 20)) + -(-64 * H * I * 2 // (16 << 20)))
+
+
+def test_group_map_oracle_partitions_and_rotates():
+    """The group-map oracle against what its reading fixes: every expert
+    is hosted by exactly one rank, the blocks are contiguous and their sizes
+    differ by at most one, a rank's own experts take slots 0, 1, ..., and
+    peer p of rank r is rank (r + 1 + p) mod N."""
+    from oracle import group_map
+    for E in (5, 16, 256):
+        for N in range(1, 9):
+            if N > E:
+                continue
+            hosts = {}
+            for r in range(N):
+                ls, pid, ps = group_map(E, N, r)
+                own = [e for e in range(E) if ls[e] >= 0]
+                assert [ls[e] for e in own] == list(range(len(own)))
+                assert own == list(range(own[0], own[0] + len(own))) if own else True
+                for e in own:
+                    hosts.setdefault(e, []).append(r)
+                for e in range(E):
+                    if ls[e] < 0:
+                        q = (r + 1 + pid[e]) % N
+                        assert q != r and 0 <= pid[e] < N - 1
+                        lq, _, _ = group_map(E, N, q)
+                        assert lq[e] == ps[e]                 # the slot the home rank keeps it in
+            assert sorted(hosts) == list(range(E)) and all(len(v) == 1 for v in hosts.values())
+            sizes = [sum(1 for e in range(E) if hosts[e] == [r]) for r in range(N)]
+            assert max(sizes) - min(sizes) <= 1
