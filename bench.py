@@ -114,12 +114,15 @@ def parse(argv=None):
                         "default for the 8K-token layer")
     p.add_argument("--no-merge-copy", action="store_true", help="skip the merge-copy baseline")
     p.add_argument("--variants", default=None,
-                   help="comma-separated weight types (fp8, nvfp4) also measured on the same workload after the "
-                        "main line, each summarised under 'variants' (default for the 8K-token bf16 layer: "
-                        "fp8,nvfp4)")
+                   help="comma-separated weight types (fp8, nvfp4, nvfp4_wide = nvfp4 with --wide-epilogue) also "
+                        "measured on the same workload after the main line, each summarised under 'variants' "
+                        "(default for the 8K-token bf16 layer: fp8,nvfp4,nvfp4_wide)")
     p.add_argument("--peer-pools", default="device", choices=["device", "host"],
                    help="where the emulated peers' pools live (host: pinned host memory, copies over the "
                         "host link, so only their writes use this GPU's HBM)")
+    p.add_argument("--wide-epilogue", action="store_true",
+                   help="NVFP4: the gate/up GEMM drains its accumulator with eight warps (faster alone, but it "
+                        "starves the overlapped copy on one GPU)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extras", action="store_true", help="skip compute-only / copy-only / e2e legs")
     args = p.parse_args(argv)
@@ -131,7 +134,7 @@ def parse(argv=None):
         args.merge_copy = False
     if args.variants is None:
         default = args.workload == "r1_moe_layer_8k" and args.dtype == "bf16" and not args.no_extras
-        args.variants = "fp8,nvfp4" if default and args.group == 4 else ""
+        args.variants = "fp8,nvfp4,nvfp4_wide" if default and args.group == 4 else ""
     return args
 
 
@@ -321,7 +324,7 @@ class Workload:
     and per-layer token batches, all resident in HBM."""
 
     def __init__(self, spec: Spec, chunk_bytes, n_copy_streams, n_layers=2, base_seed=0, wdtype="bf16",
-                 peer_pools="device", prefetch_start="route", n_stages=2):
+                 peer_pools="device", prefetch_start="route", n_stages=2, flags=0):
         import torch
 
         from moe_expert_grouped_split_gb300 import binding as B
@@ -351,7 +354,7 @@ class Workload:
         self.n_stages = n_stages
         self.rt = B.Runtime(sh.H, sh.I, sh.E, sh.k, sh.S, sh.T, n_layers, self.placement.n_remote(),
                             weight_dtype={"bf16": B.DTYPE_BF16, "fp8": B.DTYPE_E4M3, "nvfp4": B.DTYPE_NVFP4}[wdtype],
-                            n_stages=n_stages)
+                            n_stages=n_stages, flags=flags)
         for l, lw in enumerate(self.layers):
             self.rt.set_layer(l, lw)
         self.x = [I.make_tokens(sh.T, sh.H, base_seed, step=s, device="cuda") for s in range(n_layers)]
@@ -556,13 +559,20 @@ def run_e2e(wl, K):
             "h2d_bytes_per_step": T * sh.H * 2, "d2h_bytes_per_step": T * sh.H * 2}
 
 
+def wl_flags(args) -> int:
+    """dwdp_config.flags for the benchmark's options."""
+    from moe_expert_grouped_split_gb300 import binding as B
+    return B.FLAG_WIDE_EPILOGUE if getattr(args, "wide_epilogue", False) else 0
+
+
 def run_layer_bench(args):
     """The single-layer workloads (8K default, Zipf 16K, 256 tokens)."""
     import torch
     torch.cuda.set_device(0)
     spec = WORKLOADS[args.workload](group=args.group)
     wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, wdtype=args.dtype, peer_pools=args.peer_pools,
-                  prefetch_start=args.prefetch_start, n_stages=args.stages)
+                  prefetch_start=args.prefetch_start, n_stages=args.stages,
+                  flags=wl_flags(args))
     sh = wl.shape
     K, W = args.steps, args.warmup
     phases = [_events(torch, 7) for _ in range(K)]
@@ -744,7 +754,7 @@ def run_pipeline_bench(args):
     torch.cuda.set_device(0)
     spec = WORKLOADS[args.workload](group=args.group)
     wl = Workload(spec, args.chunk_mb * (1 << 20), args.copy_streams, n_layers=4, wdtype=args.dtype,
-                  prefetch_start=args.prefetch_start, n_stages=args.stages)
+                  prefetch_start=args.prefetch_start, n_stages=args.stages, flags=wl_flags(args))
     S = wl.n_stages
     sh = wl.shape
     steps = args.steps
@@ -912,7 +922,9 @@ def variant_summary(args, wdtype: str) -> dict:
 
     import torch
     a = _copy.copy(args)
-    a.dtype, a.merge_copy, a.chunk_sweep = wdtype, False, ""
+    wide = wdtype.endswith("_wide")
+    wdtype = wdtype[: -len("_wide")] if wide else wdtype
+    a.dtype, a.merge_copy, a.chunk_sweep, a.wide_epilogue = wdtype, False, "", wide
     res = run_layer_bench(a)
     wl = res.pop("wl")
     sh = wl.shape
@@ -924,7 +936,7 @@ def variant_summary(args, wdtype: str) -> dict:
     comp, copy_ms = res["compute_only_ms"], res["copy_only_ms"]
     exposed = max(0.0, res["ms_step"] - comp)
     out = {
-        "expert_weights": wdtype, "value": round(res["value"], 1), "unit": UNIT,
+        "expert_weights": wdtype, "wide_epilogue": wide, "value": round(res["value"], 1), "unit": UNIT,
         "ms_per_step": round(res["ms_step"], 4), "e2e": res["e2e"],
         "tflops": round(layer_flops(sh.T, sh.H, sh.I, sh.E, sh.k, sh.S) / (res["ms_step"] / 1e3) / 1e12, 1),
         "phase_ms": res["phase_ms"], "compute_only_phase_ms": res["compute_only_phase_ms"],
@@ -980,6 +992,7 @@ def main():
                    "remote_experts": wl.placement.n_remote(), "peer_pools": wl.placement.n_peers,
                    "chunk_mb": args.chunk_mb, "copy_streams": args.copy_streams, "expert_weights": args.dtype,
                    "prefetch_start": args.prefetch_start, "stages": args.stages,
+                   "wide_epilogue": bool(args.wide_epilogue),
                    "peer_pool_memory": args.peer_pools,
                    "layers": wl.n_layers,
                    "dwdp_group": args.group,

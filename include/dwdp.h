@@ -89,7 +89,16 @@ typedef struct {
     int32_t stage_slots;  /* experts each staging buffer holds (0 = no staging) */
     int32_t weight_dtype; /* DWDP_DTYPE_BF16, DWDP_DTYPE_E4M3 or DWDP_DTYPE_NVFP4 */
     int32_t n_stages;     /* staging buffers: 0 = 2 (the pages' double buffering); 1..DWDP_MAX_STAGES */
+    int32_t flags;        /* DWDP_FLAG_* (0 = defaults) */
 } dwdp_config;
+
+/* NVFP4 contexts: the gate/up GEMM drains its one TMEM accumulator with
+ * eight epilogue warps (two per lane quarter) instead of four, so the next
+ * tile's MMAs start sooner.  Faster when the GEMM runs alone; on one GPU a
+ * copy-engine prefetch running beside it then gets much less of the memory
+ * system (the copy, and with it the overlapped layer, takes longer), so it
+ * is off by default.  Ignored by bf16 and E4M3 contexts. */
+#define DWDP_FLAG_WIDE_EPILOGUE 1
 
 #define DWDP_MAX_STAGES 4
 

@@ -20,6 +20,7 @@ STATUS = {0: "OK", -1: "INVALID_ARG", -2: "NOT_MAPPED", -3: "CUDA", -4: "TIMEOUT
 EPI_BF16, EPI_SILU, EPI_F32 = 0, 1, 2
 DWDP_PHASE_EVENTS = 7  # dwdp_set_phase_events: route start/end, stage ready, gathered, gate/up, down, combine
 DTYPE_BF16, DTYPE_E4M3, DTYPE_NVFP4 = 0, 1, 2
+FLAG_WIDE_EPILOGUE = 1
 
 
 def weight_slot_bytes(rows: int, K: int, weight_dtype: int) -> int:
@@ -41,7 +42,7 @@ class dwdp_config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("inter", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
                 ("n_layers", ctypes.c_int32), ("stage_slots", ctypes.c_int32), ("weight_dtype", ctypes.c_int32),
-                ("n_stages", ctypes.c_int32)]
+                ("n_stages", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class dwdp_pool(ctypes.Structure):
@@ -147,10 +148,10 @@ def dwdp_version() -> int:
 
 
 def dwdp_create(hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots,
-                stage_w13=(None, None), stage_w2=(None, None), weight_dtype=DTYPE_BF16, n_stages=0) -> int:
+                stage_w13=(None, None), stage_w2=(None, None), weight_dtype=DTYPE_BF16, n_stages=0, flags=0) -> int:
     """n_stages 0 means 2; stage_w13 / stage_w2 hold one buffer (or None) per stage."""
     cfg = dwdp_config(hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots, weight_dtype,
-                      n_stages)
+                      n_stages, flags)
     n = max(len(stage_w13), len(stage_w2), n_stages or 2)
     s13 = (_VP * n)(*[_ptr(stage_w13[i]) if i < len(stage_w13) else None for i in range(n)])
     s2 = (_VP * n)(*[_ptr(stage_w2[i]) if i < len(stage_w2) else None for i in range(n)])
@@ -339,7 +340,7 @@ class Runtime:
     workspace (torch allocations); methods forward to the C ABI."""
 
     def __init__(self, hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots,
-                 device="cuda", weight_dtype=DTYPE_BF16, n_stages=2):
+                 device="cuda", weight_dtype=DTYPE_BF16, n_stages=2, flags=0):
         import torch
         self.cfg = dict(hidden=hidden, inter=inter, n_experts=n_experts, top_k=top_k, n_shared=n_shared,
                         max_tokens=max_tokens, n_layers=n_layers, stage_slots=stage_slots)
@@ -355,7 +356,7 @@ class Runtime:
             self.stage_w13 = [None] * n_stages
             self.stage_w2 = [None] * n_stages
         self.ctx = dwdp_create(hidden, inter, n_experts, top_k, n_shared, max_tokens, n_layers, stage_slots,
-                               self.stage_w13, self.stage_w2, weight_dtype, n_stages)
+                               self.stage_w13, self.stage_w2, weight_dtype, n_stages, flags)
         self.ws_bytes = max(256, dwdp_workspace_bytes(self.ctx, max_tokens))
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=device)
         self._keep = {}

@@ -318,6 +318,8 @@ int32_t dwdp_create(const dwdp_config* cfg, void* const stage_w13[], void* const
                     DWDP_MAX_EXPERTS, DWDP_MAX_TOPK, DWDP_MAX_LAYERS);
     if ((int64_t)c.max_tokens * (c.top_k + c.n_shared) >= (int64_t)1 << 31)
         return fail(nullptr, DWDP_ERR_UNSUPPORTED, "max_tokens * (k + n_shared) must stay below 2^31");
+    if (c.flags & ~DWDP_FLAG_WIDE_EPILOGUE)
+        return fail(nullptr, DWDP_ERR_INVALID_ARG, "unknown flags 0x%x", (unsigned)c.flags);
     const int n_stages = c.n_stages == 0 ? 2 : c.n_stages;
     if (n_stages < 1 || n_stages > DWDP_MAX_STAGES)
         return fail(nullptr, DWDP_ERR_INVALID_ARG, "n_stages must be 0 (= 2) or 1..%d", DWDP_MAX_STAGES);
@@ -789,7 +791,8 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
         a.bsrc[g] = m.bsrc[g];
         if (scaled) a.gscale[g] = m.scale13[g];
     }
-    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_SILU, fmt, a, ctx->n_sms, stream));
+    DWDP_CUDA(ctx, launch_grouped_gemm(EPI_SILU, fmt, a, ctx->n_sms, stream,
+                                       (c.flags & DWDP_FLAG_WIDE_EPILOGUE) != 0));
     DWDP_CUDA(ctx, mark(ctx, 4, stream));
     // G2: y = a W_down (E4M3 / NVFP4: a's rows quantized first; this phase includes it).
     if (fmt == FMT_E4M3) DWDP_CUDA(ctx, launch_quantize_rows(act, rows_all, (int)I, aq, sa, stream));

@@ -36,7 +36,6 @@ constexpr int kStages = 512 / BK_BYTES;         // 192 KiB of A + B stages eithe
 constexpr int kABytes = BM * BK_BYTES;
 constexpr int kBBytes = BN * BK_BYTES;
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kGemmThreads = 192;              // producer, MMA, 4 epilogue warps
 constexpr int kClusterCtas = 2;                // CTAs per cluster (co-scheduled on one GPC)
 
 // NVFP4 block scales as the block-scaled MMA takes them: for a row block rb
@@ -145,7 +144,10 @@ inline bool is_device_memory_of(const void* p, int dev) {
 // One grouped GEMM launch (gemm.cu) as 2-CTA clusters, one persistent CTA per
 // SM.  fmt: both operands bf16, both E4M3 codes, or both NVFP4 codes with
 // block scales (GemmArgs::sfa / bsf); K counts elements.  EPI_F32 is bf16 only.
-cudaError_t launch_grouped_gemm(int epi, int fmt, const GemmArgs& args, int n_sms, cudaStream_t stream);
+// wide_epilogue: the NVFP4 gate/up GEMM drains its accumulator with eight
+// warps instead of four (ignored otherwise).
+cudaError_t launch_grouped_gemm(int epi, int fmt, const GemmArgs& args, int n_sms, cudaStream_t stream,
+                                bool wide_epilogue = false);
 
 // K parts of the router GEMM (bf16, K = H) for T tokens and E experts: with
 // fewer 128-token tiles than SMs, as many parts as still fit one wave of

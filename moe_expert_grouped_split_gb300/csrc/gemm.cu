@@ -64,7 +64,20 @@ struct Fmt {
     // NVFP4: a seventh warp copies each stage's block scales into TMEM, so
     // the MMA warp's one thread issues only the MMAs
     static constexpr bool kSfWarp = FMT == FMT_NVFP4 && DWDP_SF_WARP;
-    static constexpr int kThreads = kGemmThreads + (kSfWarp ? 32 : 0);
+};
+
+// Warp roles of one kernel instance: producer (warp 0), MMA (warp 1),
+// EPIW epilogue warps, and for NVFP4 the scale-copy warp.  EPIW = 4 is one
+// epilogue warp per TMEM lane quarter; EPIW = 8 (NVFP4 only) is two per
+// quarter, each taking half of the tile's columns, so the single
+// accumulator is drained and handed back sooner.
+template <int FMT, int EPIW>
+struct Warps {
+    static_assert(EPIW == 4 || (EPIW == 8 && FMT == FMT_NVFP4), "8 epilogue warps are an NVFP4 variant");
+    static constexpr int kEpiWarps = EPIW;
+    static constexpr int kColSplit = EPIW / 4;
+    static constexpr int kSfWarpIdx = 2 + EPIW;  // after the producer, MMA and epilogue warps
+    static constexpr int kThreads = 32 * (2 + EPIW + (Fmt<FMT>::kSfWarp ? 1 : 0));
 };
 constexpr int kSfCol0 = BN;                             // NVFP4: first TMEM column of the scale ring
 constexpr int kSfColsPerStage = 12 * kSfStepsPerSlice;  // per K step: 4 columns of A scales, 8 of B
@@ -359,10 +372,11 @@ struct SmemLayout {
     static constexpr int kTileStart = kMisc + 16;         // int32[G+1]
 };
 
-template <int EPI, int FMT>
-__global__ void __launch_bounds__(Fmt<FMT>::kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
+template <int EPI, int FMT, int EPIW>
+__global__ void __launch_bounds__(Warps<FMT, EPIW>::kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmArgs p) {
     using SL = SmemLayout<FMT>;
     using F = Fmt<FMT>;
+    using WR = Warps<FMT, EPIW>;
     constexpr int KE = F::kKElems;     // K elements per 128-byte slice
     constexpr int KX = F::kXPerSlice;  // the slice's width in tensor-map x units
     constexpr bool kScaled = FMT != FMT_BF16;
@@ -420,7 +434,7 @@ __global__ void __launch_bounds__(Fmt<FMT>::kThreads, 1) grouped_gemm_kernel(con
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4);
+            mbar_init(tempty_bar(a), WR::kEpiWarps);
         }
         mbar_init(mdone_bar, 1);
         for (int s = 0; s < kStages; ++s) mbar_init(sf_full_bar(s), 1);
@@ -634,7 +648,7 @@ __global__ void __launch_bounds__(Fmt<FMT>::kThreads, 1) grouped_gemm_kernel(con
             tc_commit(mdone_bar);
             mbar_wait_drain(mdone_bar, 0, p.err, DERR_MMA_DONE_WAIT);
         }
-    } else if (F::kSfWarp && warp == kGemmThreads / 32) {
+    } else if (F::kSfWarp && warp == WR::kSfWarpIdx) {
         // ------------------------------------------------ scale copies ----
         // Stage by stage in the MMA warp's order: once a stage's operands have
         // landed, copy its twelve block-scale chunks into the stage's TMEM
@@ -668,6 +682,8 @@ __global__ void __launch_bounds__(Fmt<FMT>::kThreads, 1) grouped_gemm_kernel(con
     } else {
         // ------------------------------------------------ epilogue --------
         const int quad = warp & 3;  // TMEM lanes [32*quad, 32*quad+32)
+        const int half = (warp - 2) / 4;  // which share of the columns (kColSplit shares)
+        constexpr int kCS = WR::kColSplit;
         const int row_in_tile = quad * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -707,12 +723,14 @@ __global__ void __launch_bounds__(Fmt<FMT>::kThreads, 1) grouped_gemm_kernel(con
                 // the accumulator is released, and the stores follow.  (The
                 // SiLU epilogue keeps the interleaved path below: fully unrolled
                 // it ran slower.)
-                uint32_t packed[BN / 2];
+                // this warp's share: columns [cbase, cbase + BN / kCS) of the tile
+                const int cbase = half * (BN / kCS);
+                uint32_t packed[BN / 2 / kCS];
 #pragma unroll
-                for (int c = 0; c < BN / 32; c += 2) {
+                for (int c = 0; c < BN / 32 / kCS; c += 2) {
                     uint32_t v[2][32];
-                    tmem_ld32(taddr + c * 32, v[0]);
-                    tmem_ld32(taddr + (c + 1) * 32, v[1]);
+                    tmem_ld32(taddr + cbase + c * 32, v[0]);
+                    tmem_ld32(taddr + cbase + (c + 1) * 32, v[1]);
                     tmem_wait_ld();
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
@@ -725,10 +743,10 @@ __global__ void __launch_bounds__(Fmt<FMT>::kThreads, 1) grouped_gemm_kernel(con
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty_bar(acc));
                 __nv_bfloat16* D = reinterpret_cast<__nv_bfloat16*>(p.D);
-                const int col0 = n * BN;
+                const int col0 = n * BN + cbase;
                 if (valid) {
 #pragma unroll
-                    for (int c = 0; c < BN / 32; ++c) {
+                    for (int c = 0; c < BN / 32 / kCS; ++c) {
                         if (col0 + c * 32 >= p.N) break;
                         uint4* q = reinterpret_cast<uint4*>(D + grow * p.ldd + col0 + c * 32);
 #pragma unroll
@@ -748,8 +766,10 @@ __global__ void __launch_bounds__(Fmt<FMT>::kThreads, 1) grouped_gemm_kernel(con
             bool released = false;
             if (EPI == EPI_SILU) {
                 __nv_bfloat16* D = reinterpret_cast<__nv_bfloat16*>(p.D);
+                // this warp's share of the tile's 32-output chunks
+                const int c_lo = half * (BN / 2 / 32 / kCS), c_hi = c_lo + BN / 2 / 32 / kCS;
 #pragma unroll 1
-                for (int c = 0; c < BN / 2 / 32; c += 2) {
+                for (int c = c_lo; c < c_hi; c += 2) {
                     uint32_t gv[2][32], uv[2][32];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
@@ -757,7 +777,7 @@ __global__ void __launch_bounds__(Fmt<FMT>::kThreads, 1) grouped_gemm_kernel(con
                         tmem_ld32(taddr + BN / 2 + (c + h) * 32, uv[h]);
                     }
                     tmem_wait_ld();
-                    if (c + 2 >= BN / 2 / 32) {
+                    if (c + 2 >= c_hi) {
                         // the last chunks are in registers: hand the accumulator
                         // back now, so the next tile's MMAs overlap this math
                         tc_fence_before();
@@ -848,23 +868,31 @@ size_t gemm_smem_bytes(int n_groups) {
     return 1024 + SmemLayout<FMT>::kTileStart + sizeof(int32_t) * (size_t)(n_groups + 1);
 }
 
-cudaError_t launch_grouped_gemm(int epi, int fmt, const GemmArgs& args, int n_sms, cudaStream_t stream) {
+cudaError_t launch_grouped_gemm(int epi, int fmt, const GemmArgs& args, int n_sms, cudaStream_t stream,
+                                bool wide_epilogue) {
     const int G = args.n_routed + (args.shared_rows > 0 ? 1 : 0);
     size_t smem = 0;
     const void* fn = nullptr;
+    int threads = Warps<FMT_BF16, 4>::kThreads;
     if (fmt == FMT_NVFP4) {
         smem = gemm_smem_bytes<FMT_NVFP4>(G);
-        if (epi == EPI_SILU) fn = (const void*)grouped_gemm_kernel<EPI_SILU, FMT_NVFP4>;
-        if (epi == EPI_BF16) fn = (const void*)grouped_gemm_kernel<EPI_BF16, FMT_NVFP4>;
+        threads = Warps<FMT_NVFP4, 4>::kThreads;
+        if (epi == EPI_SILU && wide_epilogue) {
+            fn = (const void*)grouped_gemm_kernel<EPI_SILU, FMT_NVFP4, 8>;
+            threads = Warps<FMT_NVFP4, 8>::kThreads;
+        } else if (epi == EPI_SILU) {
+            fn = (const void*)grouped_gemm_kernel<EPI_SILU, FMT_NVFP4, 4>;
+        }
+        if (epi == EPI_BF16) fn = (const void*)grouped_gemm_kernel<EPI_BF16, FMT_NVFP4, 4>;
     } else if (fmt == FMT_E4M3) {
         smem = gemm_smem_bytes<FMT_E4M3>(G);
-        if (epi == EPI_SILU) fn = (const void*)grouped_gemm_kernel<EPI_SILU, FMT_E4M3>;
-        if (epi == EPI_BF16) fn = (const void*)grouped_gemm_kernel<EPI_BF16, FMT_E4M3>;
+        if (epi == EPI_SILU) fn = (const void*)grouped_gemm_kernel<EPI_SILU, FMT_E4M3, 4>;
+        if (epi == EPI_BF16) fn = (const void*)grouped_gemm_kernel<EPI_BF16, FMT_E4M3, 4>;
     } else if (fmt == FMT_BF16) {
         smem = gemm_smem_bytes<FMT_BF16>(G);
-        if (epi == EPI_SILU) fn = (const void*)grouped_gemm_kernel<EPI_SILU, FMT_BF16>;
-        if (epi == EPI_BF16) fn = (const void*)grouped_gemm_kernel<EPI_BF16, FMT_BF16>;
-        if (epi == EPI_F32) fn = (const void*)grouped_gemm_kernel<EPI_F32, FMT_BF16>;
+        if (epi == EPI_SILU) fn = (const void*)grouped_gemm_kernel<EPI_SILU, FMT_BF16, 4>;
+        if (epi == EPI_BF16) fn = (const void*)grouped_gemm_kernel<EPI_BF16, FMT_BF16, 4>;
+        if (epi == EPI_F32) fn = (const void*)grouped_gemm_kernel<EPI_F32, FMT_BF16, 4>;
     }
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -882,7 +910,7 @@ cudaError_t launch_grouped_gemm(int epi, int fmt, const GemmArgs& args, int n_sm
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(fmt == FMT_NVFP4 ? Fmt<FMT_NVFP4>::kThreads : kGemmThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;

@@ -121,6 +121,9 @@ def test_host_validation_without_gpu(lib):
     cfg = B.dwdp_config(256, 128, 8, 2, 0, 64, 1, 4, B.DTYPE_BF16, 3)
     bufs = (ctypes.c_void_p * 3)(256, 512, None)
     assert lib.dwdp_create(ctypes.byref(cfg), bufs, bufs, ctypes.byref(out)) == -1
+    cfg = B.dwdp_config(256, 128, 8, 2, 0, 64, 1, 0, B.DTYPE_BF16, 0, 6)   # unknown flag bits
+    assert lib.dwdp_create(ctypes.byref(cfg), None, None, ctypes.byref(out)) == -1
+    assert "flags" in B.dwdp_last_error(None)
     assert lib.dwdp_workspace_bytes(None, 10) == 0
     # activation quantization: argument checks come before any CUDA call
     x = ctypes.c_void_p(16)

@@ -384,3 +384,34 @@ def test_nvfp4_r1_layer_sample():
     # tokens covering every expert's last m-tile
     shape, pl = I.r1_layer(8192)
     _run(shape, pl, seed=4, tokens="last_tiles", chunk=32 << 20)
+
+
+@pytest.mark.parametrize("shape", [I.LayerShape(T=333, H=512, I=512, E=16, k=4, S=1),
+                                   I.LayerShape(T=2048, H=7168, I=2048, E=32, k=4, S=1)],
+                         ids=["small", "r1_widths"])
+def test_nvfp4_wide_epilogue_bit_identical(shape):
+    """DWDP_FLAG_WIDE_EPILOGUE drains the gate/up accumulator with eight warps
+    instead of four: the same arithmetic per element, so the layer's output
+    (and a, in the workspace) must not change by a single bit."""
+    build()
+    pl = I.split_placement(shape.E, shape.E // 4, 3)
+    lw = I.make_layer_nvfp4(shape, pl, 11, 0, device="cuda")
+    x = I.make_tokens(shape.T, shape.H, 11).cuda()
+    outs = []
+    for flags in (0, B.FLAG_WIDE_EPILOGUE):
+        rt = B.Runtime(shape.H, shape.I, shape.E, shape.k, shape.S, shape.T, 1, pl.n_remote(),
+                       weight_dtype=B.DTYPE_NVFP4, flags=flags)
+        try:
+            rt.set_layer(0, lw)
+            rb = B.RouteBuffers(shape.T, shape.E, shape.k)
+            out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
+            rt.prefetch(0, 0, 1 << 20, [torch.cuda.Stream()])
+            rt.route(x, lw.wr, None, rb)
+            rt.moe(0, 0, x, rb, out)
+            torch.cuda.synchronize()
+            assert rt.device_status() == 0
+            outs.append((out.clone(), rt.ws_region(shape.T, "a").clone()))
+        finally:
+            rt.close()
+    assert torch.equal(outs[0][1], outs[1][1]), "a differs between four and eight epilogue warps"
+    assert torch.equal(outs[0][0], outs[1][0]), "output differs between four and eight epilogue warps"
