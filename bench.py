@@ -114,9 +114,12 @@ def parse(argv=None):
                         "default for the 8K-token layer")
     p.add_argument("--no-merge-copy", action="store_true", help="skip the merge-copy baseline")
     p.add_argument("--variants", default=None,
-                   help="comma-separated weight types (fp8, nvfp4, nvfp4_wide = nvfp4 with --wide-epilogue) also "
-                        "measured on the same workload after the main line, each summarised under 'variants' "
-                        "(default for the 8K-token bf16 layer: fp8,nvfp4,nvfp4_wide)")
+                   help="comma-separated further measurements after the main line, each summarised under "
+                        "'variants': a weight type for the same workload (fp8, nvfp4, nvfp4_wide = nvfp4 with "
+                        "--wide-epilogue) or another workload, optionally with a weight type "
+                        "(r1_zipf_16k:nvfp4).  Default for the 8K-token bf16 layer: fp8, nvfp4, nvfp4_wide, the "
+                        "Zipf 16K layer (bf16, nvfp4), the 256-token layer with its chunk sweep and the 4-layer "
+                        "pipeline (bf16, nvfp4)")
     p.add_argument("--peer-pools", default="device", choices=["device", "host"],
                    help="where the emulated peers' pools live (host: pinned host memory, copies over the "
                         "host link, so only their writes use this GPU's HBM)")
@@ -134,7 +137,8 @@ def parse(argv=None):
         args.merge_copy = False
     if args.variants is None:
         default = args.workload == "r1_moe_layer_8k" and args.dtype == "bf16" and not args.no_extras
-        args.variants = "fp8,nvfp4,nvfp4_wide" if default and args.group == 4 else ""
+        args.variants = ("fp8,nvfp4,nvfp4_wide,r1_zipf_16k,r1_zipf_16k:nvfp4,r1_moe_layer_256,"
+                         "r1_pipeline_4layer,r1_pipeline_4layer:nvfp4") if default and args.group == 4 else ""
     return args
 
 
@@ -914,44 +918,80 @@ def cpu_baseline_sample(wl, target_s=15.0, max_tokens=512):
                       f"tokens, {dt1:.1f} s)"}
 
 
-def variant_summary(args, wdtype: str) -> dict:
-    """The same workload with other expert weights (E4M3 or NVFP4), timed
-    like the main line (overlapped steps, compute-only and copy-only legs,
-    end to end with host buffers), in compact form."""
+def parse_variant(main_workload: str, variant: str):
+    """(workload, weight type, wide epilogue) of a --variants entry."""
+    workload, wdtype = main_workload, variant
+    if variant.split(":")[0] in WORKLOADS:
+        workload, _, wdtype = variant.partition(":")
+        wdtype = wdtype or "bf16"
+    wide = wdtype.endswith("_wide")
+    wdtype = wdtype[: -len("_wide")] if wide else wdtype
+    if wdtype not in WEIGHT_BYTES:
+        raise ValueError(f"unknown variant {variant!r}")
+    return workload, wdtype, wide
+
+
+def variant_summary(args, variant: str) -> dict:
+    """One more measurement in the same run, in compact form.  variant is
+    "<dtype>[_wide]" (the main line's workload with E4M3 or NVFP4 weights,
+    _wide = NVFP4 with the eight-warp gate/up epilogue) or
+    "<workload>[:<dtype>]" (another workload of WORKLOADS, bf16 unless
+    given; the 256-token layer adds the chunk sweep over 1, 4, 16 and 64 MB
+    slices), timed like the main line: overlapped steps, compute-only and
+    copy-only legs, and (single layers) end to end with host buffers."""
     import copy as _copy
 
     import torch
     a = _copy.copy(args)
-    wide = wdtype.endswith("_wide")
-    wdtype = wdtype[: -len("_wide")] if wide else wdtype
-    a.dtype, a.merge_copy, a.chunk_sweep, a.wide_epilogue = wdtype, False, "", wide
-    res = run_layer_bench(a)
+    workload, wdtype, wide = parse_variant(args.workload, variant)
+    a.workload, a.dtype, a.merge_copy, a.wide_epilogue = workload, wdtype, False, wide
+    a.chunk_sweep = "1,4,16,64" if workload == "r1_moe_layer_256" else ""
+    a.chunk_mb = 16.0 if workload == "r1_pipeline_4layer" else 32.0
+    pipeline = workload == "r1_pipeline_4layer"
+    if pipeline:
+        a.steps = 16        # the 4-layer workload's own step count
+    res = (run_pipeline_bench if pipeline else run_layer_bench)(a)
     wl = res.pop("wl")
     sh = wl.shape
-    peaks, src = measured_peaks()
-    tc_peak, hbm, tc_note = roofline_peaks(peaks, src, wdtype)
-    wb = WEIGHT_BYTES[wdtype]
-    g1 = g1_flops(sh.T, sh.H, sh.I, sh.k, sh.S)
-    g1b = g1_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S, wb)
     comp, copy_ms = res["compute_only_ms"], res["copy_only_ms"]
     exposed = max(0.0, res["ms_step"] - comp)
     out = {
-        "expert_weights": wdtype, "wide_epilogue": wide, "value": round(res["value"], 1), "unit": UNIT,
-        "ms_per_step": round(res["ms_step"], 4), "e2e": res["e2e"],
-        "tflops": round(layer_flops(sh.T, sh.H, sh.I, sh.E, sh.k, sh.S) / (res["ms_step"] / 1e3) / 1e12, 1),
-        "phase_ms": res["phase_ms"], "compute_only_phase_ms": res["compute_only_phase_ms"],
+        "workload": workload, "T": sh.T, "expert_weights": wdtype, "wide_epilogue": wide,
+        "value": round(res["value"], 1), "unit": UNIT + (" (layer-tokens, 4 layers per step)" if pipeline else ""),
+        "ms_per_step": round(res["ms_step"], 4),
         "prefetch": {"compute_only_ms": round(comp, 4), "copy_only_ms": round(copy_ms, 4),
                      "exposed_ms": round(exposed, 4),
                      "hidden_frac": round(max(0.0, 1.0 - exposed / copy_ms), 4) if copy_ms > 0 else None},
-        "roofline": roofline_entry("gate_up_grouped_gemm", g1, g1b, res["phase_ms"]["gate_up_gemm"] / 1e3, tc_peak,
-                                   hbm, tc_note, f"{src} hbm_gbs"),
-        "roofline_alone": roofline_entry("gate_up_grouped_gemm", g1, g1b,
-                                         res["compute_only_phase_ms"]["gate_up_gemm"] / 1e3, tc_peak, hbm, tc_note,
-                                         f"{src} hbm_gbs"),
-        "step_hbm_frac": round(step_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S, wl.placement.n_remote(), wb)
-                               / (res["ms_step"] / 1e3) / 1e9 / hbm, 4),
-        "clocks": res["clocks"], "gpu_launches": kernels_per_layer(wdtype) * args.steps,
+        "clocks": res["clocks"], "chunk_mb": a.chunk_mb,
     }
+    if pipeline:
+        flops = sum(4 * (layer_flops(T, sh.H, sh.I, sh.E, sh.k, sh.S) + 2 * T * sh.H * sh.H)
+                    for T in res["tokens_per_step"]) / len(res["tokens_per_step"])
+        out["tflops"] = round(flops / (res["ms_step"] / 1e3) / 1e12, 1)
+        out["tokens_per_step"] = res["tokens_per_step"]
+        out["gpu_launches"] = args.steps * 4 * kernels_per_layer(wdtype)
+    else:
+        peaks, src = measured_peaks()
+        tc_peak, hbm, tc_note = roofline_peaks(peaks, src, wdtype)
+        wb = WEIGHT_BYTES[wdtype]
+        g1 = g1_flops(sh.T, sh.H, sh.I, sh.k, sh.S)
+        g1b = g1_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S, wb)
+        out.update({
+            "e2e": res["e2e"],
+            "tflops": round(layer_flops(sh.T, sh.H, sh.I, sh.E, sh.k, sh.S) / (res["ms_step"] / 1e3) / 1e12, 1),
+            "phase_ms": res["phase_ms"], "compute_only_phase_ms": res["compute_only_phase_ms"],
+            "roofline": roofline_entry("gate_up_grouped_gemm", g1, g1b, res["phase_ms"]["gate_up_gemm"] / 1e3,
+                                       tc_peak, hbm, tc_note, f"{src} hbm_gbs"),
+            "roofline_alone": roofline_entry("gate_up_grouped_gemm", g1, g1b,
+                                             res["compute_only_phase_ms"]["gate_up_gemm"] / 1e3, tc_peak, hbm,
+                                             tc_note, f"{src} hbm_gbs"),
+            "step_hbm_frac": round(step_bytes(sh.T, sh.H, sh.I, res["e_active"], sh.k, sh.S,
+                                              wl.placement.n_remote(), wb) / (res["ms_step"] / 1e3) / 1e9 / hbm, 4),
+            "experts_active": res["e_active"],
+            "gpu_launches": kernels_per_layer(wdtype) * args.steps,
+        })
+        if "chunk_sweep" in res:
+            out["chunk_sweep"] = res["chunk_sweep"]
     wl.rt.close()
     del wl, res
     torch.cuda.synchronize()

@@ -75,3 +75,15 @@ def test_roofline_bound_follows_the_ridge():
 def test_low_precision_peaks_scale_the_measured_bf16_burst():
     assert bench.roofline_peaks(PEAKS, "measured", "fp8")[0] == pytest.approx(2 * 1928.3)
     assert bench.roofline_peaks(PEAKS, "measured", "nvfp4")[0] == pytest.approx(6 * 1928.3)
+
+
+def test_variant_names():
+    assert bench.parse_variant("r1_moe_layer_8k", "nvfp4") == ("r1_moe_layer_8k", "nvfp4", False)
+    assert bench.parse_variant("r1_moe_layer_8k", "nvfp4_wide") == ("r1_moe_layer_8k", "nvfp4", True)
+    assert bench.parse_variant("r1_moe_layer_8k", "r1_zipf_16k") == ("r1_zipf_16k", "bf16", False)
+    assert bench.parse_variant("r1_moe_layer_8k", "r1_pipeline_4layer:nvfp4") == ("r1_pipeline_4layer", "nvfp4", False)
+    with pytest.raises(ValueError):
+        bench.parse_variant("r1_moe_layer_8k", "int3")
+    args = bench.parse([])
+    for v in args.variants.split(","):
+        bench.parse_variant(args.workload, v)       # every default variant parses
