@@ -319,7 +319,7 @@ def single_gpu_refusal(args, world: int):
                            "grouped GEMM's cluster-multicast loads are kept to one-GPU runs"}
 
 
-PHASES = ["route", "wait_stage", "gather", "gate_up_gemm", "down_gemm", "combine"]
+PHASES = ["route", "gather", "wait_stage", "gate_up_gemm", "down_gemm", "combine"]
 
 
 # -------------------------------------------------------- our arm ----------

@@ -294,8 +294,9 @@ int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t 
  *   y   = a W_down                             per expert, bf16
  *   out[t] = sum_j topk_w[t][j] y[inv_perm[t*k+j]] + y_shared[t]  (fp32 sum, bf16)
  * Each expert's weights come from the local pool or from stage `stage`, per
- * the layer's map; the stream first waits for that stage's "ready" event when
- * the layer has non-resident experts (per-layer arrival, [DWDP] §2).  route
+ * the layer's map; before the gate/up GEMM the stream waits for that stage's
+ * "ready" event when the layer has non-resident experts (per-layer arrival,
+ * [DWDP] §2).  route
  * holds dwdp_route's outputs for the same x (offsets, inv_perm and topk_w are
  * read; NVFP4 contexts also read topk_ids).  In E4M3 and NVFP4 contexts x
  * and a are quantized per row first (see DWDP_DTYPE_*) and the GEMMs run on
@@ -339,10 +340,11 @@ int32_t dwdp_device_status(dwdp_ctx* ctx);
 /* Optional phase timing.  events is a host array of DWDP_PHASE_EVENTS
  * caller-owned cudaEvent_t (or NULL to stop).  While set, dwdp_route records
  * events[0] at its start and events[1] at its end on its stream, and
- * dwdp_moe_layer records events[2] after waiting for its stage, events[3]
- * once x is in expert order (E4M3 / NVFP4: quantized), events[4] after the
- * gate/up GEMM, events[5] after the down GEMM and events[6] after the
- * combine.  The context keeps the pointers
+ * dwdp_moe_layer records events[2] once x is in expert order (E4M3 / NVFP4:
+ * quantized), events[3] after waiting for its stage (the layer puts x in
+ * expert order before it waits: only the GEMMs read staged weights),
+ * events[4] after the gate/up GEMM, events[5] after the down GEMM and
+ * events[6] after the combine.  The context keeps the pointers
  * until the next call; the caller keeps the events alive.  Errors:
  * INVALID_ARG. */
 #define DWDP_PHASE_EVENTS 7

@@ -726,8 +726,8 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     uint8_t* sfx = reinterpret_cast<uint8_t*>(w + L.sfx);
     uint8_t* sfa = reinterpret_cast<uint8_t*>(w + L.sfa);
 
-    if (m.n_remote > 0) DWDP_CUDA(ctx, cudaStreamWaitEvent(stream, ctx->ready[stage], 0));
-    DWDP_CUDA(ctx, mark(ctx, 2, stream));
+    // x goes into expert order first: only the GEMMs read the staged weights,
+    // so the copy into the stage may still run meanwhile
     if (fmt == FMT_NVFP4) {
         // x rows to NVFP4 once per token, written to each chosen expert's row
         if (!route->topk_ids || !aligned16(route->topk_ids))
@@ -742,6 +742,8 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
     } else {
         DWDP_CUDA(ctx, launch_gather(x, (int)H, route->inv_perm, (int)T, (int)k, xp, ctx->d_err, stream));
     }
+    DWDP_CUDA(ctx, mark(ctx, 2, stream));
+    if (m.n_remote > 0) DWDP_CUDA(ctx, cudaStreamWaitEvent(stream, ctx->ready[stage], 0));
     DWDP_CUDA(ctx, mark(ctx, 3, stream));
 
     GemmArgs& a = *ctx->args;
