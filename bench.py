@@ -188,10 +188,12 @@ def kernels_per_layer(wdtype: str) -> int:
 WEIGHT_BYTES = {"bf16": 2, "fp8": 1, "nvfp4": 9 / 16}
 
 
-def measured_traffic(kernel_file: str):
+def measured_traffic(kernel_file: str, algorithmic_bytes: int):
     """dram__bytes_read.sum + dram__bytes_write.sum per launch of the gate/up
-    GEMM from the committed ncu summary, or None when the kernel source has
-    changed since the counters were taken."""
+    GEMM: the committed ncu record's measured-to-algorithmic ratio (taken on
+    a smaller case of the same kernel) times this launch's algorithmic
+    bytes; None when the kernel source has changed since the counters were
+    taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "gate_up_gemm_traffic_r1_moe_layer_8k.json")
     if not os.path.exists(path):
@@ -200,7 +202,9 @@ def measured_traffic(kernel_file: str):
         rec = json.load(f)
     with open(kernel_file, "rb") as f:
         sha = hashlib.sha256(f.read()).hexdigest()
-    return rec["dram_bytes_per_launch"] if rec.get("gemm_cu_sha256") == sha else None
+    if rec.get("gemm_cu_sha256") != sha:
+        return None
+    return int(round(rec["traffic_over_algorithmic"] * algorithmic_bytes))
 
 
 class ClockSampler:
@@ -1058,10 +1062,12 @@ def main():
         layer_tflops = flops_layer / (res["ms_step"] / 1e3) / 1e12
         traffic = None
         if args.workload == "r1_moe_layer_8k" and args.dtype == "bf16":
-            traffic = measured_traffic(os.path.join(ROOT, "moe_expert_grouped_split_gb300", "csrc", "gemm.cu"))
+            traffic = measured_traffic(os.path.join(ROOT, "moe_expert_grouped_split_gb300", "csrc", "gemm.cu"), g1b)
         roof = roofline_entry("gate_up_grouped_gemm", g1, g1b, res["phase_ms"]["gate_up_gemm"] / 1e3, tc_peak, hbm,
                               tc_note, hbm_note)
         roof.update({"traffic": traffic, "algorithmic_flops_per_launch": g1, "algorithmic_bytes_per_launch": g1b,
+                     "traffic_source": "ncu DRAM bytes of this kernel on a smaller case (1024 tokens, 17 experts), "
+                                       "scaled by measured / algorithmic bytes; a lower bound" if traffic else None,
                      "timed": "CUDA events around the kernel on the compute stream, inside the overlapped step"})
         line.update({
             "tflops": round(layer_tflops, 1),
