@@ -19,6 +19,8 @@
 #include <thread>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "dwdp_internal.h"
 
 using namespace dwdp;
@@ -165,6 +167,24 @@ int32_t cuda_fail(dwdp_ctx* ctx, cudaError_t e, const char* what) {
     } while (0)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Host-side NVTX range around one ABI call, named with its layer / stage /
+// token count, so a timeline tool (nsys, ncu --nvtx) shows which call
+// enqueued which kernels and copies; without a tool attached the push and
+// pop do nothing.
+struct NvtxRange {
+    NvtxRange(const char* fmt, ...) {
+        char buf[96];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        nvtxRangePushA(buf);
+    }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 struct WsLayout {
     size_t logits = 0;  // route: fp32 [T][E] when the caller does not keep logits
@@ -559,6 +579,7 @@ int32_t dwdp_group_map(int32_t n_experts, int32_t n_ranks, int32_t rank, int32_t
 
 int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router, const float* logit_bias,
                    const dwdp_route_out* out, void* ws, size_t ws_bytes, dwdp_stream_t stream) {
+    const NvtxRange nvtx("dwdp_route T=%d", T);
     if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
     const dwdp_config& c = ctx->cfg;
     if (T < 0 || T > c.max_tokens) return fail(ctx, DWDP_ERR_INVALID_ARG, "T=%d outside [0, max_tokens]", T);
@@ -624,6 +645,7 @@ int32_t dwdp_route(dwdp_ctx* ctx, const void* x, int32_t T, const void* w_router
 
 int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t chunk_bytes,
                             dwdp_stream_t const* copy_streams, int32_t n_copy_streams) {
+    const NvtxRange nvtx("dwdp_prefetch_layer layer %d -> stage %d", layer, stage);
     if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
     const dwdp_config& c = ctx->cfg;
     if (layer < 0 || layer >= c.n_layers) return fail(ctx, DWDP_ERR_INVALID_ARG, "layer %d out of range", layer);
@@ -682,6 +704,7 @@ int32_t dwdp_prefetch_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, size_t 
 
 int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* x, int32_t T,
                        const dwdp_route_out* route, void* out, void* ws, size_t ws_bytes, dwdp_stream_t stream) {
+    const NvtxRange nvtx("dwdp_moe_layer layer %d stage %d T=%d", layer, stage, T);
     if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
     const dwdp_config& c = ctx->cfg;
     if (layer < 0 || layer >= c.n_layers) return fail(ctx, DWDP_ERR_INVALID_ARG, "layer %d out of range", layer);
