@@ -7,7 +7,8 @@
 // picks the map and the slot coordinate, so no weight byte is ever moved to
 // feed the GEMM.
 //
-// Kernel organisation (one persistent CTA per SM, 192 threads):
+// Kernel organisation (one persistent CTA per SM, 192 threads; NVFP4 224,
+// or 352 with the eight-warp drain):
 //   warp 0      TMA producer: A tile [128 rows x 128 B] + B tile [256 rows x
 //               128 B] per stage, 4-stage mbarrier ring in shared memory
 //               (128B swizzle); NVFP4 adds the tiles' block-scale chunks.
@@ -17,7 +18,11 @@
 //   warps 2..5  epilogue: tcgen05.ld the accumulator rows of their TMEM lane
 //               quarter, hand the accumulator back to warp 1 as soon as the
 //               last loads land, apply SiLU(gate)*up or plain conversion,
-//               store.
+//               store (NVFP4 option: warps 2..9, two per lane quarter, each
+//               draining half of the tile's columns).
+//   last warp   NVFP4 only: copies each stage's block scales from shared
+//               memory into its TMEM columns (tcgen05.cp) and commits to a
+//               per-stage barrier the MMA thread waits on.
 // Tiles are enumerated group by group, n-tile by n-tile, m-tile fastest, and
 // dealt to CTAs round-robin; CTAs 2c and 2c+1 form a cluster, and when their
 // tiles are sibling m-tiles of one weight tile each loads half of it and
