@@ -10,6 +10,7 @@ host, each from its home rank, once; and at every step of the plan the
 ranks pull from distinct sources (no source serves two destinations at
 once) when the ranks host equal shares, with the contended steps of an
 unequal split confined to its last expert's slices."""
+import collections
 import os
 import socket
 
@@ -49,8 +50,19 @@ def _worker(rank, world, port, q, chunk):
         dist.all_gather(gathered, pad)
         staged = sorted(int(e) for e in np.nonzero(ls < 0)[0])
         homes = {int(e): (rank + 1 + int(pid[e])) % world for e in staged}
+        # the same experts with the peers numbered in absolute rank order
+        # (peer p = the p-th other rank): every rank's plan then starts at
+        # the lowest other rank
+        others = [r for r in range(world) if r != rank]
+        pid_abs = np.array([-1 if ls[e] >= 0 else others.index(homes[e]) for e in range(E)], dtype=np.int32)
+        plan_abs = B.dwdp_plan_prefetch(E, H, I, ls, pid_abs, ps, world - 1, chunk)
+        src_abs = torch.tensor([others[p] for (p, _, _, _, _) in plan_abs], dtype=torch.int64)
+        pad_abs = torch.full((L,), -1, dtype=torch.int64)       # same slice count as the rotated plan
+        pad_abs[: src_abs.numel()] = src_abs
+        gathered_abs = [torch.zeros(L, dtype=torch.int64) for _ in range(world)]
+        dist.all_gather(gathered_abs, pad_abs)
         q.put((rank, [g.tolist() for g in gathered], staged, homes,
-               sum(n_ for (*_, n_) in plan), [tuple(x) for x in plan[:3]]))
+               sum(n_ for (*_, n_) in plan), [g.tolist() for g in gathered_abs]))
     finally:
         dist.barrier()
         dist.destroy_process_group()
@@ -91,6 +103,12 @@ def test_group_plans_cover_and_do_not_contend(world):
         srcs = [seqs[r][step] for r in range(world)]
         assert len(set(srcs)) == world, f"step {step}: sources {srcs}"
         assert all(srcs[r] != r for r in range(world))
+    # the contrast: numbered in absolute rank order, every rank's plan starts
+    # at the lowest other rank, so one source serves up to N - 1 destinations
+    abs_seqs = out[0][5]
+    worst = max(max(collections.Counter(abs_seqs[r][step] for r in range(world)).values())
+                for step in range(L))
+    assert worst == world - 1
 
 
 def test_unequal_split_contends_only_at_the_tail():
