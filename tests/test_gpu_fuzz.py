@@ -2,7 +2,8 @@
 counts 1..40 (not multiples of the warp), k = 1..min(E, 8) (the generic
 combine path for k outside {2, 4, 8}), T = 1..300, with and without the shared
 expert, random local / remote / redundant placements over 1..3 peer pools,
-random slice sizes, and all three weight formats."""
+random slice sizes, and all three weight formats (NVFP4 with four and with
+eight epilogue warps)."""
 import numpy as np
 import pytest
 import torch
@@ -75,8 +76,10 @@ def test_random_layer(seed):
     make = {"bf16": I.make_layer, "fp8": I.make_layer_fp8, "nvfp4": I.make_layer_nvfp4}[dtype]
     lw = make(shape, pl, seed, 0, device="cuda", router_std=0.3)
     x = I.make_tokens(shape.T, shape.H, seed).cuda()
+    # every other NVFP4 case drains the gate/up accumulator with eight warps
+    flags = B.FLAG_WIDE_EPILOGUE if dtype == "nvfp4" and (seed // 3) % 2 else 0
     rt = B.Runtime(shape.H, shape.I, shape.E, shape.k, shape.S, shape.T, 1, max(1, pl.n_remote()),
-                   weight_dtype=DTYPES[dtype])
+                   weight_dtype=DTYPES[dtype], flags=flags)
     try:
         rt.set_layer(0, lw)
         rb = B.RouteBuffers(shape.T, shape.E, shape.k)
