@@ -128,6 +128,10 @@ def parse(argv=None):
                         "starves the overlapped copy on one GPU)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extras", action="store_true", help="skip compute-only / copy-only / e2e legs")
+    p.add_argument("--duration-study", type=float, default=0.0,
+                   help="also run the compute-only and the overlapped step back to back for this many seconds "
+                        "each, sampling SM clock and power (long-duration overlap, the analogue of the pages' "
+                        "appendix A.2)")
     args = p.parse_args(argv)
     if args.chunk_mb is None:
         args.chunk_mb = 16.0 if args.workload == "r1_pipeline_4layer" else 32.0
@@ -259,8 +263,10 @@ class ClockSampler:
                     reasons.add(n)
         sm.sort()
         med = sm[len(sm) // 2] if sm else None
+        power_sorted = sorted(power)
         return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
-                "power_w_max": max(power) if power else None}
+                "power_w_max": max(power) if power else None,
+                "power_w_median": power_sorted[len(power_sorted) // 2] if power_sorted else None}
 
 
 def measured_peaks():
@@ -500,6 +506,42 @@ def run_compute_only(wl, K, phases=None):
     return a.elapsed_time(b) / K
 
 
+def run_duration(wl, seconds: float, overlapped: bool, K: int = 20):
+    """Steps back to back for about `seconds` (batches of 50), the last K of
+    them with phase events; clocks and power sampled throughout."""
+    torch = wl.torch
+    wl.sync()
+    if overlapped:
+        wl.prologue()
+    else:
+        for l in (0, 1):
+            wl.prefetch(l, l)
+    wl.sync()
+    phases = [_events(torch, 7) for _ in range(K)]
+    n, t0 = 0, time.perf_counter()
+    a, b = _events(torch, 2)
+    with ClockSampler(0) as clk:
+        a.record(wl.compute)
+        for c in wl.copies:
+            c.wait_stream(wl.compute)
+        while time.perf_counter() - t0 < seconds:
+            for _ in range(50):
+                wl.step(n, prefetch_next=overlapped)
+                n += 1
+            wl.compute.synchronize()
+        for i in range(K):
+            wl.step(n, prefetch_next=overlapped, phases=phases[i])
+            n += 1
+        wl.set_phases(None)
+        for c in wl.copies:
+            wl.compute.wait_stream(c)
+        b.record(wl.compute)
+        b.synchronize()
+    assert wl.rt.device_status() == 0
+    return {"steps": n, "seconds": round(a.elapsed_time(b) / 1e3, 2), "ms_per_step": round(a.elapsed_time(b) / n, 4),
+            "last_steps_phase_ms": _phase_avg(phases, K), "clocks": clk.summary()}
+
+
 def run_copy_only(wl, K):
     torch = wl.torch
     wl.sync()
@@ -614,6 +656,16 @@ def run_layer_bench(args):
                               sh.E, sh.H, sh.I, wl.placement.local_slot, wl.placement.peer_id,
                               wl.placement.peer_slot, wl.placement.n_peers, wl.chunk))})
         res["chunk_sweep"] = sweep
+    if args.duration_study > 0:
+        comp = run_duration(wl, args.duration_study, overlapped=False)
+        over = run_duration(wl, args.duration_study, overlapped=True)
+        res["duration_study"] = {
+            "compute_only": comp, "overlapped": over,
+            "step_ratio": round(over["ms_per_step"] / comp["ms_per_step"], 3),
+            "gate_up_ratio": round(over["last_steps_phase_ms"]["gate_up_gemm"]
+                                   / comp["last_steps_phase_ms"]["gate_up_gemm"], 3),
+            "sm_clock_ratio": (round(over["clocks"]["sm_mhz"] / comp["clocks"]["sm_mhz"], 3)
+                               if over["clocks"]["sm_mhz"] and comp["clocks"]["sm_mhz"] else None)}
     if args.merge_copy:
         res["merge_copy"] = run_merge_baseline(wl, K, W)
     res["wl"] = wl
@@ -1084,6 +1136,8 @@ def main():
         })
         if "chunk_sweep" in res:
             line["chunk_sweep"] = res["chunk_sweep"]
+        if "duration_study" in res:
+            line["duration_study"] = res["duration_study"]
     if "compute_only_ms" in res:
         comp, copy = res["compute_only_ms"], res["copy_only_ms"]
         exposed = max(0.0, res["ms_step"] - comp)
