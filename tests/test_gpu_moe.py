@@ -124,3 +124,55 @@ def test_bad_inverse_permutation_is_flagged():
         assert torch.equal(again, clean)
     finally:
         run.close()
+
+
+@pytest.mark.parametrize("shape", [I.LayerShape(T=300, H=512, I=256, E=12, k=2, S=1),
+                                   I.LayerShape(T=2048, H=7168, I=2048, E=32, k=4, S=1)],
+                         ids=["small", "r1_widths"])
+def test_layer_stages_bf16(shape):
+    """The bf16 layer split at its intermediates (read from the workspace with
+    dwdp_workspace_region): xp holds x's rows in grouped order, bit for bit;
+    a = SiLU(gate) * up of those rows (and of x for the shared expert) against
+    the oracle's grouped GEMM with each group's own w13; y = a W_down against
+    the oracle's grouped GEMM on the GPU's own a with each group's w2; both
+    at the layer's bars."""
+    build()
+    pl = I.split_placement(shape.E, shape.E // 3, 2)
+    lw = I.make_layer(shape, pl, 21, 0, device="cuda")
+    x = I.make_tokens(shape.T, shape.H, 21).cuda()
+    run = GpuLayerRun(shape, lw)
+    try:
+        rb, out = run.run(x)
+        T, k, H, I_ = shape.T, shape.k, shape.H, shape.I
+        rows_r, rows_all = T * k, T * (k + shape.S)
+        rt = run.rt
+        xp = rt.ws_region(T, "xp").view(torch.bfloat16).reshape(rows_r, H)
+        a = rt.ws_region(T, "a").view(torch.bfloat16).reshape(rows_all, I_)
+        y = rt.ws_region(T, "y").view(torch.bfloat16).reshape(rows_all, H)
+        perm = rb.perm[:rows_r].long()
+        assert torch.equal(xp, x[perm // k]), "xp is not x in grouped order"
+        offsets = rb.offsets.cpu().numpy().astype(np.int64)
+        bounds = np.concatenate([offsets, [rows_all]])                    # the shared expert is the last group
+        # rows checked: all of them for the small layer; at R1 widths the
+        # first and last row of every group (the last one in its ragged last
+        # m-tile)
+        sel = []
+        for g in range(shape.E + shape.S):
+            lo, hi = int(bounds[g]), int(bounds[g + 1])
+            rows = range(lo, hi) if shape.H <= 512 else sorted({lo, hi - 1} if hi > lo else set())
+            sel.append(list(rows))
+        offs_sel = np.concatenate([[0], np.cumsum([len(r) for r in sel])]).astype(np.int32)
+        flat = np.array([r for rows in sel for r in rows], dtype=np.int64)
+        w13s, w2s, sw13, sw2 = host_layer(lw)
+        o = oracle.default()
+        a_in = np.concatenate([I.bf16_bits(xp), I.bf16_bits(x)])          # routed rows, then the shared rows
+        # the oracle's sums rounded once to bf16, the layer's declared rounding points
+        as_bf16 = lambda v: (o.round_bf16_array(v).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        a_want = as_bf16(o.grouped_gemm(np.ascontiguousarray(a_in[flat]), offs_sel,
+                                        [w13s[e] for e in range(shape.E)] + [sw13], I_, 1))
+        assert_close(to_f64(a)[flat], a_want, what="gate/up output a")
+        y_want = as_bf16(o.grouped_gemm(np.ascontiguousarray(I.bf16_bits(a)[flat]), offs_sel,
+                                        [w2s[e] for e in range(shape.E)] + [sw2], H, 0))
+        assert_close(to_f64(y)[flat], y_want, what="down output y")
+    finally:
+        run.close()
