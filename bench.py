@@ -118,8 +118,8 @@ def parse(argv=None):
                         "'variants': a weight type for the same workload (fp8, nvfp4, nvfp4_wide = nvfp4 with "
                         "--wide-epilogue) or another workload, optionally with a weight type "
                         "(r1_zipf_16k:nvfp4).  Default for the 8K-token bf16 layer: fp8, nvfp4, nvfp4_wide, the "
-                        "Zipf 16K layer (bf16, nvfp4), the 256-token layer with its chunk sweep and the 4-layer "
-                        "pipeline (bf16, nvfp4)")
+                        "Zipf 16K layer and the 256-token layer (bf16 with its chunk sweep, fp8, nvfp4) and the "
+                        "4-layer pipeline (bf16, nvfp4)")
     p.add_argument("--peer-pools", default="device", choices=["device", "host"],
                    help="where the emulated peers' pools live (host: pinned host memory, copies over the "
                         "host link, so only their writes use this GPU's HBM)")
@@ -141,8 +141,9 @@ def parse(argv=None):
         args.merge_copy = False
     if args.variants is None:
         default = args.workload == "r1_moe_layer_8k" and args.dtype == "bf16" and not args.no_extras
-        args.variants = ("fp8,nvfp4,nvfp4_wide,r1_zipf_16k,r1_zipf_16k:nvfp4,r1_moe_layer_256,"
-                         "r1_pipeline_4layer,r1_pipeline_4layer:nvfp4") if default and args.group == 4 else ""
+        args.variants = ("fp8,nvfp4,nvfp4_wide,r1_zipf_16k,r1_zipf_16k:fp8,r1_zipf_16k:nvfp4,r1_moe_layer_256,"
+                         "r1_moe_layer_256:fp8,r1_moe_layer_256:nvfp4,r1_pipeline_4layer,r1_pipeline_4layer:nvfp4"
+                         ) if default and args.group == 4 else ""
     return args
 
 
@@ -992,16 +993,16 @@ def variant_summary(args, variant: str) -> dict:
     "<dtype>[_wide]" (the main line's workload with E4M3 or NVFP4 weights,
     _wide = NVFP4 with the eight-warp gate/up epilogue) or
     "<workload>[:<dtype>]" (another workload of WORKLOADS, bf16 unless
-    given; the 256-token layer adds the chunk sweep over 1, 4, 16 and 64 MB
-    slices), timed like the main line: overlapped steps, compute-only and
-    copy-only legs, and (single layers) end to end with host buffers."""
+    given; the bf16 256-token layer adds the chunk sweep over 1, 4, 16 and
+    64 MB slices), timed like the main line: overlapped steps, compute-only
+    and copy-only legs, and (single layers) end to end with host buffers."""
     import copy as _copy
 
     import torch
     a = _copy.copy(args)
     workload, wdtype, wide = parse_variant(args.workload, variant)
     a.workload, a.dtype, a.merge_copy, a.wide_epilogue = workload, wdtype, False, wide
-    a.chunk_sweep = "1,4,16,64" if workload == "r1_moe_layer_256" else ""
+    a.chunk_sweep = "1,4,16,64" if workload == "r1_moe_layer_256" and wdtype == "bf16" else ""
     a.chunk_mb = 16.0 if workload == "r1_pipeline_4layer" else 32.0
     pipeline = workload == "r1_pipeline_4layer"
     if pipeline:
