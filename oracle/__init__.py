@@ -118,6 +118,9 @@ class Oracle:
             vpp, vpp, _F32P, vpp, vpp, _F32P,
             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
             ctypes.c_int, _F64P]
+        L.oracle_e4m3_linear.restype = None
+        L.oracle_e4m3_linear.argtypes = [_U8P, _F32P, _I64, _I64, _U8P, ctypes.c_float, _I64, ctypes.c_int,
+                                         ctypes.c_int, _F64P]
         L.oracle_nvfp4_linear.restype = None
         L.oracle_nvfp4_linear.argtypes = [_U8P, _U8P, _F32P, _I64, _I64, _U8P, _U8P, ctypes.c_float, _I64,
                                           ctypes.c_int, ctypes.c_int, _F64P]
@@ -375,6 +378,21 @@ class Oracle:
                                          sc2, dp(sh[0]), dp(sh[1]), ss13, dp(sh[2]), dp(sh[3]), ss2,
                                          int(bool(mirrored)), out)
         del keep
+        return out
+
+    def e4m3_linear(self, codes, row_scale, w, w_scale, epilogue: int = 0, mirrored: bool = True) -> np.ndarray:
+        """One E4M3 linear layer on rows given as codes [n][K] and row scales
+        [n], against weight codes w [N][K] (epilogue 1: [2N][K], gate rows
+        then up rows) with tensor scale w_scale.  Epilogue 0: the product;
+        1: SiLU(gate) * up.  fp64, bf16-rounded when mirrored."""
+        codes = np.ascontiguousarray(codes, dtype=np.uint8)
+        rs = np.ascontiguousarray(row_scale, dtype=np.float32)
+        w = np.ascontiguousarray(w, dtype=np.uint8)
+        n, K = codes.shape
+        N = w.shape[0] // (2 if epilogue == 1 else 1)
+        assert w.shape[1] == K and rs.shape == (n,)
+        out = np.zeros((n, N), dtype=np.float64)
+        self.lib.oracle_e4m3_linear(codes, rs, n, K, w, float(w_scale), N, int(epilogue), int(bool(mirrored)), out)
         return out
 
     def nvfp4_linear(self, codes, sf, row_scale, w, wsf, w_scale, epilogue: int = 0,

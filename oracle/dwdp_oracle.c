@@ -722,3 +722,37 @@ void oracle_nvfp4_linear(const uint8_t* codes, const uint8_t* sf, const float* r
         }
     }
 }
+
+/* One E4M3 linear layer on rows that arrive already quantized (the halves
+ * of expert_ffn_fp8 on their own, so a caller can check each GEMM of the
+ * E4M3 layer given the codes its input rows really had):
+ *   epilogue 0:  out[r][c] = (sum_k E4M3(codes[r][k]) E4M3(w[c][k])) * row_scale[r] * w_scale
+ *   epilogue 1:  g = the same with W's row c, u = with W's row N + c,
+ *                out[r][c] = SiLU(g) * u                  (w has 2N rows)
+ * fp64 sums, rounded to bf16 in mirrored mode. */
+void oracle_e4m3_linear(const uint8_t* codes, const float* row_scale, int64_t n, int64_t K, const uint8_t* w,
+                        float w_scale, int64_t N, int epilogue, int mirrored, double* out) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n; ++r) {
+        const uint8_t* a = codes + r * K;
+#if ORACLE_MUTANT == 21
+        const double sc = (double)row_scale[r];                  /* planted: weight scale dropped */
+#else
+        const double sc = (double)row_scale[r] * (double)w_scale;
+#endif
+        for (int64_t c = 0; c < N; ++c) {
+            double s = 0.0, u = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double av = oracle_e4m3_to_double(a[k]);
+                s += av * oracle_e4m3_to_double(w[c * K + k]);
+                if (epilogue == 1) u += av * oracle_e4m3_to_double(w[(N + c) * K + k]);
+            }
+            s *= sc;
+            if (epilogue == 1) {
+                u *= sc;
+                s = s / (1.0 + exp(-s)) * u;
+            }
+            out[r * N + c] = mirrored ? rb(s) : s;
+        }
+    }
+}

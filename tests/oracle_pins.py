@@ -647,3 +647,30 @@ def pin_nvfp4_linear(o):
             assert np.all(np.abs(m - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30)
 
 ALL_PINS += [pin_nvfp4_linear]
+
+
+def pin_e4m3_linear(o):
+    """The E4M3 linear layer on given codes against numpy: rows and weights
+    decoded by torch's float8_e4m3fn, an fp64 matmul times the row and
+    tensor scales (epilogue 0), SiLU(gate) * up of the two halves (1)."""
+    rng = np.random.default_rng(19)
+    finite = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)   # no NaN codes
+    for (n, K, N) in [(6, 32, 5), (3, 128, 12)]:
+        codes = rng.choice(finite, size=(n, K))
+        rs = rng.uniform(0.001, 3.0, size=n).astype(np.float32)
+        for epi in (0, 1):
+            rows = 2 * N if epi else N
+            w = rng.choice(finite, size=(rows, K))
+            ws = np.float32(rng.uniform(0.005, 0.02))
+            A = _e4m3_decode_torch(codes) * rs[:, None].astype(np.float64)
+            W = _e4m3_decode_torch(w) * np.float64(ws)
+            with np.errstate(over="ignore"):      # exp(-g) overflows to inf for large negative g: SiLU -> 0
+                ref = A @ W.T if epi == 0 else _silu(A @ W[:N].T) * (A @ W[N:].T)
+            got = o.e4m3_linear(codes, rs, w, ws, epilogue=epi, mirrored=False)
+            assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.abs(ref).max()), f"E4M3 linear {epi} != numpy"
+            m = o.e4m3_linear(codes, rs, w, ws, epilogue=epi, mirrored=True)
+            assert np.array_equal(_decode(_bits_from_f32(m.astype(np.float32))), m)
+            assert np.all(np.abs(m - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30)
+
+
+ALL_PINS += [pin_e4m3_linear]

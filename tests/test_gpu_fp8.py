@@ -98,3 +98,73 @@ def test_fp8_r1_layer_sample():
     # tokens covering every expert's last m-tile
     shape, pl = I.r1_layer(8192)
     _run(shape, pl, seed=3, tokens="last_tiles", chunk=32 << 20)
+
+
+@pytest.mark.parametrize("shape", [I.LayerShape(T=300, H=512, I=256, E=12, k=2, S=1),
+                                   I.LayerShape(T=2048, H=7168, I=2048, E=32, k=4, S=1)],
+                         ids=["small", "r1_widths"])
+def test_fp8_layer_stages(shape):
+    """The E4M3 layer split at its quantized intermediates (workspace
+    regions): every routed row of xp holds its token's E4M3 codes and row
+    scale as the oracle quantizes x, bit for bit; a against the oracle's
+    SiLU(gate) * up of those codes with the row's expert weights; every row
+    of the GPU's a quantized by the oracle gives the codes and row scale the
+    down GEMM read, bit for bit; y against the oracle's product of those
+    codes with the expert's w2.  (Rows: all for the small layer, the first
+    and last row of every group at R1 widths.)"""
+    build()
+    pl = I.split_placement(shape.E, shape.E // 3, 2)
+    lw = I.make_layer_fp8(shape, pl, 23, 0, device="cuda")
+    x = I.make_tokens(shape.T, shape.H, 23).cuda()
+    rt = B.Runtime(shape.H, shape.I, shape.E, shape.k, shape.S, shape.T, 1, pl.n_remote(), weight_dtype=B.DTYPE_E4M3)
+    try:
+        rt.set_layer(0, lw)
+        rb = B.RouteBuffers(shape.T, shape.E, shape.k)
+        out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
+        rt.prefetch(0, 0, 1 << 20, [torch.cuda.Stream()])
+        rt.route(x, lw.wr, None, rb)
+        rt.moe(0, 0, x, rb, out)
+        torch.cuda.synchronize()
+        assert rt.device_status() == 0
+        T, k, H, I_, E = shape.T, shape.k, shape.H, shape.I, shape.E
+        rows_r, rows_all = T * k, T * (k + shape.S)
+        xp = _u8(rt.ws_region(T, "xp")).reshape(rows_r, H)
+        sxp = rt.ws_region(T, "sxp").view(torch.float32).cpu().numpy()
+        a_gpu = rt.ws_region(T, "a").view(torch.bfloat16).reshape(rows_all, I_).float().cpu().numpy()
+        aq = _u8(rt.ws_region(T, "aq")).reshape(rows_all, I_)
+        sa = rt.ws_region(T, "sa").view(torch.float32).cpu().numpy()
+        y_gpu = rt.ws_region(T, "y").view(torch.bfloat16).reshape(rows_all, H).float().cpu().numpy()
+        perm = rb.perm.cpu().numpy()[:rows_r]
+        offsets = rb.offsets.cpu().numpy()
+    finally:
+        rt.close()
+    o = oracle.default()
+    xf = x.float().cpu().numpy()
+    xq = [o.quantize_row_e4m3(xf[t]) for t in range(T)]
+    for r in range(rows_r):
+        c, s_ = xq[perm[r] // k]
+        assert np.array_equal(xp[r], c) and np.float32(s_) == sxp[r], f"xp row {r}"
+    for r in range(rows_all):
+        c, s_ = o.quantize_row_e4m3(a_gpu[r])
+        assert np.array_equal(aq[r], c) and np.float32(s_) == sa[r], f"a row {r}: codes or scale differ"
+    bounds = list(offsets) + [rows_all]
+    a_want, a_got, y_want, y_got = [], [], [], []
+    for g in range(E + shape.S):
+        lo, hi = int(bounds[g]), int(bounds[g + 1])
+        rows = list(range(lo, hi)) if H <= 512 else sorted({lo, hi - 1} if hi > lo else set())
+        if not rows:
+            continue
+        if g < E:
+            w13, w2 = _expert_codes(lw, g)
+            s13, s2 = lw.w13_scale[g], lw.w2_scale[g]
+        else:
+            w13, w2, s13, s2 = _u8(lw.shared_w13), _u8(lw.shared_w2), lw.shared_s13, lw.shared_s2
+        w13, w2 = w13.reshape(2 * I_, H), w2.reshape(H, I_)
+        toks = [perm[r] // k if r < rows_r else r - rows_r for r in rows]
+        a_want.append(o.e4m3_linear(np.stack([xq[t][0] for t in toks]),
+                                    np.array([xq[t][1] for t in toks], np.float32), w13, s13, epilogue=1))
+        a_got.append(a_gpu[rows])
+        y_want.append(o.e4m3_linear(aq[rows], sa[rows], w2, s2))
+        y_got.append(y_gpu[rows])
+    assert_close(np.concatenate(a_got), np.concatenate(a_want), what="E4M3 gate/up output a")
+    assert_close(np.concatenate(y_got), np.concatenate(y_want), what="E4M3 down output y")

@@ -28,6 +28,7 @@ MUTANTS = {
     18: "NVFP4 block scales indexed as 32-wide blocks",
     19: "NVFP4 down-projection tensor scale dropped",
     20: "NVFP4 linear layer drops the row scale",
+    21: "E4M3 linear layer drops the weight scale",
 }
 
 
