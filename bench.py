@@ -141,7 +141,8 @@ def parse(argv=None):
         args.merge_copy = False
     if args.variants is None:
         default = args.workload == "r1_moe_layer_8k" and args.dtype == "bf16" and not args.no_extras
-        args.variants = ("fp8,nvfp4,nvfp4_wide,r1_zipf_16k,r1_zipf_16k:fp8,r1_zipf_16k:nvfp4,r1_moe_layer_256,"
+        args.variants = ("fp8,nvfp4,nvfp4_wide,r1_zipf_16k,r1_zipf_16k:fp8,r1_zipf_16k:nvfp4,"
+                         "r1_zipf_16k:nvfp4_wide,r1_moe_layer_256,"
                          "r1_moe_layer_256:fp8,r1_moe_layer_256:nvfp4,r1_pipeline_4layer,r1_pipeline_4layer:nvfp4"
                          ) if default and args.group == 4 else ""
     return args
