@@ -96,7 +96,9 @@ def parse(argv=None):
     p.add_argument("--chunk-mb", type=float, default=None,
                    help="prefetch slice size in MB (default 16 for the 4-layer pipeline, as that workload "
                         "specifies, else 32: the fastest single-destination setting measured)")
-    p.add_argument("--copy-streams", type=int, default=1)
+    p.add_argument("--copy-streams", type=int, default=None,
+                   help="copy chains the prefetch graph is split into, one per peer pool modulo this count "
+                        "(default 1 for bf16 and E4M3, 2 for NVFP4: the fastest measured)")
     p.add_argument("--stages", type=int, default=2,
                    help="staging buffers (2: the pages' double buffering; 3: the copy of layer l+2 may start "
                         "while layer l computes)")
@@ -135,6 +137,9 @@ def parse(argv=None):
     args = p.parse_args(argv)
     if args.chunk_mb is None:
         args.chunk_mb = 16.0 if args.workload == "r1_pipeline_4layer" else 32.0
+    args.copy_streams_given = args.copy_streams is not None
+    if args.copy_streams is None:
+        args.copy_streams = 2 if args.dtype == "nvfp4" else 1
     if args.workload == "r1_moe_layer_8k" and not args.no_extras and args.group == 4:
         args.merge_copy = True
     if args.no_merge_copy:
@@ -1003,6 +1008,8 @@ def variant_summary(args, variant: str) -> dict:
     a = _copy.copy(args)
     workload, wdtype, wide = parse_variant(args.workload, variant)
     a.workload, a.dtype, a.merge_copy, a.wide_epilogue = workload, wdtype, False, wide
+    if not args.copy_streams_given:
+        a.copy_streams = 2 if wdtype == "nvfp4" else 1
     a.chunk_sweep = "1,4,16,64" if workload == "r1_moe_layer_256" and wdtype == "bf16" else ""
     a.chunk_mb = 16.0 if workload == "r1_pipeline_4layer" else 32.0
     pipeline = workload == "r1_pipeline_4layer"
@@ -1020,7 +1027,7 @@ def variant_summary(args, variant: str) -> dict:
         "prefetch": {"compute_only_ms": round(comp, 4), "copy_only_ms": round(copy_ms, 4),
                      "exposed_ms": round(exposed, 4),
                      "hidden_frac": round(max(0.0, 1.0 - exposed / copy_ms), 4) if copy_ms > 0 else None},
-        "clocks": res["clocks"], "chunk_mb": a.chunk_mb,
+        "clocks": res["clocks"], "chunk_mb": a.chunk_mb, "copy_streams": a.copy_streams,
     }
     if pipeline:
         flops = sum(4 * (layer_flops(T, sh.H, sh.I, sh.E, sh.k, sh.S) + 2 * T * sh.H * sh.H)
