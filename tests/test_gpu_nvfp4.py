@@ -282,6 +282,9 @@ def _a_tiles(offsets, rows_r, rows_all):
 def _down_path_case(shape, placement, seed, n_gate_rows, chunk):
     """The NVFP4 layer split at its quantized intermediate, each stage held
     to the plain bars (no allowance for requantization flips):
+      0. x: every row the gate/up GEMM reads (each routed row in expert order
+         and the shared expert's copy) holds the token's codes, block scales
+         and row scale as the oracle's row quantizer gives them, bit for bit;
       1. gate/up: the GPU's bf16 a of sampled rows against the oracle's
          SiLU(gate) * up of the same token's x codes (the oracle quantizes x
          itself) and the row's expert weights;
@@ -314,12 +317,40 @@ def _down_path_case(shape, placement, seed, n_gate_rows, chunk):
         sa = rt.ws_region(T, "sa").view(torch.float32).cpu().numpy()
         sfa = _u8(rt.ws_region(T, "sfa"))
         y_gpu = rt.ws_region(T, "y").view(torch.bfloat16).reshape(rows_all, H).float().cpu().numpy()
+        xp = _unpack_codes(_u8(rt.ws_region(T, "xp")), rows_r, H)
+        sxp = rt.ws_region(T, "sxp").view(torch.float32).cpu().numpy()
+        xq_sh = _unpack_codes(_u8(rt.ws_region(T, "xq")), T, H)
+        sx = rt.ws_region(T, "sx").view(torch.float32).cpu().numpy()
+        sfx = _u8(rt.ws_region(T, "sfx"))
         offsets = rb.offsets.cpu().numpy()
         perm = rb.perm.cpu().numpy()[:rows_r]
         o = oracle.default()
+        tile, within = _a_tiles(offsets, rows_r, rows_all)
+
+        # 0. x's codes, block scales and row scales in every row the gate/up
+        # GEMM reads (each routed row and the shared expert's copy), bit for bit
+        xf = x.float().cpu().numpy()
+        qx = [o.quantize_row_nvfp4(xf[t]) for t in range(T)]
+        cx = np.stack([q[0] for q in qx])
+        fx = np.stack([q[1] for q in qx])
+        s_x = np.array([q[2] for q in qx], dtype=np.float32)
+        tok = perm // k
+        assert np.array_equal(xp, cx[tok]), "x codes in expert order differ from the oracle's"
+        assert np.array_equal(sxp[:rows_r], s_x[tok]), "x row scales in expert order differ"
+        # block scales at their A-tile chunk positions (the gate/up GEMM's A
+        # tiles are numbered like the down GEMM's: expert by expert, then the
+        # shared rows)
+        xblk = np.arange(H // 16)
+        r_all = np.arange(rows_all)
+        m_all = within[r_all]
+        at_x = ((tile[r_all, None] * (H // 64) + xblk[None, :] // 4) * 512 + 16 * (m_all[:, None] % 32)
+                + 4 * (m_all[:, None] // 32) + xblk[None, :] % 4)
+        want_fx = np.concatenate([fx[tok], fx]) if sh.S else fx[tok]
+        assert np.array_equal(sfx[at_x[: want_fx.shape[0]]], want_fx), "x block scales differ"
+        if sh.S:
+            assert np.array_equal(xq_sh, cx) and np.array_equal(sx, s_x), "the shared expert's x codes differ"
 
         # 2. a's codes, every row
-        tile, within = _a_tiles(offsets, rows_r, rows_all)
         blk = np.arange(I_ // 16)
         for r in range(rows_all):
             c, f, s_ = o.quantize_row_nvfp4(a_gpu[r])
