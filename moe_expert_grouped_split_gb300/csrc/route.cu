@@ -698,12 +698,6 @@ __device__ __forceinline__ void tile_bases(const int32_t* __restrict__ offsets, 
 // x rows (one warp per token t): xq[t] and sx[t] for the shared expert (when
 // has_shared), and for each chosen expert j the row r = inv[t k + j] of xp /
 // sxp with its block scales, so x is read once.
-// IT > 0: the row has IT * 64 blocks (H = 1024 IT, IT <= 7) and each lane keeps its
-// IT block pairs in registers, loaded once, so the row scale and the codes
-// come from one read of the row (all of a lane's loads in flight together);
-// IT == 0: any H (a multiple of 64 elements per lane pair is not required),
-// the row is read twice, the second time from L2.
-template <int IT>
 __global__ void __launch_bounds__(256) quantize_x_nvfp4_kernel(const uint4* __restrict__ x, int H, int T, int k,
                                                                const int32_t* __restrict__ ids,
                                                                const int32_t* __restrict__ inv,
@@ -723,27 +717,7 @@ __global__ void __launch_bounds__(256) quantize_x_nvfp4_kernel(const uint4* __re
     if (t >= T) return;
     const int nb = H / 16;
     const uint4* src = x + (int64_t)t * (H / 8);
-    uint4 row[IT > 0 ? IT : 1][4];
-    float s;
-    if constexpr (IT > 0) {
-#pragma unroll
-        for (int i = 0; i < IT; ++i) load_block_pair(src, 2 * lane + 64 * i, nb, row[i]);
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < IT; ++i)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float v[16];
-                bf16x16_to_float(&row[i][2 * h], v);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
-            }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        s = amax > 0.0f ? amax / 2688.0f : 1.0f;  // as nvfp4_row_scale
-    } else {
-        s = nvfp4_row_scale(src, nb, lane);
-    }
+    const float s = nvfp4_row_scale(src, nb, lane);
     const float d = 6.0f * s;
     const int64_t n_rows = (int64_t)T * k;
     if (lane < k) {
@@ -774,8 +748,14 @@ __global__ void __launch_bounds__(256) quantize_x_nvfp4_kernel(const uint4* __re
     // adjacent scale bytes per destination
     uint4* xq4 = reinterpret_cast<uint4*>(xq);
     uint4* xp4 = reinterpret_cast<uint4*>(xp);
-    // one block pair: codes and scales to the shared copy and every destination
-    auto emit = [&](const uint4 (&cur)[4], int b) {
+    // the next pair's loads are issued before this pair is converted
+    uint4 nxt[4];
+    load_block_pair(src, 2 * lane, nb, nxt);
+    for (int b = 2 * lane; b < nb; b += 64) {
+        uint4 cur[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+        load_block_pair(src, b + 64, nb, nxt);
         uint4 c;
         const uint16_t f = (uint16_t)nvfp4_block_pair(cur, s, d, c);
         const int64_t sf_off = (int64_t)(b >> 2) * kSfChunkBytes + (b & 3);  // block b within a row's chunks
@@ -788,21 +768,6 @@ __global__ void __launch_bounds__(256) quantize_x_nvfp4_kernel(const uint4* __re
             if (r < 0) continue;
             xp4[(int64_t)r * (H / 32) + b / 2] = c;
             *reinterpret_cast<uint16_t*>(sf + dst_sf[wib][j] + sf_off) = f;
-        }
-    };
-    if constexpr (IT > 0) {
-#pragma unroll
-        for (int i = 0; i < IT; ++i) emit(row[i], 2 * lane + 64 * i);
-    } else {
-        // the next pair's loads are issued before this pair is converted
-        uint4 nxt[4];
-        load_block_pair(src, 2 * lane, nb, nxt);
-        for (int b = 2 * lane; b < nb; b += 64) {
-            uint4 cur[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
-            load_block_pair(src, b + 64, nb, nxt);
-            emit(cur, b);
         }
     }
 }
@@ -882,28 +847,9 @@ cudaError_t launch_quantize_x_nvfp4(const void* x, int H, int T, int k, const in
                                     float* sxp, uint8_t* sf, int64_t sf_tiles, int* err, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     const int warps = kQuantWarps;  // the kernel's per-warp destination tables assume it
-    const dim3 grid((T + warps - 1) / warps), block(32 * warps);
-    const uint4* xin = reinterpret_cast<const uint4*>(x);
-    uint2* xq2 = reinterpret_cast<uint2*>(xq);
-    uint2* xp2 = reinterpret_cast<uint2*>(xp);
-    // rows of 1024 IT elements (IT <= 7: at 8 the row no longer fits in
-    // registers) stay in registers between the two passes; other widths take
-    // the generic kernel
-    const int it = (H % 1024 == 0 && H / 1024 <= 7) ? H / 1024 : 0;
-#define DWDP_QX(IT)                                                                                             \
-    quantize_x_nvfp4_kernel<IT><<<grid, block, 0, s>>>(xin, H, T, k, ids, inv, offsets, E, has_shared ? 1 : 0, \
-                                                       xq2, sx, xp2, sxp, sf, sf_tiles, err)
-    switch (it) {
-        case 1: DWDP_QX(1); break;
-        case 2: DWDP_QX(2); break;
-        case 3: DWDP_QX(3); break;
-        case 4: DWDP_QX(4); break;
-        case 5: DWDP_QX(5); break;
-        case 6: DWDP_QX(6); break;
-        case 7: DWDP_QX(7); break;
-        default: DWDP_QX(0); break;
-    }
-#undef DWDP_QX
+    quantize_x_nvfp4_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(
+        reinterpret_cast<const uint4*>(x), H, T, k, ids, inv, offsets, E, has_shared ? 1 : 0,
+        reinterpret_cast<uint2*>(xq), sx, reinterpret_cast<uint2*>(xp), sxp, sf, sf_tiles, err);
     return cudaGetLastError();
 }
 
