@@ -1007,7 +1007,9 @@ def variant_summary(args, variant: str) -> dict:
     import torch
     a = _copy.copy(args)
     workload, wdtype, wide = parse_variant(args.workload, variant)
-    a.workload, a.dtype, a.merge_copy, a.wide_epilogue = workload, wdtype, False, wide
+    # the merge-copy baseline also for the main workload in the pages' weight format
+    merge = workload == "r1_moe_layer_8k" and wdtype == "nvfp4" and not wide and args.group == 4
+    a.workload, a.dtype, a.merge_copy, a.wide_epilogue = workload, wdtype, merge, wide
     if not args.copy_streams_given:
         a.copy_streams = 2 if wdtype == "nvfp4" else 1
     a.chunk_sweep = "1,4,16,64" if workload == "r1_moe_layer_256" and wdtype == "bf16" else ""
@@ -1057,6 +1059,8 @@ def variant_summary(args, variant: str) -> dict:
         })
         if "chunk_sweep" in res:
             out["chunk_sweep"] = res["chunk_sweep"]
+        if res.get("merge_copy"):
+            out["merge_copy_baseline"] = res["merge_copy"]
     wl.rt.close()
     del wl, res
     torch.cuda.synchronize()
