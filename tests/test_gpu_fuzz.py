@@ -124,3 +124,84 @@ def test_random_layer(seed):
         want = o.moe_tokens_nvfp4(xb, sub, ref["ids"], ref["w"], w[0], w[1], lw.w13_scale, w[2], w[3], lw.w2_scale,
                                   shared=shared, mirrored=True)
         assert_close_requantized(to_f64(out)[sub], want, what=what)
+
+
+def _r1_width_config(seed):
+    rng = np.random.default_rng(5000 + seed)
+    dtype = ["bf16", "fp8", "nvfp4"][seed % 3]
+    E = int(rng.integers(9, 65))
+    k = int(rng.integers(1, 9))
+    S = int(rng.integers(0, 2))
+    T = int(rng.integers(1, 1500))
+    n_local = int(rng.integers(0, E + 1))
+    n_peers = int(rng.integers(1, 4))
+    remote = list(range(n_local, E))
+    red = [int(e) for e in rng.choice(remote, size=min(len(remote), int(rng.integers(0, 4))), replace=False)] \
+        if remote else []
+    return dtype, I.LayerShape(T=T, H=7168, I=2048, E=E, k=k, S=S), I.split_placement(E, n_local, n_peers, red)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_r1_width_layer(seed):
+    """Random layers at the R1 widths (H = 7168, I = 2048: 28 / 8 K slices and
+    8 / 28 n-tiles per GEMM) with random expert counts, top-k, token counts,
+    placements and the three weight formats, in 32 MB slices; the output of
+    tokens that between them own a row of every expert's last m-tile (and the
+    shared expert's) against the oracle."""
+    from gpu_helpers import last_tile_tokens
+    build()
+    dtype, shape, pl = _r1_width_config(seed)
+    make = {"bf16": I.make_layer, "fp8": I.make_layer_fp8, "nvfp4": I.make_layer_nvfp4}[dtype]
+    # logits ~ N(0, 1), so every chosen expert carries weight
+    lw = make(shape, pl, 50 + seed, 0, device="cuda", router_std=float(1.0 / np.sqrt(shape.H)))
+    x = I.make_tokens(shape.T, shape.H, 50 + seed).cuda()
+    rt = B.Runtime(shape.H, shape.I, shape.E, shape.k, shape.S, shape.T, 1, max(1, pl.n_remote()),
+                   weight_dtype=DTYPES[dtype])
+    try:
+        rt.set_layer(0, lw)
+        rb = B.RouteBuffers(shape.T, shape.E, shape.k)
+        out = torch.empty((shape.T, shape.H), dtype=torch.bfloat16, device="cuda")
+        if pl.n_remote() > 0:
+            rt.prefetch(0, 0, 32 << 20, [torch.cuda.Stream()])
+        rt.route(x, lw.wr, None, rb)
+        rt.moe(0, 0, x, rb, out)
+        torch.cuda.synchronize()
+        assert rt.device_status() == 0
+        ids = rb.topk_ids.cpu().numpy()[: shape.T]
+        perm = rb.perm.cpu().numpy()[: shape.T * shape.k]
+        offsets = rb.offsets.cpu().numpy()
+    finally:
+        rt.close()
+    o = oracle.default()
+    xb = I.bf16_bits(x)
+    ref = o.route(xb, I.bf16_bits(lw.wr), None, shape.k)
+    same = (ids == ref["ids"]).all(axis=1)
+    assert same.mean() >= 0.9
+    sub, missed = last_tile_tokens(perm, offsets, shape.k, shape.T, same, n_shared=shape.S)
+    assert not missed
+    used = np.unique(ref["ids"][sub])
+    what = f"seed {seed}: {dtype} {shape} local {int((pl.local_slot >= 0).sum())} peers {pl.n_peers}"
+    print(f"\n{what}: {sub.size} tokens")
+    if dtype == "bf16":
+        w13s, w2s, sw13, sw2 = _weights_for_oracle(dtype, lw, used)
+        want = o.moe_tokens(xb, sub, ref["ids"], ref["w"], w13s, w2s, sw13, sw2, mirrored=True)
+        assert_close(to_f64(out)[sub], want, what=what)
+    elif dtype == "fp8":
+        w13s, w2s = _weights_for_oracle(dtype, lw, used)
+        kw = {}
+        if shape.S:
+            kw = dict(shared_w13=_u8(lw.shared_w13), shared_w2=_u8(lw.shared_w2), shared_s13=lw.shared_s13,
+                      shared_s2=lw.shared_s2)
+        want = o.moe_tokens_fp8(xb, sub, ref["ids"], ref["w"], w13s, w2s, lw.w13_scale, lw.w2_scale, mirrored=True,
+                                **kw)
+        assert_close(to_f64(out)[sub], want, what=what)
+    else:
+        w = _weights_for_oracle(dtype, lw, used)
+        shared = None
+        if shape.S:
+            c13, f13 = I.unpack_nvfp4(lw.shared_w13.cpu(), 2 * shape.I, shape.H)
+            c2, f2 = I.unpack_nvfp4(lw.shared_w2.cpu(), shape.H, shape.I)
+            shared = (c13, f13, lw.shared_s13, c2, f2, lw.shared_s2)
+        want = o.moe_tokens_nvfp4(xb, sub, ref["ids"], ref["w"], w[0], w[1], lw.w13_scale, w[2], w[3], lw.w2_scale,
+                                  shared=shared, mirrored=True)
+        assert_close_requantized(to_f64(out)[sub], want, what=what)
