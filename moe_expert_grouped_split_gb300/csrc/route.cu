@@ -659,6 +659,14 @@ __device__ __forceinline__ uint32_t nvfp4_block_pair(const uint4 (&q)[4], float 
     return f0 | (f1 << 8);
 }
 
+// The lanes that run the iteration of a two-blocks-per-lane loop (block b =
+// 2 lane + 64 i) in which this lane holds block b: lanes l with
+// 2 l + 64 i < nb.  nb is a multiple of 4, so the lanes come in pairs.
+__device__ __forceinline__ unsigned pair_lanes(int b, int lane, int nb) {
+    const int active = min(32, (nb - (b - 2 * lane)) / 2);
+    return active >= 32 ? 0xffffffffu : ((1u << active) - 1u);
+}
+
 // A row's blocks b, b + 1 (b even) as four uint4, or zeros past the row end.
 __device__ __forceinline__ void load_block_pair(const uint4* src, int b, int nb, uint4 (&q)[4]) {
 #pragma unroll
@@ -757,17 +765,23 @@ __global__ void __launch_bounds__(256) quantize_x_nvfp4_kernel(const uint4* __re
         for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
         load_block_pair(src, b + 64, nb, nxt);
         uint4 c;
-        const uint16_t f = (uint16_t)nvfp4_block_pair(cur, s, d, c);
-        const int64_t sf_off = (int64_t)(b >> 2) * kSfChunkBytes + (b & 3);  // block b within a row's chunks
+        const uint32_t f = nvfp4_block_pair(cur, s, d, c) & 0xFFFFu;
+        // lanes 2i and 2i+1 hold the four block scales of one 64-element K
+        // step (one 4-byte word of each destination's chunk): the even lane
+        // stores the word, so each destination gets one store per K step
+        const uint32_t f_hi = __shfl_xor_sync(pair_lanes(b, lane, nb), f, 1);
+        const bool even = (lane & 1) == 0;
+        const uint32_t word = f | (f_hi << 16);
+        const int64_t sf_off = (int64_t)(b >> 2) * kSfChunkBytes;  // block b's K step within a row's chunks
         if (has_shared) {
             xq4[(int64_t)t * (H / 32) + b / 2] = c;
-            *reinterpret_cast<uint16_t*>(sf + sh_sf + sf_off) = f;
+            if (even) *reinterpret_cast<uint32_t*>(sf + sh_sf + sf_off) = word;
         }
         for (int j = 0; j < k; ++j) {
             const int32_t r = dst_row[wib][j];
             if (r < 0) continue;
             xp4[(int64_t)r * (H / 32) + b / 2] = c;
-            *reinterpret_cast<uint16_t*>(sf + dst_sf[wib][j] + sf_off) = f;
+            if (even) *reinterpret_cast<uint32_t*>(sf + dst_sf[wib][j] + sf_off) = word;
         }
     }
 }
@@ -815,9 +829,10 @@ __device__ __forceinline__ void quantize_a_row(const uint4* __restrict__ a, int 
         for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
         load_block_pair(src, b + 64, nb, nxt);
         uint4 c;
-        const uint16_t f = (uint16_t)nvfp4_block_pair(cur, s, d, c);
+        const uint32_t f = nvfp4_block_pair(cur, s, d, c) & 0xFFFFu;
+        const uint32_t f_hi = __shfl_xor_sync(pair_lanes(b, lane, nb), f, 1);  // as in the x quantizer
         aq4[r * (I / 32) + b / 2] = c;
-        *reinterpret_cast<uint16_t*>(sf + base + (int64_t)(b >> 2) * kSfChunkBytes + (b & 3)) = f;
+        if ((lane & 1) == 0) *reinterpret_cast<uint32_t*>(sf + base + (int64_t)(b >> 2) * kSfChunkBytes) = f | (f_hi << 16);
     }
 }
 
