@@ -201,10 +201,10 @@ WEIGHT_BYTES = {"bf16": 2, "fp8": 1, "nvfp4": 9 / 16}
 
 def measured_traffic(kernel_file: str, algorithmic_bytes: int):
     """dram__bytes_read.sum + dram__bytes_write.sum per launch of the gate/up
-    GEMM: the committed ncu record's measured-to-algorithmic ratio (taken on
-    a smaller case of the same kernel) times this launch's algorithmic
-    bytes; None when the kernel source has changed since the counters were
-    taken."""
+    GEMM: the committed ncu record's measured-to-algorithmic ratio (a 1-pass
+    capture of the 8192-token launch) times this launch's algorithmic bytes,
+    i.e. the captured bytes; None when the kernel source has changed since
+    the counters were taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "gate_up_gemm_traffic_r1_moe_layer_8k.json")
     if not os.path.exists(path):
@@ -1131,8 +1131,9 @@ def main():
         roof = roofline_entry("gate_up_grouped_gemm", g1, g1b, res["phase_ms"]["gate_up_gemm"] / 1e3, tc_peak, hbm,
                               tc_note, hbm_note)
         roof.update({"traffic": traffic, "algorithmic_flops_per_launch": g1, "algorithmic_bytes_per_launch": g1b,
-                     "traffic_source": "ncu DRAM bytes of this kernel on a smaller case (1024 tokens, 17 experts), "
-                                       "scaled by measured / algorithmic bytes; a lower bound" if traffic else None,
+                     "traffic_source": "ncu DRAM bytes (read + write) of this kernel's launch at this workload, "
+                                       "1-pass capture of the same source (profiles/"
+                                       "gate_up_gemm_traffic_r1_moe_layer_8k.json)" if traffic else None,
                      "timed": "CUDA events around the kernel on the compute stream, inside the overlapped step"})
         line.update({
             "tflops": round(layer_tflops, 1),

@@ -87,3 +87,20 @@ def test_variant_names():
     args = bench.parse([])
     for v in args.variants.split(","):
         bench.parse_variant(args.workload, v)       # every default variant parses
+
+
+def test_traffic_record_is_the_full_size_capture():
+    """The committed DRAM record of the gate/up GEMM is a capture of the
+    8192-token launch itself: scaled to that launch's algorithmic bytes it
+    gives back the captured read + write bytes, and it is keyed to the
+    kernel source it was taken on (otherwise the bench reports no traffic)."""
+    import json
+    import os
+    path = os.path.join(bench.ROOT, "profiles", "gate_up_gemm_traffic_r1_moe_layer_8k.json")
+    rec = json.load(open(path))
+    g1b = bench.g1_bytes(T, H, I, E, K, S)
+    assert rec["algorithmic_bytes"] == g1b
+    got = bench.measured_traffic(os.path.join(bench.ROOT, "moe_expert_grouped_split_gb300", "csrc", "gemm.cu"), g1b)
+    assert got is not None, "gemm.cu changed since the capture"
+    assert got == pytest.approx(rec["dram_bytes_read"] + rec["dram_bytes_write"], rel=1e-4)
+    assert 1.0 <= got / g1b < 1.1
