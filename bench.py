@@ -616,6 +616,24 @@ def run_e2e(wl, K):
             "h2d_bytes_per_step": T * sh.H * 2, "d2h_bytes_per_step": T * sh.H * 2}
 
 
+def workload_config(args, sh, placement, n_layers) -> dict:
+    """The JSON line's config: the workload, its shapes and placement and
+    the prefetch settings (the reference arm reports the same keys)."""
+    wbytes = WEIGHT_BYTES[args.dtype]
+    return {"workload": args.workload, "T": sh.T, "H": sh.H, "I": sh.I, "E": sh.E, "k": sh.k,
+            "shared": sh.S, "local_experts": int((placement.local_slot >= 0).sum()),
+            "remote_experts": placement.n_remote(), "peer_pools": placement.n_peers,
+            "chunk_mb": args.chunk_mb, "copy_streams": args.copy_streams, "expert_weights": args.dtype,
+            "prefetch_start": args.prefetch_start, "stages": args.stages,
+            "wide_epilogue": bool(args.wide_epilogue),
+            "peer_pool_memory": args.peer_pools,
+            "layers": n_layers,
+            "dwdp_group": args.group,
+            "l2": "inputs larger than L2 ({:.1f} GB of expert weights + {:.1f} GB of copies per layer)".format(
+                (sh.E + sh.S) * 3 * sh.H * sh.I * wbytes / 1e9, placement.n_remote() * 3 * sh.H * sh.I * wbytes / 1e9),
+            "parallelism": "single rank"}
+
+
 def wl_flags(args) -> int:
     """dwdp_config.flags for the benchmark's options."""
     from moe_expert_grouped_split_gb300 import binding as B
@@ -1096,19 +1114,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(res["ms_step"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": {"bf16": "bf16", "fp8": "e4m3", "nvfp4": "nvfp4"}[args.dtype],
         "data": "synthetic (seeded N(0,1) tokens, N(0,0.02) weights; R1 MoE layer shapes)",
-        "config": {"workload": args.workload, "T": sh.T, "H": sh.H, "I": sh.I, "E": sh.E, "k": sh.k,
-                   "shared": sh.S, "local_experts": int((wl.placement.local_slot >= 0).sum()),
-                   "remote_experts": wl.placement.n_remote(), "peer_pools": wl.placement.n_peers,
-                   "chunk_mb": args.chunk_mb, "copy_streams": args.copy_streams, "expert_weights": args.dtype,
-                   "prefetch_start": args.prefetch_start, "stages": args.stages,
-                   "wide_epilogue": bool(args.wide_epilogue),
-                   "peer_pool_memory": args.peer_pools,
-                   "layers": wl.n_layers,
-                   "dwdp_group": args.group,
-                   "l2": "inputs larger than L2 ({:.1f} GB of expert weights + {:.1f} GB of copies per layer)".format(
-                       (sh.E + sh.S) * 3 * sh.H * sh.I * WEIGHT_BYTES[args.dtype] / 1e9,
-                       wl.placement.n_remote() * 3 * sh.H * sh.I * WEIGHT_BYTES[args.dtype] / 1e9),
-                   "parallelism": "single rank"},
+        "config": workload_config(args, sh, wl.placement, wl.n_layers),
         "clocks": res["clocks"],
     }
     if pipeline:
@@ -1265,8 +1271,9 @@ def main_reference(args, rank, world):
         "ms_per_layer_extrapolated": round(T / value * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded, R1 MoE layer shapes)",
-        "config": {"workload": args.workload, "T": T, "H": shape.H, "I": shape.I, "E": shape.E, "k": shape.k,
-                   "shared": shape.S, "expert_weights": wd, "dwdp_group": args.group},
+        # the same workload as the GPU arm's line (the oracle's result does not
+        # depend on the placement or the prefetch settings)
+        "config": workload_config(args, shape, spec.placement, 4 if args.workload == "r1_pipeline_4layer" else 2),
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": o.num_threads(), "kind": "oracle",
                          "sample": f"{per_step} seeded tokens per step (one per oracle thread) of the {T}-token "
                                    f"layer, {args.steps} timed steps ({total:.1f} s); ms_per_step is one such "

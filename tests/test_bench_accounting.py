@@ -104,3 +104,17 @@ def test_traffic_record_is_the_full_size_capture():
     assert got is not None, "gemm.cu changed since the capture"
     assert got == pytest.approx(rec["dram_bytes_read"] + rec["dram_bytes_write"], rel=1e-4)
     assert 1.0 <= got / g1b < 1.1
+
+
+def test_both_arms_report_the_same_workload_config():
+    """The reference arm (the oracle) and the GPU arm build their config from
+    one function, so the two lines name the same workload, shapes,
+    placement and prefetch settings."""
+    args = bench.parse([])
+    spec = bench.WORKLOADS[args.workload](group=args.group)
+    cfg = bench.workload_config(args, spec.shape, spec.placement, 2)
+    assert cfg["workload"] == "r1_moe_layer_8k" and cfg["T"] == T and cfg["E"] == E and cfg["k"] == K
+    assert (cfg["local_experts"], cfg["remote_experts"], cfg["peer_pools"]) == (64, 192, 3)
+    assert cfg["chunk_mb"] == 32.0 and cfg["expert_weights"] == "bf16" and cfg["layers"] == 2
+    src = open(bench.__file__).read()
+    assert src.count("\"config\": workload_config(args,") == 2     # the GPU arm's line and the reference arm's
