@@ -346,7 +346,8 @@ int32_t dwdp_device_status(dwdp_ctx* ctx);
  * events[4] after the gate/up GEMM, events[5] after the down GEMM and
  * events[6] after the combine.  The context keeps the pointers
  * until the next call; the caller keeps the events alive.  Errors:
- * INVALID_ARG. */
+ * INVALID_ARG (a NULL event or a wrong count; the previous events, or
+ * none, stay in effect). */
 #define DWDP_PHASE_EVENTS 7
 int32_t dwdp_set_phase_events(dwdp_ctx* ctx, void* const* events, int32_t n_events);
 

@@ -18,7 +18,7 @@ DWDP_OK = 0
 STATUS = {0: "OK", -1: "INVALID_ARG", -2: "NOT_MAPPED", -3: "CUDA", -4: "TIMEOUT", -5: "UNSUPPORTED",
           -6: "DEVICE_CHECK"}
 EPI_BF16, EPI_SILU, EPI_F32 = 0, 1, 2
-DWDP_PHASE_EVENTS = 7  # dwdp_set_phase_events: route start/end, stage ready, gathered, gate/up, down, combine
+DWDP_PHASE_EVENTS = 7  # dwdp_set_phase_events: route start/end, rows in expert order, stage waited for, gate/up, down, combine
 DTYPE_BF16, DTYPE_E4M3, DTYPE_NVFP4 = 0, 1, 2
 FLAG_WIDE_EPILOGUE = 1
 

@@ -898,10 +898,10 @@ int32_t dwdp_set_phase_events(dwdp_ctx* ctx, void* const* events, int32_t n_even
         return DWDP_OK;
     }
     if (n_events != DWDP_PHASE_EVENTS) return fail(ctx, DWDP_ERR_INVALID_ARG, "need %d events", DWDP_PHASE_EVENTS);
-    for (int i = 0; i < DWDP_PHASE_EVENTS; ++i) {
+    // all checked before any is taken: a rejected call leaves the previous set
+    for (int i = 0; i < DWDP_PHASE_EVENTS; ++i)
         if (!events[i]) return fail(ctx, DWDP_ERR_INVALID_ARG, "event %d is NULL", i);
-        ctx->phase[i] = static_cast<cudaEvent_t>(events[i]);
-    }
+    for (int i = 0; i < DWDP_PHASE_EVENTS; ++i) ctx->phase[i] = static_cast<cudaEvent_t>(events[i]);
     ctx->phases_on = true;
     return DWDP_OK;
 }

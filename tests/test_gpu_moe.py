@@ -8,6 +8,7 @@ import torch
 
 import oracle
 from gpu_helpers import GpuLayerRun, assert_close, host_layer, to_f64
+from moe_expert_grouped_split_gb300 import binding as B
 from moe_expert_grouped_split_gb300 import inputs as I
 from moe_expert_grouped_split_gb300.build import build
 
@@ -174,5 +175,38 @@ def test_layer_stages_bf16(shape):
         y_want = as_bf16(o.grouped_gemm(np.ascontiguousarray(I.bf16_bits(a)[flat]), offs_sel,
                                         [w2s[e] for e in range(shape.E)] + [sw2], H, 0))
         assert_close(to_f64(y)[flat], y_want, what="down output y")
+    finally:
+        run.close()
+
+
+def test_phase_events_in_order_and_kept_on_a_rejected_call():
+    """dwdp_set_phase_events: the seven events of a layer step come in the
+    documented order (route start, route end, x in expert order, stage
+    waited for, gate/up, down, combine), and a call with a NULL event is
+    rejected without touching the events in effect."""
+    import ctypes
+
+    build()
+    shape = I.LayerShape(T=300, H=512, I=256, E=12, k=2, S=1)
+    pl = I.split_placement(shape.E, shape.E // 3, 2)
+    lw = I.make_layer(shape, pl, 41, 0, device="cuda")
+    x = I.make_tokens(shape.T, shape.H, 41).cuda()
+    run = GpuLayerRun(shape, lw)
+    try:
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(B.DWDP_PHASE_EVENTS)]
+        for e in evs:
+            e.record()                    # torch creates the CUDA event on its first record
+        B.dwdp_set_phase_events(run.rt.ctx, evs)
+        run.run(x)
+        gaps = [evs[i].elapsed_time(evs[i + 1]) for i in range(B.DWDP_PHASE_EVENTS - 1)]
+        assert all(g >= 0.0 for g in gaps), gaps
+        bad = (ctypes.c_void_p * B.DWDP_PHASE_EVENTS)(*[e.cuda_event for e in evs])
+        bad[3] = None
+        assert B.lib().dwdp_set_phase_events(run.rt.ctx, bad, B.DWDP_PHASE_EVENTS) == -1   # INVALID_ARG
+        mark = torch.cuda.Event(enable_timing=True)
+        mark.record()
+        run.run(x)                        # the first set is still in effect: re-recorded after `mark`
+        assert mark.elapsed_time(evs[0]) >= 0.0 and evs[0].elapsed_time(evs[6]) >= 0.0
+        B.dwdp_set_phase_events(run.rt.ctx, None)
     finally:
         run.close()
