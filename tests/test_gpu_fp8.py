@@ -81,6 +81,14 @@ def test_fp8_small_layer_with_shared_expert():
     _run(I.LayerShape(T=200, H=256, I=128, E=8, k=2, S=1), I.split_placement(8, 4, 1), seed=0)
 
 
+@pytest.mark.parametrize("H, I_", [(64, 64), (64, 192), (192, 64)])
+def test_fp8_rows_narrower_than_a_slice(H, I_):
+    # E4M3 rows of 64 bytes (H or I = 64) are narrower than the GEMMs'
+    # 128-byte K slice, and 192 bytes end half-way into the second one: the
+    # slice's tail past the row end must contribute nothing
+    _run(I.LayerShape(T=97, H=H, I=I_, E=6, k=2, S=1), I.split_placement(6, 2, 2), seed=5)
+
+
 def test_fp8_ragged_many_experts():
     _run(I.LayerShape(T=333, H=512, I=256, E=16, k=4, S=0), I.split_placement(16, 5, 3), seed=1)
 
