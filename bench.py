@@ -188,9 +188,10 @@ def step_bytes(T, H, I, E_active, k, S, R, wb=2):
 def kernels_per_layer(wdtype: str) -> int:
     """This library's kernel launches per layer step: route = router GEMM,
     top-k and the three grouping kernels; the layer = (quantizers,) scatter
-    into expert order (fused into the NVFP4 x quantizer), the two GEMMs and
-    the combine.  (The ncu launch lists in profiles/ show the same counts.)"""
-    layer = {"bf16": 4, "fp8": 6, "nvfp4": 5}[wdtype]
+    into expert order (fused into the E4M3 and NVFP4 x quantizers), the two
+    GEMMs and the combine.  (The ncu launch lists in profiles/ show the same
+    counts.)"""
+    layer = {"bf16": 4, "fp8": 5, "nvfp4": 5}[wdtype]
     return 5 + layer
 
 

@@ -759,9 +759,10 @@ int32_t dwdp_moe_layer(dwdp_ctx* ctx, int32_t layer, int32_t stage, const void* 
                                                route->offsets, (int)E, S > 0, xq, sx, xp, sxp, sfx, L.sf_tiles,
                                                ctx->d_err, stream));
     } else if (fmt == FMT_E4M3) {
-        // x rows to E4M3 (per-token scales), then copied into expert order
-        DWDP_CUDA(ctx, launch_quantize_rows(x, T, (int)H, xq, sx, stream));
-        DWDP_CUDA(ctx, launch_gather_fp8(xq, sx, (int)H, route->inv_perm, (int)T, (int)k, xp, sxp, ctx->d_err, stream));
+        // x rows to E4M3 (per-token scales) once, written to xq and into
+        // expert order in the same pass
+        DWDP_CUDA(ctx, launch_quantize_x_e4m3(x, (int)H, route->inv_perm, (int)T, (int)k, xq, sx, xp, sxp, ctx->d_err,
+                                              stream));
     } else {
         DWDP_CUDA(ctx, launch_gather(x, (int)H, route->inv_perm, (int)T, (int)k, xp, ctx->d_err, stream));
     }

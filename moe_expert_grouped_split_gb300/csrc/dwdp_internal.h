@@ -184,9 +184,10 @@ cudaError_t launch_gather(const void* x, int H, const int32_t* inv, int T, int k
                           cudaStream_t s);
 // E4M3 rows: codes[r][:] and scale[r] of bf16 rows (scale = amax / 448).
 cudaError_t launch_quantize_rows(const void* in, int64_t rows, int cols, void* codes, float* scale, cudaStream_t s);
-// Expert-ordered E4M3 rows: xp[inv[t k + j]] = xq[t], sxp[inv[t k + j]] = sx[t].
-cudaError_t launch_gather_fp8(const void* xq, const float* sx, int H, const int32_t* inv, int T, int k,
-                              void* xp, float* sxp, int* err, cudaStream_t s);
+// x rows to E4M3 as launch_quantize_rows does (xq, sx), each also written to
+// its chosen experts' rows: xp[inv[t k + j]] = xq[t], sxp[inv[t k + j]] = sx[t].
+cudaError_t launch_quantize_x_e4m3(const void* x, int H, const int32_t* inv, int T, int k, void* xq, float* sx,
+                                   void* xp, float* sxp, int* err, cudaStream_t s);
 // NVFP4 activations (block scales in the GEMM's A-tile chunk layout): x
 // rows quantized once per token and written to the shared-expert copy (xq,
 // sx) and to each chosen expert's row of xp / sxp; a rows (routed rows in

@@ -326,8 +326,8 @@ __global__ void __launch_bounds__(kChunk) chunk_place_kernel(const int32_t* __re
 }
 
 // Expert-ordered copies of the token rows: xp[inv[t k + j]][:] = x[t][:]
-// for every chosen expert j of token t (and sxp[inv[t k + j]] = sx[t] for
-// E4M3 rows).  One warp per token reads its row from HBM once and stores
+// for every chosen expert j of token t (and sxp[inv[t k + j]] = sx[t] when
+// sxp is given).  One warp per token reads its row from HBM once and stores
 // it to its k slots, so the pass moves T rows in and T k rows out; walking
 // the permuted rows instead reads each token row k times at random
 // distances, which L2 does not hold.  The stores are streaming
@@ -495,17 +495,24 @@ __global__ void __launch_bounds__(256) combine_kernel_k(const uint4* __restrict_
     }
 }
 
-// E4M3 rows, one warp per row: amax of the row (binary32, exact for bf16
-// inputs), scale = amax / 448 (1 for an all-zero row), code = E4M3 of the
-// binary32 quotient v / scale, rounded to nearest even and saturated to
-// +-448.  cols is a multiple of 8.
-__global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restrict__ in, int64_t rows, int cols,
-                                                            uint2* __restrict__ codes, float* __restrict__ scale) {
-    const int lane = threadIdx.x & 31;
-    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (r >= rows) return;
-    const int nv = cols / 8;
-    const uint4* src = in + r * nv;
+// Eight bf16 values to E4M3 codes (byte i of the result is value i): the
+// binary32 quotient v / s, rounded to nearest even, saturated to +-448.
+__device__ __forceinline__ uint2 e4m3_codes8(uint4 q, float s) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+    uint32_t w[2] = {0, 0};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(h[j]);
+        const uint32_t c0 = __nv_cvt_float_to_fp8(f.x / s, __NV_SATFINITE, __NV_E4M3);
+        const uint32_t c1 = __nv_cvt_float_to_fp8(f.y / s, __NV_SATFINITE, __NV_E4M3);
+        w[j >> 1] |= (c0 | (c1 << 8)) << ((j & 1) * 16);
+    }
+    return make_uint2(w[0], w[1]);
+}
+
+// binary32 amax of a warp's bf16 row (exact for bf16 inputs), all lanes
+// holding it.
+__device__ __forceinline__ float row_amax_bf16(const uint4* __restrict__ src, int nv, int lane) {
     float amax = 0.0f;
     for (int i = lane; i < nv; i += 32) {
         const uint4 q = __ldg(src + i);
@@ -518,21 +525,76 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restr
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    return amax;
+}
+
+// E4M3 rows, one warp per row: amax of the row (binary32, exact for bf16
+// inputs), scale = amax / 448 (1 for an all-zero row), code = E4M3 of the
+// binary32 quotient v / scale, rounded to nearest even and saturated to
+// +-448.  cols is a multiple of 8.
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const uint4* __restrict__ in, int64_t rows, int cols,
+                                                            uint2* __restrict__ codes, float* __restrict__ scale) {
+    const int lane = threadIdx.x & 31;
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (r >= rows) return;
+    const int nv = cols / 8;
+    const uint4* src = in + r * nv;
+    const float amax = row_amax_bf16(src, nv, lane);
     const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
     if (lane == 0) scale[r] = s;
     uint2* dst = codes + r * nv;
-    for (int i = lane; i < nv; i += 32) {
-        const uint4 q = __ldg(src + i);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
-        uint32_t w[2] = {0, 0};
+    for (int i = lane; i < nv; i += 32) dst[i] = e4m3_codes8(__ldg(src + i), s);
+}
+
+// x rows to E4M3 once per token, written to the shared expert's copy (xq,
+// sx) and straight into each chosen expert's row of xp / sxp (inv[t k + j]),
+// so x's codes are not read back for a separate scatter.  One warp per token,
+// the same arithmetic as quantize_rows_kernel; the second pass re-reads the
+// row from L2.  KC > 0 fixes k at compile time.  A destination outside
+// [0, T k) is flagged in err and not written.
+template <int KC>
+__global__ void __launch_bounds__(256) quantize_x_e4m3_kernel(const uint4* __restrict__ x, int nv,
+                                                              const int32_t* __restrict__ inv, int T, int k,
+                                                              uint2* __restrict__ xq, float* __restrict__ sx,
+                                                              uint2* __restrict__ xp, float* __restrict__ sxp,
+                                                              int* __restrict__ err) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const int kk = KC > 0 ? KC : k;
+    const int64_t n_rows = (int64_t)T * kk;
+    const int32_t* it = inv + (int64_t)t * kk;
+    uint32_t ok = 0;  // bit j: destination j is in range
+    for (int j = 0; j < kk; ++j) {
+        const int32_t r = it[j];
+        if (r >= 0 && r < n_rows) ok |= 1u << j;
+    }
+    if (ok != (kk == 32 ? 0xffffffffu : (1u << kk) - 1u) && lane == 0) atomicOr(err, DERR_BAD_INDEX);
+    const uint4* src = x + (int64_t)t * nv;
+    const float amax = row_amax_bf16(src, nv, lane);
+    const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    if (lane == 0) sx[t] = s;
+    for (int j = lane; j < kk; j += 32)
+        if ((ok >> j) & 1u) sxp[it[j]] = s;
+    uint2* own = xq + (int64_t)t * nv;
+    if constexpr (KC > 0) {
+        int64_t dst[KC];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 f = __bfloat1622float2(h[j]);
-            const uint32_t c0 = __nv_cvt_float_to_fp8(f.x / s, __NV_SATFINITE, __NV_E4M3);
-            const uint32_t c1 = __nv_cvt_float_to_fp8(f.y / s, __NV_SATFINITE, __NV_E4M3);
-            w[j >> 1] |= (c0 | (c1 << 8)) << ((j & 1) * 16);
+        for (int j = 0; j < KC; ++j) dst[j] = (int64_t)it[j] * nv;
+        for (int i = lane; i < nv; i += 32) {
+            const uint2 c = e4m3_codes8(__ldg(src + i), s);
+            own[i] = c;
+#pragma unroll
+            for (int j = 0; j < KC; ++j)
+                if ((ok >> j) & 1u) __stcs(xp + dst[j] + i, c);
         }
-        dst[i] = make_uint2(w[0], w[1]);
+    } else {
+        for (int i = lane; i < nv; i += 32) {
+            const uint2 c = e4m3_codes8(__ldg(src + i), s);
+            own[i] = c;
+            for (int j = 0; j < kk; ++j)
+                if ((ok >> j) & 1u) __stcs(xp + (int64_t)it[j] * nv + i, c);
+        }
     }
 }
 
@@ -909,9 +971,21 @@ cudaError_t launch_quantize_rows(const void* in, int64_t rows, int cols, void* c
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather_fp8(const void* xq, const float* sx, int H, const int32_t* inv, int T, int k,
-                              void* xp, float* sxp, int* err, cudaStream_t s) {
-    return scatter_rows(xq, H / 16, inv, T, k, xp, sx, sxp, err, s);
+cudaError_t launch_quantize_x_e4m3(const void* x, int H, const int32_t* inv, int T, int k, void* xq, float* sx,
+                                   void* xp, float* sxp, int* err, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    const int warps = 8;
+    const dim3 grid((T + warps - 1) / warps), block(32 * warps);
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    uint2* qv = reinterpret_cast<uint2*>(xq);
+    uint2* pv = reinterpret_cast<uint2*>(xp);
+    switch (k) {
+        case 2: quantize_x_e4m3_kernel<2><<<grid, block, 0, s>>>(xv, H / 8, inv, T, k, qv, sx, pv, sxp, err); break;
+        case 4: quantize_x_e4m3_kernel<4><<<grid, block, 0, s>>>(xv, H / 8, inv, T, k, qv, sx, pv, sxp, err); break;
+        case 8: quantize_x_e4m3_kernel<8><<<grid, block, 0, s>>>(xv, H / 8, inv, T, k, qv, sx, pv, sxp, err); break;
+        default: quantize_x_e4m3_kernel<0><<<grid, block, 0, s>>>(xv, H / 8, inv, T, k, qv, sx, pv, sxp, err);
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_topk(const float* logits, int parts, int64_t part_stride, const float* bias, int T, int E,
