@@ -334,8 +334,19 @@ int32_t dwdp_stage_layer(const dwdp_ctx* ctx, int32_t stage);
 /* Read and clear the device error word (synchronises the device).  OK, or
  * DEVICE_CHECK with the failing check described by dwdp_last_error: bits
  * 0-5 a bounded wait inside the grouped GEMM ran out, bit 6 an index outside
- * its buffer was skipped, bit 7 a router logit was not finite. */
+ * its buffer was skipped, bit 7 a router logit was not finite, bit 8 the
+ * wait of dwdp_selftest_bounded_wait ran out (as that call intends). */
 int32_t dwdp_device_status(dwdp_ctx* ctx);
+
+/* Diagnostic (the pages have no counterpart): enqueues on `stream` one
+ * one-thread kernel that waits, with the same bounded mbarrier wait every
+ * grouped-GEMM role uses, for a barrier phase that nothing completes.  The
+ * wait gives up after limit_us microseconds, sets bit 8 of the context's
+ * device error word and the kernel returns: no trap, no hang, the context
+ * stays usable.  The next dwdp_device_status then returns DEVICE_CHECK
+ * (and clears the word).  limit_us in [1, 1000000].  Errors: INVALID_ARG,
+ * CUDA. */
+int32_t dwdp_selftest_bounded_wait(dwdp_ctx* ctx, uint32_t limit_us, dwdp_stream_t stream);
 
 /* Optional phase timing.  events is a host array of DWDP_PHASE_EVENTS
  * caller-owned cudaEvent_t (or NULL to stop).  While set, dwdp_route records

@@ -82,6 +82,7 @@ SIGNATURES = [
     ("dwdp_stage_layer", _I32, [_VP, _I32]),
     ("dwdp_device_status", _I32, [_VP]),
     ("dwdp_set_phase_events", _I32, [_VP, ctypes.POINTER(_VP), _I32]),
+    ("dwdp_selftest_bounded_wait", _I32, [_VP, ctypes.c_uint32, _VP]),
     ("dwdp_set_expert_scales", _I32, [_VP, _I32, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float),
                                       ctypes.c_float, ctypes.c_float]),
     ("dwdp_grouped_gemm", _I32, [_VP, _I32, _VP, ctypes.c_int64, _I32, _I32, _VP, _I32, ctypes.POINTER(dwdp_pool),
@@ -237,6 +238,11 @@ def dwdp_set_phase_events(ctx, events) -> None:
         return
     arr = (_VP * len(events))(*[e.cuda_event for e in events])
     _check(ctx, lib().dwdp_set_phase_events(ctx, arr, len(events)))
+
+
+def dwdp_selftest_bounded_wait(ctx, limit_us: int, stream=None) -> None:
+    """Enqueue the bounded-wait diagnostic (its wait runs out by design)."""
+    _check(ctx, lib().dwdp_selftest_bounded_wait(ctx, int(limit_us), _stream(stream)))
 
 
 def dwdp_grouped_gemm(ctx, epilogue, a, a_rows, K, N, row_offsets, G, bufs, buf_slot, d, stream=None) -> None:

@@ -907,6 +907,14 @@ int32_t dwdp_set_phase_events(dwdp_ctx* ctx, void* const* events, int32_t n_even
     return DWDP_OK;
 }
 
+int32_t dwdp_selftest_bounded_wait(dwdp_ctx* ctx, uint32_t limit_us, dwdp_stream_t stream) {
+    if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
+    if (limit_us < 1 || limit_us > 1000000)
+        return fail(ctx, DWDP_ERR_INVALID_ARG, "limit_us %u outside [1, 1000000]", limit_us);
+    DWDP_CUDA(ctx, launch_bounded_wait_selftest(ctx->d_err, (uint64_t)limit_us * 1000ull, stream));
+    return DWDP_OK;
+}
+
 int32_t dwdp_device_status(dwdp_ctx* ctx) {
     if (!ctx) return fail(nullptr, DWDP_ERR_INVALID_ARG, "ctx is NULL");
     return check_device_error_word(ctx);

@@ -72,7 +72,12 @@ enum DeviceError : int {
     DERR_MMA_DONE_WAIT = 1 << 5,
     DERR_BAD_INDEX = 1 << 6,
     DERR_NONFINITE_LOGIT = 1 << 7,  // a router logit is NaN or infinite
+    DERR_SELFTEST_WAIT = 1 << 8,    // dwdp_selftest_bounded_wait's wait ran out (its expected result)
 };
+
+// One-thread kernel whose bounded mbarrier wait (the grouped GEMM's) runs
+// out after limit_ns and records DERR_SELFTEST_WAIT in err (gemm.cu).
+cudaError_t launch_bounded_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t stream);
 
 // Everything one grouped-GEMM launch needs; passed by value (grid constant).
 // Group g < n_routed has rows [row_offsets[g], row_offsets[g+1]) of A0 and D;

@@ -118,14 +118,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // aborting (another role gave up) or when this wait ran out of time, in which
 // case it raises the abort flag and records `code` in the error word.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err, int code) {
+                                          int* err, int code, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort_flag) return false;
-            if (global_timer() - t0 > kWaitLimitNs) {
+            if (global_timer() - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicOr(err, code);
                 return false;
@@ -866,7 +866,26 @@ __global__ void __launch_bounds__(Warps<FMT, EPIW>::kThreads, 1) grouped_gemm_ke
     }
 }
 
+// The bounded-wait check of dwdp_selftest_bounded_wait: one thread waits,
+// with the GEMM's own mbar_wait and the given limit, for a phase of an
+// mbarrier that nothing arrives at, so the wait runs out and records
+// DERR_SELFTEST_WAIT.  The loop reads the global timer, so it always ends.
+__global__ void bounded_wait_selftest_kernel(int* err, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_wait(smem_u32(&bar), 0u, &abort_flag, err, DERR_SELFTEST_WAIT, limit_ns);
+}
+
 }  // namespace
+
+cudaError_t launch_bounded_wait_selftest(int* err, uint64_t limit_ns, cudaStream_t stream) {
+    bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+    return cudaGetLastError();
+}
 
 template <int FMT>
 size_t gemm_smem_bytes(int n_groups) {

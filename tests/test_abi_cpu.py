@@ -125,6 +125,7 @@ def test_host_validation_without_gpu(lib):
     assert lib.dwdp_create(ctypes.byref(cfg), None, None, ctypes.byref(out)) == -1
     assert "flags" in B.dwdp_last_error(None)
     assert lib.dwdp_workspace_bytes(None, 10) == 0
+    assert lib.dwdp_selftest_bounded_wait(None, 1000, None) == -1            # no context: nothing enqueued
     # activation quantization: argument checks come before any CUDA call
     x = ctypes.c_void_p(16)
     assert lib.dwdp_quantize_rows(B.DTYPE_BF16, x, 4, 64, x, x, x, None) == -1      # not a quantized type

@@ -210,3 +210,37 @@ def test_phase_events_in_order_and_kept_on_a_rejected_call():
         B.dwdp_set_phase_events(run.rt.ctx, None)
     finally:
         run.close()
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """The bounded mbarrier wait every grouped-GEMM role uses, made to run out
+    (dwdp_selftest_bounded_wait: a barrier phase that nothing completes):
+    the kernel returns after about the limit, the host reads DEVICE_CHECK
+    with bit 8, the error word is cleared, and the context then runs a layer
+    as before."""
+    build()
+    shape = I.LayerShape(T=64, H=256, I=128, E=8, k=2, S=1)
+    pl = I.split_placement(8, 4, 1)
+    lw = I.make_layer(shape, pl, 43, 0, device="cuda")
+    x = I.make_tokens(shape.T, shape.H, 43).cuda()
+    run = GpuLayerRun(shape, lw)
+    try:
+        _, before = run.run(x)
+        before = before.clone()
+        with pytest.raises(B.DwdpError):
+            B.dwdp_selftest_bounded_wait(run.rt.ctx, 0)            # limit outside [1, 1e6] us
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream = torch.cuda.current_stream()
+        start.record(stream)
+        B.dwdp_selftest_bounded_wait(run.rt.ctx, 20_000, stream)  # 20 ms
+        end.record(stream)
+        torch.cuda.synchronize()
+        ms = start.elapsed_time(end)
+        assert 19.0 <= ms < 1000.0, f"the wait took {ms} ms"
+        assert run.rt.device_status() == -6                         # DEVICE_CHECK
+        assert "0x100" in B.dwdp_last_error(run.rt.ctx)
+        assert run.rt.device_status() == 0                          # cleared by the read
+        _, after = run.run(x)
+        assert torch.equal(after, before)
+    finally:
+        run.close()
