@@ -176,3 +176,8 @@ def test_fp8_layer_stages(shape):
         y_got.append(y_gpu[rows])
     assert_close(np.concatenate(a_got), np.concatenate(a_want), what="E4M3 gate/up output a")
     assert_close(np.concatenate(y_got), np.concatenate(y_want), what="E4M3 down output y")
+
+
+def test_fp8_layer_at_the_limits():
+    # 1024 experts, top-32, shared expert (1025 groups)
+    _run(I.LayerShape(T=48, H=128, I=128, E=1024, k=32, S=1), I.split_placement(1024, 512, 2), seed=45)

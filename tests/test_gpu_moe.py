@@ -244,3 +244,10 @@ def test_bounded_wait_gives_up_and_reports():
         assert torch.equal(after, before)
     finally:
         run.close()
+
+
+def test_layer_at_the_limits():
+    """1024 experts (the ABI's maximum) with top-32 (its maximum k) and the
+    shared expert: 1025 groups in the GEMMs' tile tables, the generic
+    scatter and combine paths, half the experts staged from two pools."""
+    _run_and_check(I.LayerShape(T=48, H=128, I=64, E=1024, k=32, S=1), I.split_placement(1024, 512, 2), seed=44)

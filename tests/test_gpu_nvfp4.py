@@ -446,3 +446,9 @@ def test_nvfp4_wide_epilogue_bit_identical(shape):
             rt.close()
     assert torch.equal(outs[0][1], outs[1][1]), "a differs between four and eight epilogue warps"
     assert torch.equal(outs[0][0], outs[1][0]), "output differs between four and eight epilogue warps"
+
+
+def test_nvfp4_layer_at_the_limits():
+    # 1024 experts, top-32, shared expert: 1025 groups, the largest tile
+    # table beside the NVFP4 GEMM's shared-memory ring
+    _run(I.LayerShape(T=48, H=256, I=256, E=1024, k=32, S=1), I.split_placement(1024, 512, 2), seed=46)

@@ -147,3 +147,12 @@ def test_tensor_mapped_inputs_must_be_this_devices_memory():
         assert rt.device_status() == 0
     finally:
         rt.close()
+
+
+@pytest.mark.parametrize("T, H, E, k", [(200, 256, 1024, 32), (300, 128, 300, 16), (129, 256, 512, 5)],
+                         ids=["E1024_k32", "E300_k16", "E512_k5"])
+def test_routing_at_the_limits(T, H, E, k):
+    # the largest expert count and top-k the ABI accepts (32 logits per lane,
+    # a four-n-tile router GEMM), E not a multiple of the warp, k beyond the
+    # specialised widths
+    _route_case(T, H, E, k, seed=8, router_std=0.05)
