@@ -86,6 +86,17 @@ WORKLOADS = {
 }
 
 
+def default_chunk_mb(workload: str, wdtype: str) -> float:
+    """Prefetch slice size: 16 MB for the 4-layer pipeline (its workload's
+    own figure); otherwise the fastest measured on one GB300 (same-box A/B,
+    two to three runs each): 64 MB for bf16 and E4M3 (against 32 MB: C1
+    bf16 -1.5%, E4M3 -2%, the 256-token layer -4.8%; 128 MB no better), 32
+    MB for NVFP4 (0.3% ahead of 64 MB, with two copy chains)."""
+    if workload == "r1_pipeline_4layer":
+        return 16.0
+    return 32.0 if wdtype == "nvfp4" else 64.0
+
+
 def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -95,7 +106,7 @@ def parse(argv=None):
     p.add_argument("--workload", default="r1_moe_layer_8k", choices=sorted(WORKLOADS))
     p.add_argument("--chunk-mb", type=float, default=None,
                    help="prefetch slice size in MB (default 16 for the 4-layer pipeline, as that workload "
-                        "specifies, else 32: the fastest single-destination setting measured)")
+                        "specifies; else the fastest measured: 64 for bf16 and E4M3, 32 for NVFP4)")
     p.add_argument("--copy-streams", type=int, default=None,
                    help="copy chains the prefetch graph is split into, one per peer pool modulo this count "
                         "(default 1 for bf16 and E4M3, 2 for NVFP4: the fastest measured)")
@@ -136,7 +147,7 @@ def parse(argv=None):
                         "appendix A.2)")
     args = p.parse_args(argv)
     if args.chunk_mb is None:
-        args.chunk_mb = 16.0 if args.workload == "r1_pipeline_4layer" else 32.0
+        args.chunk_mb = default_chunk_mb(args.workload, args.dtype)
     args.copy_streams_given = args.copy_streams is not None
     if args.copy_streams is None:
         args.copy_streams = 2 if args.dtype == "nvfp4" else 1
@@ -1032,7 +1043,7 @@ def variant_summary(args, variant: str) -> dict:
     if not args.copy_streams_given:
         a.copy_streams = 2 if wdtype == "nvfp4" else 1
     a.chunk_sweep = "1,4,16,64" if workload == "r1_moe_layer_256" and wdtype == "bf16" else ""
-    a.chunk_mb = 16.0 if workload == "r1_pipeline_4layer" else 32.0
+    a.chunk_mb = default_chunk_mb(workload, wdtype)
     pipeline = workload == "r1_pipeline_4layer"
     if pipeline:
         a.steps = 16        # the 4-layer workload's own step count

@@ -115,6 +115,8 @@ def test_both_arms_report_the_same_workload_config():
     cfg = bench.workload_config(args, spec.shape, spec.placement, 2)
     assert cfg["workload"] == "r1_moe_layer_8k" and cfg["T"] == T and cfg["E"] == E and cfg["k"] == K
     assert (cfg["local_experts"], cfg["remote_experts"], cfg["peer_pools"]) == (64, 192, 3)
-    assert cfg["chunk_mb"] == 32.0 and cfg["expert_weights"] == "bf16" and cfg["layers"] == 2
+    assert cfg["chunk_mb"] == 64.0 and cfg["expert_weights"] == "bf16" and cfg["layers"] == 2
+    assert bench.default_chunk_mb("r1_moe_layer_8k", "nvfp4") == 32.0
+    assert bench.default_chunk_mb("r1_pipeline_4layer", "bf16") == 16.0
     src = open(bench.__file__).read()
     assert src.count("\"config\": workload_config(args,") == 2     # the GPU arm's line and the reference arm's
