@@ -97,6 +97,14 @@ def default_chunk_mb(workload: str, wdtype: str) -> float:
     return 32.0 if wdtype == "nvfp4" else 64.0
 
 
+def default_copy_streams(workload: str, wdtype: str) -> int:
+    """Copy chains of the prefetch graph: two for NVFP4 layers and for the
+    copy-bound 256-token layer (same-box A/B: NVFP4 C1 -1.5%, 256 tokens bf16
+    -1.7%), one otherwise (two slow the GEMMs beside them more than they
+    speed the copy: C1 bf16 +0.8%, E4M3 +0.6%)."""
+    return 2 if wdtype == "nvfp4" or workload == "r1_moe_layer_256" else 1
+
+
 def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -109,7 +117,7 @@ def parse(argv=None):
                         "specifies; else the fastest measured: 64 for bf16 and E4M3, 32 for NVFP4)")
     p.add_argument("--copy-streams", type=int, default=None,
                    help="copy chains the prefetch graph is split into, one per peer pool modulo this count "
-                        "(default 1 for bf16 and E4M3, 2 for NVFP4: the fastest measured)")
+                        "(default 2 for NVFP4 and for the 256-token layer, else 1: the fastest measured)")
     p.add_argument("--stages", type=int, default=2,
                    help="staging buffers (2: the pages' double buffering; 3: the copy of layer l+2 may start "
                         "while layer l computes)")
@@ -150,7 +158,7 @@ def parse(argv=None):
         args.chunk_mb = default_chunk_mb(args.workload, args.dtype)
     args.copy_streams_given = args.copy_streams is not None
     if args.copy_streams is None:
-        args.copy_streams = 2 if args.dtype == "nvfp4" else 1
+        args.copy_streams = default_copy_streams(args.workload, args.dtype)
     if args.workload == "r1_moe_layer_8k" and not args.no_extras and args.group == 4:
         args.merge_copy = True
     if args.no_merge_copy:
@@ -1041,7 +1049,7 @@ def variant_summary(args, variant: str) -> dict:
     merge = workload == "r1_moe_layer_8k" and wdtype == "nvfp4" and not wide and args.group == 4
     a.workload, a.dtype, a.merge_copy, a.wide_epilogue = workload, wdtype, merge, wide
     if not args.copy_streams_given:
-        a.copy_streams = 2 if wdtype == "nvfp4" else 1
+        a.copy_streams = default_copy_streams(workload, wdtype)
     a.chunk_sweep = "1,4,16,64" if workload == "r1_moe_layer_256" and wdtype == "bf16" else ""
     a.chunk_mb = default_chunk_mb(workload, wdtype)
     pipeline = workload == "r1_pipeline_4layer"

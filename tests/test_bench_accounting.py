@@ -118,5 +118,8 @@ def test_both_arms_report_the_same_workload_config():
     assert cfg["chunk_mb"] == 64.0 and cfg["expert_weights"] == "bf16" and cfg["layers"] == 2
     assert bench.default_chunk_mb("r1_moe_layer_8k", "nvfp4") == 32.0
     assert bench.default_chunk_mb("r1_pipeline_4layer", "bf16") == 16.0
+    assert bench.default_copy_streams("r1_moe_layer_8k", "bf16") == 1
+    assert bench.default_copy_streams("r1_moe_layer_8k", "nvfp4") == 2
+    assert bench.default_copy_streams("r1_moe_layer_256", "bf16") == 2
     src = open(bench.__file__).read()
     assert src.count("\"config\": workload_config(args,") == 2     # the GPU arm's line and the reference arm's
