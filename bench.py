@@ -98,11 +98,14 @@ def default_chunk_mb(workload: str, wdtype: str) -> float:
 
 
 def default_copy_streams(workload: str, wdtype: str) -> int:
-    """Copy chains of the prefetch graph: two for NVFP4 layers and for the
-    copy-bound 256-token layer (same-box A/B: NVFP4 C1 -1.5%, 256 tokens bf16
-    -1.7%), one otherwise (two slow the GEMMs beside them more than they
-    speed the copy: C1 bf16 +0.8%, E4M3 +0.6%)."""
-    return 2 if wdtype == "nvfp4" or workload == "r1_moe_layer_256" else 1
+    """Copy chains of the prefetch graph: two for NVFP4 layers, for the
+    copy-bound 256-token layer and for the 4-layer pipeline, whose 16 MB
+    slices make the copy the longer side (same-box A/B: NVFP4 C1 -1.5%, 256
+    tokens bf16 -1.7%, pipeline bf16 -5%), one otherwise (two slow the GEMMs
+    beside them more than they speed the copy: C1 bf16 +0.8%, E4M3 +0.6%)."""
+    if wdtype == "nvfp4" or workload in ("r1_moe_layer_256", "r1_pipeline_4layer"):
+        return 2
+    return 1
 
 
 def parse(argv=None):
@@ -117,7 +120,8 @@ def parse(argv=None):
                         "specifies; else the fastest measured: 64 for bf16 and E4M3, 32 for NVFP4)")
     p.add_argument("--copy-streams", type=int, default=None,
                    help="copy chains the prefetch graph is split into, one per peer pool modulo this count "
-                        "(default 2 for NVFP4 and for the 256-token layer, else 1: the fastest measured)")
+                        "(default 2 for NVFP4, the 256-token layer and the 4-layer pipeline, else 1: the "
+                        "fastest measured)")
     p.add_argument("--stages", type=int, default=2,
                    help="staging buffers (2: the pages' double buffering; 3: the copy of layer l+2 may start "
                         "while layer l computes)")

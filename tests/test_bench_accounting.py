@@ -121,5 +121,6 @@ def test_both_arms_report_the_same_workload_config():
     assert bench.default_copy_streams("r1_moe_layer_8k", "bf16") == 1
     assert bench.default_copy_streams("r1_moe_layer_8k", "nvfp4") == 2
     assert bench.default_copy_streams("r1_moe_layer_256", "bf16") == 2
+    assert bench.default_copy_streams("r1_pipeline_4layer", "bf16") == 2
     src = open(bench.__file__).read()
     assert src.count("\"config\": workload_config(args,") == 2     # the GPU arm's line and the reference arm's
